@@ -1,0 +1,226 @@
+/*
+ * moe.h -- C ABI of the GB300 (sm_103a) Mixture-of-Experts layer forward.
+ *
+ * One MoE layer forward in four stages, every stage a CUDA kernel of this
+ * library, all enqueued on the caller's stream with no device-to-host
+ * readback and no host synchronisation:
+ *
+ *   1. moe_route           router top-k and gate weights
+ *   2. moe_build_metadata  per-expert histogram, ragged offsets, stable
+ *                          expert-sorted dispatch / combine indices, gate_scal
+ *   3. moe_grouped_ffn     per-expert SwiGLU / SwiGLU-OAI FFN over each
+ *                          expert's contiguous slice (grouped GEMM), gate
+ *                          scale and scatter back to token-slot order
+ *   4. moe_combine         sum of a token's k weighted expert outputs
+ *   moe_forward            1 -> 4 in one call
+ *
+ * Sources (page title, section):
+ *  [R1] "Reuse topk SparseMatrix routing metadata in GPT-OSS MoE forward"
+ *       (vLLM PR #45457 report), 实现拆解 and 关键源码片段
+ *       (routing_data_from_sparse_topk, topk_fn(logits, k, apply_softmax=True)).
+ *  [R2] "MoE feed-forward performs ~3xnum_experts device->host syncs per
+ *       layer, per forward" (MiniMind issue #835), Summary and "It is
+ *       removable in plain PyTorch".
+ *  [R3] "CuteDSL NVFP4 MoE adds SwiGLU-OAI and ReLU2" (vLLM PR #47106
+ *       report), 关键源码片段 (apply, reorder_w13_to_w31_for_flashinfer_cutedsl)
+ *       and 评论区精华 (parameter defaults).
+ *
+ * Notation: n tokens, E experts, k experts per token (n_expts_act), H hidden
+ * size, I expert intermediate size; f = t*k + j is the flat slot index of
+ * token t's j-th choice; p is a position in the expert-sorted order.
+ * bf16 values travel as uint16_t bit patterns.
+ *
+ * Conventions for every call:
+ *  - Pointers named d_* / device buffers are CUDA device pointers on the
+ *    current device. The caller allocates and owns every buffer, including
+ *    the workspace; the library never allocates, frees, synchronises or
+ *    copies device-to-host (moe_read_status is the one documented
+ *    exception and is for debugging only).
+ *  - `stream` is a cudaStream_t (NULL = the legacy default stream). All
+ *    work is enqueued on it; outputs are valid in stream order.
+ *  - Arguments are validated on the host before any launch; a rejected call
+ *    launches nothing and returns MOE_ERR_INVALID_ARG / MOE_ERR_UNSUPPORTED /
+ *    MOE_ERR_MISALIGNED / MOE_ERR_WORKSPACE_TOO_SMALL. A failed launch
+ *    returns MOE_ERR_CUDA (cudaGetLastError, which does not synchronise).
+ *  - n = 0 is a valid no-op.
+ *  - Limits: 1 <= E <= 256, 1 <= k <= min(E, 8), n*k < 2^31; H and I
+ *    multiples of 64; bf16 tensors 16-byte aligned.
+ *  - Device-side waits are bounded. A wait that gives up records
+ *    MOE_ERR_TIMEOUT in the workspace's status word and the kernel returns;
+ *    read it with moe_read_status.
+ */
+#ifndef MOE_GB300_H
+#define MOE_GB300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define MOE_ABI_VERSION 1
+
+typedef void *moe_stream;  /* a cudaStream_t */
+
+typedef enum {
+  MOE_OK = 0,
+  MOE_ERR_INVALID_ARG = 1,         /* null pointer, size out of range, bad enum */
+  MOE_ERR_UNSUPPORTED = 2,         /* valid request this library does not implement */
+  MOE_ERR_WORKSPACE_TOO_SMALL = 3, /* workspace_bytes < moe_workspace_size(...) */
+  MOE_ERR_CUDA = 4,                /* a CUDA runtime call or launch failed */
+  MOE_ERR_TIMEOUT = 5,             /* a bounded device-side wait gave up */
+  MOE_ERR_MISALIGNED = 6           /* a pointer breaks the 16-byte alignment rule */
+} moe_status;
+
+/* Gate weights [R1] 关键源码片段 (apply_softmax=True) and [R2] Summary. */
+typedef enum {
+  MOE_GATING_SOFTMAX_TOPK = 0, /* softmax over the k selected logits */
+  MOE_GATING_SOFTMAX_ALL = 1   /* softmax over all E logits; keep the k selected, no renormalising */
+} moe_gating;
+
+/* Gated activation [R3] 关键源码片段 (apply). */
+typedef enum {
+  MOE_ACT_SWIGLU = 0,    /* h = gate * sigmoid(gate) * up */
+  MOE_ACT_SWIGLU_OAI = 1 /* g = min(gate, limit), u = clamp(up, -limit, limit),
+                            h = g * sigmoid(alpha * g) * (u + beta) */
+} moe_activation;
+
+/* Row order of w13 [E, 2I, H] [R3] 关键源码片段 (reorder_w13_to_w31_for_flashinfer_cutedsl). */
+typedef enum {
+  MOE_W13_PACKED = 0,     /* rows [gate_0 .. gate_{I-1}, up_0 .. up_{I-1}] */
+  MOE_W13_INTERLEAVED = 1 /* rows [gate_0, up_0, gate_1, up_1, ...] (gpt-oss checkpoints) */
+} moe_w13_layout;
+
+/* Flags of moe_params.set: a value whose flag is clear is NOT used; the
+ * activation keeps its own default ([R3] 关键源码片段 / 评论区精华: unset
+ * parameters must not override the kernel defaults). SwiGLU-OAI defaults:
+ * alpha 1.702, beta 1.0, limit 7.0. Plain SwiGLU takes no parameters. */
+#define MOE_SET_ALPHA 1u
+#define MOE_SET_BETA 2u
+#define MOE_SET_LIMIT 4u
+
+typedef struct {
+  int32_t gating;     /* moe_gating */
+  int32_t activation; /* moe_activation */
+  int32_t w13_layout; /* moe_w13_layout */
+  uint32_t set;       /* MOE_SET_* bits */
+  float alpha, beta, limit;
+} moe_params;
+
+/* Routing metadata [R1] 关键源码片段 (routing_data_from_sparse_topk),
+ * all device pointers, caller-owned:
+ *   col_sum[E]      per-expert count of routed slots (the histogram; also
+ *                   the ragged batch block sizes)
+ *   offs[E+1]       exclusive scan of col_sum: expert e owns sorted
+ *                   positions [offs[e], offs[e+1])
+ *   col_sorted[n*k] combine_indx: p -> f. Slots listed expert by expert,
+ *                   ascending f (token order) within an expert: the stable
+ *                   sort of [R2] "It is removable in plain PyTorch"
+ *   row_sorted[n*k] dispatch_indx: f -> p, the inverse permutation
+ *   gate_scal[n*k]  bf16 gate weight in sorted order, topk_vals_flat[col_sorted[p]]
+ * GatherIndx = (src col_sorted, dst row_sorted) and ScatterIndx = (src
+ * row_sorted, dst col_sorted) are these same two arrays. */
+typedef struct {
+  int32_t *col_sum;
+  int32_t *offs;
+  int32_t *col_sorted;
+  int32_t *row_sorted;
+  uint16_t *gate_scal;
+} moe_routing_meta;
+
+/* Version of this ABI (MOE_ABI_VERSION). */
+int32_t moe_abi_version(void);
+
+/* Human-readable name of a status code; never NULL. */
+const char *moe_status_string(moe_status status);
+
+/* Bytes of workspace that moe_build_metadata, moe_grouped_ffn and
+ * moe_forward need for these sizes (a few KB of control data plus, for the
+ * FFN, the expert-sorted activations, the intermediate h and, when k > 1,
+ * the per-slot outputs). Returns 0 for invalid sizes. */
+size_t moe_workspace_size(int64_t n, int32_t E, int32_t k, int32_t H, int32_t I);
+
+/* Prepare a freshly allocated workspace: zero its control block (the first
+ * 4 KB: status word and grid-barrier counters). Must run once, in stream
+ * order, before the workspace's first use; later calls leave the block
+ * consistent. */
+moe_status moe_workspace_init(void *workspace, size_t workspace_bytes, moe_stream stream);
+
+/* Stage 1 -- router top-k and gate weights. [R1] 关键源码片段
+ * (topk_fn(logits, k, apply_softmax=True)), [R2] Summary.
+ *   logits     [n, E] fp32, row-major, device. Finite values (NaN sorts last).
+ *   topk_indx  [n, k] int32 out: the k experts of largest logit, descending;
+ *              equal logits (compared as fp32, -0.0 == +0.0) go to the
+ *              lower expert id.
+ *   topk_vals  [n, k] bf16 out: gate weights per `gating`, computed in fp32
+ *              and rounded to nearest even. */
+moe_status moe_route(const float *logits, int64_t n, int32_t E, int32_t k, int32_t gating,
+                     int32_t *topk_indx, uint16_t *topk_vals, moe_stream stream);
+
+/* Stage 2 -- routing metadata from a top-k result. [R1] 关键源码片段.
+ *   topk_indx [n, k] int32 (each value in [0, E)), topk_vals [n, k] bf16.
+ *   meta      the five output arrays described at moe_routing_meta.
+ * Bit-reproducible: no atomic decides any position. One cooperative kernel
+ * with a bounded grid-wide barrier (MOE_ERR_TIMEOUT in the status word if
+ * it gives up). `workspace` as sized by moe_workspace_size and initialised
+ * by moe_workspace_init. */
+moe_status moe_build_metadata(const int32_t *topk_indx, const uint16_t *topk_vals, int64_t n,
+                              int32_t E, int32_t k, const moe_routing_meta *meta,
+                              void *workspace, size_t workspace_bytes, moe_stream stream);
+
+/* Stage 3 -- grouped expert FFN. [R2] Summary and "It is removable in plain
+ * PyTorch" (each expert runs on its contiguous slice; the weight multiplies
+ * the expert output), [R3] 关键源码片段 (activations, w13 layouts).
+ *   x       [n, H] bf16 tokens.
+ *   meta    metadata from moe_build_metadata (offs, col_sorted, gate_scal read).
+ *   w13     [E, 2I, H] bf16, row-major (each expert's [2I, H] block in
+ *           params->w13_layout order).
+ *   w2      [E, H, I] bf16, row-major.
+ *   y_flat  [n*k, H] bf16 out, token-slot order: row f = gate_scal[row_sorted[f]]
+ *           * (w2_e . h), e = topk_indx_flat[f], h = act(w13_e . x_t) rounded
+ *           to bf16; fp32 accumulation in both contractions. */
+moe_status moe_grouped_ffn(const uint16_t *x, const moe_routing_meta *meta, const uint16_t *w13,
+                           const uint16_t *w2, int64_t n, int32_t E, int32_t k, int32_t H,
+                           int32_t I, const moe_params *params, uint16_t *y_flat,
+                           void *workspace, size_t workspace_bytes, moe_stream stream);
+
+/* Stage 4 -- combine. [R2] Summary (y.index_add_ of the k weighted expert
+ * outputs of each token).
+ *   y_flat [n*k, H] bf16, out [n, H] bf16: out[t] = sum_{j<k} y_flat[t*k+j],
+ *   summed in fp32 in slot order j, rounded once to bf16. Deterministic. */
+moe_status moe_combine(const uint16_t *y_flat, int64_t n, int32_t k, int32_t H, uint16_t *out,
+                       moe_stream stream);
+
+/* Stages 1-4 in one call, zero host synchronisations, CUDA-graph friendly.
+ *   x [n, H] bf16, logits [n, E] fp32, w13 [E, 2I, H] bf16, w2 [E, H, I] bf16,
+ *   out [n, H] bf16.
+ *   topk_indx / topk_vals ([n, k]) and meta: optional outputs (NULL = keep
+ *   them inside the workspace). When given, all five meta arrays must be
+ *   non-NULL. */
+moe_status moe_forward(const uint16_t *x, const float *logits, const uint16_t *w13,
+                       const uint16_t *w2, int64_t n, int32_t E, int32_t k, int32_t H, int32_t I,
+                       const moe_params *params, uint16_t *out, int32_t *topk_indx,
+                       uint16_t *topk_vals, const moe_routing_meta *meta, void *workspace,
+                       size_t workspace_bytes, moe_stream stream);
+
+/* DEBUG ONLY -- synchronises `stream`, returns the status word recorded by
+ * device-side bounded waits since the last reset (MOE_OK if none), and
+ * resets it and the barrier counters when `reset` is non-zero. */
+moe_status moe_read_status(void *workspace, size_t workspace_bytes, int32_t reset,
+                           moe_stream stream);
+
+/* DIAGNOSTIC -- launches one thread that waits, through the library's
+ * bounded device-side wait, on a control word that nothing ever sets. After
+ * `timeout_ns` (1 .. 1e9) the wait gives up, records MOE_ERR_TIMEOUT in the
+ * status word and the kernel returns: the error path of every bounded wait
+ * (the metadata kernel's grid barrier uses the same one), exercised without
+ * a fault or a hang. Read the result with moe_read_status. */
+moe_status moe_selftest_wait_timeout(void *workspace, size_t workspace_bytes, uint64_t timeout_ns,
+                                     moe_stream stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MOE_GB300_H */

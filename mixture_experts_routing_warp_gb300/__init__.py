@@ -1,1 +1,17 @@
-"""GB300-native Mixture-of-Experts layer forward (placeholder; binding follows)."""
+"""GB300-native (sm_103a) Mixture-of-Experts layer forward.
+
+route -> routing metadata -> grouped SwiGLU / SwiGLU-OAI expert FFN ->
+gate-weighted combine, every stage a CUDA kernel in libmoe_gb300.so behind
+the C ABI of include/moe.h. This package is the thin Python binding
+(argument marshalling over torch tensors) plus the seeded input generators
+(`inputs`).
+"""
+from ._binding import (ACT, GATING, LAYOUT, MoEError, MoeParams, RoutingMeta, build_metadata,
+                       combine, empty_meta, forward, grouped_ffn, lib, library_path, make_params,
+                       read_status, route, selftest_wait_timeout, status_string, workspace,
+                       workspace_size)
+
+__all__ = ["ACT", "GATING", "LAYOUT", "MoEError", "MoeParams", "RoutingMeta", "build_metadata",
+           "combine", "empty_meta", "forward", "grouped_ffn", "lib", "library_path",
+           "make_params", "read_status", "route", "selftest_wait_timeout", "status_string",
+           "workspace", "workspace_size"]

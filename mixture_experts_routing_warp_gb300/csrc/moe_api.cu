@@ -1,0 +1,246 @@
+// moe_api.cu -- the extern "C" entry points declared in include/moe.h:
+// argument validation, workspace carving, and the launch sequence of each
+// stage on the caller's stream. No allocation, no synchronisation, no
+// device-to-host copy (moe_read_status excepted, documented as debug-only).
+#include <math.h>
+#include <string.h>
+
+#include "moe_internal.cuh"
+
+using namespace moe;
+
+namespace {
+
+inline bool aligned(const void *p, size_t a) { return ((uintptr_t)p % a) == 0; }
+
+moe_status check_sizes(int64_t n, int E, int k, int H, int I, bool need_hi) {
+  if (n < 0 || E < 1 || E > kMaxExperts || k < 1 || k > kMaxTopk || k > E)
+    return MOE_ERR_INVALID_ARG;
+  if (n * (int64_t)k >= (int64_t)INT32_MAX) return MOE_ERR_INVALID_ARG;
+  if (need_hi) {
+    if (H < 64 || I < 64 || H % 64 != 0 || I % 64 != 0) return MOE_ERR_INVALID_ARG;
+    if ((int64_t)2 * I > (int64_t)INT32_MAX / 2 || H > 65536) return MOE_ERR_INVALID_ARG;
+  }
+  return MOE_OK;
+}
+
+moe_status resolve_params(const moe_params *p, ActParams &out, int *gating) {
+  if (!p) return MOE_ERR_INVALID_ARG;
+  if (p->gating != MOE_GATING_SOFTMAX_TOPK && p->gating != MOE_GATING_SOFTMAX_ALL)
+    return MOE_ERR_INVALID_ARG;
+  if (p->activation != MOE_ACT_SWIGLU && p->activation != MOE_ACT_SWIGLU_OAI)
+    return MOE_ERR_INVALID_ARG;
+  if (p->w13_layout != MOE_W13_PACKED && p->w13_layout != MOE_W13_INTERLEAVED)
+    return MOE_ERR_INVALID_ARG;
+  if (p->set & ~(MOE_SET_ALPHA | MOE_SET_BETA | MOE_SET_LIMIT)) return MOE_ERR_INVALID_ARG;
+  out.act = p->activation;
+  out.layout = p->w13_layout;
+  if (p->activation == MOE_ACT_SWIGLU_OAI) {
+    // Only the parameters the caller set replace the SwiGLU-OAI defaults.
+    out.alpha = (p->set & MOE_SET_ALPHA) ? p->alpha : 1.702f;
+    out.beta = (p->set & MOE_SET_BETA) ? p->beta : 1.0f;
+    out.limit = (p->set & MOE_SET_LIMIT) ? p->limit : 7.0f;
+    if (!isfinite(out.alpha) || !isfinite(out.beta) || isnan(out.limit) || out.limit < 0.f)
+      return MOE_ERR_INVALID_ARG;
+  } else {
+    // Plain SwiGLU takes no alpha / beta; a clamp limit (SiLU + clamp) is
+    // not implemented.
+    if (p->set & MOE_SET_LIMIT) return MOE_ERR_UNSUPPORTED;
+    out.alpha = 1.f;
+    out.beta = 0.f;
+    out.limit = INFINITY;
+  }
+  if (gating) *gating = p->gating;
+  return MOE_OK;
+}
+
+// The per-slot arrays may be NULL when there are no slots (n = 0).
+moe_status check_meta(const moe_routing_meta *m, int64_t n) {
+  if (!m || !m->col_sum || !m->offs) return MOE_ERR_INVALID_ARG;
+  if (n > 0 && (!m->col_sorted || !m->row_sorted || !m->gate_scal)) return MOE_ERR_INVALID_ARG;
+  if (!aligned(m->col_sum, 4) || !aligned(m->offs, 4) || !aligned(m->col_sorted, 4) ||
+      !aligned(m->row_sorted, 4) || !aligned(m->gate_scal, 2))
+    return MOE_ERR_MISALIGNED;
+  return MOE_OK;
+}
+
+inline moe_status from_cuda(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA; }
+
+template <typename T>
+T *ws_at(void *ws, size_t off) {
+  return reinterpret_cast<T *>(static_cast<char *>(ws) + off);
+}
+
+}  // namespace
+
+extern "C" {
+
+int32_t moe_abi_version(void) { return MOE_ABI_VERSION; }
+
+const char *moe_status_string(moe_status s) {
+  switch (s) {
+    case MOE_OK: return "MOE_OK";
+    case MOE_ERR_INVALID_ARG: return "MOE_ERR_INVALID_ARG: invalid argument";
+    case MOE_ERR_UNSUPPORTED: return "MOE_ERR_UNSUPPORTED: not implemented for these arguments";
+    case MOE_ERR_WORKSPACE_TOO_SMALL: return "MOE_ERR_WORKSPACE_TOO_SMALL: workspace too small";
+    case MOE_ERR_CUDA: return "MOE_ERR_CUDA: a CUDA call or kernel launch failed";
+    case MOE_ERR_TIMEOUT: return "MOE_ERR_TIMEOUT: a bounded device-side wait gave up";
+    case MOE_ERR_MISALIGNED: return "MOE_ERR_MISALIGNED: pointer breaks the alignment rule";
+  }
+  return "unknown moe_status";
+}
+
+size_t moe_workspace_size(int64_t n, int32_t E, int32_t k, int32_t H, int32_t I) {
+  if (check_sizes(n, E, k, H, I, true) != MOE_OK) return 0;
+  return workspace_layout(n, E, k, H, I).total;
+}
+
+moe_status moe_workspace_init(void *workspace, size_t workspace_bytes, moe_stream stream) {
+  if (!workspace || workspace_bytes < kCtrlBytes) return MOE_ERR_INVALID_ARG;
+  if (!aligned(workspace, kAlign)) return MOE_ERR_MISALIGNED;
+  return from_cuda(cudaMemsetAsync(workspace, 0, kCtrlBytes, (cudaStream_t)stream));
+}
+
+moe_status moe_route(const float *logits, int64_t n, int32_t E, int32_t k, int32_t gating,
+                     int32_t *topk_indx, uint16_t *topk_vals, moe_stream stream) {
+  moe_status st = check_sizes(n, E, k, 64, 64, false);
+  if (st != MOE_OK) return st;
+  if (gating != MOE_GATING_SOFTMAX_TOPK && gating != MOE_GATING_SOFTMAX_ALL)
+    return MOE_ERR_INVALID_ARG;
+  if (n == 0) return MOE_OK;
+  if (!logits || !topk_indx || !topk_vals) return MOE_ERR_INVALID_ARG;
+  if (!aligned(logits, 4) || !aligned(topk_indx, 4) || !aligned(topk_vals, 2))
+    return MOE_ERR_MISALIGNED;
+  return from_cuda(launch_route(logits, n, E, k, gating, topk_indx, topk_vals,
+                                (cudaStream_t)stream));
+}
+
+moe_status moe_build_metadata(const int32_t *topk_indx, const uint16_t *topk_vals, int64_t n,
+                              int32_t E, int32_t k, const moe_routing_meta *meta,
+                              void *workspace, size_t workspace_bytes, moe_stream stream) {
+  moe_status st = check_sizes(n, E, k, 64, 64, false);
+  if (st != MOE_OK) return st;
+  if ((st = check_meta(meta, n)) != MOE_OK) return st;
+  if (!workspace) return MOE_ERR_INVALID_ARG;
+  if (!aligned(workspace, kAlign)) return MOE_ERR_MISALIGNED;
+  const WorkspaceLayout L = workspace_layout(n, E, k, 64, 64);
+  if (workspace_bytes < L.topk_indx) return MOE_ERR_WORKSPACE_TOO_SMALL;
+  if (n > 0 && (!topk_indx || !topk_vals)) return MOE_ERR_INVALID_ARG;
+  if (!aligned(topk_indx, 4) || !aligned(topk_vals, 2)) return MOE_ERR_MISALIGNED;
+  return from_cuda(launch_metadata(topk_indx, topk_vals, n, E, k, *meta,
+                                   ws_at<int32_t>(workspace, L.hist),
+                                   ws_at<uint32_t>(workspace, L.ctrl), (cudaStream_t)stream));
+}
+
+moe_status moe_grouped_ffn(const uint16_t *x, const moe_routing_meta *meta, const uint16_t *w13,
+                           const uint16_t *w2, int64_t n, int32_t E, int32_t k, int32_t H,
+                           int32_t I, const moe_params *params, uint16_t *y_flat,
+                           void *workspace, size_t workspace_bytes, moe_stream stream) {
+  moe_status st = check_sizes(n, E, k, H, I, true);
+  if (st != MOE_OK) return st;
+  ActParams act;
+  if ((st = resolve_params(params, act, nullptr)) != MOE_OK) return st;
+  if ((st = check_meta(meta, n)) != MOE_OK) return st;
+  if (n == 0) return MOE_OK;
+  if (!x || !w13 || !w2 || !y_flat || !workspace) return MOE_ERR_INVALID_ARG;
+  if (!aligned(x, 16) || !aligned(w13, 16) || !aligned(w2, 16) || !aligned(y_flat, 16) ||
+      !aligned(workspace, kAlign))
+    return MOE_ERR_MISALIGNED;
+  const WorkspaceLayout L = workspace_layout(n, E, k, H, I);
+  if (workspace_bytes < L.total) return MOE_ERR_WORKSPACE_TOO_SMALL;
+  cudaStream_t s = (cudaStream_t)stream;
+  const int64_t N = n * k;
+  uint16_t *x_sorted = ws_at<uint16_t>(workspace, L.x_sorted);
+  cudaError_t err = launch_gather_rows(x, meta->col_sorted, N, k, H, x_sorted, s);
+  if (err != cudaSuccess) return MOE_ERR_CUDA;
+  return from_cuda(launch_ffn(x_sorted, meta->offs, meta->col_sorted, meta->gate_scal, w13, w2, N,
+                              E, H, I, act, ws_at<uint16_t>(workspace, L.h), y_flat,
+                              ws_at<uint32_t>(workspace, L.ctrl), s));
+}
+
+moe_status moe_combine(const uint16_t *y_flat, int64_t n, int32_t k, int32_t H, uint16_t *out,
+                       moe_stream stream) {
+  if (n < 0 || k < 1 || k > kMaxTopk || H < 64 || H % 64 != 0) return MOE_ERR_INVALID_ARG;
+  if (n == 0) return MOE_OK;
+  if (!y_flat || !out) return MOE_ERR_INVALID_ARG;
+  if (!aligned(y_flat, 16) || !aligned(out, 16)) return MOE_ERR_MISALIGNED;
+  return from_cuda(launch_combine(y_flat, n, k, H, out, (cudaStream_t)stream));
+}
+
+moe_status moe_forward(const uint16_t *x, const float *logits, const uint16_t *w13,
+                       const uint16_t *w2, int64_t n, int32_t E, int32_t k, int32_t H, int32_t I,
+                       const moe_params *params, uint16_t *out, int32_t *topk_indx,
+                       uint16_t *topk_vals, const moe_routing_meta *meta, void *workspace,
+                       size_t workspace_bytes, moe_stream stream) {
+  moe_status st = check_sizes(n, E, k, H, I, true);
+  if (st != MOE_OK) return st;
+  ActParams act;
+  int gating = 0;
+  if ((st = resolve_params(params, act, &gating)) != MOE_OK) return st;
+  if (meta && (st = check_meta(meta, n)) != MOE_OK) return st;
+  if ((topk_indx == nullptr) != (topk_vals == nullptr)) return MOE_ERR_INVALID_ARG;
+  if (n == 0) return MOE_OK;
+  if (!x || !logits || !w13 || !w2 || !out || !workspace) return MOE_ERR_INVALID_ARG;
+  if (!aligned(x, 16) || !aligned(w13, 16) || !aligned(w2, 16) || !aligned(out, 16) ||
+      !aligned(logits, 4) || !aligned(workspace, kAlign) || !aligned(topk_indx, 4) ||
+      !aligned(topk_vals, 2))
+    return MOE_ERR_MISALIGNED;
+  const WorkspaceLayout L = workspace_layout(n, E, k, H, I);
+  if (workspace_bytes < L.total) return MOE_ERR_WORKSPACE_TOO_SMALL;
+
+  cudaStream_t s = (cudaStream_t)stream;
+  int32_t *indx = topk_indx ? topk_indx : ws_at<int32_t>(workspace, L.topk_indx);
+  uint16_t *vals = topk_vals ? topk_vals : ws_at<uint16_t>(workspace, L.topk_vals);
+  moe_routing_meta m;
+  if (meta) {
+    m = *meta;
+  } else {
+    m.col_sum = ws_at<int32_t>(workspace, L.col_sum);
+    m.offs = ws_at<int32_t>(workspace, L.offs);
+    m.col_sorted = ws_at<int32_t>(workspace, L.col_sorted);
+    m.row_sorted = ws_at<int32_t>(workspace, L.row_sorted);
+    m.gate_scal = ws_at<uint16_t>(workspace, L.gate_scal);
+  }
+  uint32_t *ctrl = ws_at<uint32_t>(workspace, L.ctrl);
+  const int64_t N = n * k;
+  // k = 1: slot f is token t, so the w2 epilogue writes the output directly.
+  uint16_t *y_flat = k == 1 ? out : ws_at<uint16_t>(workspace, L.y_flat);
+
+  if (launch_route(logits, n, E, k, gating, indx, vals, s) != cudaSuccess) return MOE_ERR_CUDA;
+  if (launch_metadata(indx, vals, n, E, k, m, ws_at<int32_t>(workspace, L.hist), ctrl, s) !=
+      cudaSuccess)
+    return MOE_ERR_CUDA;
+  uint16_t *x_sorted = ws_at<uint16_t>(workspace, L.x_sorted);
+  if (launch_gather_rows(x, m.col_sorted, N, k, H, x_sorted, s) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  if (launch_ffn(x_sorted, m.offs, m.col_sorted, m.gate_scal, w13, w2, N, E, H, I, act,
+                 ws_at<uint16_t>(workspace, L.h), y_flat, ctrl, s) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  if (k > 1 && launch_combine(y_flat, n, k, H, out, s) != cudaSuccess) return MOE_ERR_CUDA;
+  return MOE_OK;
+}
+
+moe_status moe_read_status(void *workspace, size_t workspace_bytes, int32_t reset,
+                           moe_stream stream) {
+  if (!workspace || workspace_bytes < kCtrlBytes) return MOE_ERR_INVALID_ARG;
+  cudaStream_t s = (cudaStream_t)stream;
+  uint32_t word = 0;
+  if (cudaStreamSynchronize(s) != cudaSuccess) return MOE_ERR_CUDA;
+  if (cudaMemcpy(&word, workspace, sizeof word, cudaMemcpyDeviceToHost) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  if (reset) {
+    if (cudaMemsetAsync(workspace, 0, kCtrlBytes, s) != cudaSuccess) return MOE_ERR_CUDA;
+    if (cudaStreamSynchronize(s) != cudaSuccess) return MOE_ERR_CUDA;
+  }
+  return (moe_status)word;
+}
+
+moe_status moe_selftest_wait_timeout(void *workspace, size_t workspace_bytes,
+                                     uint64_t timeout_ns, moe_stream stream) {
+  if (!workspace || workspace_bytes < kCtrlBytes) return MOE_ERR_INVALID_ARG;
+  if (timeout_ns == 0 || timeout_ns > kWaitTimeoutNs) return MOE_ERR_INVALID_ARG;
+  return from_cuda(launch_wait_selftest(ws_at<uint32_t>(workspace, 0), timeout_ns,
+                                        (cudaStream_t)stream));
+}
+
+}  // extern "C"

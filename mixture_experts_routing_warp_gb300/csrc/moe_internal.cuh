@@ -1,0 +1,170 @@
+// moe_internal.cuh -- shared pieces of the CUDA path: workspace layout,
+// bounded device-side waits, bf16 helpers, kernel launcher declarations.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/moe.h"
+
+namespace moe {
+
+// ---------------------------------------------------------------- limits --
+constexpr int kMaxExperts = 256;
+constexpr int kMaxTopk = 8;
+constexpr int kMetaMaxCtas = 1024;       // cap on the metadata kernel's grid
+constexpr size_t kCtrlBytes = 4096;      // control block at the start of the workspace
+constexpr size_t kAlign = 256;
+
+// Control block words (uint32 index into the control block).
+constexpr int kCtrlStatus = 0;           // sticky moe_status from device-side waits
+constexpr int kCtrlBarArrive = 32;       // grid barrier: arrivals of the current round
+constexpr int kCtrlBarGen = 64;          // grid barrier: generation, bumped per round
+
+// Default limit of a device-side wait (ns). Legitimate waits last microseconds.
+constexpr unsigned long long kWaitTimeoutNs = 1000000000ull;
+
+// ------------------------------------------------------ workspace layout --
+struct WorkspaceLayout {
+  size_t ctrl, hist, topk_indx, topk_vals, col_sum, offs, col_sorted, row_sorted, gate_scal;
+  size_t x_sorted, h, y_flat, total;
+};
+
+inline size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+
+// Regions: control block; per-CTA histograms of the metadata kernel; the
+// routing result and metadata used when moe_forward's caller keeps them
+// internal; the expert-sorted activations X_sorted [N, H]; the intermediate
+// h [N, I]; the per-slot outputs y_flat [N, H] (k > 1 only). N = n * k.
+inline WorkspaceLayout workspace_layout(int64_t n, int E, int k, int H, int I) {
+  WorkspaceLayout L{};
+  const size_t N = (size_t)n * (size_t)k;
+  size_t o = 0;
+  auto take = [&](size_t bytes) { size_t at = o; o = align_up(o + bytes, kAlign); return at; };
+  L.ctrl = take(kCtrlBytes);
+  L.hist = take((size_t)kMetaMaxCtas * (size_t)E * 4);
+  L.topk_indx = take(N * 4);
+  L.topk_vals = take(N * 2);
+  L.col_sum = take((size_t)E * 4);
+  L.offs = take((size_t)(E + 1) * 4);
+  L.col_sorted = take(N * 4);
+  L.row_sorted = take(N * 4);
+  L.gate_scal = take(N * 2);
+  L.x_sorted = take(N * (size_t)H * 2);
+  L.h = take(N * (size_t)I * 2);
+  L.y_flat = take(k > 1 ? N * (size_t)H * 2 : 0);
+  L.total = o;
+  return L;
+}
+
+// ------------------------------------------------------- device helpers --
+__device__ __forceinline__ unsigned long long global_timer_ns() {
+  unsigned long long t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+__device__ __forceinline__ uint32_t ld_acquire_gpu(const uint32_t *p) {
+  uint32_t v;
+  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+
+__device__ __forceinline__ void st_release_gpu(uint32_t *p, uint32_t v) {
+  asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
+__device__ __forceinline__ void record_status(uint32_t *ctrl, moe_status s) {
+  atomicCAS(ctrl + kCtrlStatus, (uint32_t)MOE_OK, (uint32_t)s);
+}
+
+// Grid-wide barrier for a cooperative launch, bounded by `timeout_ns`.
+// Thread 0 of each CTA reads the generation, arrives; the last arrival
+// resets the arrival count and bumps the generation; the others wait for
+// the bump. Returns false (and records MOE_ERR_TIMEOUT) when the wait
+// gives up; the caller must then return without touching shared outputs.
+__device__ __forceinline__ bool grid_barrier(uint32_t *ctrl, unsigned long long timeout_ns) {
+  __shared__ int s_ok;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    uint32_t *arrive = ctrl + kCtrlBarArrive;
+    uint32_t *gen = ctrl + kCtrlBarGen;
+    const uint32_t my_gen = ld_acquire_gpu(gen);
+    __threadfence();
+    const uint32_t ticket = atomicAdd(arrive, 1u);
+    int ok = 1;
+    if (ticket == gridDim.x - 1) {
+      atomicExch(arrive, 0u);
+      __threadfence();
+      st_release_gpu(gen, my_gen + 1);
+    } else {
+      const unsigned long long t0 = global_timer_ns();
+      while (ld_acquire_gpu(gen) == my_gen) {
+        if (global_timer_ns() - t0 > timeout_ns) {
+          ok = 0;
+          record_status(ctrl, MOE_ERR_TIMEOUT);
+          break;
+        }
+        __nanosleep(64);
+      }
+    }
+    __threadfence();
+    s_ok = ok;
+  }
+  __syncthreads();
+  return s_ok != 0;
+}
+
+__device__ __forceinline__ float bf16_bits_to_float(uint16_t b) {
+  return __uint_as_float(((uint32_t)b) << 16);
+}
+
+__device__ __forceinline__ uint16_t float_to_bf16_bits(float f) {
+  __nv_bfloat16 h = __float2bfloat16_rn(f);
+  return *reinterpret_cast<uint16_t *>(&h);
+}
+
+// Resolved activation parameters handed to the FFN kernels.
+struct ActParams {
+  int act;      // moe_activation
+  int layout;   // moe_w13_layout
+  float alpha, beta, limit;
+};
+
+// SwiGLU: (g * sigmoid(g)) * u.  SwiGLU-OAI: g = min(g, limit),
+// u = clamp(u, -limit, limit), (g * sigmoid(alpha g)) * (u + beta).
+__device__ __forceinline__ float activate(float g, float u, const ActParams &p) {
+  if (p.act == MOE_ACT_SWIGLU_OAI) {
+    g = fminf(g, p.limit);
+    u = fminf(fmaxf(u, -p.limit), p.limit);
+    return (g * (1.0f / (1.0f + expf(-p.alpha * g)))) * (u + p.beta);
+  }
+  return (g * (1.0f / (1.0f + expf(-g)))) * u;
+}
+
+// ----------------------------------------------------- kernel launchers --
+// All return the launch's cudaError_t (cudaGetLastError after the launch).
+int device_sm_count();
+
+cudaError_t launch_route(const float *logits, int64_t n, int E, int k, int gating,
+                         int32_t *topk_indx, uint16_t *topk_vals, cudaStream_t s);
+
+cudaError_t launch_metadata(const int32_t *topk_indx, const uint16_t *topk_vals, int64_t n, int E,
+                            int k, const moe_routing_meta &meta, int32_t *ws_hist,
+                            uint32_t *ctrl, cudaStream_t s);
+
+cudaError_t launch_gather_rows(const uint16_t *x, const int32_t *col_sorted, int64_t N, int k,
+                               int H, uint16_t *x_sorted, cudaStream_t s);
+
+cudaError_t launch_combine(const uint16_t *y_flat, int64_t n, int k, int H, uint16_t *out,
+                           cudaStream_t s);
+
+cudaError_t launch_ffn(const uint16_t *x_sorted, const int32_t *offs, const int32_t *col_sorted,
+                       const uint16_t *gate_scal, const uint16_t *w13, const uint16_t *w2,
+                       int64_t N, int E, int H, int I, const ActParams &act, uint16_t *h_buf,
+                       uint16_t *y_flat, uint32_t *ctrl, cudaStream_t s);
+
+cudaError_t launch_wait_selftest(uint32_t *ctrl, unsigned long long timeout_ns, cudaStream_t s);
+
+}  // namespace moe

@@ -27,6 +27,8 @@ Workload shapes follow the pages:
 from __future__ import annotations
 
 import dataclasses
+import os
+from concurrent.futures import ThreadPoolExecutor
 from typing import Optional
 
 import numpy as np
@@ -144,18 +146,30 @@ def expert_w2(case: LayerCase, e: int) -> np.ndarray:
     return normal_bf16((case.H, case.I), case.w_std, case.seed, _TAG_W2, e, case.I, case.H)
 
 
-def all_w13(case: LayerCase) -> np.ndarray:
-    out = np.empty((case.E, 2 * case.I, case.H), dtype=np.uint16)
-    for e in range(case.E):
-        out[e] = expert_w13(case, e)
+def _per_expert(case: LayerCase, shape, fn) -> np.ndarray:
+    """Stack fn(case, e) over experts; threads over experts (each expert has
+    its own seed, so the result does not depend on the thread count)."""
+    out = np.empty((case.E, *shape), dtype=np.uint16)
+
+    def one(e):
+        out[e] = fn(case, e)
+
+    workers = max(1, min(case.E, os.cpu_count() or 1))
+    if workers == 1 or out.nbytes < (8 << 20):
+        for e in range(case.E):
+            one(e)
+    else:
+        with ThreadPoolExecutor(workers) as ex:
+            list(ex.map(one, range(case.E)))
     return out
+
+
+def all_w13(case: LayerCase) -> np.ndarray:
+    return _per_expert(case, (2 * case.I, case.H), expert_w13)
 
 
 def all_w2(case: LayerCase) -> np.ndarray:
-    out = np.empty((case.E, case.H, case.I), dtype=np.uint16)
-    for e in range(case.E):
-        out[e] = expert_w2(case, e)
-    return out
+    return _per_expert(case, (case.H, case.I), expert_w2)
 
 
 def layer_logits(case: LayerCase, x: Optional[np.ndarray] = None) -> np.ndarray:

@@ -1,0 +1,142 @@
+"""The C ABI without a GPU: the library loads, exports every function that
+include/moe.h declares, and rejects bad arguments on the host before any
+launch (these calls never reach the CUDA runtime)."""
+import ctypes
+import os
+import re
+import subprocess
+
+import pytest
+
+import mixture_experts_routing_warp_gb300 as moe
+from mixture_experts_routing_warp_gb300 import build as cuda_build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "moe.h")
+
+
+@pytest.fixture(scope="module")
+def L():
+    cuda_build.build()
+    return moe.lib()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(moe_[a-z_0-9]+)\s*\(", text)))
+
+
+def test_header_compiles_as_c99(tmp_path):
+    src = tmp_path / "t.c"
+    src.write_text('#include "moe.h"\nint main(void) { moe_params p = {0}; (void)p; '
+                   'return moe_abi_version() == MOE_ABI_VERSION ? 0 : 1; }\n')
+    subprocess.run(["gcc", "-std=c99", "-Wall", "-Wextra", "-Werror", "-pedantic",
+                    f"-I{os.path.join(ROOT, 'include')}", "-c", str(src), "-o",
+                    str(tmp_path / "t.o")], check=True)
+
+
+def test_exports_every_declared_function(L):
+    names = declared_functions()
+    assert len(names) >= 10, names
+    for name in names:
+        assert hasattr(L, name), f"{name} declared in moe.h but not exported"
+    assert set(names) == set(moe._binding.SIGNATURES), "binding and header disagree"
+
+
+def test_abi_and_status_strings(L):
+    assert L.moe_abi_version() == 1
+    for code in range(7):
+        s = moe.status_string(code)
+        assert s.startswith("MOE_"), s
+    assert moe.status_string(99) == "unknown moe_status"
+
+
+def test_workspace_size(L):
+    assert moe.workspace_size(33, 8, 2, 64, 128) > 0
+    for bad in [(-1, 8, 2, 64, 128), (33, 0, 2, 64, 128), (33, 300, 2, 64, 128),
+                (33, 8, 9, 64, 128), (33, 4, 5, 64, 128), (33, 8, 2, 65, 128),
+                (33, 8, 2, 64, 100), (1 << 30, 8, 4, 64, 64)]:
+        assert moe.workspace_size(*bad) == 0, bad
+    a = moe.workspace_size(1000, 8, 1, 512, 1408)
+    b = moe.workspace_size(1000, 8, 2, 512, 1408)
+    assert b > a   # per-slot outputs only when k > 1
+    assert moe.workspace_size(0, 8, 2, 64, 128) > 0
+
+
+def _p(v):
+    return ctypes.c_void_p(v)
+
+
+def test_route_rejects_before_launch(L):
+    good = _p(1 << 20)
+    # invalid sizes / enums
+    assert L.moe_route(good, 4, 0, 1, 0, good, good, None) == 1
+    assert L.moe_route(good, 4, 8, 9, 0, good, good, None) == 1
+    assert L.moe_route(good, 4, 4, 5, 0, good, good, None) == 1
+    assert L.moe_route(good, -1, 8, 2, 0, good, good, None) == 1
+    assert L.moe_route(good, 4, 8, 2, 7, good, good, None) == 1
+    # null and misaligned pointers
+    assert L.moe_route(None, 4, 8, 2, 0, good, good, None) == 1
+    assert L.moe_route(_p((1 << 20) + 2), 4, 8, 2, 0, good, good, None) == 6
+    # n = 0 is a no-op
+    assert L.moe_route(None, 0, 8, 2, 0, None, None, None) == 0
+
+
+def test_ffn_and_forward_parameter_rules(L):
+    good = _p(1 << 20)
+    ws = _p(1 << 20)
+    meta = moe.RoutingMeta(1 << 20, 1 << 20, 1 << 20, 1 << 20, 1 << 20)
+    big = moe.workspace_size(8, 4, 2, 64, 64)
+
+    def ffn(params, **kw):
+        a = dict(n=8, E=4, k=2, H=64, I=64, ws_bytes=big)
+        a.update(kw)
+        return L.moe_grouped_ffn(good, ctypes.byref(meta), good, good, a["n"], a["E"], a["k"],
+                                 a["H"], a["I"], ctypes.byref(params), good, ws, a["ws_bytes"],
+                                 None)
+
+    # a clamp limit on plain SwiGLU is not implemented
+    assert ffn(moe.make_params(act="swiglu", limit=7.0)) == 2
+    # alpha / beta are not parameters of plain SwiGLU: ignored, and n = 0 is a no-op
+    assert ffn(moe.make_params(act="swiglu", alpha=2.0), n=0) == 0
+    assert ffn(moe.make_params(act="swiglu_oai", limit=-1.0)) == 1
+    assert ffn(moe.make_params(act="swiglu_oai", alpha=float("nan"))) == 1
+    bad = moe.make_params()
+    bad.w13_layout = 5
+    assert ffn(bad) == 1
+    bad = moe.make_params()
+    bad.set = 8
+    assert ffn(bad) == 1
+    assert ffn(moe.make_params(), ws_bytes=big - 1) == 3
+    assert ffn(moe.make_params(), H=96) == 1
+    assert L.moe_grouped_ffn(_p((1 << 20) + 8), ctypes.byref(meta), good, good, 8, 4, 2, 64, 64,
+                             ctypes.byref(moe.make_params()), good, ws, big, None) == 6
+    assert L.moe_grouped_ffn(good, None, good, good, 8, 4, 2, 64, 64,
+                             ctypes.byref(moe.make_params()), good, ws, big, None) == 1
+    # forward: topk outputs come as a pair
+    assert L.moe_forward(good, good, good, good, 8, 4, 2, 64, 64,
+                         ctypes.byref(moe.make_params()), good, good, None, None, ws, big,
+                         None) == 1
+    assert L.moe_combine(good, 8, 2, 100, good, None) == 1
+    assert L.moe_combine(None, 0, 2, 64, None, None) == 0
+    assert L.moe_read_status(None, 0, 0, None) == 1
+    assert L.moe_selftest_wait_timeout(ws, 4096, 0, None) == 1
+    assert L.moe_selftest_wait_timeout(ws, 4096, 10 ** 10, None) == 1
+
+
+def test_binding_fails_loudly_without_library(monkeypatch, tmp_path):
+    monkeypatch.setattr(moe._binding, "_LIB", None)
+    monkeypatch.setattr(moe._binding, "library_path", lambda: str(tmp_path / "missing.so"))
+    with pytest.raises(RuntimeError, match="missing"):
+        moe.lib()
+
+
+def test_product_does_not_import_the_oracle():
+    pkg = os.path.join(ROOT, "mixture_experts_routing_warp_gb300")
+    for dirpath, _, files in os.walk(pkg):
+        for f in files:
+            if f.endswith((".py", ".cu", ".cuh", ".h")):
+                text = open(os.path.join(dirpath, f)).read()
+                assert "import oracle" not in text and "from oracle" not in text, f
+                assert "moe_oracle" not in text, f

@@ -1,0 +1,185 @@
+"""The whole MoE layer on the GPU (through the C ABI) against the CPU oracle.
+
+Routing and metadata must match bit for bit; the layer output within
+|gpu - ref| <= 3e-2 + 2e-2 |ref| elementwise and cosine > 0.99.
+Workloads: the tiny layer, the MiniMind layer (E = 4, 8, 16, top-1, softmax
+over all experts), the GPT-OSS layer (decode n = 1, 8, 64 checked in full;
+prefill n = 2048, 8192 on sampled tokens), the skewed 128-expert prefill
+(n = 16384, sampled tokens), and variants over layouts, activations,
+activation parameters and ragged tile tails."""
+import numpy as np
+import pytest
+import torch
+
+import mixture_experts_routing_warp_gb300 as moe
+import oracle
+from mixture_experts_routing_warp_gb300 import inputs as I
+
+from helpers import assert_layer_close, dev, dev_bf16, host_bits
+
+pytestmark = pytest.mark.gpu
+
+
+class Layer:
+    """Host inputs of a case plus their device copies and one GPU forward."""
+
+    def __init__(self, case: I.LayerCase, act_kw=None):
+        self.case = case
+        self.act_kw = act_kw or {}
+        self.h = I.layer_inputs(case)
+        self.x = dev_bf16(self.h["x"])
+        self.logits = dev(self.h["logits"])
+        self.w13 = dev_bf16(self.h["w13"])
+        self.w2 = dev_bf16(self.h["w2"])
+        self.params = moe.make_params(case.gating, case.act, case.layout, **self.act_kw)
+
+    def forward(self):
+        c = self.case
+        ws = moe.workspace(c.n, c.E, c.k, c.H, c.I)
+        indx = torch.empty((c.n, c.k), dtype=torch.int32, device="cuda")
+        vals = torch.empty((c.n, c.k), dtype=torch.bfloat16, device="cuda")
+        meta = moe.empty_meta(c.n * c.k, c.E, "cuda")
+        out = moe.forward(self.x, self.logits, self.w13, self.w2, c.k, self.params, ws,
+                          topk=(indx, vals), meta=meta)
+        torch.cuda.synchronize()
+        assert moe.read_status(ws) == 0
+        return out, indx, vals, meta
+
+    def oracle_kw(self):
+        return dict(act=self.case.act, layout=self.case.layout, **self.act_kw)
+
+
+def _check_routing(L, indx, vals, meta):
+    ref_i, ref_v = oracle.route(L.h["logits"], L.case.k, L.case.gating)
+    np.testing.assert_array_equal(indx.cpu().numpy(), ref_i)
+    d = np.abs(host_bits(vals).astype(np.int32) - ref_v.astype(np.int32))
+    assert d.max(initial=0) <= 1
+    ref_m = oracle.metadata(indx.cpu().numpy(), host_bits(vals), L.case.E)
+    for key in ("col_sum", "offs", "col_sorted", "row_sorted"):
+        np.testing.assert_array_equal(meta[key].cpu().numpy(), ref_m[key], err_msg=key)
+    np.testing.assert_array_equal(host_bits(meta["gate_scal"]), ref_m["gate_scal"])
+    return ref_m
+
+
+def _check_full(L):
+    out, indx, vals, meta = L.forward()
+    _check_routing(L, indx, vals, meta)
+    # the layer output is compared on the GPU's own routing (same bf16 gates)
+    ref = oracle.ffn(L.h["x"], indx.cpu().numpy(), host_bits(vals), L.h["w13"], L.h["w2"],
+                     **L.oracle_kw())
+    return assert_layer_close(host_bits(out), ref, L.case.name)
+
+
+def _sample_tokens(indx: np.ndarray, col_sum: np.ndarray, count: int = 48) -> np.ndarray:
+    n = indx.shape[0]
+    rng = np.random.default_rng(123)
+    pick = {0, n - 1}
+    rare = np.nonzero((col_sum > 0) & (col_sum <= 4))[0]
+    for e in rare[:16]:  # tokens that reach the rarest experts (ragged tails)
+        pick.add(int(np.nonzero((indx == e).any(axis=1))[0][0]))
+    while len(pick) < min(n, count):
+        pick.add(int(rng.integers(0, n)))
+    return np.array(sorted(pick), dtype=np.int64)
+
+
+def _check_sampled(L):
+    out, indx, vals, meta = L.forward()
+    _check_routing(L, indx, vals, meta)
+    ind = indx.cpu().numpy()
+    toks = _sample_tokens(ind, meta["col_sum"].cpu().numpy())
+    ref = oracle.ffn(L.h["x"], ind, host_bits(vals), L.h["w13"], L.h["w2"], tokens=toks,
+                     **L.oracle_kw())
+    got = host_bits(out)[toks]
+    return assert_layer_close(got, ref, L.case.name)
+
+
+def test_tiny_layer_and_golden():
+    L = Layer(I.TINY)
+    _check_full(L)
+    import importlib.util
+    import os
+    path = os.path.join(os.path.dirname(__file__), "golden", "make_golden.py")
+    spec = importlib.util.spec_from_file_location("make_golden", path)
+    mg = importlib.util.module_from_spec(spec)
+    spec.loader.exec_module(mg)
+    g = mg.load()
+    out, indx, _, meta = L.forward()
+    np.testing.assert_array_equal(indx.cpu().numpy(), g["topk_indx"])
+    for key in ("col_sum", "offs", "col_sorted", "row_sorted"):
+        np.testing.assert_array_equal(meta[key].cpu().numpy(), g[key])
+    assert_layer_close(host_bits(out), g["out"], "tiny vs golden")
+
+
+@pytest.mark.parametrize("case", [I.MINIMIND_E4, I.MINIMIND_E8, I.MINIMIND_E16],
+                         ids=lambda c: c.name)
+def test_minimind_layer(case):
+    _check_full(Layer(case))
+
+
+@pytest.mark.parametrize("n", I.GPTOSS_DECODE_N)
+def test_gptoss_decode(n):
+    _check_full(Layer(I.GPTOSS.with_n(n)))
+
+
+@pytest.mark.parametrize("n", I.GPTOSS_PREFILL_N)
+def test_gptoss_prefill_sampled(n):
+    _check_sampled(Layer(I.GPTOSS.with_n(n)))
+
+
+def test_skewed_prefill_sampled():
+    L = Layer(I.SKEWED)
+    stats = _check_sampled(L)
+    assert stats["cos"] > 0.99
+
+
+VARIANTS = [
+    # name, H, E, k, I, act, layout, act_kw
+    ("packed_swiglu", 192, 8, 3, 320, "swiglu", "packed", {}),
+    ("interleaved_swiglu", 192, 8, 3, 320, "swiglu", "interleaved", {}),
+    ("packed_oai", 128, 6, 2, 192, "swiglu_oai", "packed", {}),
+    ("interleaved_oai_params", 256, 5, 2, 128, "swiglu_oai", "interleaved",
+     {"alpha": 1.5, "beta": 0.5, "limit": 3.0}),
+    ("oai_limit_only", 128, 4, 4, 256, "swiglu_oai", "interleaved", {"limit": 2.0}),
+    ("k8_e16", 64, 16, 8, 64, "swiglu", "packed", {}),
+]
+
+
+@pytest.mark.parametrize("name,H,E,k,Idim,act,layout,act_kw", VARIANTS,
+                         ids=[v[0] for v in VARIANTS])
+@pytest.mark.parametrize("n", [1, 37, 300])
+def test_variants(name, H, E, k, Idim, act, layout, act_kw, n):
+    case = I.LayerCase(f"{name}@n{n}", n=n, H=H, E=E, k=k, I=Idim, act=act, layout=layout,
+                       seed=n, w_std=0.1)
+    _check_full(Layer(case, act_kw))
+
+
+def test_stages_compose_to_forward():
+    """route -> build_metadata -> grouped_ffn -> combine equals moe_forward bit for bit,
+    and the per-slot outputs match the oracle's gate-weighted expert outputs."""
+    case = I.LayerCase("stages", n=200, H=128, E=8, k=3, I=192, act="swiglu_oai",
+                       layout="interleaved", w_std=0.1)
+    L = Layer(case)
+    out_fwd = L.forward()[0]
+    ws = moe.workspace(case.n, case.E, case.k, case.H, case.I)
+    indx, vals = moe.route(L.logits, case.k, case.gating)
+    meta = moe.build_metadata(indx, vals, case.E, ws)
+    y_flat = moe.grouped_ffn(L.x, meta, L.w13, L.w2, case.k, ws, L.params)
+    out = moe.combine(y_flat, case.n, case.k)
+    torch.cuda.synchronize()
+    assert torch.equal(out.view(torch.int16), out_fwd.view(torch.int16))
+    ref_out, y_slot, _ = oracle.ffn(L.h["x"], indx.cpu().numpy(), host_bits(vals), L.h["w13"],
+                                    L.h["w2"], want_slots=True, **L.oracle_kw())
+    ref_y = oracle.f64_to_bf16(y_slot.reshape(case.n * case.k, case.H))
+    assert_layer_close(host_bits(y_flat), ref_y, "y_flat")
+    assert_layer_close(host_bits(out), ref_out, "out")
+
+
+def test_empty_batch_is_a_noop():
+    c = I.TINY
+    L = Layer(c)
+    ws = moe.workspace(0, c.E, c.k, c.H, c.I)
+    x = torch.empty((0, c.H), dtype=torch.bfloat16, device="cuda")
+    logits = torch.empty((0, c.E), dtype=torch.float32, device="cuda")
+    out = moe.forward(x, logits, L.w13, L.w2, c.k, L.params, ws)
+    torch.cuda.synchronize()
+    assert out.shape == (0, c.H)
