@@ -1,0 +1,539 @@
+#!/usr/bin/env python3
+"""MoE layer forward benchmark on GB300 (prints ONE JSON line on rank 0).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                    [--workload NAME] [--no-extras]
+
+A step is one whole MoE layer forward (route -> metadata -> dispatch
+gather -> w13 GEMM + activation -> w2 GEMM + gate scale + scatter ->
+combine) through the C ABI, on synthetic seeded inputs already resident in
+HBM. Default workload: the GPT-OSS-shaped prefill (8192 tokens, hidden
+2880, 32 experts, top-4, intermediate 2880, SwiGLU-OAI, interleaved w13).
+
+value        tokens/s over all ranks (each rank runs its own batch: weak scaling)
+roofline     the stage with the largest device time, algorithmic FLOPs or
+             bytes per launch / its mean CUDA-event duration, against the
+             measured peak in MEASURED_PEAKS.json
+e2e          the same metric with host (pinned) buffers: x and logits copied
+             host->device and the output device->host inside the timed region
+cpu_baseline the CPU oracle timed on this host's cores on a bounded sample
+also         routing + metadata us/call at 16384 tokens x 128 experts (top-4)
+             and the MiniMind-shaped layer, each with its own roofline figure
+
+--impl reference times the CPU oracle (the reference for this method) on
+the same workload and prints its line with "impl": "reference".
+"""
+from __future__ import annotations
+
+import argparse
+import ctypes
+import dataclasses
+import hashlib
+import json
+import os
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+os.environ.setdefault("OMP_NUM_THREADS", str(os.cpu_count() or 1))
+
+import numpy as np  # noqa: E402
+
+from mixture_experts_routing_warp_gb300 import inputs as I  # noqa: E402
+
+METRIC = "MoE-layer tokens/s and routing-metadata µs/call on 1 GB300; % of roofline"
+WORKLOADS = {
+    "gptoss_prefill_n8192": I.GPTOSS.with_n(8192),
+    "gptoss_prefill_n2048": I.GPTOSS.with_n(2048),
+    "minimind_e4": I.MINIMIND_E4,
+    "minimind_e8": I.MINIMIND_E8,
+    "minimind_e16": I.MINIMIND_E16,
+    "skewed_n16384": I.SKEWED,
+}
+DEFAULT_WORKLOAD = "gptoss_prefill_n8192"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+def log(*a):
+    print(*a, file=sys.stderr, flush=True)
+
+
+# --------------------------------------------------------------- setup --
+def parse_args():
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=50)
+    p.add_argument("--warmup", type=int, default=5)
+    p.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    p.add_argument("--workload", choices=sorted(WORKLOADS), default=DEFAULT_WORKLOAD)
+    p.add_argument("--no-extras", action="store_true", help="skip the routing / MiniMind extras")
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    a = p.parse_args()
+    a.warmup = max(a.warmup, 3)
+    return a
+
+
+def dist_setup(args):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    pg = None
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if args.impl == "ours" else "gloo"
+        dist.init_process_group(backend=backend)
+        pg = dist
+    return rank, world, local, pg
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return {k: float(d[k]) for k in ("hbm_gbs", "bf16_tflops", "bf16_tflops_sustained")}, \
+            "measured"
+    except (OSError, KeyError, ValueError):
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clocks / throttle reasons sampled every 50 ms in the background."""
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.samples = []
+        self.proc = None
+        self.thread = None
+        self.window = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.QUERY}", "--format=csv,noheader,nounits",
+                 "-lms", "50", "-i", str(self.gpu)], stdout=subprocess.PIPE,
+                stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) >= 9:
+                self.samples.append((time.time(), parts))
+
+    def mark(self, t0, t1):
+        self.window = (t0, t1)
+
+    def stop(self):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+        if self.thread is not None:
+            self.thread.join(timeout=5)
+
+    def summary(self):
+        rows = self.samples
+        if self.window:
+            inside = [r for t, r in rows if self.window[0] <= t <= self.window[1]]
+            rows_used = inside if inside else [r for _, r in rows]
+        else:
+            rows_used = [r for _, r in rows]
+        if not rows_used:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+
+        def num(x):
+            try:
+                return float(x)
+            except ValueError:
+                return None
+
+        sm = [num(r[1]) for r in rows_used if num(r[1]) is not None]
+        smax = [num(r[2]) for r in rows_used if num(r[2]) is not None]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows_used for i in range(4)
+                          if r[5 + i].lower().startswith("active")})
+        return {"sm_mhz": float(np.median(sm)) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None, "reasons": reasons,
+                "samples": len(rows_used)}
+
+
+# ---------------------------------------------------------- algorithmic --
+def stage_work(c: I.LayerCase) -> dict:
+    """Algorithmic FLOPs / bytes of one launch of each stage kernel."""
+    n, E, k, H, Idim = c.n, c.E, c.k, c.H, c.I
+    N = n * k
+    return {
+        "route": ("hbm", n * E * 4 + N * (4 + 2)),
+        "metadata": ("hbm", N * (4 + 2) + N * (4 + 4 + 2) + (2 * E + 1) * 4),
+        "gather": ("hbm", n * H * 2 + N * H * 2),
+        "ffn1": ("tensor", 2.0 * N * H * 2 * Idim),
+        "ffn2": ("tensor", 2.0 * N * Idim * H),
+        "combine": ("hbm", (N * H * 2 + n * H * 2) if k > 1 else 0),
+    }
+
+
+def roofline_entry(bound, work, seconds, pk, source):
+    if bound == "tensor":
+        achieved = work / seconds / 1e12
+        return {"bound": "tensor", "achieved": round(achieved, 2),
+                "peak": pk["bf16_tflops"], "unit": "TFLOP/s",
+                "frac": round(achieved / pk["bf16_tflops"], 4),
+                "peak_source": f"bf16_tflops ({source}, burst)"}
+    achieved = work / seconds / 1e9
+    return {"bound": "hbm", "achieved": round(achieved, 1), "peak": pk["hbm_gbs"], "unit": "GB/s",
+            "frac": round(achieved / pk["hbm_gbs"], 4), "peak_source": f"hbm_gbs ({source})"}
+
+
+def kernel_source_digest() -> str:
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "mixture_experts_routing_warp_gb300", "csrc")
+    for name in sorted(os.listdir(csrc)):
+        if name.endswith((".cu", ".cuh")):
+            with open(os.path.join(csrc, name), "rb") as f:
+                h.update(name.encode() + f.read())
+    return h.hexdigest()[:16]
+
+
+def ncu_traffic(stage: str, workload: str):
+    """Per-launch DRAM bytes from the committed ncu summary, if it was taken
+    on the current kernel sources (else None)."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+    except (OSError, ValueError):
+        return None
+    ent = d.get(f"{workload}:{stage}")
+    if not ent or ent.get("source_digest") != kernel_source_digest():
+        return None
+    return ent.get("dram_bytes_per_launch")
+
+
+# ------------------------------------------------------------ GPU arm --
+class DeviceCase:
+    """A workload's inputs on the device, with R rotated (x, logits) sets and
+    W rotated weight sets so that the inputs of consecutive steps exceed L2."""
+
+    def __init__(self, c: I.LayerCase, device, l2_bytes: int, rank: int = 0):
+        import torch
+        import mixture_experts_routing_warp_gb300 as moe
+
+        def bf16(a):
+            return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(
+                torch.bfloat16).to(device)
+
+        self.c = c
+        weights_bytes = 2 * c.E * 3 * c.H * c.I
+        act_bytes = c.n * c.H * 2 + c.n * c.E * 4
+        self.n_wsets = max(1, min(16, -(-2 * l2_bytes // max(weights_bytes, 1))))
+        self.n_xsets = max(2, min(8, -(-2 * l2_bytes // max(act_bytes, 1))))
+        self.x, self.logits, self.host_x, self.host_logits = [], [], [], []
+        for r in range(self.n_xsets):
+            cr = dataclasses.replace(c, seed=c.seed + 1000 * rank + r)
+            hx = I.layer_x(cr)
+            hl = I.layer_logits(cr, hx)
+            self.x.append(bf16(hx))
+            self.logits.append(torch.from_numpy(hl).to(device))
+            self.host_x.append(torch.from_numpy(hx.view(np.int16)).view(torch.bfloat16)
+                               .pin_memory())
+            self.host_logits.append(torch.from_numpy(hl).pin_memory())
+        self.w13, self.w2 = [], []
+        for r in range(self.n_wsets):
+            cw = dataclasses.replace(c, seed=c.seed + r)
+            self.w13.append(bf16(I.all_w13(cw)))
+            self.w2.append(bf16(I.all_w2(cw)))
+        self.params = moe.make_params(c.gating, c.act, c.layout)
+        self.ws = moe.workspace(c.n, c.E, c.k, c.H, c.I, device)
+        self.out = torch.empty((c.n, c.H), dtype=torch.bfloat16, device=device)
+        self.host_out = torch.empty((c.n, c.H), dtype=torch.bfloat16).pin_memory()
+
+    def args(self, i):
+        return (self.x[i % self.n_xsets], self.logits[i % self.n_xsets],
+                self.w13[i % self.n_wsets], self.w2[i % self.n_wsets])
+
+
+def time_layer(dc: DeviceCase, steps, warmup, pg, sampler=None, timed_stages=True):
+    import torch
+    import mixture_experts_routing_warp_gb300 as moe
+    c = dc.c
+    S = len(moe.STAGES)
+    for i in range(warmup):
+        moe.forward(*dc.args(i), c.k, dc.params, dc.ws, out=dc.out)
+    torch.cuda.synchronize()
+    events = [[torch.cuda.Event(enable_timing=True) for _ in range(S + 1)] for _ in range(steps)]
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    if pg is not None:
+        pg.barrier()
+    torch.cuda.synchronize()
+    t0 = time.time()
+    start.record()
+    for i in range(steps):
+        if timed_stages:
+            moe.forward_timed(*dc.args(warmup + i), c.k, dc.params, dc.ws, events[i], out=dc.out)
+        else:
+            moe.forward(*dc.args(warmup + i), c.k, dc.params, dc.ws, out=dc.out)
+    end.record()
+    torch.cuda.synchronize()
+    t1 = time.time()
+    if pg is not None:
+        pg.barrier()
+    if sampler is not None:
+        sampler.mark(t0, t1)
+    total_ms = start.elapsed_time(end)
+    stage_ms = None
+    if timed_stages:
+        stage_ms = {name: sum(ev[j].elapsed_time(ev[j + 1]) for ev in events) / steps
+                    for j, name in enumerate(moe.STAGES)}
+    status = moe.read_status(dc.ws)
+    if status != 0:
+        raise RuntimeError(f"device status {status} after the timed region")
+    return total_ms, stage_ms
+
+
+def time_e2e(dc: DeviceCase, steps, warmup):
+    """Same forward with host buffers: H2D x + logits, forward, D2H out."""
+    import torch
+    import mixture_experts_routing_warp_gb300 as moe
+    c = dc.c
+    xd = torch.empty_like(dc.x[0])
+    ld = torch.empty_like(dc.logits[0])
+
+    def step(i):
+        j = i % dc.n_xsets
+        xd.copy_(dc.host_x[j], non_blocking=True)
+        ld.copy_(dc.host_logits[j], non_blocking=True)
+        moe.forward(xd, ld, dc.w13[i % dc.n_wsets], dc.w2[i % dc.n_wsets], c.k, dc.params, dc.ws,
+                    out=dc.out)
+        dc.host_out.copy_(dc.out, non_blocking=True)
+
+    for i in range(warmup):
+        step(i)
+    torch.cuda.synchronize()
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    start.record()
+    for i in range(steps):
+        step(warmup + i)
+    end.record()
+    torch.cuda.synchronize()
+    ms = start.elapsed_time(end) / steps
+    h2d = dc.host_x[0].numel() * 2 + dc.host_logits[0].numel() * 4
+    d2h = dc.host_out.numel() * 2
+    return ms, h2d, d2h
+
+
+def time_routing(n, E, k, steps, device, l2_bytes, pk, source):
+    """moe_route + moe_build_metadata per call, logits rotated over > 2 x L2."""
+    import torch
+    import mixture_experts_routing_warp_gb300 as moe
+    sets = max(2, min(64, -(-2 * l2_bytes // (n * E * 4))))
+    logits = [torch.from_numpy(I.route_logits(n, E, seed=s)).to(device) for s in range(sets)]
+    indx = torch.empty((n, k), dtype=torch.int32, device=device)
+    vals = torch.empty((n, k), dtype=torch.bfloat16, device=device)
+    ws = moe.workspace(n, E, k, 64, 64, device)
+    meta = moe.empty_meta(n * k, E, device)
+    L = moe.lib()
+    stream = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+    ms = moe._binding._meta_struct(meta)
+
+    def call(i, ev=None):
+        if ev:
+            ev[0].record()
+        L.moe_route(logits[i % sets].data_ptr(), n, E, k, 0, indx.data_ptr(), vals.data_ptr(),
+                    stream)
+        if ev:
+            ev[1].record()
+        L.moe_build_metadata(indx.data_ptr(), vals.data_ptr(), n, E, k, ctypes.byref(ms),
+                             ws.data_ptr(), ws.numel(), stream)
+        if ev:
+            ev[2].record()
+
+    for i in range(5):
+        call(i)
+    torch.cuda.synchronize()
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(steps)]
+    for i in range(steps):
+        call(5 + i, ev[i])
+    torch.cuda.synchronize()
+    assert moe.read_status(ws) == 0
+    route_ms = sum(e[0].elapsed_time(e[1]) for e in ev) / steps
+    meta_ms = sum(e[1].elapsed_time(e[2]) for e in ev) / steps
+    total_us = (route_ms + meta_ms) * 1e3
+    w = stage_work(I.LayerCase("routing", n=n, H=64, E=E, k=k, I=64))
+    alg = n * E * 4 + n * k * (4 + 2 + 4 + 4 + 2) + (2 * E + 1) * 4
+    return {"workload": f"route+metadata n{n} E{E} k{k} (fp32 N(0,1) logits, {sets} rotated sets)",
+            "us_per_call": round(total_us, 3), "route_us": round(route_ms * 1e3, 3),
+            "metadata_us": round(meta_ms * 1e3, 3), "algorithmic_bytes": alg,
+            "achieved_gbs": round(alg / (total_us * 1e-6) / 1e9, 1),
+            "frac_of_hbm": round(alg / (total_us * 1e-6) / 1e9 / pk["hbm_gbs"], 4),
+            "frac_of_8tbs": round(alg / (total_us * 1e-6) / 8e12, 4),
+            "route_roofline": roofline_entry("hbm", w["route"][1], route_ms * 1e-3, pk, source),
+            "metadata_roofline": roofline_entry("hbm", w["metadata"][1], meta_ms * 1e-3, pk,
+                                                source)}
+
+
+# ------------------------------------------------------------ CPU arm --
+def oracle_inputs(c: I.LayerCase) -> dict:
+    hx = I.layer_x(c)
+    return {"x": hx, "logits": I.layer_logits(c, hx), "w13": I.all_w13(c), "w2": I.all_w2(c)}
+
+
+def oracle_sample(c: I.LayerCase, d: dict, budget_s: float = 12.0, max_tokens: int = 4096):
+    """Time the CPU oracle on a bounded sample of the workload: routing and
+    metadata over all n tokens plus the FFN and combine on the first m tokens,
+    m grown until about budget_s of CPU work. Returns the layer's tokens/s
+    (routing + metadata time prorated per token)."""
+    import oracle
+    t = time.perf_counter()
+    indx, vals = oracle.route(d["logits"], c.k, c.gating)
+    oracle.metadata(indx, vals, c.E)
+    route_meta_s = time.perf_counter() - t
+    m, spent = 8, 0.0
+    while True:
+        toks = np.arange(min(m, c.n), dtype=np.int64)
+        t = time.perf_counter()
+        oracle.ffn(d["x"], indx, vals, d["w13"], d["w2"], tokens=toks, act=c.act,
+                   layout=c.layout)
+        dt = time.perf_counter() - t
+        spent += dt
+        rate = 1.0 / (dt / toks.size + route_meta_s / c.n)
+        if dt >= budget_s * 0.4 or toks.size >= min(c.n, max_tokens) or spent >= budget_s:
+            break
+        m = int(min(c.n, max_tokens, max(2 * m, toks.size * budget_s * 0.5 / max(dt, 1e-3))))
+    cores = int(os.environ.get("OMP_NUM_THREADS", os.cpu_count() or 1))
+    return {"value": round(rate, 3), "unit": "tokens/s", "cores": cores, "kind": "oracle",
+            "sample": f"route+metadata over all {c.n} tokens, FFN+combine over the first "
+                      f"{toks.size} tokens ({dt:.1f} s); float64 C oracle, OpenMP over tokens"}
+
+
+def run_reference(args, rank, world, pg):
+    if rank != 0:
+        return 0
+    c = WORKLOADS[args.workload]
+    d = oracle_inputs(c)
+    budget = max(1.0, 90.0 / max(args.steps + args.warmup, 1))
+    for _ in range(args.warmup):
+        oracle_sample(c, d, budget_s=budget, max_tokens=64)
+    steps_v = []
+    t0 = time.time()
+    for i in range(args.steps):
+        r = oracle_sample(c, d, budget_s=budget, max_tokens=512)
+        steps_v.append(r["value"])
+    wall = time.time() - t0
+    value = float(np.median(steps_v))
+    line = {"impl": "reference", "metric": METRIC, "value": round(value, 3), "unit": "tokens/s",
+            "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(1e3 * c.n / value, 1) if value else None,
+            "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": c.name, "n_tokens": c.n, "hidden": c.H, "n_experts": c.E,
+                       "topk": c.k, "intermediate": c.I, "gating": c.gating,
+                       "activation": c.act, "w13_layout": c.layout, "l2": "n/a (CPU)"},
+            "cpu_baseline": {"value": round(value, 3), "unit": "tokens/s", "kind": "oracle",
+                             "cores": r["cores"], "sample": r["sample"]},
+            "e2e": {"value": round(value, 3), "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0},
+            "gpu_launches": 0, "wall_s": round(wall, 1)}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def run_ours(args, rank, world, local, pg):
+    import torch
+    import mixture_experts_routing_warp_gb300 as moe
+    moe.lib()
+    device = torch.device("cuda", local)
+    torch.cuda.set_device(device)
+    props = torch.cuda.get_device_properties(device)
+    l2 = int(getattr(props, "L2_cache_size", 0) or 132 * 1024 * 1024)
+    pk, source = peaks()
+    c = WORKLOADS[args.workload]
+    dc = DeviceCase(c, device, l2, rank)
+    sampler = ClockSampler(local)
+    sampler.start()
+    total_ms, stage_ms = time_layer(dc, args.steps, args.warmup, pg, sampler)
+    sampler.stop()
+    if pg is not None:
+        t = torch.tensor([total_ms], dtype=torch.float64, device=device)
+        pg.all_reduce(t, op=pg.ReduceOp.MAX)
+        total_ms = float(t.item())
+    ms_per_step = total_ms / args.steps
+    value = world * c.n / (ms_per_step * 1e-3)
+    work = stage_work(c)
+    dom = max(stage_ms, key=stage_ms.get)
+    bound, w = work[dom]
+    roof = roofline_entry(bound, w, stage_ms[dom] * 1e-3, pk, source)
+    roof["kernel"] = dom
+    roof["traffic"] = ncu_traffic(dom, args.workload)
+    kernels_per_step = 5 + (1 if c.k > 1 else 0)
+    line = {"metric": METRIC, "value": round(value, 1), "unit": "tokens/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 4),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic (seeded numpy PCG64, N(0,1) tokens, N(0,0.02) weights)",
+            "config": {"workload": c.name, "n_tokens": c.n, "hidden": c.H, "n_experts": c.E,
+                       "topk": c.k, "intermediate": c.I, "gating": c.gating,
+                       "activation": c.act, "w13_layout": c.layout,
+                       "l2": f"inputs rotated over {dc.n_xsets} token sets and {dc.n_wsets} "
+                             f"weight sets (> 2x L2 per step cycle)",
+                       "parallelism": f"replicas x{world} (token batches per rank)"},
+            "roofline": roof,
+            "stage_ms": {k: round(v, 4) for k, v in stage_ms.items()},
+            "gpu_launches": kernels_per_step * args.steps,
+            "clocks": sampler.summary()}
+    if rank == 0:
+        e2e_ms, h2d, d2h = time_e2e(dc, max(3, min(args.steps, 20)), args.warmup)
+        line["e2e"] = {"value": round(world * c.n / (e2e_ms * 1e-3), 1), "unit": "tokens/s",
+                       "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                       "ms_per_step": round(e2e_ms, 4)}
+        if not args.no_extras:
+            also = {"routing_metadata_16k": time_routing(16384, 128, 4, 200, device, l2, pk,
+                                                         source)}
+            also["routing_metadata_16k_e32"] = time_routing(16384, 32, 4, 200, device, l2, pk,
+                                                            source)
+            if args.workload != "minimind_e4":
+                mm = DeviceCase(I.MINIMIND_E4, device, l2)
+                mms, mstage = time_layer(mm, 50, 5, None)
+                mdom = max(mstage, key=mstage.get)
+                mwork = stage_work(I.MINIMIND_E4)
+                mroof = roofline_entry(mwork[mdom][0], mwork[mdom][1], mstage[mdom] * 1e-3, pk,
+                                       source)
+                mroof["kernel"] = mdom
+                also["minimind_e4"] = {"tokens_per_s": round(I.MINIMIND_E4.n / (mms / 50e3), 1),
+                                       "ms_per_step": round(mms / 50, 4),
+                                       "stage_ms": {k: round(v, 4) for k, v in mstage.items()},
+                                       "roofline": mroof}
+                del mm
+            line["also"] = also
+        if not args.no_cpu_baseline:
+            line["cpu_baseline"] = oracle_sample(c, oracle_inputs(c))
+        print(json.dumps(line), flush=True)
+    return 0
+
+
+def main():
+    args = parse_args()
+    rank, world, local, pg = dist_setup(args)
+    try:
+        if args.impl == "reference":
+            return run_reference(args, rank, world, pg)
+        return run_ours(args, rank, world, local, pg)
+    finally:
+        if pg is not None:
+            pg.destroy_process_group()
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -204,6 +204,29 @@ moe_status moe_forward(const uint16_t *x, const float *logits, const uint16_t *w
                        uint16_t *topk_vals, const moe_routing_meta *meta, void *workspace,
                        size_t workspace_bytes, moe_stream stream);
 
+/* Stage kernels of moe_forward, in launch order (indices of the events of
+ * moe_forward_timed). */
+#define MOE_STAGE_ROUTE 0    /* top-k + gate weights                       */
+#define MOE_STAGE_METADATA 1 /* histogram, offsets, sorted indices         */
+#define MOE_STAGE_GATHER 2   /* expert-sorted copy of the token rows       */
+#define MOE_STAGE_FFN1 3     /* w13 contraction + activation -> h          */
+#define MOE_STAGE_FFN2 4     /* w2 contraction + gate scale + scatter      */
+#define MOE_STAGE_COMBINE 5  /* sum over the k slots (no kernel when k = 1) */
+#define MOE_STAGE_COUNT 6
+
+/* moe_forward plus timing: `events` holds MOE_STAGE_COUNT + 1 cudaEvent_t
+ * handles (created by the caller); events[i] is recorded on `stream` just
+ * before stage i's kernel and events[MOE_STAGE_COUNT] after the last one,
+ * so cudaEventElapsedTime(events[i], events[i+1]) is stage i's device time.
+ * n_events must be MOE_STAGE_COUNT + 1. Same results as moe_forward. */
+moe_status moe_forward_timed(const uint16_t *x, const float *logits, const uint16_t *w13,
+                             const uint16_t *w2, int64_t n, int32_t E, int32_t k, int32_t H,
+                             int32_t I, const moe_params *params, uint16_t *out,
+                             int32_t *topk_indx, uint16_t *topk_vals,
+                             const moe_routing_meta *meta, void *workspace,
+                             size_t workspace_bytes, void *const *events, int32_t n_events,
+                             moe_stream stream);
+
 /* DEBUG ONLY -- synchronises `stream`, returns the status word recorded by
  * device-side bounded waits since the last reset (MOE_OK if none), and
  * resets it and the barrier counters when `reset` is non-zero. */

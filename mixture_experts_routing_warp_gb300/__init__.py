@@ -7,11 +7,11 @@ the C ABI of include/moe.h. This package is the thin Python binding
 (`inputs`).
 """
 from ._binding import (ACT, GATING, LAYOUT, MoEError, MoeParams, RoutingMeta, build_metadata,
-                       combine, empty_meta, forward, grouped_ffn, lib, library_path, make_params,
+                       STAGES, combine, empty_meta, forward, forward_timed, grouped_ffn, lib, library_path, make_params,
                        read_status, route, selftest_wait_timeout, status_string, workspace,
                        workspace_size)
 
 __all__ = ["ACT", "GATING", "LAYOUT", "MoEError", "MoeParams", "RoutingMeta", "build_metadata",
-           "combine", "empty_meta", "forward", "grouped_ffn", "lib", "library_path",
+           "STAGES", "combine", "empty_meta", "forward", "forward_timed", "grouped_ffn", "lib", "library_path",
            "make_params", "read_status", "route", "selftest_wait_timeout", "status_string",
            "workspace", "workspace_size"]

@@ -64,6 +64,8 @@ SIGNATURES = {
     "moe_combine": (_I32, [_P, _I64, _I32, _I32, _P, _P]),
     "moe_forward": (_I32, [_P, _P, _P, _P, _I64, _I32, _I32, _I32, _I32, _PP, _P, _P, _P, _PM,
                            _P, _SZ, _P]),
+    "moe_forward_timed": (_I32, [_P, _P, _P, _P, _I64, _I32, _I32, _I32, _I32, _PP, _P, _P, _P,
+                                 _PM, _P, _SZ, _P, _I32, _P]),
     "moe_read_status": (_I32, [_P, _SZ, _I32, _P]),
     "moe_selftest_wait_timeout": (_I32, [_P, _SZ, _U64, _P]),
 }
@@ -241,6 +243,29 @@ def forward(x: torch.Tensor, logits: torch.Tensor, w13: torch.Tensor, w2: torch.
     _check(lib().moe_forward(_ptr(x), _ptr(logits), _ptr(w13), _ptr(w2), n, E, k, H, I,
                              ctypes.byref(params), _ptr(out), _ptr(indx), _ptr(vals), mstruct,
                              _ptr(ws), ws.numel(), _stream(x.device)), "moe_forward")
+    return out
+
+
+STAGES = ("route", "metadata", "gather", "ffn1", "ffn2", "combine")
+
+
+def forward_timed(x: torch.Tensor, logits: torch.Tensor, w13: torch.Tensor, w2: torch.Tensor,
+                  k: int, params: MoeParams, ws: torch.Tensor, events: list,
+                  out: Optional[torch.Tensor] = None) -> torch.Tensor:
+    """forward() that records len(STAGES) + 1 torch.cuda.Event objects between
+    the stage kernels (events[i] before stage i, the last after the end)."""
+    n, H = x.shape
+    E = logits.shape[1]
+    I = w13.shape[1] // 2
+    if out is None:
+        out = torch.empty((n, H), dtype=torch.bfloat16, device=x.device)
+    if len(events) != len(STAGES) + 1:
+        raise ValueError("need len(STAGES) + 1 events")
+    arr = (ctypes.c_void_p * len(events))(*[ctypes.c_void_p(e.cuda_event) for e in events])
+    _check(lib().moe_forward_timed(_ptr(x), _ptr(logits), _ptr(w13), _ptr(w2), n, E, k, H, I,
+                                   ctypes.byref(params), _ptr(out), None, None, None, _ptr(ws),
+                                   ws.numel(), arr, len(events), _stream(x.device)),
+           "moe_forward_timed")
     return out
 
 

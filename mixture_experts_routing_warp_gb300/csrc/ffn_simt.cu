@@ -157,14 +157,16 @@ __global__ void __launch_bounds__(SB_THREADS) ffn2_simt_kernel(
 cudaError_t launch_ffn(const uint16_t *x_sorted, const int32_t *offs, const int32_t *col_sorted,
                        const uint16_t *gate_scal, const uint16_t *w13, const uint16_t *w2,
                        int64_t N, int E, int H, int I, const ActParams &act, uint16_t *h_buf,
-                       uint16_t *y_flat, uint32_t *ctrl, cudaStream_t s) {
+                       uint16_t *y_flat, uint32_t *ctrl, cudaStream_t s, cudaEvent_t *ev_ffn) {
   (void)ctrl;
   if (N == 0) return cudaSuccess;
+  if (ev_ffn && cudaEventRecord(ev_ffn[0], s) != cudaSuccess) return cudaErrorUnknown;
   const unsigned mtiles = (unsigned)((N + SB_M - 1) / SB_M + E);
   ffn1_simt_kernel<<<dim3(mtiles, (I + SB_N - 1) / SB_N), SB_THREADS, 0, s>>>(x_sorted, offs, E, H,
                                                                              I, w13, act, h_buf);
   cudaError_t err = cudaGetLastError();
   if (err != cudaSuccess) return err;
+  if (ev_ffn && cudaEventRecord(ev_ffn[1], s) != cudaSuccess) return cudaErrorUnknown;
   ffn2_simt_kernel<<<dim3(mtiles, (H + SB_N - 1) / SB_N), SB_THREADS, 0, s>>>(
       h_buf, offs, col_sorted, gate_scal, E, H, I, w2, y_flat);
   return cudaGetLastError();

@@ -167,11 +167,12 @@ moe_status moe_combine(const uint16_t *y_flat, int64_t n, int32_t k, int32_t H, 
   return from_cuda(launch_combine(y_flat, n, k, H, out, (cudaStream_t)stream));
 }
 
-moe_status moe_forward(const uint16_t *x, const float *logits, const uint16_t *w13,
-                       const uint16_t *w2, int64_t n, int32_t E, int32_t k, int32_t H, int32_t I,
-                       const moe_params *params, uint16_t *out, int32_t *topk_indx,
-                       uint16_t *topk_vals, const moe_routing_meta *meta, void *workspace,
-                       size_t workspace_bytes, moe_stream stream) {
+static moe_status forward_impl(const uint16_t *x, const float *logits, const uint16_t *w13,
+                               const uint16_t *w2, int64_t n, int32_t E, int32_t k, int32_t H,
+                               int32_t I, const moe_params *params, uint16_t *out,
+                               int32_t *topk_indx, uint16_t *topk_vals,
+                               const moe_routing_meta *meta, void *workspace,
+                               size_t workspace_bytes, cudaStream_t s, cudaEvent_t *ev) {
   moe_status st = check_sizes(n, E, k, H, I, true);
   if (st != MOE_OK) return st;
   ActParams act;
@@ -188,7 +189,6 @@ moe_status moe_forward(const uint16_t *x, const float *logits, const uint16_t *w
   const WorkspaceLayout L = workspace_layout(n, E, k, H, I);
   if (workspace_bytes < L.total) return MOE_ERR_WORKSPACE_TOO_SMALL;
 
-  cudaStream_t s = (cudaStream_t)stream;
   int32_t *indx = topk_indx ? topk_indx : ws_at<int32_t>(workspace, L.topk_indx);
   uint16_t *vals = topk_vals ? topk_vals : ws_at<uint16_t>(workspace, L.topk_vals);
   moe_routing_meta m;
@@ -205,19 +205,54 @@ moe_status moe_forward(const uint16_t *x, const float *logits, const uint16_t *w
   const int64_t N = n * k;
   // k = 1: slot f is token t, so the w2 epilogue writes the output directly.
   uint16_t *y_flat = k == 1 ? out : ws_at<uint16_t>(workspace, L.y_flat);
-
-  if (launch_route(logits, n, E, k, gating, indx, vals, s) != cudaSuccess) return MOE_ERR_CUDA;
-  if (launch_metadata(indx, vals, n, E, k, m, ws_at<int32_t>(workspace, L.hist), ctrl, s) !=
-      cudaSuccess)
-    return MOE_ERR_CUDA;
   uint16_t *x_sorted = ws_at<uint16_t>(workspace, L.x_sorted);
-  if (launch_gather_rows(x, m.col_sorted, N, k, H, x_sorted, s) != cudaSuccess)
+  uint16_t *h = ws_at<uint16_t>(workspace, L.h);
+  auto mark = [&](int i) {
+    return ev ? cudaEventRecord(ev[i], s) : cudaSuccess;
+  };
+
+  if (mark(MOE_STAGE_ROUTE) != cudaSuccess ||
+      launch_route(logits, n, E, k, gating, indx, vals, s) != cudaSuccess)
     return MOE_ERR_CUDA;
-  if (launch_ffn(x_sorted, m.offs, m.col_sorted, m.gate_scal, w13, w2, N, E, H, I, act,
-                 ws_at<uint16_t>(workspace, L.h), y_flat, ctrl, s) != cudaSuccess)
+  if (mark(MOE_STAGE_METADATA) != cudaSuccess ||
+      launch_metadata(indx, vals, n, E, k, m, ws_at<int32_t>(workspace, L.hist), ctrl, s) !=
+          cudaSuccess)
     return MOE_ERR_CUDA;
+  if (mark(MOE_STAGE_GATHER) != cudaSuccess ||
+      launch_gather_rows(x, m.col_sorted, N, k, H, x_sorted, s) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  if (launch_ffn(x_sorted, m.offs, m.col_sorted, m.gate_scal, w13, w2, N, E, H, I, act, h, y_flat,
+                 ctrl, s, ev ? ev + MOE_STAGE_FFN1 : nullptr) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  if (mark(MOE_STAGE_COMBINE) != cudaSuccess) return MOE_ERR_CUDA;
   if (k > 1 && launch_combine(y_flat, n, k, H, out, s) != cudaSuccess) return MOE_ERR_CUDA;
+  if (mark(MOE_STAGE_COUNT) != cudaSuccess) return MOE_ERR_CUDA;
   return MOE_OK;
+}
+
+moe_status moe_forward(const uint16_t *x, const float *logits, const uint16_t *w13,
+                       const uint16_t *w2, int64_t n, int32_t E, int32_t k, int32_t H, int32_t I,
+                       const moe_params *params, uint16_t *out, int32_t *topk_indx,
+                       uint16_t *topk_vals, const moe_routing_meta *meta, void *workspace,
+                       size_t workspace_bytes, moe_stream stream) {
+  return forward_impl(x, logits, w13, w2, n, E, k, H, I, params, out, topk_indx, topk_vals, meta,
+                      workspace, workspace_bytes, (cudaStream_t)stream, nullptr);
+}
+
+moe_status moe_forward_timed(const uint16_t *x, const float *logits, const uint16_t *w13,
+                             const uint16_t *w2, int64_t n, int32_t E, int32_t k, int32_t H,
+                             int32_t I, const moe_params *params, uint16_t *out,
+                             int32_t *topk_indx, uint16_t *topk_vals,
+                             const moe_routing_meta *meta, void *workspace,
+                             size_t workspace_bytes, void *const *events, int32_t n_events,
+                             moe_stream stream) {
+  if (!events || n_events != MOE_STAGE_COUNT + 1) return MOE_ERR_INVALID_ARG;
+  for (int i = 0; i <= MOE_STAGE_COUNT; ++i)
+    if (!events[i]) return MOE_ERR_INVALID_ARG;
+  cudaEvent_t ev[MOE_STAGE_COUNT + 1];
+  for (int i = 0; i <= MOE_STAGE_COUNT; ++i) ev[i] = (cudaEvent_t)events[i];
+  return forward_impl(x, logits, w13, w2, n, E, k, H, I, params, out, topk_indx, topk_vals, meta,
+                      workspace, workspace_bytes, (cudaStream_t)stream, ev);
 }
 
 moe_status moe_read_status(void *workspace, size_t workspace_bytes, int32_t reset,

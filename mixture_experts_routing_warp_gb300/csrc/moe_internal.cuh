@@ -144,6 +144,8 @@ __device__ __forceinline__ float activate(float g, float u, const ActParams &p) 
 }
 
 // ----------------------------------------------------- kernel launchers --
+// launch_ffn records ev_ffn[0] before the w13 kernel and ev_ffn[1] before the
+// w2 kernel when ev_ffn is given (stage timing of moe_forward_timed).
 // All return the launch's cudaError_t (cudaGetLastError after the launch).
 int device_sm_count();
 
@@ -163,7 +165,8 @@ cudaError_t launch_combine(const uint16_t *y_flat, int64_t n, int k, int H, uint
 cudaError_t launch_ffn(const uint16_t *x_sorted, const int32_t *offs, const int32_t *col_sorted,
                        const uint16_t *gate_scal, const uint16_t *w13, const uint16_t *w2,
                        int64_t N, int E, int H, int I, const ActParams &act, uint16_t *h_buf,
-                       uint16_t *y_flat, uint32_t *ctrl, cudaStream_t s);
+                       uint16_t *y_flat, uint32_t *ctrl, cudaStream_t s,
+                       cudaEvent_t *ev_ffn = nullptr);
 
 cudaError_t launch_wait_selftest(uint32_t *ctrl, unsigned long long timeout_ns, cudaStream_t s);
 
