@@ -275,6 +275,9 @@ def time_layer(dc: DeviceCase, steps, warmup, pg, sampler=None, timed_stages=Tru
         moe.forward(*dc.args(i), c.k, dc.params, dc.ws, out=dc.out)
     torch.cuda.synchronize()
     events = [[torch.cuda.Event(enable_timing=True) for _ in range(S + 1)] for _ in range(steps)]
+    for ev in events:   # torch creates each CUDA event on its first record
+        for e in ev:
+            e.record()
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     if pg is not None:
         pg.barrier()

@@ -261,6 +261,9 @@ def forward_timed(x: torch.Tensor, logits: torch.Tensor, w13: torch.Tensor, w2: 
         out = torch.empty((n, H), dtype=torch.bfloat16, device=x.device)
     if len(events) != len(STAGES) + 1:
         raise ValueError("need len(STAGES) + 1 events")
+    for e in events:
+        if not e.cuda_event:  # torch creates the CUDA event on its first record
+            e.record()
     arr = (ctypes.c_void_p * len(events))(*[ctypes.c_void_p(e.cuda_event) for e in events])
     _check(lib().moe_forward_timed(_ptr(x), _ptr(logits), _ptr(w13), _ptr(w2), n, E, k, H, I,
                                    ctypes.byref(params), _ptr(out), None, None, None, _ptr(ws),
