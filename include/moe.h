@@ -169,6 +169,33 @@ moe_status moe_build_metadata(const int32_t *topk_indx, const uint16_t *topk_val
                               int32_t E, int32_t k, const moe_routing_meta *meta,
                               void *workspace, size_t workspace_bytes, moe_stream stream);
 
+/* Stage 2 without a workspace -- the paper has no counterpart to this call;
+ * it exists for callers that cannot give the library any device memory of
+ * their own: a plugin that must enqueue into a framework whose allocator
+ * owns all device memory, a latency-critical path where cudaMalloc (which
+ * may synchronise the device) is forbidden, or any code that may not
+ * allocate where it runs. Same results as moe_build_metadata, bit for bit;
+ * it allocates nothing and takes no workspace.
+ *   Scratch: a fixed array inside the library (4 KB of control words plus
+ *   256 x 256 int32 histogram counters, 266,240 bytes), present on every GPU
+ *   that loads the library until the process exits. The grid is capped at
+ *   256 CTAs, so every valid size fits; sizes beyond the library's limits
+ *   (E > 256, k > 8 or k > E, n*k >= 2^31) return MOE_ERR_INVALID_ARG.
+ *   The first call on a device looks up the array's device address (once
+ *   per device, with that device current); make that first call before any
+ *   stream capture.
+ *   Every call shares the one array: calls whose work overlaps on the GPU
+ *   (different streams, no ordering between them) race and give wrong
+ *   results. Each call clears the control words it needs at zero.
+ *   status_out: optional device int32 (NULL = not reported) that receives,
+ *   in stream order, the call's device status (MOE_OK, or MOE_ERR_TIMEOUT if
+ *   the bounded grid barrier gave up, MOE_ERR_INVALID_ARG if an expert id
+ *   was outside [0, E)). */
+moe_status moe_build_metadata_noalloc(const int32_t *topk_indx, const uint16_t *topk_vals,
+                                      int64_t n, int32_t E, int32_t k,
+                                      const moe_routing_meta *meta, int32_t *status_out,
+                                      moe_stream stream);
+
 /* Stage 3 -- grouped expert FFN. [R2] Summary and "It is removable in plain
  * PyTorch" (each expert runs on its contiguous slice; the weight multiplies
  * the expert output), [R3] 关键源码片段 (activations, w13 layouts).

@@ -59,6 +59,7 @@ SIGNATURES = {
     "moe_workspace_init": (_I32, [_P, _SZ, _P]),
     "moe_route": (_I32, [_P, _I64, _I32, _I32, _I32, _P, _P, _P]),
     "moe_build_metadata": (_I32, [_P, _P, _I64, _I32, _I32, _PM, _P, _SZ, _P]),
+    "moe_build_metadata_noalloc": (_I32, [_P, _P, _I64, _I32, _I32, _PM, _P, _P]),
     "moe_grouped_ffn": (_I32, [_P, _PM, _P, _P, _I64, _I32, _I32, _I32, _I32, _PP, _P, _P, _SZ,
                                _P]),
     "moe_combine": (_I32, [_P, _I64, _I32, _I32, _P, _P]),

@@ -11,6 +11,8 @@
 //    y.index_add_ of the weighted expert outputs.
 #include <cooperative_groups.h>
 
+#include <mutex>
+
 #include "moe_internal.cuh"
 
 namespace moe {
@@ -304,6 +306,101 @@ cudaError_t launch_metadata(const int32_t *topk_indx, const uint16_t *topk_vals,
   return cudaGetLastError();
 }
 
+// ======================================== metadata without a workspace ==
+//
+// Some callers cannot hand this library any device memory beyond the
+// tensors they already own: code that runs while a framework's allocator
+// owns every byte (a plugin asked to enqueue work with no workspace of its
+// own), code on a latency-critical path where any cudaMalloc is forbidden
+// because it can synchronise the device, or code inside a region that must
+// not allocate at all. For them moe_build_metadata_noalloc runs the same
+// metadata kernel with its scratch (the control block and the per-CTA
+// histograms) in the fixed array below instead of a caller workspace.
+//
+// The array lives in every GPU that loads the library, until the process
+// exits: 4 KB of control words plus 256 CTAs x 256 experts of int32
+// counters (266,240 bytes). The kernel never needs more: this variant caps
+// its grid at 256 CTAs, each CTA looping over as many slots as it must.
+constexpr int kNoAllocMaxCtas = 256;
+constexpr size_t kNoAllocScratchBytes =
+    kCtrlBytes + (size_t)kNoAllocMaxCtas * (size_t)kMaxExperts * sizeof(int32_t);
+
+static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
+
+namespace {
+constexpr int kNoAllocMaxDevices = 64;
+std::mutex g_noalloc_mu;
+void *g_noalloc_ptr[kNoAllocMaxDevices] = {};
+
+// Device address of g_noalloc_scratch on the current device. In host code
+// the array's name is only a host-side stand-in, so the address comes from
+// cudaGetSymbolAddress, once per device, with that device current.
+cudaError_t noalloc_scratch(void **out) {
+  int dev = -1;
+  cudaError_t err = cudaGetDevice(&dev);
+  if (err != cudaSuccess) return err;
+  if (dev < 0 || dev >= kNoAllocMaxDevices) return cudaErrorInvalidDevice;
+  std::lock_guard<std::mutex> lock(g_noalloc_mu);
+  if (!g_noalloc_ptr[dev]) {
+    void *p = nullptr;
+    err = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+    if (err != cudaSuccess) return err;
+    g_noalloc_ptr[dev] = p;
+  }
+  *out = g_noalloc_ptr[dev];
+  return cudaSuccess;
+}
+}  // namespace
+
+// Same kernel and the same results as launch_metadata; scratch in the
+// static array. Clears the control words first (barrier counters and the
+// status word must start at zero; the histograms are overwritten by every
+// CTA before they are read), then copies the status word to status_out.
+cudaError_t launch_metadata_noalloc(const int32_t *topk_indx, const uint16_t *topk_vals,
+                                    int64_t n, int E, int k, const moe_routing_meta &meta,
+                                    int32_t *status_out, cudaStream_t s) {
+  void *scratch = nullptr;
+  cudaError_t err = noalloc_scratch(&scratch);
+  if (err != cudaSuccess) return err;
+  uint32_t *ctrl = static_cast<uint32_t *>(scratch);
+  int32_t *hist = reinterpret_cast<int32_t *>(static_cast<char *>(scratch) + kCtrlBytes);
+  err = cudaMemsetAsync(scratch, 0, kCtrlBytes, s);
+  if (err != cudaSuccess) return err;
+
+  int N = (int)(n * k);
+  int per_sm = 0;
+  err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, metadata_kernel, kMetaThreads, 0);
+  if (err != cudaSuccess) return err;
+  int64_t B = (N + 1023) / 1024;
+  const int64_t cap = (int64_t)device_sm_count() * (per_sm > 0 ? per_sm : 1);
+  if (B > cap) B = cap;
+  if (B > kNoAllocMaxCtas) B = kNoAllocMaxCtas;
+  if (B < 1) B = 1;
+  int chunk = (int)((N + B - 1) / B);
+  unsigned long long timeout = kWaitTimeoutNs;
+  void *args[] = {(void *)&topk_indx, (void *)&topk_vals, (void *)&N, (void *)&E,
+                  (void *)&chunk, (void *)&meta.col_sum, (void *)&meta.offs,
+                  (void *)&meta.col_sorted, (void *)&meta.row_sorted, (void *)&meta.gate_scal,
+                  (void *)&hist, (void *)&ctrl, (void *)&timeout};
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)B);
+  cfg.blockDim = dim3(kMetaThreads);
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeCooperative;
+  attr[0].val.cooperative = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  err = cudaLaunchKernelExC(&cfg, (const void *)metadata_kernel, args);
+  if (err != cudaSuccess) return err;
+  if (status_out) {
+    err = cudaMemcpyAsync(status_out, ctrl + kCtrlStatus, sizeof(int32_t),
+                          cudaMemcpyDeviceToDevice, s);
+    if (err != cudaSuccess) return err;
+  }
+  return cudaGetLastError();
+}
+
 // ======================================================= gather rows ==
 // X_sorted[p] = x[col_sorted[p] / k]: the dispatch index_select of the
 // MiniMind issue ("It is removable in plain PyTorch"), 16 bytes per thread.
@@ -403,3 +500,28 @@ cudaError_t launch_wait_selftest(uint32_t *ctrl, unsigned long long timeout_ns, 
 }
 
 }  // namespace moe
+
+// The C entry point of the no-allocation variant (declared in include/moe.h).
+extern "C" moe_status moe_build_metadata_noalloc(const int32_t *topk_indx,
+                                                 const uint16_t *topk_vals, int64_t n, int32_t E,
+                                                 int32_t k, const moe_routing_meta *meta,
+                                                 int32_t *status_out, moe_stream stream) {
+  using namespace moe;
+  // Sizes beyond what this variant (and its fixed scratch) handles.
+  if (n < 0 || E < 1 || E > kMaxExperts || k < 1 || k > kMaxTopk || k > E)
+    return MOE_ERR_INVALID_ARG;
+  if (n * (int64_t)k >= (int64_t)INT32_MAX) return MOE_ERR_INVALID_ARG;
+  if (!meta || !meta->col_sum || !meta->offs) return MOE_ERR_INVALID_ARG;
+  if (n > 0 && (!meta->col_sorted || !meta->row_sorted || !meta->gate_scal || !topk_indx ||
+                !topk_vals))
+    return MOE_ERR_INVALID_ARG;
+  auto misaligned = [](const void *p, uintptr_t a) { return ((uintptr_t)p % a) != 0; };
+  if (misaligned(meta->col_sum, 4) || misaligned(meta->offs, 4) ||
+      misaligned(meta->col_sorted, 4) || misaligned(meta->row_sorted, 4) ||
+      misaligned(meta->gate_scal, 2) || misaligned(topk_indx, 4) || misaligned(topk_vals, 2) ||
+      misaligned(status_out, 4))
+    return MOE_ERR_MISALIGNED;
+  cudaError_t err = launch_metadata_noalloc(topk_indx, topk_vals, n, E, k, *meta, status_out,
+                                            (cudaStream_t)stream);
+  return err == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+}
