@@ -17,8 +17,9 @@ roofline     the stage with the largest device time, algorithmic FLOPs or
 e2e          the same metric with host (pinned) buffers: x and logits copied
              host->device and the output device->host inside the timed region
 cpu_baseline the CPU oracle timed on this host's cores on a bounded sample
-also         routing + metadata us/call at 16384 tokens x 128 experts (top-4)
-             and the MiniMind-shaped layer, each with its own roofline figure
+also         routing + metadata us/call at 16384 tokens (E = 128 and 32, top-4) and
+             the MiniMind-shaped layer (E = 4, 16), timed by CUDA-graph replay
+             (their steps are too short for eager launches to keep the GPU busy)
 
 --impl reference times the CPU oracle (the reference for this method) on
 the same workload and prints its line with "impl": "reference".
@@ -66,12 +67,15 @@ def log(*a):
 def parse_args():
     p = argparse.ArgumentParser()
     p.add_argument("--gpus", type=int, default=1)
-    p.add_argument("--steps", type=int, default=50)
+    p.add_argument("--steps", type=int, default=200)
     p.add_argument("--warmup", type=int, default=5)
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
     p.add_argument("--workload", choices=sorted(WORKLOADS), default=DEFAULT_WORKLOAD)
     p.add_argument("--no-extras", action="store_true", help="skip the routing / MiniMind extras")
     p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--profile-only", action="store_true",
+                   help="only the warm-up and timed steps (for ncu): no e2e, extras, "
+                        "CPU baseline or clock sampling")
     a = p.parse_args()
     a.warmup = max(a.warmup, 3)
     return a
@@ -102,7 +106,7 @@ def peaks():
 
 
 class ClockSampler:
-    """nvidia-smi clocks / throttle reasons sampled every 50 ms in the background."""
+    """nvidia-smi clocks / throttle reasons sampled every 20 ms in the background."""
     QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
@@ -118,7 +122,7 @@ class ClockSampler:
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", f"--query-gpu={self.QUERY}", "--format=csv,noheader,nounits",
-                 "-lms", "50", "-i", str(self.gpu)], stdout=subprocess.PIPE,
+                 "-lms", "20", "-i", str(self.gpu)], stdout=subprocess.PIPE,
                 stderr=subprocess.DEVNULL, text=True)
         except OSError:
             self.proc = None
@@ -338,8 +342,39 @@ def time_e2e(dc: DeviceCase, steps, warmup):
     return ms, h2d, d2h
 
 
-def time_routing(n, E, k, steps, device, l2_bytes, pk, source):
-    """moe_route + moe_build_metadata per call, logits rotated over > 2 x L2."""
+def graph_time_ms(fn, reps: int, replays: int = 5) -> float:
+    """Capture reps calls of fn(i) in one CUDA graph, replay it, and return
+    the device time per call (median over replays)."""
+    import torch
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        for i in range(3):
+            fn(i)
+    torch.cuda.current_stream().wait_stream(s)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        for i in range(reps):
+            fn(i)
+    g.replay()
+    torch.cuda.synchronize()
+    times = []
+    for _ in range(replays):
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        g.replay()
+        b.record()
+        torch.cuda.synchronize()
+        times.append(a.elapsed_time(b) / reps)
+    del g
+    return float(np.median(times))
+
+
+def time_routing(n, E, k, device, l2_bytes, pk, source):
+    """moe_route + moe_build_metadata per call: CUDA-graph replays of back-to-
+    back calls (so host launch overhead is not counted), logits rotated over
+    more than 2 x L2."""
     import torch
     import mixture_experts_routing_warp_gb300 as moe
     sets = max(2, min(64, -(-2 * l2_bytes // (n * E * 4))))
@@ -349,43 +384,84 @@ def time_routing(n, E, k, steps, device, l2_bytes, pk, source):
     ws = moe.workspace(n, E, k, 64, 64, device)
     meta = moe.empty_meta(n * k, E, device)
     L = moe.lib()
-    stream = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
     ms = moe._binding._meta_struct(meta)
 
-    def call(i, ev=None):
-        if ev:
-            ev[0].record()
-        L.moe_route(logits[i % sets].data_ptr(), n, E, k, 0, indx.data_ptr(), vals.data_ptr(),
-                    stream)
-        if ev:
-            ev[1].record()
-        L.moe_build_metadata(indx.data_ptr(), vals.data_ptr(), n, E, k, ctypes.byref(ms),
-                             ws.data_ptr(), ws.numel(), stream)
-        if ev:
-            ev[2].record()
+    def stream():
+        return ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
 
-    for i in range(5):
-        call(i)
-    torch.cuda.synchronize()
-    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(steps)]
-    for i in range(steps):
-        call(5 + i, ev[i])
-    torch.cuda.synchronize()
+    def route(i):
+        L.moe_route(logits[i % sets].data_ptr(), n, E, k, 0, indx.data_ptr(), vals.data_ptr(),
+                    stream())
+
+    def metadata(i):
+        L.moe_build_metadata(indx.data_ptr(), vals.data_ptr(), n, E, k, ctypes.byref(ms),
+                             ws.data_ptr(), ws.numel(), stream())
+
+    def both(i):
+        route(i)
+        metadata(i)
+
+    reps = 2 * sets
+    route_ms = graph_time_ms(route, reps)
+    both_ms = graph_time_ms(both, reps)
+    meta_ms = graph_time_ms(metadata, reps)   # same indices each call (L2-warm input)
     assert moe.read_status(ws) == 0
-    route_ms = sum(e[0].elapsed_time(e[1]) for e in ev) / steps
-    meta_ms = sum(e[1].elapsed_time(e[2]) for e in ev) / steps
-    total_us = (route_ms + meta_ms) * 1e3
+    total_us = both_ms * 1e3
     w = stage_work(I.LayerCase("routing", n=n, H=64, E=E, k=k, I=64))
     alg = n * E * 4 + n * k * (4 + 2 + 4 + 4 + 2) + (2 * E + 1) * 4
-    return {"workload": f"route+metadata n{n} E{E} k{k} (fp32 N(0,1) logits, {sets} rotated sets)",
+    return {"workload": f"route+metadata n{n} E{E} k{k} (fp32 N(0,1) logits, {sets} rotated "
+                        f"sets; CUDA-graph replay of {reps} calls)",
             "us_per_call": round(total_us, 3), "route_us": round(route_ms * 1e3, 3),
-            "metadata_us": round(meta_ms * 1e3, 3), "algorithmic_bytes": alg,
+            "metadata_us_warm_input": round(meta_ms * 1e3, 3), "algorithmic_bytes": alg,
             "achieved_gbs": round(alg / (total_us * 1e-6) / 1e9, 1),
             "frac_of_hbm": round(alg / (total_us * 1e-6) / 1e9 / pk["hbm_gbs"], 4),
             "frac_of_8tbs": round(alg / (total_us * 1e-6) / 8e12, 4),
-            "route_roofline": roofline_entry("hbm", w["route"][1], route_ms * 1e-3, pk, source),
-            "metadata_roofline": roofline_entry("hbm", w["metadata"][1], meta_ms * 1e-3, pk,
-                                                source)}
+            "route_roofline": roofline_entry("hbm", w["route"][1], route_ms * 1e-3, pk, source)}
+
+
+def time_layer_graph(dc, reps, pk, source):
+    """Whole-layer steps replayed from a CUDA graph (stage events captured as
+    event-record nodes): for workloads whose step is too short for eager
+    launches to keep the GPU busy."""
+    import torch
+    import mixture_experts_routing_warp_gb300 as moe
+    c = dc.c
+    S = len(moe.STAGES)
+    events = [[torch.cuda.Event(enable_timing=True) for _ in range(S + 1)] for _ in range(reps)]
+    for ev in events:
+        for e in ev:
+            e.record()
+    torch.cuda.synchronize()
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        for i in range(3):
+            moe.forward(*dc.args(i), c.k, dc.params, dc.ws, out=dc.out)
+    torch.cuda.current_stream().wait_stream(s)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        for i in range(reps):
+            moe.forward_timed(*dc.args(i), c.k, dc.params, dc.ws, events[i], out=dc.out)
+    g.replay()
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record()
+    g.replay()
+    b.record()
+    torch.cuda.synchronize()
+    total_ms = a.elapsed_time(b) / reps
+    stage_ms = {name: sum(ev[j].elapsed_time(ev[j + 1]) for ev in events) / reps
+                for j, name in enumerate(moe.STAGES)}
+    assert moe.read_status(dc.ws) == 0
+    work = stage_work(c)
+    dom = max(stage_ms, key=stage_ms.get)
+    roof = roofline_entry(work[dom][0], work[dom][1], stage_ms[dom] * 1e-3, pk, source)
+    roof["kernel"] = dom
+    del g
+    return {"workload": c.name, "tokens_per_s": round(c.n / (total_ms * 1e-3), 1),
+            "ms_per_step": round(total_ms, 4), "timing": f"CUDA-graph replay of {reps} steps",
+            "stage_ms": {k: round(v, 4) for k, v in stage_ms.items()}, "roofline": roof}
 
 
 # ------------------------------------------------------------ CPU arm --
@@ -465,6 +541,12 @@ def run_ours(args, rank, world, local, pg):
     pk, source = peaks()
     c = WORKLOADS[args.workload]
     dc = DeviceCase(c, device, l2, rank)
+    if args.profile_only:
+        total_ms, _ = time_layer(dc, args.steps, args.warmup, pg, None, timed_stages=False)
+        if rank == 0:
+            print(json.dumps({"profile_only": True, "workload": c.name,
+                              "ms_per_step": round(total_ms / args.steps, 4)}), flush=True)
+        return 0
     sampler = ClockSampler(local)
     sampler.start()
     total_ms, stage_ms = time_layer(dc, args.steps, args.warmup, pg, sampler)
@@ -502,23 +584,15 @@ def run_ours(args, rank, world, local, pg):
                        "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                        "ms_per_step": round(e2e_ms, 4)}
         if not args.no_extras:
-            also = {"routing_metadata_16k": time_routing(16384, 128, 4, 200, device, l2, pk,
-                                                         source)}
-            also["routing_metadata_16k_e32"] = time_routing(16384, 32, 4, 200, device, l2, pk,
-                                                            source)
-            if args.workload != "minimind_e4":
-                mm = DeviceCase(I.MINIMIND_E4, device, l2)
-                mms, mstage = time_layer(mm, 50, 5, None)
-                mdom = max(mstage, key=mstage.get)
-                mwork = stage_work(I.MINIMIND_E4)
-                mroof = roofline_entry(mwork[mdom][0], mwork[mdom][1], mstage[mdom] * 1e-3, pk,
-                                       source)
-                mroof["kernel"] = mdom
-                also["minimind_e4"] = {"tokens_per_s": round(I.MINIMIND_E4.n / (mms / 50e3), 1),
-                                       "ms_per_step": round(mms / 50, 4),
-                                       "stage_ms": {k: round(v, 4) for k, v in mstage.items()},
-                                       "roofline": mroof}
-                del mm
+            also = {"routing_metadata_16k_e128": time_routing(16384, 128, 4, device, l2, pk,
+                                                              source),
+                    "routing_metadata_16k_e32": time_routing(16384, 32, 4, device, l2, pk,
+                                                             source)}
+            for name in ("minimind_e4", "minimind_e16"):
+                if WORKLOADS[name] != c:
+                    mm = DeviceCase(WORKLOADS[name], device, l2)
+                    also[name] = time_layer_graph(mm, 64, pk, source)
+                    del mm
             line["also"] = also
         if not args.no_cpu_baseline:
             line["cpu_baseline"] = oracle_sample(c, oracle_inputs(c))
