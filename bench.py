@@ -190,13 +190,19 @@ def stage_work(c: I.LayerCase) -> dict:
     }
 
 
-def roofline_entry(bound, work, seconds, pk, source):
+def roofline_entry(bound, work, seconds, pk, source, sustained=False):
+    """achieved = algorithmic work per launch / mean launch time. A tensor
+    kernel timed inside a long loop of steps (power cap engaged) is set
+    against the measured sustained bf16 peak, one timed in short bursts
+    against the burst peak; frac_of_burst is given either way."""
     if bound == "tensor":
         achieved = work / seconds / 1e12
-        return {"bound": "tensor", "achieved": round(achieved, 2),
-                "peak": pk["bf16_tflops"], "unit": "TFLOP/s",
-                "frac": round(achieved / pk["bf16_tflops"], 4),
-                "peak_source": f"bf16_tflops ({source}, burst)"}
+        peak = pk["bf16_tflops_sustained"] if sustained else pk["bf16_tflops"]
+        return {"bound": "tensor", "achieved": round(achieved, 2), "peak": peak,
+                "unit": "TFLOP/s", "frac": round(achieved / peak, 4),
+                "frac_of_burst": round(achieved / pk["bf16_tflops"], 4),
+                "peak_source": f"{'bf16_tflops_sustained' if sustained else 'bf16_tflops'} "
+                               f"({source}, {'sustained' if sustained else 'burst'})"}
     achieved = work / seconds / 1e9
     return {"bound": "hbm", "achieved": round(achieved, 1), "peak": pk["hbm_gbs"], "unit": "GB/s",
             "frac": round(achieved / pk["hbm_gbs"], 4), "peak_source": f"hbm_gbs ({source})"}
@@ -560,7 +566,8 @@ def run_ours(args, rank, world, local, pg):
     work = stage_work(c)
     dom = max(stage_ms, key=stage_ms.get)
     bound, w = work[dom]
-    roof = roofline_entry(bound, w, stage_ms[dom] * 1e-3, pk, source)
+    roof = roofline_entry(bound, w, stage_ms[dom] * 1e-3, pk, source,
+                          sustained=total_ms > 100.0)
     roof["kernel"] = dom
     roof["traffic"] = ncu_traffic(dom, args.workload)
     kernels_per_step = 5 + (1 if c.k > 1 else 0)

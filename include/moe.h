@@ -245,8 +245,8 @@ moe_status moe_forward(const uint16_t *x, const float *logits, const uint16_t *w
  * handles (created by the caller); events[i] is recorded on `stream` just
  * before stage i's kernel and events[MOE_STAGE_COUNT] after the last one,
  * so cudaEventElapsedTime(events[i], events[i+1]) is stage i's device time.
- * The records are external (cudaEventRecordExternal): inside a stream
- * capture they become event-record nodes of the graph.
+ * While `stream` is capturing, the records are external
+ * (cudaEventRecordExternal), i.e. event-record nodes of the graph.
  * n_events must be MOE_STAGE_COUNT + 1. Same results as moe_forward. */
 moe_status moe_forward_timed(const uint16_t *x, const float *logits, const uint16_t *w13,
                              const uint16_t *w2, int64_t n, int32_t E, int32_t k, int32_t H,

@@ -579,16 +579,14 @@ cudaError_t launch_ffn(const uint16_t *x_sorted, const int32_t *offs, const int3
   a.ctrl = ctrl;
   a.timeout_ns = kWaitTimeoutNs;
 
-  if (ev_ffn && cudaEventRecordWithFlags(ev_ffn[0], s, cudaEventRecordExternal) != cudaSuccess)
-    return cudaErrorUnknown;
+  if (ev_ffn && record_stage_event(ev_ffn[0], s) != cudaSuccess) return cudaErrorUnknown;
   a.num_kb = H / BK;
   a.n_tiles = (I + BN / 2 - 1) / (BN / 2);  // each tile yields 128 h columns
   cudaError_t err = packed ? launch_gemm<EPI_ACT, true>(ta1, tb1, a, s)
                            : launch_gemm<EPI_ACT, false>(ta1, tb1, a, s);
   if (err != cudaSuccess) return err;
 
-  if (ev_ffn && cudaEventRecordWithFlags(ev_ffn[1], s, cudaEventRecordExternal) != cudaSuccess)
-    return cudaErrorUnknown;
+  if (ev_ffn && record_stage_event(ev_ffn[1], s) != cudaSuccess) return cudaErrorUnknown;
   a.num_kb = I / BK;
   a.n_tiles = (H + BN - 1) / BN;
   return launch_gemm<EPI_SCATTER, false>(ta2, tb2, a, s);

@@ -207,11 +207,9 @@ static moe_status forward_impl(const uint16_t *x, const float *logits, const uin
   uint16_t *y_flat = k == 1 ? out : ws_at<uint16_t>(workspace, L.y_flat);
   uint16_t *x_sorted = ws_at<uint16_t>(workspace, L.x_sorted);
   uint16_t *h = ws_at<uint16_t>(workspace, L.h);
-  // External records: inside a stream capture they become event-record nodes,
-  // so stage timing works for graph replays too.
-  auto mark = [&](int i) {
-    return ev ? cudaEventRecordWithFlags(ev[i], s, cudaEventRecordExternal) : cudaSuccess;
-  };
+  // Inside a stream capture the records become event-record nodes, so stage
+  // timing works for graph replays too.
+  auto mark = [&](int i) { return ev ? record_stage_event(ev[i], s) : cudaSuccess; };
 
   if (mark(MOE_STAGE_ROUTE) != cudaSuccess ||
       launch_route(logits, n, E, k, gating, indx, vals, s) != cudaSuccess)

@@ -143,6 +143,17 @@ __device__ __forceinline__ float activate(float g, float u, const ActParams &p) 
   return (g * (1.0f / (1.0f + expf(-g)))) * u;
 }
 
+// Stage-timing event record: a plain record on an eager stream, an external
+// record (an event-record node of the graph) while the stream is capturing.
+inline cudaError_t record_stage_event(cudaEvent_t ev, cudaStream_t s) {
+  cudaStreamCaptureStatus st = cudaStreamCaptureStatusNone;
+  cudaError_t err = cudaStreamIsCapturing(s, &st);
+  if (err != cudaSuccess) return err;
+  return st == cudaStreamCaptureStatusActive
+             ? cudaEventRecordWithFlags(ev, s, cudaEventRecordExternal)
+             : cudaEventRecord(ev, s);
+}
+
 // ----------------------------------------------------- kernel launchers --
 // launch_ffn records ev_ffn[0] before the w13 kernel and ev_ffn[1] before the
 // w2 kernel when ev_ffn is given (stage timing of moe_forward_timed).
