@@ -56,6 +56,8 @@ WORKLOADS = {
     "skewed_n16384": I.SKEWED,
 }
 DEFAULT_WORKLOAD = "gptoss_prefill_n8192"
+# routing-only workloads (--profile-only): one moe_route_metadata call per step
+ROUTING_WORKLOADS = {"routing_n16384_e128": (16384, 128, 4), "routing_n16384_e32": (16384, 32, 4)}
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
 
@@ -70,7 +72,8 @@ def parse_args():
     p.add_argument("--steps", type=int, default=200)
     p.add_argument("--warmup", type=int, default=5)
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    p.add_argument("--workload", choices=sorted(WORKLOADS), default=DEFAULT_WORKLOAD)
+    p.add_argument("--workload", choices=sorted(WORKLOADS) + sorted(ROUTING_WORKLOADS),
+                   default=DEFAULT_WORKLOAD)
     p.add_argument("--no-extras", action="store_true", help="skip the routing / MiniMind extras")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--profile-only", action="store_true",
@@ -403,20 +406,21 @@ def time_routing(n, E, k, device, l2_bytes, pk, source):
         L.moe_build_metadata(indx.data_ptr(), vals.data_ptr(), n, E, k, ctypes.byref(ms),
                              ws.data_ptr(), ws.numel(), stream())
 
-    def both(i):
-        route(i)
-        metadata(i)
+    def fused(i):
+        L.moe_route_metadata(logits[i % sets].data_ptr(), n, E, k, 0, indx.data_ptr(),
+                             vals.data_ptr(), ctypes.byref(ms), ws.data_ptr(), ws.numel(),
+                             stream())
 
     reps = 2 * sets
     route_ms = graph_time_ms(route, reps)
-    both_ms = graph_time_ms(both, reps)
+    both_ms = graph_time_ms(fused, reps)
     meta_ms = graph_time_ms(metadata, reps)   # same indices each call (L2-warm input)
     assert moe.read_status(ws) == 0
     total_us = both_ms * 1e3
     w = stage_work(I.LayerCase("routing", n=n, H=64, E=E, k=k, I=64))
     alg = n * E * 4 + n * k * (4 + 2 + 4 + 4 + 2) + (2 * E + 1) * 4
-    return {"workload": f"route+metadata n{n} E{E} k{k} (fp32 N(0,1) logits, {sets} rotated "
-                        f"sets; CUDA-graph replay of {reps} calls)",
+    return {"workload": f"moe_route_metadata n{n} E{E} k{k} (fp32 N(0,1) logits, {sets} "
+                        f"rotated sets; CUDA-graph replay of {reps} calls)",
             "us_per_call": round(total_us, 3), "route_us": round(route_ms * 1e3, 3),
             "metadata_us_warm_input": round(meta_ms * 1e3, 3), "algorithmic_bytes": alg,
             "achieved_gbs": round(alg / (total_us * 1e-6) / 1e9, 1),
@@ -536,6 +540,25 @@ def run_reference(args, rank, world, pg):
     return 0
 
 
+def profile_routing(args, device, l2):
+    """--profile-only on a routing workload: warm-up + timed moe_route_metadata calls."""
+    import torch
+    import mixture_experts_routing_warp_gb300 as moe
+    n, E, k = ROUTING_WORKLOADS[args.workload]
+    sets = max(2, min(64, -(-2 * l2 // (n * E * 4))))
+    logits = [torch.from_numpy(I.route_logits(n, E, seed=s)).to(device) for s in range(sets)]
+    ws = moe.workspace(n, E, k, 64, 64, device)
+    meta = moe.empty_meta(n * k, E, device)
+    topk = (torch.empty((n, k), dtype=torch.int32, device=device),
+            torch.empty((n, k), dtype=torch.bfloat16, device=device))
+    for i in range(args.warmup + args.steps):
+        moe.route_metadata(logits[i % sets], k, ws=ws, meta=meta, topk=topk)
+    torch.cuda.synchronize()
+    assert moe.read_status(ws) == 0
+    print(json.dumps({"profile_only": True, "workload": args.workload}), flush=True)
+    return 0
+
+
 def run_ours(args, rank, world, local, pg):
     import torch
     import mixture_experts_routing_warp_gb300 as moe
@@ -545,6 +568,10 @@ def run_ours(args, rank, world, local, pg):
     props = torch.cuda.get_device_properties(device)
     l2 = int(getattr(props, "L2_cache_size", 0) or 132 * 1024 * 1024)
     pk, source = peaks()
+    if args.workload in ROUTING_WORKLOADS:
+        if not args.profile_only:
+            raise SystemExit("routing workloads are for --profile-only runs")
+        return profile_routing(args, device, l2)
     c = WORKLOADS[args.workload]
     dc = DeviceCase(c, device, l2, rank)
     if args.profile_only:

@@ -169,6 +169,18 @@ moe_status moe_build_metadata(const int32_t *topk_indx, const uint16_t *topk_val
                               int32_t E, int32_t k, const moe_routing_meta *meta,
                               void *workspace, size_t workspace_bytes, moe_stream stream);
 
+/* Stages 1 + 2 in one call -- moe_route followed by moe_build_metadata,
+ * same results bit for bit ([R1] 实现拆解 / 关键源码片段: the metadata is
+ * built once from the top-k result, with no second pass). Runs as one
+ * cooperative kernel (staged logit rows, shared-memory histogram, bounded
+ * grid barrier, stable scatter) when each SM's share of the slots fits in
+ * shared memory, else as the two kernels. Workspace as for
+ * moe_build_metadata. */
+moe_status moe_route_metadata(const float *logits, int64_t n, int32_t E, int32_t k,
+                              int32_t gating, int32_t *topk_indx, uint16_t *topk_vals,
+                              const moe_routing_meta *meta, void *workspace,
+                              size_t workspace_bytes, moe_stream stream);
+
 /* Stage 2 without a workspace -- the paper has no counterpart to this call;
  * it exists for callers that cannot give the library any device memory of
  * their own: a plugin that must enqueue into a framework whose allocator

@@ -8,10 +8,10 @@ the C ABI of include/moe.h. This package is the thin Python binding
 """
 from ._binding import (ACT, GATING, LAYOUT, MoEError, MoeParams, RoutingMeta, build_metadata,
                        STAGES, combine, empty_meta, forward, forward_timed, grouped_ffn, lib, library_path, make_params,
-                       read_status, route, selftest_wait_timeout, status_string, workspace,
+                       read_status, route, route_metadata, selftest_wait_timeout, status_string, workspace,
                        workspace_size)
 
 __all__ = ["ACT", "GATING", "LAYOUT", "MoEError", "MoeParams", "RoutingMeta", "build_metadata",
            "STAGES", "combine", "empty_meta", "forward", "forward_timed", "grouped_ffn", "lib", "library_path",
-           "make_params", "read_status", "route", "selftest_wait_timeout", "status_string",
+           "make_params", "read_status", "route", "route_metadata", "selftest_wait_timeout", "status_string",
            "workspace", "workspace_size"]

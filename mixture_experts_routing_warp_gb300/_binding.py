@@ -59,6 +59,7 @@ SIGNATURES = {
     "moe_workspace_init": (_I32, [_P, _SZ, _P]),
     "moe_route": (_I32, [_P, _I64, _I32, _I32, _I32, _P, _P, _P]),
     "moe_build_metadata": (_I32, [_P, _P, _I64, _I32, _I32, _PM, _P, _SZ, _P]),
+    "moe_route_metadata": (_I32, [_P, _I64, _I32, _I32, _I32, _P, _P, _PM, _P, _SZ, _P]),
     "moe_build_metadata_noalloc": (_I32, [_P, _P, _I64, _I32, _I32, _PM, _P, _P]),
     "moe_grouped_ffn": (_I32, [_P, _PM, _P, _P, _I64, _I32, _I32, _I32, _I32, _PP, _P, _P, _SZ,
                                _P]),
@@ -194,6 +195,24 @@ def build_metadata(topk_indx: torch.Tensor, topk_vals: torch.Tensor, E: int,
                                     ctypes.byref(_meta_struct(m)), _ptr(ws), ws.numel(),
                                     _stream(topk_indx.device)), "moe_build_metadata")
     return m
+
+
+def route_metadata(logits: torch.Tensor, k: int, E: Optional[int] = None,
+                   gating: str = "softmax_topk", ws: Optional[torch.Tensor] = None,
+                   meta: Optional[dict] = None, topk: Optional[tuple] = None):
+    """Stages 1 + 2 in one call -> (topk_indx, topk_vals, meta dict)."""
+    _need(logits, "logits", torch.float32)
+    n, E = logits.shape
+    if ws is None:
+        ws = workspace(max(n, 1), E, k, 64, 64, logits.device)
+    indx, vals = topk if topk is not None else (
+        torch.empty((n, k), dtype=torch.int32, device=logits.device),
+        torch.empty((n, k), dtype=torch.bfloat16, device=logits.device))
+    m = meta if meta is not None else empty_meta(n * k, E, logits.device)
+    _check(lib().moe_route_metadata(_ptr(logits), n, E, k, GATING[gating], _ptr(indx), _ptr(vals),
+                                    ctypes.byref(_meta_struct(m)), _ptr(ws), ws.numel(),
+                                    _stream(logits.device)), "moe_route_metadata")
+    return indx, vals, m
 
 
 def grouped_ffn(x: torch.Tensor, meta: dict, w13: torch.Tensor, w2: torch.Tensor, k: int,

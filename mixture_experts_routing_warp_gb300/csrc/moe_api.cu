@@ -111,7 +111,7 @@ moe_status moe_route(const float *logits, int64_t n, int32_t E, int32_t k, int32
   if (!logits || !topk_indx || !topk_vals) return MOE_ERR_INVALID_ARG;
   if (!aligned(logits, 4) || !aligned(topk_indx, 4) || !aligned(topk_vals, 2))
     return MOE_ERR_MISALIGNED;
-  return from_cuda(launch_route(logits, n, E, k, gating, topk_indx, topk_vals,
+  return from_cuda(launch_route(logits, n, E, k, gating, topk_indx, topk_vals, nullptr,
                                 (cudaStream_t)stream));
 }
 
@@ -130,6 +130,33 @@ moe_status moe_build_metadata(const int32_t *topk_indx, const uint16_t *topk_val
   return from_cuda(launch_metadata(topk_indx, topk_vals, n, E, k, *meta,
                                    ws_at<int32_t>(workspace, L.hist),
                                    ws_at<uint32_t>(workspace, L.ctrl), (cudaStream_t)stream));
+}
+
+moe_status moe_route_metadata(const float *logits, int64_t n, int32_t E, int32_t k,
+                              int32_t gating, int32_t *topk_indx, uint16_t *topk_vals,
+                              const moe_routing_meta *meta, void *workspace,
+                              size_t workspace_bytes, moe_stream stream) {
+  moe_status st = check_sizes(n, E, k, 64, 64, false);
+  if (st != MOE_OK) return st;
+  if (gating != MOE_GATING_SOFTMAX_TOPK && gating != MOE_GATING_SOFTMAX_ALL)
+    return MOE_ERR_INVALID_ARG;
+  if ((st = check_meta(meta, n)) != MOE_OK) return st;
+  if (!workspace) return MOE_ERR_INVALID_ARG;
+  if (!aligned(workspace, kAlign)) return MOE_ERR_MISALIGNED;
+  const WorkspaceLayout L = workspace_layout(n, E, k, 64, 64);
+  if (workspace_bytes < L.topk_indx) return MOE_ERR_WORKSPACE_TOO_SMALL;
+  if (n > 0 && (!logits || !topk_indx || !topk_vals)) return MOE_ERR_INVALID_ARG;
+  if (!aligned(logits, 4) || !aligned(topk_indx, 4) || !aligned(topk_vals, 2))
+    return MOE_ERR_MISALIGNED;
+  cudaStream_t s = (cudaStream_t)stream;
+  int32_t *hist = ws_at<int32_t>(workspace, L.hist);
+  uint32_t *ctrl = ws_at<uint32_t>(workspace, L.ctrl);
+  if (n > 0 && route_metadata_fits(n, k))
+    return from_cuda(launch_route_metadata(logits, n, E, k, gating, topk_indx, topk_vals, *meta,
+                                           hist, ctrl, s));
+  if (launch_route(logits, n, E, k, gating, topk_indx, topk_vals, ctrl, s) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  return from_cuda(launch_metadata(topk_indx, topk_vals, n, E, k, *meta, hist, ctrl, s));
 }
 
 moe_status moe_grouped_ffn(const uint16_t *x, const moe_routing_meta *meta, const uint16_t *w13,
@@ -211,13 +238,22 @@ static moe_status forward_impl(const uint16_t *x, const float *logits, const uin
   // timing works for graph replays too.
   auto mark = [&](int i) { return ev ? record_stage_event(ev[i], s) : cudaSuccess; };
 
-  if (mark(MOE_STAGE_ROUTE) != cudaSuccess ||
-      launch_route(logits, n, E, k, gating, indx, vals, s) != cudaSuccess)
-    return MOE_ERR_CUDA;
-  if (mark(MOE_STAGE_METADATA) != cudaSuccess ||
-      launch_metadata(indx, vals, n, E, k, m, ws_at<int32_t>(workspace, L.hist), ctrl, s) !=
-          cudaSuccess)
-    return MOE_ERR_CUDA;
+  int32_t *hist = ws_at<int32_t>(workspace, L.hist);
+  if (route_metadata_fits(n, k)) {
+    // one cooperative kernel for both stages; the metadata stage time is 0
+    if (mark(MOE_STAGE_ROUTE) != cudaSuccess ||
+        launch_route_metadata(logits, n, E, k, gating, indx, vals, m, hist, ctrl, s) !=
+            cudaSuccess ||
+        mark(MOE_STAGE_METADATA) != cudaSuccess)
+      return MOE_ERR_CUDA;
+  } else {
+    if (mark(MOE_STAGE_ROUTE) != cudaSuccess ||
+        launch_route(logits, n, E, k, gating, indx, vals, ctrl, s) != cudaSuccess)
+      return MOE_ERR_CUDA;
+    if (mark(MOE_STAGE_METADATA) != cudaSuccess ||
+        launch_metadata(indx, vals, n, E, k, m, hist, ctrl, s) != cudaSuccess)
+      return MOE_ERR_CUDA;
+  }
   if (mark(MOE_STAGE_GATHER) != cudaSuccess ||
       launch_gather_rows(x, m.col_sorted, N, k, H, x_sorted, s) != cudaSuccess)
     return MOE_ERR_CUDA;

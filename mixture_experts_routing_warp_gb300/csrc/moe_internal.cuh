@@ -43,7 +43,7 @@ inline WorkspaceLayout workspace_layout(int64_t n, int E, int k, int H, int I) {
   size_t o = 0;
   auto take = [&](size_t bytes) { size_t at = o; o = align_up(o + bytes, kAlign); return at; };
   L.ctrl = take(kCtrlBytes);
-  L.hist = take((size_t)kMetaMaxCtas * (size_t)E * 4);
+  L.hist = take((size_t)kMetaMaxCtas * (size_t)((E + 3) & ~3) * 4);  // rows padded to 4
   L.topk_indx = take(N * 4);
   L.topk_vals = take(N * 2);
   L.col_sum = take((size_t)E * 4);
@@ -75,8 +75,10 @@ __device__ __forceinline__ void st_release_gpu(uint32_t *p, uint32_t v) {
   asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
 }
 
+// Sticky first error in the control block (no-op without one, as for
+// moe_route, which takes no workspace).
 __device__ __forceinline__ void record_status(uint32_t *ctrl, moe_status s) {
-  atomicCAS(ctrl + kCtrlStatus, (uint32_t)MOE_OK, (uint32_t)s);
+  if (ctrl) atomicCAS(ctrl + kCtrlStatus, (uint32_t)MOE_OK, (uint32_t)s);
 }
 
 // Grid-wide barrier for a cooperative launch, bounded by `timeout_ns`.
@@ -161,7 +163,16 @@ inline cudaError_t record_stage_event(cudaEvent_t ev, cudaStream_t s) {
 int device_sm_count();
 
 cudaError_t launch_route(const float *logits, int64_t n, int E, int k, int gating,
-                         int32_t *topk_indx, uint16_t *topk_vals, cudaStream_t s);
+                         int32_t *topk_indx, uint16_t *topk_vals, uint32_t *ctrl,
+                         cudaStream_t s);
+
+// Fused route + metadata (one cooperative kernel) for moe_forward, when
+// route_metadata_fits(n, k).
+bool route_metadata_fits(int64_t n, int k);
+cudaError_t launch_route_metadata(const float *logits, int64_t n, int E, int k, int gating,
+                                  int32_t *topk_indx, uint16_t *topk_vals,
+                                  const moe_routing_meta &meta, int32_t *ws_hist,
+                                  uint32_t *ctrl, cudaStream_t s);
 
 cudaError_t launch_metadata(const int32_t *topk_indx, const uint16_t *topk_vals, int64_t n, int E,
                             int k, const moe_routing_meta &meta, int32_t *ws_hist,

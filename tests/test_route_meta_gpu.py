@@ -134,3 +134,28 @@ def test_run_to_run_bit_identical():
                                else ma[key],
                                mb[key].view(torch.int16) if mb[key].dtype == torch.bfloat16
                                else mb[key]), key
+
+
+@pytest.mark.parametrize("n,E,k", [(16384, 128, 4), (4096, 32, 4), (33, 8, 2), (1, 4, 1),
+                                   (777, 100, 5), (5000, 7, 3), (3000, 256, 8),
+                                   (600_000, 16, 4)])
+@pytest.mark.parametrize("gating", ["softmax_topk", "softmax_all"])
+def test_route_metadata_equals_route_then_build(n, E, k, gating):
+    """The fused call (one cooperative kernel when each SM's slots fit in
+    shared memory, else two kernels) gives the two-call result bit for bit."""
+    logits = dev(I.route_logits(n, E, seed=n % 97, tie_heavy=True))
+    i1, v1 = moe.route(logits, k, gating)
+    ws1 = moe.workspace(n, E, k, 64, 64)
+    m1 = moe.build_metadata(i1, v1, E, ws1)
+    i2, v2, m2 = moe.route_metadata(logits, k, gating=gating)
+    torch.cuda.synchronize()
+    assert torch.equal(i1, i2)
+    assert torch.equal(v1.view(torch.int16), v2.view(torch.int16))
+    for key in m1:
+        a, b = m1[key], m2[key]
+        if a.dtype == torch.bfloat16:
+            a, b = a.view(torch.int16), b.view(torch.int16)
+        assert torch.equal(a, b), key
+    if n <= 20000:
+        ref_i, _ = oracle.route(logits.cpu().numpy(), k, gating)
+        np.testing.assert_array_equal(i2.cpu().numpy(), ref_i)
