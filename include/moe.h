@@ -142,7 +142,7 @@ const char *moe_status_string(moe_status status);
 size_t moe_workspace_size(int64_t n, int32_t E, int32_t k, int32_t H, int32_t I);
 
 /* Prepare a freshly allocated workspace: zero its control block (the first
- * 4 KB: status word and grid-barrier counters). Must run once, in stream
+ * 4 KB: status word and the grid-barrier counter). Must run once, in stream
  * order, before the workspace's first use; later calls leave the block
  * consistent. */
 moe_status moe_workspace_init(void *workspace, size_t workspace_bytes, moe_stream stream);
@@ -172,8 +172,8 @@ moe_status moe_build_metadata(const int32_t *topk_indx, const uint16_t *topk_val
 /* Stages 1 + 2 in one call -- moe_route followed by moe_build_metadata,
  * same results bit for bit ([R1] 实现拆解 / 关键源码片段: the metadata is
  * built once from the top-k result, with no second pass). Runs as one
- * cooperative kernel (staged logit rows, shared-memory histogram, bounded
- * grid barrier, stable scatter) when each SM's share of the slots fits in
+ * cooperative kernel (G lanes per token, shared-memory histogram, bounded
+ * grid barrier, cross-CTA prefix, stable scatter) when each SM's share of the slots fits in
  * shared memory, else as the two kernels. Workspace as for
  * moe_build_metadata. */
 moe_status moe_route_metadata(const float *logits, int64_t n, int32_t E, int32_t k,
@@ -269,8 +269,10 @@ moe_status moe_forward_timed(const uint16_t *x, const float *logits, const uint1
                              moe_stream stream);
 
 /* DEBUG ONLY -- synchronises `stream`, returns the status word recorded by
- * device-side bounded waits since the last reset (MOE_OK if none), and
- * resets it and the barrier counters when `reset` is non-zero. */
+ * device-side bounded waits since the last reset (MOE_OK if none). With
+ * `reset` non-zero it also zeroes the control block (status word and the
+ * grid-barrier counter), which a workspace needs after a MOE_ERR_TIMEOUT
+ * before it can be used again. */
 moe_status moe_read_status(void *workspace, size_t workspace_bytes, int32_t reset,
                            moe_stream stream);
 
@@ -278,7 +280,7 @@ moe_status moe_read_status(void *workspace, size_t workspace_bytes, int32_t rese
  * bounded device-side wait, on a control word that nothing ever sets. After
  * `timeout_ns` (1 .. 1e9) the wait gives up, records MOE_ERR_TIMEOUT in the
  * status word and the kernel returns: the error path of every bounded wait
- * (the metadata kernel's grid barrier uses the same one), exercised without
+ * (the metadata kernels' grid barrier is bounded the same way), exercised without
  * a fault or a hang. Read the result with moe_read_status. */
 moe_status moe_selftest_wait_timeout(void *workspace, size_t workspace_bytes, uint64_t timeout_ns,
                                      moe_stream stream);

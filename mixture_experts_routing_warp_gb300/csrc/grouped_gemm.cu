@@ -186,13 +186,13 @@ __device__ __forceinline__ void tmem_wait_ld() {
 __device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity,
                                              volatile int *abort_flag, const GemmArgs &a) {
   if (mbar_try_wait(bar, parity)) return true;
-  const unsigned long long t0 = global_timer_ns();
+  const long long deadline = wait_deadline(a.timeout_ns);
   uint32_t spins = 0;
   while (true) {
     if (mbar_try_wait(bar, parity)) return true;
     if ((++spins & 15u) == 0) {
       if (*abort_flag) return false;
-      if (global_timer_ns() - t0 > a.timeout_ns) {
+      if (clock64() > deadline) {
         *abort_flag = 1;
         record_status(a.ctrl, MOE_ERR_TIMEOUT);
         return false;
@@ -204,9 +204,9 @@ __device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity,
 // Bounded wait used while draining, independent of the abort flag.
 __device__ __forceinline__ void wait_drain(uint32_t bar, uint32_t parity,
                                            unsigned long long timeout_ns) {
-  const unsigned long long t0 = global_timer_ns();
+  const long long deadline = wait_deadline(timeout_ns);
   while (!mbar_try_wait(bar, parity))
-    if (global_timer_ns() - t0 > timeout_ns) return;
+    if (clock64() > deadline) return;
 }
 
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {

@@ -299,7 +299,7 @@ moe_status moe_read_status(void *workspace, size_t workspace_bytes, int32_t rese
   if (cudaStreamSynchronize(s) != cudaSuccess) return MOE_ERR_CUDA;
   if (cudaMemcpy(&word, workspace, sizeof word, cudaMemcpyDeviceToHost) != cudaSuccess)
     return MOE_ERR_CUDA;
-  if (reset) {
+  if (reset) {  // status word and grid-barrier counter back to zero
     if (cudaMemsetAsync(workspace, 0, kCtrlBytes, s) != cudaSuccess) return MOE_ERR_CUDA;
     if (cudaStreamSynchronize(s) != cudaSuccess) return MOE_ERR_CUDA;
   }

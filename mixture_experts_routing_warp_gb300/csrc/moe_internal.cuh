@@ -19,8 +19,8 @@ constexpr size_t kAlign = 256;
 
 // Control block words (uint32 index into the control block).
 constexpr int kCtrlStatus = 0;           // sticky moe_status from device-side waits
-constexpr int kCtrlBarArrive = 32;       // grid barrier: arrivals of the current round
-constexpr int kCtrlBarGen = 64;          // grid barrier: generation, bumped per round
+constexpr int kCtrlBarArrive = 32;       // grid barrier counter (top bit flips per barrier)
+constexpr int kCtrlNeverSet = 96;        // a word no kernel writes (bounded-wait self-test)
 
 // Default limit of a device-side wait (ns). Legitimate waits last microseconds.
 constexpr unsigned long long kWaitTimeoutNs = 1000000000ull;
@@ -59,20 +59,17 @@ inline WorkspaceLayout workspace_layout(int64_t n, int E, int k, int H, int I) {
 }
 
 // ------------------------------------------------------- device helpers --
-__device__ __forceinline__ unsigned long long global_timer_ns() {
-  unsigned long long t;
-  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
-  return t;
-}
-
 __device__ __forceinline__ uint32_t ld_acquire_gpu(const uint32_t *p) {
   uint32_t v;
   asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
   return v;
 }
 
-__device__ __forceinline__ void st_release_gpu(uint32_t *p, uint32_t v) {
-  asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+__device__ __forceinline__ uint32_t atom_add_release_gpu(uint32_t *p, uint32_t v) {
+  uint32_t old;
+  asm volatile("atom.add.release.gpu.global.u32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v)
+               : "memory");
+  return old;
 }
 
 // Sticky first error in the control block (no-op without one, as for
@@ -81,37 +78,43 @@ __device__ __forceinline__ void record_status(uint32_t *ctrl, moe_status s) {
   if (ctrl) atomicCAS(ctrl + kCtrlStatus, (uint32_t)MOE_OK, (uint32_t)s);
 }
 
+// Deadline of a bounded wait in SM clock cycles: timeout_ns at 3 cycles/ns,
+// so the real limit is at least timeout_ns (clocks <= 2.1 GHz) and at most
+// 3x it at low clocks. clock64 is a cheap per-SM counter; reading it costs
+// nothing like %globaltimer, so it is only sampled after a poll misses.
+__device__ __forceinline__ long long wait_deadline(unsigned long long timeout_ns) {
+  return clock64() + (long long)(timeout_ns * 3ull);
+}
+
 // Grid-wide barrier for a cooperative launch, bounded by `timeout_ns`.
-// Thread 0 of each CTA reads the generation, arrives; the last arrival
-// resets the arrival count and bumps the generation; the others wait for
-// the bump. Returns false (and records MOE_ERR_TIMEOUT) when the wait
-// gives up; the caller must then return without touching shared outputs.
+// Thread 0 of each CTA adds to one counter with release semantics: CTA 0
+// adds 2^31 - (gridDim.x - 1), the others 1, so when every CTA has arrived
+// the counter's top bit has flipped and its low bits are back where they
+// started (no reset step, and any grid size may use the same counter next
+// time). Each thread 0 then polls with acquire loads until the top bit
+// differs from the value its own add returned. Returns false (and records
+// MOE_ERR_TIMEOUT) when the wait gives up; the caller must then return
+// without touching shared outputs. After a timeout the counter is off and
+// later barriers on this workspace time out too, until the control block is
+// cleared (moe_read_status with reset).
 __device__ __forceinline__ bool grid_barrier(uint32_t *ctrl, unsigned long long timeout_ns) {
   __shared__ int s_ok;
   __syncthreads();
   if (threadIdx.x == 0) {
-    uint32_t *arrive = ctrl + kCtrlBarArrive;
-    uint32_t *gen = ctrl + kCtrlBarGen;
-    const uint32_t my_gen = ld_acquire_gpu(gen);
-    __threadfence();
-    const uint32_t ticket = atomicAdd(arrive, 1u);
+    uint32_t *ctr = ctrl + kCtrlBarArrive;
+    const uint32_t inc = blockIdx.x == 0 ? (0x80000000u - (gridDim.x - 1u)) : 1u;
+    const uint32_t old = atom_add_release_gpu(ctr, inc);
     int ok = 1;
-    if (ticket == gridDim.x - 1) {
-      atomicExch(arrive, 0u);
-      __threadfence();
-      st_release_gpu(gen, my_gen + 1);
-    } else {
-      const unsigned long long t0 = global_timer_ns();
-      while (ld_acquire_gpu(gen) == my_gen) {
-        if (global_timer_ns() - t0 > timeout_ns) {
+    if (((ld_acquire_gpu(ctr) ^ old) & 0x80000000u) == 0u) {
+      const long long deadline = wait_deadline(timeout_ns);
+      while (((ld_acquire_gpu(ctr) ^ old) & 0x80000000u) == 0u) {
+        if (clock64() > deadline) {
           ok = 0;
           record_status(ctrl, MOE_ERR_TIMEOUT);
           break;
         }
-        __nanosleep(64);
       }
     }
-    __threadfence();
     s_ok = ok;
   }
   __syncthreads();

@@ -29,28 +29,26 @@ int device_sm_count() {
 
 // ================================================================ route ==
 //
-// Router top-k, one warp per token. A CTA owns a contiguous block of tokens;
-// their logit rows are staged into shared memory with cp.async.bulk in
-// chunks of 32 tokens, one mbarrier per chunk, so warps start on the first
-// chunk while the others are still in flight. Lane l holds experts
-// [l*EPL, l*EPL + EPL) as 32-bit order keys (an order-preserving image of
-// the fp32 value: -0.0 folded onto +0.0, NaN = 1 below every number,
-// absent experts = 0). Each of the k rounds takes the warp maximum with
-// redux.sync; among lanes holding it the lowest lane (lowest expert ids)
-// wins, and within that lane the lowest slot, so equal logits go to the
-// lower expert id. Gate weights: softmax in fp32 over the k selected
-// (or over all E), rounded to bf16.
+// Router top-k. G consecutive lanes share a token (G = 1, 2, 4, 8 for E up
+// to 16, 32, 64, 256: at most 16 elements per lane up to E = 128, so that
+// enough warps are in flight to hide the compare chains): lane g of the
+// group loads the 16-byte
+// chunks g, g+G, g+2G, ... of the token's fp32 row (all its loads in flight
+// at once; the G lanes of a token read adjacent chunks), and keeps the K
+// largest 32-bit order keys (an order-preserving image of the value: -0.0
+// folded onto +0.0, NaN = 1 below every number) of its elements in
+// registers. Within a lane the elements arrive in ascending expert id and
+// a key enters only if strictly larger, so equal logits keep the lower id;
+// the lanes of a group then merge their lists in log2(G) shuffle steps,
+// ordering by (value descending, expert id ascending). Gate weights:
+// softmax in fp32 over the K selected (or over all E), rounded to bf16.
 
-constexpr int kRouteThreads = 512;
-constexpr int kRouteWarps = kRouteThreads / 32;
-constexpr int kChunkTok = 32;                 // tokens per staged chunk (one mbarrier)
-constexpr int kMaxChunks = 32;                // chunks per staging round
-constexpr int kStageBytes = 96 * 1024;        // staging buffer per CTA
-constexpr int kStagePad = 1024;               // vector over-read slack after the last row
-constexpr int kSlotCap = 8192;                // slots a fused CTA keeps in shared memory
+constexpr int kRouteThreads = 256;
+constexpr int kFusedThreads = 1024;
+constexpr int kSlotCap = 8192;  // slots a fused CTA keeps in shared memory
 
 __device__ __forceinline__ uint32_t order_key(float v) {
-  if (v != v) return 1u;                       // NaN: below every number, above "absent"
+  if (v != v) return 1u;                         // NaN: below every number
   const uint32_t u = __float_as_uint(v + 0.0f);  // -0.0 + 0.0 = +0.0: the two zeros tie
   return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
 }
@@ -59,266 +57,277 @@ __device__ __forceinline__ float key_to_float(uint32_t key) {
   return __uint_as_float((key & 0x80000000u) ? (key & 0x7fffffffu) : ~key);
 }
 
-// Tokens [r0, r0 + ntok) of one staging round: rows in smem (row j at
-// stage + j*E). Returns in lanes r < k the r-th expert and its weight.
-template <int EPL, bool VEC>
-__device__ __forceinline__ void topk_row(const float *row, int E, int k, int gating, int lane,
-                                         int &sel_e, float &sel_w) {
-  float v[EPL];
-  if (VEC && EPL >= 4) {
+template <int K>
+struct TopK {
+  uint32_t key[K];
+  int e[K];
+  __device__ __forceinline__ void init() {
 #pragma unroll
-    for (int q = 0; q < EPL / 4; ++q) {
-      const float4 x = reinterpret_cast<const float4 *>(row + lane * EPL)[q];
-      v[4 * q] = x.x;
-      v[4 * q + 1] = x.y;
-      v[4 * q + 2] = x.z;
-      v[4 * q + 3] = x.w;
+    for (int i = 0; i < K; ++i) {
+      key[i] = 0u;  // below every present element
+      e[i] = 0x7fffffff;
     }
-  } else if (VEC && EPL == 2) {
-    const float2 x = reinterpret_cast<const float2 *>(row + lane * 2)[0];
-    v[0] = x.x;
-    v[1] = x.y;
-  } else {
-#pragma unroll
-    for (int c = 0; c < EPL; ++c) v[c] = row[min(lane * EPL + c, E - 1)];
   }
-  uint32_t key[EPL];
-  uint32_t lmax = 0u;
+  // Elements arriving in ascending id: enter only if strictly larger.
+  __device__ __forceinline__ void push_ascending(uint32_t kv, int ev) {
+    if (kv > key[K - 1]) {
 #pragma unroll
-  for (int c = 0; c < EPL; ++c) {
-    key[c] = (lane * EPL + c < E) ? order_key(v[c]) : 0u;
-    lmax = max(lmax, key[c]);
-  }
-  uint32_t m0 = 0u, my_key = 0u;
-  int my_e = 0;
-  for (int r = 0; r < k; ++r) {
-    const uint32_t m = __reduce_max_sync(0xffffffffu, lmax);
-    const unsigned holders = __ballot_sync(0xffffffffu, lmax == m);
-    const int wl = __ffs(holders) - 1;
-    int e_sel = 0;
-    if (lane == wl) {
-      int cw = EPL - 1;
-#pragma unroll
-      for (int c = EPL - 1; c >= 0; --c)
-        if (key[c] == m) cw = c;
-      e_sel = lane * EPL + cw;
-      lmax = 0u;
-#pragma unroll
-      for (int c = 0; c < EPL; ++c) {
-        if (c == cw) key[c] = 0u;
-        lmax = max(lmax, key[c]);
+      for (int i = K - 1; i > 0; --i) {
+        const bool above = kv > key[i - 1];
+        const bool here = kv > key[i];
+        key[i] = above ? key[i - 1] : (here ? kv : key[i]);
+        e[i] = above ? e[i - 1] : (here ? ev : e[i]);
+      }
+      if (kv > key[0]) {
+        key[0] = kv;
+        e[0] = ev;
       }
     }
-    e_sel = __shfl_sync(0xffffffffu, e_sel, wl);
-    if (lane == r) {
-      my_e = e_sel;
-      my_key = m;
-    }
-    if (r == 0) m0 = m;
   }
-  const float v0 = key_to_float(m0);
-  const float num = lane < k ? expf(key_to_float(my_key) - v0) : 0.f;
-  float denom;
-  if (gating == MOE_GATING_SOFTMAX_TOPK) {
-    denom = num;  // lanes >= k hold 0; k <= 8
+  // Any order: (key descending, id ascending).
+  __device__ __forceinline__ static bool before(uint32_t ka, int ea, uint32_t kb, int eb) {
+    return ka > kb || (ka == kb && ea < eb);
+  }
+  __device__ __forceinline__ void push_any(uint32_t kv, int ev) {
+    if (before(kv, ev, key[K - 1], e[K - 1])) {
 #pragma unroll
-    for (int off = 4; off > 0; off >>= 1) denom += __shfl_xor_sync(0xffffffffu, denom, off);
+      for (int i = K - 1; i > 0; --i) {
+        const bool above = before(kv, ev, key[i - 1], e[i - 1]);
+        const bool here = before(kv, ev, key[i], e[i]);
+        key[i] = above ? key[i - 1] : (here ? kv : key[i]);
+        e[i] = above ? e[i - 1] : (here ? ev : e[i]);
+      }
+      if (before(kv, ev, key[0], e[0])) {
+        key[0] = kv;
+        e[0] = ev;
+      }
+    }
+  }
+};
+
+// Top-K of token row `row` (E fp32) by the G lanes of a group; lane g =
+// lane % G. On return every lane of the group holds the merged list and
+// the K gate weights. `valid` is uniform within a group.
+__device__ __forceinline__ unsigned long long pack_key(uint32_t key, int e) {
+  return ((unsigned long long)key << 32) | (uint32_t)~(uint32_t)e;
+}
+
+// compare-exchange: a gets the larger, b the smaller
+__device__ __forceinline__ void cx(unsigned long long &a, unsigned long long &b) {
+  const bool s = b > a;
+  const unsigned long long hi = s ? b : a, lo = s ? a : b;
+  a = hi;
+  b = lo;
+}
+
+__device__ __forceinline__ void sort4_desc(unsigned long long (&c)[4]) {
+  cx(c[0], c[1]);
+  cx(c[2], c[3]);
+  cx(c[0], c[2]);
+  cx(c[1], c[3]);
+  cx(c[1], c[2]);
+}
+
+// top <- the 4 largest of top (sorted) and o (sorted), sorted descending:
+// elementwise max of top and reversed o is bitonic; two half-cleaner stages.
+__device__ __forceinline__ void merge4_desc(unsigned long long (&top)[4],
+                                            const unsigned long long (&o)[4]) {
+#pragma unroll
+  for (int j = 0; j < 4; ++j) top[j] = top[j] > o[3 - j] ? top[j] : o[3 - j];
+  cx(top[0], top[2]);
+  cx(top[1], top[3]);
+  cx(top[0], top[1]);
+  cx(top[2], top[3]);
+}
+
+// vec4: rows are 16-byte aligned (E % 4 == 0 and a 16-byte aligned base),
+// so a chunk is one 128-bit load; otherwise four 32-bit loads.
+template <int K, int G, int NQ>  // NQ chunks of 4 elements per lane: NQ*4*G >= E
+__device__ __forceinline__ void topk_group(const float *__restrict__ row, bool valid, int E,
+                                           int gating, bool vec4, TopK<K> &tk, float (&w)[K]) {
+  const int lane = threadIdx.x & 31, g = lane % G;
+  tk.init();
+  const int nq = (E + 3) >> 2;  // chunks of 4 elements in the row
+  float4 x[NQ];
+  if (vec4) {
+#pragma unroll
+    for (int i = 0; i < NQ; ++i) {
+      const int q = i * G + g;
+      x[i] = (valid && q < nq) ? __ldg(reinterpret_cast<const float4 *>(row) + q)
+                               : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
   } else {
-    float s = 0.f;
 #pragma unroll
-    for (int c = 0; c < EPL; ++c)
-      if (lane * EPL + c < E) s += expf(v[c] - v0);
+    for (int i = 0; i < NQ; ++i) {
+      const int e0 = (i * G + g) * 4;
+      const bool ok = valid && e0 < E;
+      x[i].x = ok ? __ldg(row + e0) : 0.f;
+      x[i].y = ok && e0 + 1 < E ? __ldg(row + e0 + 1) : 0.f;
+      x[i].z = ok && e0 + 2 < E ? __ldg(row + e0 + 2) : 0.f;
+      x[i].w = ok && e0 + 3 < E ? __ldg(row + e0 + 3) : 0.f;
+    }
+  }
+  if constexpr (K <= 4) {
+    // Branch-free: packed keys ((order key << 32) | ~id) are unique and
+    // "larger" means (value descending, id ascending). Sort each chunk of 4
+    // with a 5-comparator network, then bitonic-merge the sorted 4-lists
+    // (inside the lane, then across the G lanes), keeping the top 4.
+    unsigned long long top[4];
 #pragma unroll
-    for (int off = 16; off > 0; off >>= 1) s += __shfl_xor_sync(0xffffffffu, s, off);
+    for (int i = 0; i < NQ; ++i) {
+      const int e0 = (i * G + g) * 4;
+      unsigned long long c[4];
+      c[0] = e0 < E ? pack_key(order_key(x[i].x), e0) : 0ull;
+      c[1] = e0 + 1 < E ? pack_key(order_key(x[i].y), e0 + 1) : 0ull;
+      c[2] = e0 + 2 < E ? pack_key(order_key(x[i].z), e0 + 2) : 0ull;
+      c[3] = e0 + 3 < E ? pack_key(order_key(x[i].w), e0 + 3) : 0ull;
+      sort4_desc(c);
+      if (i == 0) {
+#pragma unroll
+        for (int j = 0; j < 4; ++j) top[j] = c[j];
+      } else {
+        merge4_desc(top, c);
+      }
+    }
+#pragma unroll
+    for (int off = 1; off < G; off <<= 1) {
+      unsigned long long o[4];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) o[j] = __shfl_xor_sync(0xffffffffu, top[j], off);
+      merge4_desc(top, o);
+    }
+#pragma unroll
+    for (int j = 0; j < K; ++j) {
+      tk.key[j] = (uint32_t)(top[j] >> 32);
+      tk.e[j] = (int)~(uint32_t)top[j];
+    }
+  } else {
+#pragma unroll
+    for (int i = 0; i < NQ; ++i) {
+      const int e0 = (i * G + g) * 4;
+      if (e0 < E) {
+        tk.push_ascending(order_key(x[i].x), e0);
+        if (e0 + 1 < E) tk.push_ascending(order_key(x[i].y), e0 + 1);
+        if (e0 + 2 < E) tk.push_ascending(order_key(x[i].z), e0 + 2);
+        if (e0 + 3 < E) tk.push_ascending(order_key(x[i].w), e0 + 3);
+      }
+    }
+#pragma unroll
+    for (int off = 1; off < G; off <<= 1) {  // butterfly merge inside the group
+      uint32_t pk[K];
+      int pe[K];
+#pragma unroll
+      for (int i = 0; i < K; ++i) {
+        pk[i] = __shfl_xor_sync(0xffffffffu, tk.key[i], off);
+        pe[i] = __shfl_xor_sync(0xffffffffu, tk.e[i], off);
+      }
+#pragma unroll
+      for (int i = 0; i < K; ++i) tk.push_any(pk[i], pe[i]);
+    }
+  }
+  const float v0 = key_to_float(tk.key[0]);
+  float ex[K];
+  float denom = 0.f;
+#pragma unroll
+  for (int i = 0; i < K; ++i) {
+    ex[i] = expf(key_to_float(tk.key[i]) - v0);
+    denom += ex[i];
+  }
+  if (gating == MOE_GATING_SOFTMAX_ALL) {
+    float s = 0.f;  // this lane's elements, ascending chunks, then a fixed tree
+#pragma unroll
+    for (int i = 0; i < NQ; ++i) {
+      const int e0 = (i * G + g) * 4;
+      if (e0 < E) s += expf(x[i].x - v0);
+      if (e0 + 1 < E) s += expf(x[i].y - v0);
+      if (e0 + 2 < E) s += expf(x[i].z - v0);
+      if (e0 + 3 < E) s += expf(x[i].w - v0);
+    }
+#pragma unroll
+    for (int off = 1; off < G; off <<= 1) s += __shfl_xor_sync(0xffffffffu, s, off);
     denom = s;
   }
-  sel_e = my_e;
-  sel_w = num / denom;
+#pragma unroll
+  for (int i = 0; i < K; ++i) w[i] = ex[i] / denom;
 }
 
-// Staged routing of tokens [t0, t1) by one CTA. Chunk barriers `bars`
-// (kMaxChunks of them, initialised with count 1) keep their phases in
-// `phase_bits` across rounds. With KEEP, the CTA's slots (expert, bf16
-// weight) also go to s_slot_e / s_slot_v (index (t - t0)*k + j) and to the
-// shared histogram s_hist.
-template <int EPL, bool VEC, bool KEEP>
-__device__ void route_block(const float *__restrict__ logits, int64_t t0, int64_t t1, int E, int k,
-                            int gating, int TR, bool bulk_ok, int32_t *__restrict__ topk_indx,
-                            uint16_t *__restrict__ topk_vals, float *stage, uint64_t *bars,
-                            uint32_t &phase_bits, unsigned *s_plain, uint8_t *s_slot_e,
-                            uint16_t *s_slot_v, int *s_hist, uint32_t *ctrl,
-                            unsigned long long timeout_ns) {
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  for (int64_t r0 = t0; r0 < t1; r0 += TR) {
-    const int ntok = (int)min((int64_t)TR, t1 - r0);
-    const int nch = (ntok + kChunkTok - 1) / kChunkTok;
-    __syncthreads();  // the previous round's rows are no longer read
-    if (tid == 0) {
-      unsigned plain = 0;
-      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-      for (int c = 0; c < nch; ++c) {
-        const int rows = min(kChunkTok, ntok - c * kChunkTok);
-        const uint32_t bytes = (uint32_t)rows * (uint32_t)E * 4u;
-        if (bulk_ok && (bytes & 15u) == 0) {
-          const uint32_t bar = (uint32_t)__cvta_generic_to_shared(bars + c);
-          const uint32_t dst =
-              (uint32_t)__cvta_generic_to_shared(stage + (size_t)c * kChunkTok * E);
-          const float *src = logits + (r0 + (int64_t)c * kChunkTok) * E;
-          asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar),
-                       "r"(bytes)
-                       : "memory");
-          asm volatile(
-              "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, "
-              "[%3];" ::"r"(dst),
-              "l"(src), "r"(bytes), "r"(bar)
-              : "memory");
-        } else {
-          plain |= 1u << c;
-        }
-      }
-      *s_plain = plain;
+// Outputs of one token: lane g of the group writes entries j = g, g+G, ...
+template <int K, int G, bool KEEP>
+__device__ __forceinline__ void write_token(int64_t t, int64_t t0, const TopK<K> &tk,
+                                            const float (&w)[K], int32_t *__restrict__ topk_indx,
+                                            uint16_t *__restrict__ topk_vals, uint8_t *s_slot_e,
+                                            uint16_t *s_slot_v, int *s_hist) {
+  const int g = (threadIdx.x & 31) % G;
+#pragma unroll
+  for (int j = 0; j < K; ++j) {
+    if (j % G != g) continue;
+    const uint16_t wb = float_to_bf16_bits(w[j]);
+    topk_indx[t * K + j] = tk.e[j];
+    topk_vals[t * K + j] = wb;
+    if (KEEP) {
+      const int s = (int)(t - t0) * K + j;
+      s_slot_e[s] = (uint8_t)tk.e[j];
+      s_slot_v[s] = wb;
+      atomicAdd(&s_hist[tk.e[j]], 1);
     }
-    __syncthreads();
-    const unsigned plain = *s_plain;
-    if (plain) {  // chunks that cannot go through the bulk copy (size or alignment)
-      for (int c = 0; c < nch; ++c) {
-        if (!(plain >> c & 1u)) continue;
-        const int rows = min(kChunkTok, ntok - c * kChunkTok);
-        const float *src = logits + (r0 + (int64_t)c * kChunkTok) * E;
-        float *dst = stage + (size_t)c * kChunkTok * E;
-        for (int i = tid; i < rows * E; i += kRouteThreads) dst[i] = src[i];
-      }
-      __syncthreads();
-    }
-    const uint32_t used = (nch >= 32 ? 0xffffffffu : ((1u << nch) - 1u)) & ~plain;
-    for (int j = warp; j < ntok; j += kRouteWarps) {
-      const int c = j / kChunkTok;
-      if (!(plain >> c & 1u)) {
-        const uint32_t bar = (uint32_t)__cvta_generic_to_shared(bars + c);
-        const uint32_t parity = (phase_bits >> c) & 1u;
-        bool ok = false;
-        const unsigned long long t_start = global_timer_ns();
-        while (true) {
-          uint32_t done;
-          asm volatile(
-              "{\n\t.reg .pred p;\n\t"
-              "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-              "selp.u32 %0, 1, 0, p;\n\t}"
-              : "=r"(done)
-              : "r"(bar), "r"(parity)
-              : "memory");
-          if (done) {
-            ok = true;
-            break;
-          }
-          if (global_timer_ns() - t_start > timeout_ns) break;
-        }
-        if (!__all_sync(0xffffffffu, ok)) {
-          if (lane == 0) record_status(ctrl, MOE_ERR_TIMEOUT);
-          continue;
-        }
-      }
-      int e_sel;
-      float w;
-      topk_row<EPL, VEC>(stage + (size_t)j * E, E, k, gating, lane, e_sel, w);
-      if (lane < k) {
-        const int64_t t = r0 + j;
-        const uint16_t wb = float_to_bf16_bits(w);
-        topk_indx[t * k + lane] = e_sel;
-        topk_vals[t * k + lane] = wb;
-        if (KEEP) {
-          const int i = (int)(t - t0) * k + lane;
-          s_slot_e[i] = (uint8_t)e_sel;
-          s_slot_v[i] = wb;
-          atomicAdd(&s_hist[e_sel], 1);
-        }
-      }
-    }
-    phase_bits ^= used;
   }
 }
 
-__device__ __forceinline__ float *aligned_stage(uint8_t *raw) {
-  const uint32_t a = (uint32_t)__cvta_generic_to_shared(raw);
-  return reinterpret_cast<float *>(raw + ((128u - (a & 127u)) & 127u));
-}
-
-__device__ __forceinline__ void init_chunk_bars(uint64_t *bars) {
-  if (threadIdx.x == 0) {
-    for (int c = 0; c < kMaxChunks; ++c)
-      asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(
-                       (uint32_t)__cvta_generic_to_shared(bars + c))
-                   : "memory");
-    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-  }
-}
-
-template <int EPL, bool VEC>
+template <int K, int G, int NQ>
 __global__ void __launch_bounds__(kRouteThreads) route_kernel(
-    const float *__restrict__ logits, int64_t n, int E, int k, int gating, int T, int TR,
-    int bulk_ok, int32_t *__restrict__ topk_indx, uint16_t *__restrict__ topk_vals,
-    uint32_t *ctrl, unsigned long long timeout_ns) {
-  extern __shared__ uint8_t smem_raw[];
-  __shared__ __align__(8) uint64_t bars[kMaxChunks];
-  __shared__ unsigned s_plain;
-  float *stage = aligned_stage(smem_raw);
-  init_chunk_bars(bars);
-  uint32_t phase_bits = 0;
-  const int64_t t0 = (int64_t)blockIdx.x * T;
-  const int64_t t1 = min(n, t0 + T);
-  route_block<EPL, VEC, false>(logits, t0, t1, E, k, gating, TR, bulk_ok != 0, topk_indx,
-                               topk_vals, stage, bars, phase_bits, &s_plain, nullptr, nullptr,
-                               nullptr, ctrl, timeout_ns);
+    const float *__restrict__ logits, int64_t n, int E, int gating, int vec4,
+    int32_t *__restrict__ topk_indx, uint16_t *__restrict__ topk_vals) {
+  const int64_t groups = (int64_t)gridDim.x * (kRouteThreads / G);
+  for (int64_t t0 = (int64_t)blockIdx.x * (kRouteThreads / G); t0 < n; t0 += groups) {
+    const int64_t t = t0 + threadIdx.x / G;  // the loop bound is uniform over the block
+    const bool valid = t < n;
+    TopK<K> tk;
+    float w[K];
+    topk_group<K, G, NQ>(logits + (valid ? t : 0) * E, valid, E, gating, vec4 != 0, tk, w);
+    if (valid) write_token<K, G, false>(t, 0, tk, w, topk_indx, topk_vals, nullptr, nullptr,
+                                        nullptr);
+  }
 }
-
-// Tokens per staging round for E experts: whole chunks, at most kMaxChunks,
-// within kStageBytes.
-int staging_round_tokens(int E) {
-  int chunks = kStageBytes / (kChunkTok * E * 4);
-  if (chunks > kMaxChunks) chunks = kMaxChunks;
-  if (chunks < 1) chunks = 1;
-  return chunks * kChunkTok;
-}
-
-int epl_for(int E) { return E <= 32 ? 1 : E <= 64 ? 2 : E <= 128 ? 4 : 8; }
 
 template <typename F>
-cudaError_t dispatch_epl(int E, F &&f) {
-  const bool vec = (E % 4) == 0;
-  switch (epl_for(E)) {
-    case 1: return vec ? f.template go<1, true>() : f.template go<1, false>();
-    case 2: return vec ? f.template go<2, true>() : f.template go<2, false>();
-    case 4: return vec ? f.template go<4, true>() : f.template go<4, false>();
-    default: return vec ? f.template go<8, true>() : f.template go<8, false>();
+cudaError_t dispatch_kg(int k, int E, F &&f) {
+  // (G, NQ) by expert count: E <= 16: (1, 4); <= 32: (2, 4); <= 64: (4, 4);
+  // <= 128: (8, 4); <= 256: (8, 8)
+#define MOE_G_CASES(K_)                                   \
+  if (E <= 16) return f.template go<K_, 1, 4>();          \
+  if (E <= 32) return f.template go<K_, 2, 4>();          \
+  if (E <= 64) return f.template go<K_, 4, 4>();          \
+  if (E <= 128) return f.template go<K_, 8, 4>();         \
+  return f.template go<K_, 8, 8>();
+  switch (k) {
+    case 1: MOE_G_CASES(1)
+    case 2: MOE_G_CASES(2)
+    case 3: MOE_G_CASES(3)
+    case 4: MOE_G_CASES(4)
+    case 5: MOE_G_CASES(5)
+    case 6: MOE_G_CASES(6)
+    case 7: MOE_G_CASES(7)
+    default: MOE_G_CASES(8)
   }
+#undef MOE_G_CASES
 }
 
 struct RouteLaunch {
   const float *logits;
   int64_t n;
-  int E, k, gating;
+  int E, gating;
   int32_t *indx;
   uint16_t *vals;
-  uint32_t *ctrl;
   cudaStream_t s;
-  template <int EPL, bool VEC>
+  template <int K, int G, int NQ>
   cudaError_t go() {
-    const int sms = device_sm_count();
-    int64_t T = (n + 2 * sms - 1) / (2 * sms);  // about two CTAs per SM
-    T = (T + 3) / 4 * 4;
-    if (T < 4) T = 4;
-    const int TR = (int)min((int64_t)staging_round_tokens(E), (T + kChunkTok - 1) / kChunkTok *
-                                                                 kChunkTok);
-    const int smem = TR * E * 4 + kStagePad + 128;
-    auto kern = route_kernel<EPL, VEC>;
-    cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                           kStageBytes + kStagePad + 128);
-    if (err != cudaSuccess) return err;
-    const int bulk_ok = ((uintptr_t)logits % 16) == 0;
-    const int64_t blocks = (n + T - 1) / T;
-    kern<<<(unsigned)blocks, kRouteThreads, smem, s>>>(logits, n, E, k, gating, (int)T, TR,
-                                                       bulk_ok, indx, vals, ctrl,
-                                                       kWaitTimeoutNs);
+    const int per_cta = kRouteThreads / G;
+    int64_t blocks = (n + per_cta - 1) / per_cta;
+    const int64_t cap = (int64_t)device_sm_count() * 8;
+    if (blocks > cap) blocks = cap;
+    const int vec4 = (E % 4) == 0 && ((uintptr_t)logits % 16) == 0;
+    route_kernel<K, G, NQ><<<(unsigned)blocks, kRouteThreads, 0, s>>>(logits, n, E, gating, vec4,
+                                                                   indx, vals);
     return cudaGetLastError();
   }
 };
@@ -326,79 +335,118 @@ struct RouteLaunch {
 cudaError_t launch_route(const float *logits, int64_t n, int E, int k, int gating,
                          int32_t *topk_indx, uint16_t *topk_vals, uint32_t *ctrl,
                          cudaStream_t s) {
+  (void)ctrl;
   if (n == 0) return cudaSuccess;
-  return dispatch_epl(E, RouteLaunch{logits, n, E, k, gating, topk_indx, topk_vals, ctrl, s});
+  return dispatch_kg(k, E, RouteLaunch{logits, n, E, gating, topk_indx, topk_vals, s});
 }
 
 // ============================================================= metadata ==
 //
 // Cross-CTA part of the metadata, shared by the kernels below. CTA b of B
-// owns a contiguous range of slots. After its shared-memory histogram is
-// published to ws_hist[b][0..E) (row stride `stride` = E rounded up to 4)
-// and the bounded grid barrier:
-//  prefix  total[e] = sum_b ws_hist[b][e] and before[e] = sum_{b'<b}
-//          ws_hist[b'][e], read as int4 by (expert group, part of the CTA
-//          rows) threads, parts summed and scanned by warp 0:
-//          offs = exclusive scan of total; CTA 0 writes col_sum and offs;
-//          base[e] = offs[e] + before[e]
-//  scatter rounds of blockDim slots: a slot's rank among equal experts of
-//          its warp (match_any + popc) plus the counts of lower warps plus
-//          base[e] is its sorted position p. Stable in f; no atomic decides
-//          any position.
+// owns a contiguous range of slots and counts them per expert in shared
+// memory. Then:
+//  barrier  the counts go to row b of ws_hist (stride = E rounded up to 4);
+//           bounded grid barrier
+//  prefix   (expert group of 4, part of the rows) threads load the rows as
+//           int4, all rows of a batch in flight together:
+//           total[e] = sum_b counts[b][e], before[e] = sum_{b'<b} counts[b'][e];
+//           parts summed per expert, warp 0 scans: offs = exclusive scan of
+//           total; CTA 0 writes col_sum and offs; base[e] = offs[e] + before[e]
+//  scatter  rounds of blockDim slots: a slot's rank among equal experts of
+//           its warp (match_any + popc) plus the slots of that expert in
+//           lower warps plus base[e] is its sorted position p. Stable in f;
+//           no atomic decides any position.
 
-constexpr int kMetaThreads = 512;
-constexpr int kMetaWarps = kMetaThreads / 32;
+constexpr int kMetaThreads = 512;   // metadata_kernel
 constexpr int kMaxParts = 32;
 
-struct MetaShared {
+template <int THREADS>
+struct __align__(16) MetaShared {  // tot / pre take int4 stores
+  static constexpr int kWarps = THREADS / 32;
+  // rows loaded together per thread in the prefix (fewer with more threads:
+  // registers per thread halve, rows per thread halve)
+  static constexpr int kBatch = THREADS >= 1024 ? 8 : 16;
+  static constexpr int kPartInts = 1024;  // parts * stride never exceeds this
   int base[kMaxExperts];
-  int cnt[kMetaWarps][kMaxExperts];
-  int tot[2048];
-  int pre[2048];
+  int cnt[kWarps][kMaxExperts];
+  int tot[kPartInts];
+  int pre[kPartInts];
   int bad;
 };
 
-__device__ __forceinline__ int hist_stride(int E) { return (E + 3) & ~3; }
+// Threads of the prefix: `parts` groups of E4 threads, each part summing a
+// range of CTA rows into tot/pre[part * stride ..]; parts * stride must fit
+// in kPartInts and parts * E4 in the block.
+__host__ __device__ __forceinline__ int prefix_parts(int threads, int stride) {
+  int parts = threads / (stride / 4);
+  if (parts > kMaxParts) parts = kMaxParts;
+  if (parts > 1024 / stride) parts = 1024 / stride;
+  return parts < 1 ? 1 : parts;
+}
 
-__device__ void meta_prefix(const int32_t *__restrict__ ws_hist, int E, MetaShared &sh,
-                            int32_t *__restrict__ col_sum, int32_t *__restrict__ offs) {
+__host__ __device__ __forceinline__ int hist_stride(int E) { return (E + 3) & ~3; }
+
+// Publish this CTA's counts (in sh.base[0..E)), pass the grid barrier, read
+// every CTA's and build sh.base = offs + before. Returns false after a
+// timeout.
+template <int THREADS>
+__device__ bool meta_barrier_prefix(int32_t *__restrict__ ws_hist, int E, MetaShared<THREADS> &sh,
+                                    int32_t *__restrict__ col_sum, int32_t *__restrict__ offs,
+                                    uint32_t *ctrl, unsigned long long timeout_ns) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int b = blockIdx.x, B = gridDim.x;
   const int stride = hist_stride(E), E4 = stride / 4;
-  int parts = kMetaThreads / E4;
-  if (parts > kMaxParts) parts = kMaxParts;
+  int32_t *row = ws_hist + (size_t)b * stride;
+  for (int e = tid; e < stride; e += THREADS) row[e] = e < E ? sh.base[e] : 0;
+  if (!grid_barrier(ctrl, timeout_ns)) return false;
+
+  const int parts = prefix_parts(THREADS, stride);
   if (tid < parts * E4) {
     const int g = tid % E4, part = tid / E4;
     const int b0 = (int)((int64_t)B * part / parts), b1 = (int)((int64_t)B * (part + 1) / parts);
     int4 tot = make_int4(0, 0, 0, 0), pre = make_int4(0, 0, 0, 0);
-#pragma unroll 4
-    for (int bb = b0; bb < b1; ++bb) {
-      const int4 v = __ldcg(reinterpret_cast<const int4 *>(ws_hist + (size_t)bb * stride) + g);
-      tot.x += v.x;
-      tot.y += v.y;
-      tot.z += v.z;
-      tot.w += v.w;
-      if (bb < b) {
-        pre.x += v.x;
-        pre.y += v.y;
-        pre.z += v.z;
-        pre.w += v.w;
+    for (int base = b0; base < b1; base += MetaShared<THREADS>::kBatch) {
+      int4 v[MetaShared<THREADS>::kBatch];
+#pragma unroll
+      for (int q = 0; q < MetaShared<THREADS>::kBatch; ++q)
+        v[q] = base + q < b1
+                   ? __ldcg(reinterpret_cast<const int4 *>(ws_hist + (size_t)(base + q) * stride) +
+                            g)
+                   : make_int4(0, 0, 0, 0);
+#pragma unroll
+      for (int q = 0; q < MetaShared<THREADS>::kBatch; ++q) {
+        tot.x += v[q].x;
+        tot.y += v[q].y;
+        tot.z += v[q].z;
+        tot.w += v[q].w;
+        if (base + q < b) {
+          pre.x += v[q].x;
+          pre.y += v[q].y;
+          pre.z += v[q].z;
+          pre.w += v[q].w;
+        }
       }
     }
     reinterpret_cast<int4 *>(sh.tot + part * stride)[g] = tot;
     reinterpret_cast<int4 *>(sh.pre + part * stride)[g] = pre;
   }
   __syncthreads();
-  if (warp == 0) {  // sum the parts, scan the totals 32 experts at a time
+  for (int e = tid; e < E; e += THREADS) {  // sum the parts, one thread per expert
+    int tot = 0, pre = 0;
+    for (int part = 0; part < parts; ++part) {
+      tot += sh.tot[part * stride + e];
+      pre += sh.pre[part * stride + e];
+    }
+    sh.tot[e] = tot;  // part 0's row now holds the sums
+    sh.pre[e] = pre;
+  }
+  __syncthreads();
+  if (warp == 0) {  // exclusive scan of the totals, 32 experts at a time
     int carry = 0;
     for (int e0 = 0; e0 < E; e0 += 32) {
       const int e = e0 + lane;
-      int tot = 0, pre = 0;
-      if (e < E)
-        for (int part = 0; part < parts; ++part) {
-          tot += sh.tot[part * stride + e];
-          pre += sh.pre[part * stride + e];
-        }
+      const int tot = e < E ? sh.tot[e] : 0;
+      const int pre = e < E ? sh.pre[e] : 0;
       int incl = tot;
 #pragma unroll
       for (int off = 1; off < 32; off <<= 1) {
@@ -418,17 +466,18 @@ __device__ void meta_prefix(const int32_t *__restrict__ ws_hist, int E, MetaShar
     if (b == 0 && lane == 0) offs[E] = carry;
   }
   __syncthreads();
+  return true;
 }
 
 // Positions of slots [f_lo, f_lo + count); slot i's expert and weight come
-// from get(i) -> (e, w) (e = -1 for an invalid id).
-template <typename Get>
-__device__ void meta_scatter(int64_t f_lo, int count, int E, MetaShared &sh, Get get,
+// from get(i, e, w) (e = -1 for an invalid id).
+template <int THREADS, typename Get>
+__device__ void meta_scatter(int64_t f_lo, int count, int E, MetaShared<THREADS> &sh, Get get,
                              int32_t *__restrict__ col_sorted, int32_t *__restrict__ row_sorted,
                              uint16_t *__restrict__ gate_scal) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const unsigned lt_mask = (1u << lane) - 1u;
-  for (int r0 = 0; r0 < count; r0 += kMetaThreads) {
+  for (int r0 = 0; r0 < count; r0 += THREADS) {
     for (int e = lane; e < E; e += 32) sh.cnt[warp][e] = 0;
     __syncwarp();
     const int i = r0 + tid;
@@ -439,19 +488,24 @@ __device__ void meta_scatter(int64_t f_lo, int count, int E, MetaShared &sh, Get
     const int rank = __popc(peers & lt_mask);
     if (e >= 0 && rank == 0) sh.cnt[warp][e] = __popc(peers);
     __syncthreads();
+    // cnt[w][e] -> base[e] + (slots of expert e in warps < w); base[e] += all
+    for (int ee = tid; ee < E; ee += THREADS) {
+      int run = sh.base[ee];
+#pragma unroll
+      for (int ww = 0; ww < MetaShared<THREADS>::kWarps; ++ww) {
+        const int c = sh.cnt[ww][ee];
+        sh.cnt[ww][ee] = run;
+        run += c;
+      }
+      sh.base[ee] = run;
+    }
+    __syncthreads();
     if (e >= 0) {
-      int p = sh.base[e] + rank;
-      for (int ww = 0; ww < warp; ++ww) p += sh.cnt[ww][e];
+      const int p = sh.cnt[warp][e] + rank;
       const int32_t f = (int32_t)(f_lo + i);
       col_sorted[p] = f;
       row_sorted[f] = p;
       gate_scal[p] = w;
-    }
-    __syncthreads();
-    for (int ee = tid; ee < E; ee += kMetaThreads) {
-      int add = 0;
-      for (int ww = 0; ww < kMetaWarps; ++ww) add += sh.cnt[ww][ee];
-      sh.base[ee] += add;
     }
     __syncthreads();
   }
@@ -464,14 +518,13 @@ __global__ void __launch_bounds__(kMetaThreads) metadata_kernel(
     int32_t *__restrict__ col_sorted, int32_t *__restrict__ row_sorted,
     uint16_t *__restrict__ gate_scal, int32_t *__restrict__ ws_hist, uint32_t *ctrl,
     unsigned long long timeout_ns) {
-  __shared__ MetaShared sh;
+  __shared__ MetaShared<kMetaThreads> sh;
   const int tid = threadIdx.x;
   const int b = blockIdx.x;
   const int lo = (int)min((int64_t)N, (int64_t)b * chunk);
   const int hi = (int)min((int64_t)N, (int64_t)lo + chunk);
-  const int stride = hist_stride(E);
 
-  for (int e = tid; e < stride; e += kMetaThreads) sh.base[e] = 0;
+  for (int e = tid; e < E; e += kMetaThreads) sh.base[e] = 0;
   if (tid == 0) sh.bad = 0;
   __syncthreads();
   for (int f = lo + tid; f < hi; f += kMetaThreads) {
@@ -480,11 +533,9 @@ __global__ void __launch_bounds__(kMetaThreads) metadata_kernel(
     else sh.bad = 1;
   }
   __syncthreads();
-  if (sh.bad) record_status(ctrl, MOE_ERR_INVALID_ARG);
-  for (int e = tid; e < stride; e += kMetaThreads) ws_hist[(size_t)b * stride + e] = sh.base[e];
+  if (sh.bad && tid == 0) record_status(ctrl, MOE_ERR_INVALID_ARG);
 
-  if (!grid_barrier(ctrl, timeout_ns)) return;
-  meta_prefix(ws_hist, E, sh, col_sum, offs);
+  if (!meta_barrier_prefix(ws_hist, E, sh, col_sum, offs, ctrl, timeout_ns)) return;
   meta_scatter(
       lo, hi - lo, E, sh,
       [&](int i, int &e, uint16_t &w) {
@@ -545,45 +596,42 @@ cudaError_t launch_metadata(const int32_t *topk_indx, const uint16_t *topk_vals,
 
 // ================================================= fused route + metadata ==
 //
-// moe_forward's first two stages in one cooperative kernel, one CTA per SM:
-// CTA b routes tokens [b*T, b*T + T) (staged as above) keeping its slots
-// and histogram in shared memory, publishes the histogram, passes the
-// bounded grid barrier, and scatters its slots from shared memory.
-template <int EPL, bool VEC>
-__global__ void __launch_bounds__(kRouteThreads, 1) route_metadata_kernel(
-    const float *__restrict__ logits, int64_t n, int E, int k, int gating, int T, int TR,
-    int bulk_ok, int32_t *__restrict__ topk_indx, uint16_t *__restrict__ topk_vals,
+// moe_route_metadata / moe_forward's first two stages in one cooperative
+// kernel, one CTA per SM: CTA b routes tokens [b*T, b*T + T) (G lanes per
+// token as above), keeping its slots and histogram in shared memory, then
+// publishes, gathers and scatters its slots from shared memory.
+template <int K, int G, int NQ>
+__global__ void __launch_bounds__(kFusedThreads, 1) route_metadata_kernel(
+    const float *__restrict__ logits, int64_t n, int E, int gating, int T, int vec4,
+    int32_t *__restrict__ topk_indx, uint16_t *__restrict__ topk_vals,
     int32_t *__restrict__ col_sum, int32_t *__restrict__ offs, int32_t *__restrict__ col_sorted,
     int32_t *__restrict__ row_sorted, uint16_t *__restrict__ gate_scal,
     int32_t *__restrict__ ws_hist, uint32_t *ctrl, unsigned long long timeout_ns) {
   extern __shared__ uint8_t smem_raw[];
-  __shared__ MetaShared sh;
-  __shared__ __align__(8) uint64_t bars[kMaxChunks];
-  __shared__ unsigned s_plain;
-  float *stage = aligned_stage(smem_raw);
-  uint8_t *s_slot_e = reinterpret_cast<uint8_t *>(stage) + (size_t)TR * E * 4 + kStagePad;
-  uint16_t *s_slot_v = reinterpret_cast<uint16_t *>(s_slot_e + (((size_t)T * k + 15) & ~15ull));
+  __shared__ MetaShared<kFusedThreads> sh;
+  uint8_t *s_slot_e = smem_raw;
+  uint16_t *s_slot_v = reinterpret_cast<uint16_t *>(smem_raw + (((size_t)T * K + 15) & ~15ull));
 
   const int tid = threadIdx.x;
-  const int stride = hist_stride(E);
-  for (int e = tid; e < stride; e += kRouteThreads) sh.base[e] = 0;
-  init_chunk_bars(bars);
+  for (int e = tid; e < E; e += kFusedThreads) sh.base[e] = 0;
   __syncthreads();
 
   const int64_t t0 = min(n, (int64_t)blockIdx.x * T);
   const int64_t t1 = min(n, t0 + T);
-  uint32_t phase_bits = 0;
-  route_block<EPL, VEC, true>(logits, t0, t1, E, k, gating, TR, bulk_ok != 0, topk_indx,
-                              topk_vals, stage, bars, phase_bits, &s_plain, s_slot_e, s_slot_v,
-                              sh.base, ctrl, timeout_ns);
+  constexpr int per_pass = kFusedThreads / G;
+  for (int64_t tb = t0; tb < t1; tb += per_pass) {  // uniform over the block
+    const int64_t t = tb + tid / G;
+    const bool valid = t < t1;
+    TopK<K> tk;
+    float w[K];
+    topk_group<K, G, NQ>(logits + (valid ? t : 0) * E, valid, E, gating, vec4 != 0, tk, w);
+    if (valid)
+      write_token<K, G, true>(t, t0, tk, w, topk_indx, topk_vals, s_slot_e, s_slot_v, sh.base);
+  }
   __syncthreads();
-  for (int e = tid; e < stride; e += kRouteThreads)
-    ws_hist[(size_t)blockIdx.x * stride + e] = sh.base[e];
-
-  if (!grid_barrier(ctrl, timeout_ns)) return;
-  meta_prefix(ws_hist, E, sh, col_sum, offs);
+  if (!meta_barrier_prefix(ws_hist, E, sh, col_sum, offs, ctrl, timeout_ns)) return;
   meta_scatter(
-      t0 * k, (int)(t1 - t0) * k, E, sh,
+      t0 * K, (int)(t1 - t0) * K, E, sh,
       [&](int i, int &e, uint16_t &w) {
         e = s_slot_e[i];
         w = s_slot_v[i];
@@ -591,49 +639,48 @@ __global__ void __launch_bounds__(kRouteThreads, 1) route_metadata_kernel(
       col_sorted, row_sorted, gate_scal);
 }
 
+// Tokens per CTA of the fused kernel: spread over the SMs, a multiple of 4.
+int64_t fused_tokens_per_cta(int64_t n) {
+  const int sms = device_sm_count();
+  int64_t T = (n + sms - 1) / sms;
+  if (T < 4) T = 4;
+  return (T + 3) / 4 * 4;
+}
+
 struct RouteMetaLaunch {
   const float *logits;
   int64_t n;
-  int E, k, gating;
+  int E, gating;
   int32_t *indx;
   uint16_t *vals;
   const moe_routing_meta *meta;
   int32_t *ws_hist;
   uint32_t *ctrl;
   cudaStream_t s;
-  template <int EPL, bool VEC>
+  template <int K, int G, int NQ>
   cudaError_t go() {
-    const int sms = device_sm_count();
-    int64_t B = (n + 3) / 4;
-    if (B > sms) B = sms;
-    if (B < 1) B = 1;
-    int64_t T = (n + B - 1) / B;
-    T = (T + 3) / 4 * 4;
-    B = (n + T - 1) / T;
-    if (B < 1) B = 1;
-    const int TR = (int)min((int64_t)staging_round_tokens(E),
-                            (T + kChunkTok - 1) / kChunkTok * kChunkTok);
-    const size_t slots = (size_t)T * k;
-    const size_t smem = 128 + (size_t)TR * E * 4 + kStagePad + ((slots + 15) & ~(size_t)15) +
-                        slots * 2;
-    auto kern = route_metadata_kernel<EPL, VEC>;
-    const int max_smem = 128 + kStageBytes + kStagePad + kSlotCap * 3 + 16;
+    const int64_t T = fused_tokens_per_cta(n);
+    const int64_t B = (n + T - 1) / T;
+    const size_t slots = (size_t)T * K;
+    const size_t smem = ((slots + 15) & ~(size_t)15) + slots * 2;
+    auto kern = route_metadata_kernel<K, G, NQ>;
+    const int max_smem = kSlotCap * 3 + 16;
     cudaError_t err =
         cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, max_smem);
     if (err != cudaSuccess) return err;
-    int bulk_ok = ((uintptr_t)logits % 16) == 0;
     int Ti = (int)T;
     int64_t nn = n;
-    int E_ = E, k_ = k, g_ = gating;
+    int E_ = E, g_ = gating;
+    int vec4 = (E % 4) == 0 && ((uintptr_t)logits % 16) == 0;
     unsigned long long timeout = kWaitTimeoutNs;
-    void *args[] = {(void *)&logits, (void *)&nn, (void *)&E_, (void *)&k_, (void *)&g_,
-                    (void *)&Ti, (void *)&TR, (void *)&bulk_ok, (void *)&indx, (void *)&vals,
-                    (void *)&meta->col_sum, (void *)&meta->offs, (void *)&meta->col_sorted,
-                    (void *)&meta->row_sorted, (void *)&meta->gate_scal, (void *)&ws_hist,
-                    (void *)&ctrl, (void *)&timeout};
+    void *args[] = {(void *)&logits, (void *)&nn, (void *)&E_, (void *)&g_, (void *)&Ti,
+                    (void *)&vec4, (void *)&indx, (void *)&vals, (void *)&meta->col_sum, (void *)&meta->offs,
+                    (void *)&meta->col_sorted, (void *)&meta->row_sorted,
+                    (void *)&meta->gate_scal, (void *)&ws_hist, (void *)&ctrl,
+                    (void *)&timeout};
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)B);
-    cfg.blockDim = dim3(kRouteThreads);
+    cfg.blockDim = dim3(kFusedThreads);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = s;
     cudaLaunchAttribute attr[1];
@@ -648,20 +695,15 @@ struct RouteMetaLaunch {
 };
 
 // True when the fused kernel can take (n, k): each CTA's slots fit in
-// shared memory. Otherwise moe_forward runs route_kernel + metadata_kernel.
-bool route_metadata_fits(int64_t n, int k) {
-  const int sms = device_sm_count();
-  int64_t T = (n + sms - 1) / sms;
-  T = (T + 3) / 4 * 4;
-  return T * k <= kSlotCap;
-}
+// shared memory. Otherwise the two kernels run.
+bool route_metadata_fits(int64_t n, int k) { return fused_tokens_per_cta(n) * k <= kSlotCap; }
 
 cudaError_t launch_route_metadata(const float *logits, int64_t n, int E, int k, int gating,
                                   int32_t *topk_indx, uint16_t *topk_vals,
                                   const moe_routing_meta &meta, int32_t *ws_hist,
                                   uint32_t *ctrl, cudaStream_t s) {
-  return dispatch_epl(E, RouteMetaLaunch{logits, n, E, k, gating, topk_indx, topk_vals, &meta,
-                                         ws_hist, ctrl, s});
+  return dispatch_kg(k, E, RouteMetaLaunch{logits, n, E, gating, topk_indx, topk_vals, &meta,
+                                           ws_hist, ctrl, s});
 }
 
 // ======================================== metadata without a workspace ==
@@ -711,9 +753,10 @@ cudaError_t noalloc_scratch(void **out) {
 }  // namespace
 
 // Same kernel and the same results as launch_metadata; scratch in the
-// static array. Clears the control words first (barrier counters and the
-// status word must start at zero; the histograms are overwritten by every
-// CTA before they are read), then copies the status word to status_out.
+// static array. Clears the control words first (the grid-barrier counter
+// and the status word must start at zero; the histograms are overwritten by
+// every CTA before they are read), then copies the status word to
+// status_out.
 cudaError_t launch_metadata_noalloc(const int32_t *topk_indx, const uint16_t *topk_vals,
                                     int64_t n, int E, int k, const moe_routing_meta &meta,
                                     int32_t *status_out, cudaStream_t s) {
@@ -818,10 +861,10 @@ cudaError_t launch_combine(const uint16_t *y_flat, int64_t n, int k, int H, uint
 // and return (no trap, no hang).
 __global__ void wait_selftest_kernel(uint32_t *ctrl, unsigned long long timeout_ns) {
   if (threadIdx.x != 0) return;
-  const uint32_t *never = ctrl + kCtrlBarGen + 1;  // a word no kernel writes
-  const unsigned long long t0 = global_timer_ns();
+  const uint32_t *never = ctrl + kCtrlNeverSet;
+  const long long deadline = wait_deadline(timeout_ns);
   while (ld_acquire_gpu(never) == 0u) {
-    if (global_timer_ns() - t0 > timeout_ns) {
+    if (clock64() > deadline) {
       record_status(ctrl, MOE_ERR_TIMEOUT);
       return;
     }

@@ -159,3 +159,23 @@ def test_route_metadata_equals_route_then_build(n, E, k, gating):
     if n <= 20000:
         ref_i, _ = oracle.route(logits.cpu().numpy(), k, gating)
         np.testing.assert_array_equal(i2.cpu().numpy(), ref_i)
+
+
+@pytest.mark.parametrize("E,k", [(128, 4), (32, 4), (6, 2)])
+def test_logits_base_only_4_byte_aligned(E, k):
+    """The API asks only 4-byte alignment of logits: a base offset by one
+    float must route exactly like an aligned copy (scalar-load path)."""
+    n = 1000
+    host = I.route_logits(n, E, seed=9)
+    flat = torch.empty(n * E + 1, dtype=torch.float32, device="cuda")
+    shifted = flat[1:].view(n, E)
+    shifted.copy_(torch.from_numpy(host))
+    assert shifted.data_ptr() % 16 != 0
+    i1, v1 = moe.route(shifted, k)
+    i2, v2 = moe.route(dev(host), k)
+    i3, v3, _ = moe.route_metadata(shifted, k)
+    torch.cuda.synchronize()
+    assert torch.equal(i1, i2) and torch.equal(i1, i3)
+    assert torch.equal(v1.view(torch.int16), v2.view(torch.int16))
+    ref_i, _ = oracle.route(host, k)
+    np.testing.assert_array_equal(i1.cpu().numpy(), ref_i)
