@@ -54,6 +54,9 @@ WORKLOADS = {
     "minimind_e8": I.MINIMIND_E8,
     "minimind_e16": I.MINIMIND_E16,
     "skewed_n16384": I.SKEWED,
+    "gptoss_decode_n1": I.GPTOSS.with_n(1),
+    "gptoss_decode_n8": I.GPTOSS.with_n(8),
+    "gptoss_decode_n64": I.GPTOSS.with_n(64),
 }
 DEFAULT_WORKLOAD = "gptoss_prefill_n8192"
 # routing-only workloads (--profile-only): one moe_route_metadata call per step
@@ -241,7 +244,7 @@ class DeviceCase:
     """A workload's inputs on the device, with R rotated (x, logits) sets and
     W rotated weight sets so that the inputs of consecutive steps exceed L2."""
 
-    def __init__(self, c: I.LayerCase, device, l2_bytes: int, rank: int = 0):
+    def __init__(self, c: I.LayerCase, device, l2_bytes: int, rank: int = 0, weights=None):
         import torch
         import mixture_experts_routing_warp_gb300 as moe
 
@@ -265,7 +268,10 @@ class DeviceCase:
                                .pin_memory())
             self.host_logits.append(torch.from_numpy(hl).pin_memory())
         self.w13, self.w2 = [], []
-        for r in range(self.n_wsets):
+        if weights is not None:  # another case's weight sets (same E, H, I)
+            self.n_wsets = weights.n_wsets
+            self.w13, self.w2 = weights.w13, weights.w2
+        for r in range(len(self.w13), self.n_wsets):
             cw = dataclasses.replace(c, seed=c.seed + r)
             self.w13.append(bf16(I.all_w13(cw)))
             self.w2.append(bf16(I.all_w2(cw)))
@@ -460,7 +466,20 @@ def time_layer_graph(dc, reps, pk, source):
     g.replay()
     b.record()
     torch.cuda.synchronize()
+    total_events_ms = a.elapsed_time(b) / reps
+    # the same steps without event-record nodes: the step time reported
+    g2 = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g2):
+        for i in range(reps):
+            moe.forward(*dc.args(i), c.k, dc.params, dc.ws, out=dc.out)
+    g2.replay()
+    torch.cuda.synchronize()
+    a.record()
+    g2.replay()
+    b.record()
+    torch.cuda.synchronize()
     total_ms = a.elapsed_time(b) / reps
+    del g2
     stage_ms = {name: sum(ev[j].elapsed_time(ev[j + 1]) for ev in events) / reps
                 for j, name in enumerate(moe.STAGES)}
     assert moe.read_status(dc.ws) == 0
@@ -471,6 +490,7 @@ def time_layer_graph(dc, reps, pk, source):
     del g
     return {"workload": c.name, "tokens_per_s": round(c.n / (total_ms * 1e-3), 1),
             "ms_per_step": round(total_ms, 4), "timing": f"CUDA-graph replay of {reps} steps",
+            "ms_per_step_with_stage_events": round(total_events_ms, 4),
             "stage_ms": {k: round(v, 4) for k, v in stage_ms.items()}, "roofline": roof}
 
 
@@ -627,6 +647,11 @@ def run_ours(args, rank, world, local, pg):
                     mm = DeviceCase(WORKLOADS[name], device, l2)
                     also[name] = time_layer_graph(mm, 64, pk, source)
                     del mm
+            if (c.E, c.H, c.I) == (I.GPTOSS.E, I.GPTOSS.H, I.GPTOSS.I):
+                for nd in I.GPTOSS_DECODE_N:  # decode batches on the same weights
+                    cd = DeviceCase(I.GPTOSS.with_n(nd), device, l2, weights=dc)
+                    also[f"gptoss_decode_n{nd}"] = time_layer_graph(cd, 64, pk, source)
+                    del cd
             line["also"] = also
         if not args.no_cpu_baseline:
             line["cpu_baseline"] = oracle_sample(c, oracle_inputs(c))

@@ -545,6 +545,7 @@ cudaError_t launch_gemm(const CUtensorMap &ta, const CUtensorMap &tb, const Gemm
     cudaError_t err =
         cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
     if (err != cudaSuccess) return err;
+    if ((err = uniform_carveout(kern)) != cudaSuccess) return err;
     attr_set = true;
   }
   kern<<<device_sm_count(), kThreads, kSmemBytes, s>>>(ta, tb, a);

@@ -159,6 +159,16 @@ inline cudaError_t record_stage_event(cudaEvent_t ev, cudaStream_t s) {
              : cudaEventRecord(ev, s);
 }
 
+// Every kernel of the library asks for the same L1 / shared-memory split
+// (all shared: the grouped GEMM needs ~200 KB), so that consecutive kernels
+// never wait for an SM to drain and reconfigure. Call once per kernel
+// before its first launch (cheap: a flag per kernel).
+template <typename Kern>
+inline cudaError_t uniform_carveout(Kern kern) {
+  return cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout,
+                              (int)cudaSharedmemCarveoutMaxShared);
+}
+
 // ----------------------------------------------------- kernel launchers --
 // launch_ffn records ev_ffn[0] before the w13 kernel and ev_ffn[1] before the
 // w2 kernel when ev_ffn is given (stage timing of moe_forward_timed).

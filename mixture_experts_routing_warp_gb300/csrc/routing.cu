@@ -326,6 +326,12 @@ struct RouteLaunch {
     const int64_t cap = (int64_t)device_sm_count() * 8;
     if (blocks > cap) blocks = cap;
     const int vec4 = (E % 4) == 0 && ((uintptr_t)logits % 16) == 0;
+    static bool configured = false;
+    if (!configured) {
+      cudaError_t err = uniform_carveout(route_kernel<K, G, NQ>);
+      if (err != cudaSuccess) return err;
+      configured = true;
+    }
     route_kernel<K, G, NQ><<<(unsigned)blocks, kRouteThreads, 0, s>>>(logits, n, E, gating, vec4,
                                                                    indx, vals);
     return cudaGetLastError();
@@ -386,6 +392,39 @@ __host__ __device__ __forceinline__ int prefix_parts(int threads, int stride) {
 
 __host__ __device__ __forceinline__ int hist_stride(int E) { return (E + 3) & ~3; }
 
+// Warp 0: exclusive scan of the totals sh.tot[0..E) 32 experts at a time;
+// sh.base[e] = offs[e] + sh.pre[e]; CTA 0 writes col_sum and offs.
+template <int THREADS>
+__device__ void meta_scan(int E, MetaShared<THREADS> &sh, int32_t *__restrict__ col_sum,
+                          int32_t *__restrict__ offs) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  if (warp == 0) {
+    int carry = 0;
+    for (int e0 = 0; e0 < E; e0 += 32) {
+      const int e = e0 + lane;
+      const int tot = e < E ? sh.tot[e] : 0;
+      const int pre = e < E ? sh.pre[e] : 0;
+      int incl = tot;
+#pragma unroll
+      for (int off = 1; off < 32; off <<= 1) {
+        const int o = __shfl_up_sync(0xffffffffu, incl, off);
+        if (lane >= off) incl += o;
+      }
+      const int excl = carry + incl - tot;
+      if (e < E) {
+        sh.base[e] = excl + pre;
+        if (blockIdx.x == 0) {
+          col_sum[e] = tot;
+          offs[e] = excl;
+        }
+      }
+      carry += __shfl_sync(0xffffffffu, incl, 31);
+    }
+    if (blockIdx.x == 0 && lane == 0) offs[E] = carry;
+  }
+  __syncthreads();
+}
+
 // Publish this CTA's counts (in sh.base[0..E)), pass the grid barrier, read
 // every CTA's and build sh.base = offs + before. Returns false after a
 // timeout.
@@ -393,9 +432,18 @@ template <int THREADS>
 __device__ bool meta_barrier_prefix(int32_t *__restrict__ ws_hist, int E, MetaShared<THREADS> &sh,
                                     int32_t *__restrict__ col_sum, int32_t *__restrict__ offs,
                                     uint32_t *ctrl, unsigned long long timeout_ns) {
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int tid = threadIdx.x;
   const int b = blockIdx.x, B = gridDim.x;
   const int stride = hist_stride(E), E4 = stride / 4;
+  if (B == 1) {  // one CTA holds every slot: no exchange, no barrier
+    for (int e = tid; e < E; e += THREADS) {
+      sh.tot[e] = sh.base[e];
+      sh.pre[e] = 0;
+    }
+    __syncthreads();
+    meta_scan(E, sh, col_sum, offs);
+    return true;
+  }
   int32_t *row = ws_hist + (size_t)b * stride;
   for (int e = tid; e < stride; e += THREADS) row[e] = e < E ? sh.base[e] : 0;
   if (!grid_barrier(ctrl, timeout_ns)) return false;
@@ -441,36 +489,10 @@ __device__ bool meta_barrier_prefix(int32_t *__restrict__ ws_hist, int E, MetaSh
     sh.pre[e] = pre;
   }
   __syncthreads();
-  if (warp == 0) {  // exclusive scan of the totals, 32 experts at a time
-    int carry = 0;
-    for (int e0 = 0; e0 < E; e0 += 32) {
-      const int e = e0 + lane;
-      const int tot = e < E ? sh.tot[e] : 0;
-      const int pre = e < E ? sh.pre[e] : 0;
-      int incl = tot;
-#pragma unroll
-      for (int off = 1; off < 32; off <<= 1) {
-        const int o = __shfl_up_sync(0xffffffffu, incl, off);
-        if (lane >= off) incl += o;
-      }
-      const int excl = carry + incl - tot;
-      if (e < E) {
-        sh.base[e] = excl + pre;
-        if (b == 0) {
-          col_sum[e] = tot;
-          offs[e] = excl;
-        }
-      }
-      carry += __shfl_sync(0xffffffffu, incl, 31);
-    }
-    if (b == 0 && lane == 0) offs[E] = carry;
-  }
-  __syncthreads();
+  meta_scan(E, sh, col_sum, offs);
   return true;
 }
 
-// Positions of slots [f_lo, f_lo + count); slot i's expert and weight come
-// from get(i, e, w) (e = -1 for an invalid id).
 template <int THREADS, typename Get>
 __device__ void meta_scatter(int64_t f_lo, int count, int E, MetaShared<THREADS> &sh, Get get,
                              int32_t *__restrict__ col_sorted, int32_t *__restrict__ row_sorted,
@@ -561,6 +583,12 @@ int metadata_ctas_per_sm() {
 cudaError_t launch_metadata_kernel(const int32_t *topk_indx, const uint16_t *topk_vals, int N,
                                    int E, const moe_routing_meta &meta, int32_t *ws_hist,
                                    uint32_t *ctrl, int max_ctas, cudaStream_t s) {
+  static bool configured = false;
+  if (!configured) {
+    cudaError_t err = uniform_carveout(metadata_kernel);
+    if (err != cudaSuccess) return err;
+    configured = true;
+  }
   const int64_t slots_per_cta = 1024;
   int64_t B = (N + slots_per_cta - 1) / slots_per_cta;
   const int64_t cap = (int64_t)device_sm_count() * metadata_ctas_per_sm();
@@ -581,7 +609,7 @@ cudaError_t launch_metadata_kernel(const int32_t *topk_indx, const uint16_t *top
   attr[0].id = cudaLaunchAttributeCooperative;
   attr[0].val.cooperative = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = B > 1 ? 1 : 0;  // one CTA needs no co-residency guarantee
   cudaError_t err = cudaLaunchKernelExC(&cfg, (const void *)metadata_kernel, args);
   if (err != cudaSuccess) return err;
   return cudaGetLastError();
@@ -639,8 +667,11 @@ __global__ void __launch_bounds__(kFusedThreads, 1) route_metadata_kernel(
       col_sorted, row_sorted, gate_scal);
 }
 
-// Tokens per CTA of the fused kernel: spread over the SMs, a multiple of 4.
-int64_t fused_tokens_per_cta(int64_t n) {
+// Tokens per CTA of the fused kernel: spread over the SMs, a multiple of 4;
+// a batch that one pass of one CTA covers (1024 / G tokens) gets one CTA,
+// which skips the cross-CTA exchange.
+int64_t fused_tokens_per_cta(int64_t n, int per_pass) {
+  if (n <= per_pass) return (n + 3) / 4 * 4;
   const int sms = device_sm_count();
   int64_t T = (n + sms - 1) / sms;
   if (T < 4) T = 4;
@@ -659,15 +690,21 @@ struct RouteMetaLaunch {
   cudaStream_t s;
   template <int K, int G, int NQ>
   cudaError_t go() {
-    const int64_t T = fused_tokens_per_cta(n);
+    const int64_t T = fused_tokens_per_cta(n, kFusedThreads / G);
     const int64_t B = (n + T - 1) / T;
     const size_t slots = (size_t)T * K;
     const size_t smem = ((slots + 15) & ~(size_t)15) + slots * 2;
     auto kern = route_metadata_kernel<K, G, NQ>;
-    const int max_smem = kSlotCap * 3 + 16;
-    cudaError_t err =
-        cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, max_smem);
-    if (err != cudaSuccess) return err;
+    static bool configured = false;
+    if (!configured) {
+      const int max_smem = kSlotCap * 3 + 16;
+      cudaError_t e1 =
+          cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, max_smem);
+      if (e1 != cudaSuccess) return e1;
+      if ((e1 = uniform_carveout(kern)) != cudaSuccess) return e1;
+      configured = true;
+    }
+    cudaError_t err = cudaSuccess;
     int Ti = (int)T;
     int64_t nn = n;
     int E_ = E, g_ = gating;
@@ -687,7 +724,7 @@ struct RouteMetaLaunch {
     attr[0].id = cudaLaunchAttributeCooperative;
     attr[0].val.cooperative = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = B > 1 ? 1 : 0;  // one CTA needs no co-residency guarantee
     err = cudaLaunchKernelExC(&cfg, (const void *)kern, args);
     if (err != cudaSuccess) return err;
     return cudaGetLastError();
@@ -696,7 +733,9 @@ struct RouteMetaLaunch {
 
 // True when the fused kernel can take (n, k): each CTA's slots fit in
 // shared memory. Otherwise the two kernels run.
-bool route_metadata_fits(int64_t n, int k) { return fused_tokens_per_cta(n) * k <= kSlotCap; }
+bool route_metadata_fits(int64_t n, int k) {
+  return fused_tokens_per_cta(n, 0) * k <= kSlotCap;  // the larger of the two T
+}
 
 cudaError_t launch_route_metadata(const float *logits, int64_t n, int E, int k, int gating,
                                   int32_t *topk_indx, uint16_t *topk_vals,
@@ -781,77 +820,134 @@ cudaError_t launch_metadata_noalloc(const int32_t *topk_indx, const uint16_t *to
 
 // ======================================================= gather rows ==
 // X_sorted[p] = x[col_sorted[p] / k]: the dispatch index_select of the
-// MiniMind issue ("It is removable in plain PyTorch"), 16 bytes per thread.
-__global__ void __launch_bounds__(256) gather_rows_kernel(const uint4 *__restrict__ x,
-                                                          const int32_t *__restrict__ col_sorted,
-                                                          int64_t N, int k, int vec_per_row,
-                                                          uint4 *__restrict__ x_sorted) {
-  const int64_t total = N * vec_per_row;
-  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total;
-       i += (int64_t)gridDim.x * blockDim.x) {
-    const int64_t p = i / vec_per_row;
-    const int c = (int)(i - p * vec_per_row);
+// MiniMind issue ("It is removable in plain PyTorch"). A warp per (row,
+// group of 128 16-byte chunks): up to 4 loads in flight per thread and one
+// memory round trip per unit, so a few rows cost about one round trip.
+constexpr int kCopyThreads = 256;
+
+constexpr int kChunksPerLane = 4;  // 16-byte chunks in flight per thread
+
+__global__ void __launch_bounds__(kCopyThreads) gather_rows_kernel(
+    const uint4 *__restrict__ x, const int32_t *__restrict__ col_sorted, int64_t N, int k,
+    int vec_per_row, int groups_per_row, uint4 *__restrict__ x_sorted) {
+  const int lane = threadIdx.x & 31;
+  const int64_t units = N * groups_per_row;  // (row, group of 32 * kChunksPerLane chunks)
+  const int64_t warps = (int64_t)gridDim.x * (kCopyThreads / 32);
+  for (int64_t u = (int64_t)blockIdx.x * (kCopyThreads / 32) + (threadIdx.x >> 5); u < units;
+       u += warps) {
+    const int64_t p = u / groups_per_row;
+    const int c0 = (int)(u - p * groups_per_row) * 32 * kChunksPerLane + lane;
     const int32_t f = __ldg(col_sorted + p);
     // positions whose slot carried an out-of-range expert id are never
     // written by the metadata kernel (which flags MOE_ERR_INVALID_ARG)
     if ((uint32_t)f >= (uint32_t)N) continue;
-    x_sorted[i] = __ldg(x + (int64_t)(f / k) * vec_per_row + c);
+    const uint4 *src = x + (int64_t)(f / k) * vec_per_row;
+    uint4 *dst = x_sorted + p * vec_per_row;
+    uint4 v[kChunksPerLane];
+#pragma unroll
+    for (int q = 0; q < kChunksPerLane; ++q)
+      if (c0 + 32 * q < vec_per_row) v[q] = __ldg(src + c0 + 32 * q);
+#pragma unroll
+    for (int q = 0; q < kChunksPerLane; ++q)
+      if (c0 + 32 * q < vec_per_row) dst[c0 + 32 * q] = v[q];
   }
 }
 
 cudaError_t launch_gather_rows(const uint16_t *x, const int32_t *col_sorted, int64_t N, int k,
                                int H, uint16_t *x_sorted, cudaStream_t s) {
   if (N == 0) return cudaSuccess;
-  const int vpr = H / 8;
-  int64_t blocks = (N * vpr + 255) / 256;
-  const int64_t cap = (int64_t)device_sm_count() * 8;
+  static bool configured = false;
+  if (!configured) {
+    cudaError_t err = uniform_carveout(gather_rows_kernel);
+    if (err != cudaSuccess) return err;
+    configured = true;
+  }
+  const int vpr = H / 8, gpr = (vpr + 32 * kChunksPerLane - 1) / (32 * kChunksPerLane);
+  int64_t blocks = (N * gpr + kCopyThreads / 32 - 1) / (kCopyThreads / 32);
+  const int64_t cap = (int64_t)device_sm_count() * 16;
   if (blocks > cap) blocks = cap;
-  gather_rows_kernel<<<(unsigned)blocks, 256, 0, s>>>(reinterpret_cast<const uint4 *>(x),
-                                                      col_sorted, N, k, vpr,
-                                                      reinterpret_cast<uint4 *>(x_sorted));
+  gather_rows_kernel<<<(unsigned)blocks, kCopyThreads, 0, s>>>(
+      reinterpret_cast<const uint4 *>(x), col_sorted, N, k, vpr, gpr,
+      reinterpret_cast<uint4 *>(x_sorted));
   return cudaGetLastError();
 }
 
 // ============================================================= combine ==
 // out[t] = sum_{j<k} y_flat[t*k + j] in fp32, j ascending, one bf16 rounding.
-__global__ void __launch_bounds__(256) combine_kernel(const uint4 *__restrict__ y_flat, int64_t n,
-                                                      int k, int vec_per_row,
-                                                      uint4 *__restrict__ out) {
-  const int64_t total = n * vec_per_row;
-  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total;
-       i += (int64_t)gridDim.x * blockDim.x) {
-    const int64_t t = i / vec_per_row;
-    const int c = (int)(i - t * vec_per_row);
-    float acc[8];
+// A warp per (token, group of 64 16-byte chunks), 2 chunks x k slots in
+// flight per thread.
+__device__ __forceinline__ void add_bf16x8(float (&acc)[8], const uint4 &v) {
+  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
-    for (int q = 0; q < 8; ++q) acc[q] = 0.f;
-    for (int j = 0; j < k; ++j) {
-      const uint4 v = __ldcs(y_flat + (t * k + j) * vec_per_row + c);
-      const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+  for (int q = 0; q < 4; ++q) {
+    acc[2 * q] += __uint_as_float(w[q] << 16);
+    acc[2 * q + 1] += __uint_as_float(w[q] & 0xffff0000u);
+  }
+}
+
+template <int K>
+__global__ void __launch_bounds__(kCopyThreads) combine_kernel(const uint4 *__restrict__ y_flat,
+                                                               int64_t n, int vec_per_row,
+                                                               int groups_per_row,
+                                                               uint4 *__restrict__ out) {
+  constexpr int CPL = 2;  // chunks per lane: 2*K loads in flight
+  const int lane = threadIdx.x & 31;
+  const int64_t units = n * groups_per_row;  // (token, group of 64 chunks) per warp
+  const int64_t warps = (int64_t)gridDim.x * (kCopyThreads / 32);
+  for (int64_t u = (int64_t)blockIdx.x * (kCopyThreads / 32) + (threadIdx.x >> 5); u < units;
+       u += warps) {
+    const int64_t t = u / groups_per_row;
+    const int c0 = (int)(u - t * groups_per_row) * 32 * CPL + lane;
+    const uint4 *src = y_flat + t * K * vec_per_row;
+    uint4 v[CPL][K];
 #pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        acc[2 * q] += __uint_as_float(w[q] << 16);
-        acc[2 * q + 1] += __uint_as_float(w[q] & 0xffff0000u);
-      }
+    for (int q = 0; q < CPL; ++q)
+#pragma unroll
+      for (int j = 0; j < K; ++j)
+        if (c0 + 32 * q < vec_per_row)
+          v[q][j] = __ldcs(src + (int64_t)j * vec_per_row + c0 + 32 * q);
+#pragma unroll
+    for (int q = 0; q < CPL; ++q) {
+      const int c = c0 + 32 * q;
+      if (c >= vec_per_row) continue;
+      float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+      for (int j = 0; j < K; ++j) add_bf16x8(acc, v[q][j]);
+      uint32_t o[4];
+#pragma unroll
+      for (int w = 0; w < 4; ++w)
+        o[w] = (uint32_t)float_to_bf16_bits(acc[2 * w]) |
+               ((uint32_t)float_to_bf16_bits(acc[2 * w + 1]) << 16);
+      out[t * vec_per_row + c] = make_uint4(o[0], o[1], o[2], o[3]);
     }
-    uint32_t o[4];
-#pragma unroll
-    for (int q = 0; q < 4; ++q)
-      o[q] = (uint32_t)float_to_bf16_bits(acc[2 * q]) |
-             ((uint32_t)float_to_bf16_bits(acc[2 * q + 1]) << 16);
-    out[i] = make_uint4(o[0], o[1], o[2], o[3]);
   }
 }
 
 cudaError_t launch_combine(const uint16_t *y_flat, int64_t n, int k, int H, uint16_t *out,
                            cudaStream_t s) {
   if (n == 0) return cudaSuccess;
-  const int vpr = H / 8;
-  int64_t blocks = (n * vpr + 255) / 256;
-  const int64_t cap = (int64_t)device_sm_count() * 8;
+  const int vpr = H / 8, gpr = (vpr + 63) / 64;
+  int64_t blocks = (n * gpr + kCopyThreads / 32 - 1) / (kCopyThreads / 32);
+  const int64_t cap = (int64_t)device_sm_count() * 16;
   if (blocks > cap) blocks = cap;
-  combine_kernel<<<(unsigned)blocks, 256, 0, s>>>(reinterpret_cast<const uint4 *>(y_flat), n, k,
-                                                  vpr, reinterpret_cast<uint4 *>(out));
+  const uint4 *y = reinterpret_cast<const uint4 *>(y_flat);
+  uint4 *o = reinterpret_cast<uint4 *>(out);
+  static bool configured[9] = {};
+  switch (k) {
+#define MOE_COMBINE_CASE(K_)                                                       \
+  case K_:                                                                         \
+    if (!configured[K_]) {                                                         \
+      cudaError_t err = uniform_carveout(combine_kernel<K_>);                      \
+      if (err != cudaSuccess) return err;                                          \
+      configured[K_] = true;                                                       \
+    }                                                                              \
+    combine_kernel<K_><<<(unsigned)blocks, kCopyThreads, 0, s>>>(y, n, vpr, gpr, o); \
+    break;
+    MOE_COMBINE_CASE(1) MOE_COMBINE_CASE(2) MOE_COMBINE_CASE(3) MOE_COMBINE_CASE(4)
+    MOE_COMBINE_CASE(5) MOE_COMBINE_CASE(6) MOE_COMBINE_CASE(7) MOE_COMBINE_CASE(8)
+#undef MOE_COMBINE_CASE
+    default: return cudaErrorInvalidValue;
+  }
   return cudaGetLastError();
 }
 
