@@ -78,6 +78,8 @@ def parse_args():
     p.add_argument("--workload", choices=sorted(WORKLOADS) + sorted(ROUTING_WORKLOADS),
                    default=DEFAULT_WORKLOAD)
     p.add_argument("--no-extras", action="store_true", help="skip the routing / MiniMind extras")
+    p.add_argument("--ffn-kernel", choices=["auto", "tiled", "swap"], default="auto",
+                   help="grouped-GEMM kernel of the expert FFN (auto: by batch size)")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--profile-only", action="store_true",
                    help="only the warm-up and timed steps (for ncu): no e2e, extras, "
@@ -244,7 +246,8 @@ class DeviceCase:
     """A workload's inputs on the device, with R rotated (x, logits) sets and
     W rotated weight sets so that the inputs of consecutive steps exceed L2."""
 
-    def __init__(self, c: I.LayerCase, device, l2_bytes: int, rank: int = 0, weights=None):
+    def __init__(self, c: I.LayerCase, device, l2_bytes: int, rank: int = 0, weights=None,
+                 ffn_kernel: str = "auto"):
         import torch
         import mixture_experts_routing_warp_gb300 as moe
 
@@ -275,7 +278,7 @@ class DeviceCase:
             cw = dataclasses.replace(c, seed=c.seed + r)
             self.w13.append(bf16(I.all_w13(cw)))
             self.w2.append(bf16(I.all_w2(cw)))
-        self.params = moe.make_params(c.gating, c.act, c.layout)
+        self.params = moe.make_params(c.gating, c.act, c.layout, ffn_kernel=ffn_kernel)
         self.ws = moe.workspace(c.n, c.E, c.k, c.H, c.I, device)
         self.out = torch.empty((c.n, c.H), dtype=torch.bfloat16, device=device)
         self.host_out = torch.empty((c.n, c.H), dtype=torch.bfloat16).pin_memory()
@@ -593,7 +596,7 @@ def run_ours(args, rank, world, local, pg):
             raise SystemExit("routing workloads are for --profile-only runs")
         return profile_routing(args, device, l2)
     c = WORKLOADS[args.workload]
-    dc = DeviceCase(c, device, l2, rank)
+    dc = DeviceCase(c, device, l2, rank, ffn_kernel=args.ffn_kernel)
     if args.profile_only:
         total_ms, _ = time_layer(dc, args.steps, args.warmup, pg, None, timed_stages=False)
         if rank == 0:
@@ -624,7 +627,7 @@ def run_ours(args, rank, world, local, pg):
             "data": "synthetic (seeded numpy PCG64, N(0,1) tokens, N(0,0.02) weights)",
             "config": {"workload": c.name, "n_tokens": c.n, "hidden": c.H, "n_experts": c.E,
                        "topk": c.k, "intermediate": c.I, "gating": c.gating,
-                       "activation": c.act, "w13_layout": c.layout,
+                       "activation": c.act, "w13_layout": c.layout, "ffn_kernel": args.ffn_kernel,
                        "l2": f"inputs rotated over {dc.n_xsets} token sets and {dc.n_wsets} "
                              f"weight sets (> 2x L2 per step cycle)",
                        "parallelism": f"replicas x{world} (token batches per rank)"},
@@ -649,9 +652,12 @@ def run_ours(args, rank, world, local, pg):
                     del mm
             if (c.E, c.H, c.I) == (I.GPTOSS.E, I.GPTOSS.H, I.GPTOSS.I):
                 for nd in I.GPTOSS_DECODE_N:  # decode batches on the same weights
-                    cd = DeviceCase(I.GPTOSS.with_n(nd), device, l2, weights=dc)
-                    also[f"gptoss_decode_n{nd}"] = time_layer_graph(cd, 64, pk, source)
-                    del cd
+                    for fk in ("auto", "tiled"):
+                        cd = DeviceCase(I.GPTOSS.with_n(nd), device, l2, weights=dc,
+                                        ffn_kernel=fk)
+                        key = f"gptoss_decode_n{nd}" + ("" if fk == "auto" else "_tiled")
+                        also[key] = time_layer_graph(cd, 64, pk, source)
+                        del cd
             line["also"] = also
         if not args.no_cpu_baseline:
             line["cpu_baseline"] = oracle_sample(c, oracle_inputs(c))

@@ -59,7 +59,7 @@
 extern "C" {
 #endif
 
-#define MOE_ABI_VERSION 1
+#define MOE_ABI_VERSION 2
 
 typedef void *moe_stream;  /* a cudaStream_t */
 
@@ -100,12 +100,30 @@ typedef enum {
 #define MOE_SET_BETA 2u
 #define MOE_SET_LIMIT 4u
 
+/* Which grouped-GEMM kernel runs the two expert contractions of stage 3.
+ * Both compute the result moe_grouped_ffn documents (fp32 accumulation, h
+ * rounded to bf16); they tile the work differently, so the last bits of an
+ * output may differ between them. No counterpart on the pages: a choice of
+ * this implementation.
+ *   AUTO   SWAP when n*k <= 32*E (on average at most one 32-row token tile
+ *          per expert: decode), else TILED.
+ *   TILED  128 sorted rows x 256 weight rows per tile (the tokens on the
+ *          MMA's M side): large per-expert batches.
+ *   SWAP   128 weight rows x 32 sorted rows per tile (the weights on the
+ *          MMA's M side): small per-expert batches. */
+typedef enum {
+  MOE_FFN_AUTO = 0,
+  MOE_FFN_TILED = 1,
+  MOE_FFN_SWAP = 2
+} moe_ffn_kernel;
+
 typedef struct {
   int32_t gating;     /* moe_gating */
   int32_t activation; /* moe_activation */
   int32_t w13_layout; /* moe_w13_layout */
   uint32_t set;       /* MOE_SET_* bits */
   float alpha, beta, limit;
+  int32_t ffn_kernel; /* moe_ffn_kernel; 0 = AUTO */
 } moe_params;
 
 /* Routing metadata [R1] 关键源码片段 (routing_data_from_sparse_topk),

@@ -21,6 +21,8 @@ GATING = {"softmax_topk": 0, "softmax_all": 1}
 ACT = {"swiglu": 0, "swiglu_oai": 1}
 LAYOUT = {"packed": 0, "interleaved": 1}
 SET_ALPHA, SET_BETA, SET_LIMIT = 1, 2, 4
+FFN_KERNEL = {"auto": 0, "tiled": 1, "swap": 2}
+ABI_VERSION = 2
 
 STATUS = {0: "MOE_OK", 1: "MOE_ERR_INVALID_ARG", 2: "MOE_ERR_UNSUPPORTED",
           3: "MOE_ERR_WORKSPACE_TOO_SMALL", 4: "MOE_ERR_CUDA", 5: "MOE_ERR_TIMEOUT",
@@ -36,7 +38,8 @@ class MoEError(RuntimeError):
 class MoeParams(ctypes.Structure):
     _fields_ = [("gating", ctypes.c_int32), ("activation", ctypes.c_int32),
                 ("w13_layout", ctypes.c_int32), ("set", ctypes.c_uint32),
-                ("alpha", ctypes.c_float), ("beta", ctypes.c_float), ("limit", ctypes.c_float)]
+                ("alpha", ctypes.c_float), ("beta", ctypes.c_float), ("limit", ctypes.c_float),
+                ("ffn_kernel", ctypes.c_int32)]
 
 
 class RoutingMeta(ctypes.Structure):
@@ -91,7 +94,7 @@ def lib() -> ctypes.CDLL:
             f = getattr(L, name)
             f.restype = res
             f.argtypes = args
-        if L.moe_abi_version() != 1:
+        if L.moe_abi_version() != ABI_VERSION:
             raise RuntimeError("libmoe_gb300.so ABI version mismatch")
         _LIB = L
     return _LIB
@@ -123,10 +126,13 @@ def _ptr(t: Optional[torch.Tensor]) -> ctypes.c_void_p:
 
 def make_params(gating: str = "softmax_topk", act: str = "swiglu", layout: str = "packed",
                 alpha: Optional[float] = None, beta: Optional[float] = None,
-                limit: Optional[float] = None) -> MoeParams:
+                limit: Optional[float] = None, ffn_kernel: str = "auto") -> MoeParams:
     """moe_params with the `set` bits of the values that are not None, so
-    unset parameters keep the activation's defaults."""
-    p = MoeParams(GATING[gating], ACT[act], LAYOUT[layout], 0, 0.0, 0.0, 0.0)
+    unset parameters keep the activation's defaults. ffn_kernel picks the
+    grouped-GEMM kernel: "auto", "tiled" (large per-expert batches) or
+    "swap" (small ones)."""
+    p = MoeParams(GATING[gating], ACT[act], LAYOUT[layout], 0, 0.0, 0.0, 0.0,
+                  FFN_KERNEL[ffn_kernel])
     if alpha is not None:
         p.set |= SET_ALPHA
         p.alpha = float(alpha)

@@ -34,14 +34,12 @@
 // Every mbarrier wait is bounded: on timeout the kernel records
 // MOE_ERR_TIMEOUT, the other roles see the abort flag and leave, in-flight
 // copies and MMAs are drained (bounded), TMEM is freed, and the kernel returns.
-#include <cudaTypedefs.h>
-
-#include <mutex>
-
-#include "moe_internal.cuh"
+#include "tc_ptx.cuh"
 
 namespace moe {
 namespace {
+
+using namespace tc;
 
 constexpr int BM = 128;                 // rows per tile (UMMA M)
 constexpr int BN = 256;                 // accumulator columns per tile (UMMA N)
@@ -57,11 +55,7 @@ constexpr int kNumBars = 2 * STAGES + 2 + 2 + 1;
 constexpr int kSmemBytes = 1024 /*alignment slack*/ + STAGES * (A_BYTES + B_BYTES) +
                            kNumBars * 8 + 16 + 2 * (kMaxExperts + 1) * 4 + 16;
 
-// Instruction descriptor of tcgen05.mma kind::f16: D fp32 (bits 4-5 = 1),
-// A and B bf16 (bits 7-9 = 1, bits 10-12 = 1), both K-major (bits 15, 16 =
-// 0), N >> 3 in bits 17-22, M >> 4 in bits 24-28.
-constexpr uint32_t kIdesc = (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(BN >> 3) << 17) |
-                            ((uint32_t)(BM >> 4) << 24);
+constexpr uint32_t kIdesc = make_idesc_bf16(BM, BN);
 
 enum { EPI_ACT = 0, EPI_SCATTER = 1 };
 
@@ -79,160 +73,6 @@ struct GemmArgs {
   uint32_t *ctrl;
   unsigned long long timeout_ns;
 };
-
-// ------------------------------------------------------------ PTX wrappers --
-__device__ __forceinline__ uint32_t smem_u32(const void *p) {
-  return (uint32_t)__cvta_generic_to_shared(p);
-}
-
-__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
-  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
-}
-
-__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
-  uint32_t ok;
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-      "selp.u32 %0, 1, 0, p;\n\t}"
-      : "=r"(ok)
-      : "r"(bar), "r"(parity)
-      : "memory");
-  return ok != 0;
-}
-
-__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
-  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
-               : "memory");
-}
-
-__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
-  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
-}
-
-__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *map, uint32_t bar,
-                                            int c0, int c1) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes"
-      " [%0], [%1, {%3, %4}], [%2];" ::"r"(dst),
-      "l"((uint64_t)map), "r"(bar), "r"(c0), "r"(c1)
-      : "memory");
-}
-
-__device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap *map, uint32_t bar,
-                                            int c0, int c1, int c2) {
-  asm volatile(
-      "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes"
-      " [%0], [%1, {%3, %4, %5}], [%2];" ::"r"(dst),
-      "l"((uint64_t)map), "r"(bar), "r"(c0), "r"(c1), "r"(c2)
-      : "memory");
-}
-
-__device__ __forceinline__ void prefetch_tmap(const CUtensorMap *map) {
-  asm volatile("prefetch.tensormap [%0];" ::"l"((uint64_t)map) : "memory");
-}
-
-// Shared-memory matrix descriptor: K-major operand, 128-byte swizzle, rows
-// of 128 bytes, 8-row groups 1024 bytes apart (SBO); LBO unused for this
-// layout; bits 46-47 = 1 (descriptor version); bits 61-63 = 2 (SWIZZLE_128B).
-__device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr) {
-  return (uint64_t)((saddr & 0x3FFFFu) >> 4) | ((uint64_t)1 << 16) |
-         ((uint64_t)(1024 >> 4) << 32) | ((uint64_t)1 << 46) | ((uint64_t)2 << 61);
-}
-
-__device__ __forceinline__ void umma_bf16(uint32_t tmem_d, uint64_t adesc, uint64_t bdesc,
-                                          uint32_t accumulate) {
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "setp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(tmem_d),
-      "l"(adesc), "l"(bdesc), "r"(kIdesc), "r"(accumulate)
-      : "memory");
-}
-
-__device__ __forceinline__ void umma_commit(uint32_t bar) {
-  asm volatile(
-      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
-      : "memory");
-}
-
-__device__ __forceinline__ void tc_fence_before() {
-  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
-}
-
-__device__ __forceinline__ void tc_fence_after() {
-  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-}
-
-#define TMEM_LD32(taddr, r)                                                                      \
-  asm volatile(                                                                                  \
-      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, "   \
-      "%11, %12, %13, %14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, "    \
-      "%28, %29, %30, %31}, [%32];"                                                              \
-      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),     \
-        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), \
-        "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]),           \
-        "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]),           \
-        "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])            \
-      : "r"(taddr))
-
-__device__ __forceinline__ void tmem_wait_ld() {
-  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-}
-
-// Bounded mbarrier wait. Returns false when this wait gave up (records
-// MOE_ERR_TIMEOUT and raises the CTA's abort flag) or another role already
-// aborted.
-__device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity,
-                                             volatile int *abort_flag, const GemmArgs &a) {
-  if (mbar_try_wait(bar, parity)) return true;
-  const long long deadline = wait_deadline(a.timeout_ns);
-  uint32_t spins = 0;
-  while (true) {
-    if (mbar_try_wait(bar, parity)) return true;
-    if ((++spins & 15u) == 0) {
-      if (*abort_flag) return false;
-      if (clock64() > deadline) {
-        *abort_flag = 1;
-        record_status(a.ctrl, MOE_ERR_TIMEOUT);
-        return false;
-      }
-    }
-  }
-}
-
-// Bounded wait used while draining, independent of the abort flag.
-__device__ __forceinline__ void wait_drain(uint32_t bar, uint32_t parity,
-                                           unsigned long long timeout_ns) {
-  const long long deadline = wait_deadline(timeout_ns);
-  while (!mbar_try_wait(bar, parity))
-    if (clock64() > deadline) return;
-}
-
-__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
-  return (uint32_t)float_to_bf16_bits(lo) | ((uint32_t)float_to_bf16_bits(hi) << 16);
-}
-
-struct Tile {
-  int e, m0, m_end, nt;
-};
-
-__device__ __forceinline__ Tile decode_tile(int t, int n_tiles, const int *s_tstart,
-                                            const int *s_offs, int E) {
-  Tile d;
-  const int mt = t / n_tiles;
-  d.nt = t - mt * n_tiles;
-  int lo = 0, hi = E - 1;  // last expert whose first m-tile is <= mt owns it
-  while (lo < hi) {
-    const int mid = (lo + hi + 1) >> 1;
-    if (s_tstart[mid] <= mt) lo = mid;
-    else hi = mid - 1;
-  }
-  d.e = lo;
-  d.m0 = s_offs[lo] + (mt - s_tstart[lo]) * BM;
-  d.m_end = min(d.m0 + BM, s_offs[lo + 1]);
-  return d;
-}
 
 // ------------------------------------------------------------------ kernel --
 template <int EPI, bool PACKED>
@@ -288,22 +128,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   for (int i = threadIdx.x; i <= E; i += kThreads) s_offs[i] = args.offs[i];
   __syncthreads();
-  if (warp == 0) {  // exclusive prefix of m-tiles over experts
-    int carry = 0;
-    for (int e0 = 0; e0 < E; e0 += 32) {
-      const int e = e0 + lane;
-      const int cnt = e < E ? (s_offs[e + 1] - s_offs[e] + BM - 1) / BM : 0;
-      int incl = cnt;
-#pragma unroll
-      for (int off = 1; off < 32; off <<= 1) {
-        const int o = __shfl_up_sync(0xffffffffu, incl, off);
-        if (lane >= off) incl += o;
-      }
-      if (e < E) s_tstart[e] = carry + incl - cnt;
-      carry += __shfl_sync(0xffffffffu, incl, 31);
-    }
-    if (lane == 0) s_tstart[E] = carry;
-  }
+  if (warp == 0) row_tile_prefix(s_offs, E, BM, s_tstart);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -319,9 +144,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t issued = 0;  // stages filled whose consumption we have not seen
       bool ok = true;
       for (int t = blockIdx.x; ok && t < total; t += gridDim.x) {
-        const Tile d = decode_tile(t, args.n_tiles, s_tstart, s_offs, E);
+        const Tile d = decode_tile(t, args.n_tiles, s_tstart, s_offs, E, BM);
         for (int kb = 0; kb < num_kb; ++kb) {
-          if (!wait_bounded(empty_bar(stage), phase ^ 1u, s_abort, args)) {
+          if (!wait_bounded(empty_bar(stage), phase ^ 1u, s_abort, args.ctrl, args.timeout_ns)) {
             ok = false;
             break;
           }
@@ -366,11 +191,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int t = blockIdx.x; ok && t < total; t += gridDim.x, ++local) {
         const int acc = local & 1;
         const uint32_t acc_phase = (uint32_t)(local >> 1) & 1u;
-        if (!wait_bounded(tempty_bar(acc), acc_phase ^ 1u, s_abort, args)) break;
+        if (!wait_bounded(tempty_bar(acc), acc_phase ^ 1u, s_abort, args.ctrl, args.timeout_ns)) break;
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + (uint32_t)(acc * BN);
         for (int kb = 0; kb < num_kb; ++kb) {
-          if (!wait_bounded(full_bar(stage), phase, s_abort, args)) {
+          if (!wait_bounded(full_bar(stage), phase, s_abort, args.ctrl, args.timeout_ns)) {
             ok = false;
             break;
           }
@@ -379,7 +204,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint64_t bdesc = sw128_desc(sB_addr + stage * B_BYTES);
 #pragma unroll
           for (int kk = 0; kk < BK / UK; ++kk)  // +32 bytes along K per step = +2 in the descriptor
-            umma_bf16(d_tmem, adesc + 2u * kk, bdesc + 2u * kk, (kb | kk) != 0 ? 1u : 0u);
+            umma_bf16(d_tmem, adesc + 2u * kk, bdesc + 2u * kk, kIdesc, (kb | kk) != 0 ? 1u : 0u);
           umma_commit(empty_bar(stage));
           if (++stage == STAGES) {
             stage = 0;
@@ -398,10 +223,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int row = q * 32 + lane;
     int local = 0;
     for (int t = blockIdx.x; t < total; t += gridDim.x, ++local) {
-      const Tile d = decode_tile(t, args.n_tiles, s_tstart, s_offs, E);
+      const Tile d = decode_tile(t, args.n_tiles, s_tstart, s_offs, E, BM);
       const int acc = local & 1;
       const uint32_t acc_phase = (uint32_t)(local >> 1) & 1u;
-      if (!wait_bounded(tfull_bar(acc), acc_phase, s_abort, args)) break;
+      if (!wait_bounded(tfull_bar(acc), acc_phase, s_abort, args.ctrl, args.timeout_ns)) break;
       tc_fence_after();
       const uint32_t tbase = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * BN);
       const int p = d.m0 + row;
@@ -494,48 +319,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-// -------------------------------------------------------------- host side --
-PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
-  static std::once_flag once;
-  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-  std::call_once(once, [] {
-    void *p = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
-                                         &q) == cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
-  });
-  return fn;
-}
-
-// bf16 [rows, cols] row-major, boxes of 64 columns x box_rows rows, 128B swizzle.
-bool map_2d(CUtensorMap *m, const void *base, uint64_t rows, uint64_t cols, uint32_t box_rows) {
-  auto enc = tensor_map_encoder();
-  if (!enc) return false;
-  cuuint64_t dims[2] = {cols, rows};
-  cuuint64_t strides[1] = {cols * 2};
-  cuuint32_t box[2] = {BK, box_rows};
-  cuuint32_t estr[2] = {1, 1};
-  return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base), dims, strides, box,
-             estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
-// bf16 [E, rows, cols] row-major, boxes of 64 columns x box_rows rows x 1 expert.
-bool map_3d(CUtensorMap *m, const void *base, uint64_t E, uint64_t rows, uint64_t cols,
-            uint32_t box_rows) {
-  auto enc = tensor_map_encoder();
-  if (!enc) return false;
-  cuuint64_t dims[3] = {cols, rows, E};
-  cuuint64_t strides[2] = {cols * 2, rows * cols * 2};
-  cuuint32_t box[3] = {BK, box_rows, 1};
-  cuuint32_t estr[3] = {1, 1, 1};
-  return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims, strides, box,
-             estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
 template <int EPI, bool PACKED>
 cudaError_t launch_gemm(const CUtensorMap &ta, const CUtensorMap &tb, const GemmArgs &a,
                         cudaStream_t s) {
@@ -559,6 +342,9 @@ cudaError_t launch_ffn(const uint16_t *x_sorted, const int32_t *offs, const int3
                        int64_t N, int E, int H, int I, const ActParams &act, uint16_t *h_buf,
                        uint16_t *y_flat, uint32_t *ctrl, cudaStream_t s, cudaEvent_t *ev_ffn) {
   if (N == 0) return cudaSuccess;
+  if (act.ffn_kernel == MOE_FFN_SWAP || (act.ffn_kernel == MOE_FFN_AUTO && use_swap_ffn(N, E)))
+    return launch_ffn_swap(x_sorted, offs, col_sorted, gate_scal, w13, w2, N, E, H, I, act, h_buf,
+                           y_flat, ctrl, s, ev_ffn);
   const bool packed = act.layout == MOE_W13_PACKED;
   CUtensorMap ta1, tb1, ta2, tb2;
   if (!map_2d(&ta1, x_sorted, (uint64_t)N, (uint64_t)H, BM) ||

@@ -33,8 +33,12 @@ moe_status resolve_params(const moe_params *p, ActParams &out, int *gating) {
   if (p->w13_layout != MOE_W13_PACKED && p->w13_layout != MOE_W13_INTERLEAVED)
     return MOE_ERR_INVALID_ARG;
   if (p->set & ~(MOE_SET_ALPHA | MOE_SET_BETA | MOE_SET_LIMIT)) return MOE_ERR_INVALID_ARG;
+  if (p->ffn_kernel != MOE_FFN_AUTO && p->ffn_kernel != MOE_FFN_TILED &&
+      p->ffn_kernel != MOE_FFN_SWAP)
+    return MOE_ERR_INVALID_ARG;
   out.act = p->activation;
   out.layout = p->w13_layout;
+  out.ffn_kernel = p->ffn_kernel;
   if (p->activation == MOE_ACT_SWIGLU_OAI) {
     // Only the parameters the caller set replace the SwiGLU-OAI defaults.
     out.alpha = (p->set & MOE_SET_ALPHA) ? p->alpha : 1.702f;

@@ -132,9 +132,10 @@ __device__ __forceinline__ uint16_t float_to_bf16_bits(float f) {
 
 // Resolved activation parameters handed to the FFN kernels.
 struct ActParams {
-  int act;      // moe_activation
-  int layout;   // moe_w13_layout
+  int act;         // moe_activation
+  int layout;      // moe_w13_layout
   float alpha, beta, limit;
+  int ffn_kernel;  // moe_ffn_kernel (host-side choice of the GEMM kernel)
 };
 
 // SwiGLU: (g * sigmoid(g)) * u.  SwiGLU-OAI: g = min(g, limit),
@@ -202,6 +203,15 @@ cudaError_t launch_ffn(const uint16_t *x_sorted, const int32_t *offs, const int3
                        int64_t N, int E, int H, int I, const ActParams &act, uint16_t *h_buf,
                        uint16_t *y_flat, uint32_t *ctrl, cudaStream_t s,
                        cudaEvent_t *ev_ffn = nullptr);
+
+// The swap-operand grouped GEMM (weights on the MMA's M side) for small
+// per-expert batches; launch_ffn hands over to it per act.ffn_kernel.
+bool use_swap_ffn(int64_t N, int E);
+cudaError_t launch_ffn_swap(const uint16_t *x_sorted, const int32_t *offs,
+                            const int32_t *col_sorted, const uint16_t *gate_scal,
+                            const uint16_t *w13, const uint16_t *w2, int64_t N, int E, int H,
+                            int I, const ActParams &act, uint16_t *h_buf, uint16_t *y_flat,
+                            uint32_t *ctrl, cudaStream_t s, cudaEvent_t *ev_ffn);
 
 cudaError_t launch_wait_selftest(uint32_t *ctrl, unsigned long long timeout_ns, cudaStream_t s);
 

@@ -45,7 +45,7 @@ def test_exports_every_declared_function(L):
 
 
 def test_abi_and_status_strings(L):
-    assert L.moe_abi_version() == 1
+    assert L.moe_abi_version() == 2
     for code in range(7):
         s = moe.status_string(code)
         assert s.startswith("MOE_"), s
@@ -107,6 +107,9 @@ def test_ffn_and_forward_parameter_rules(L):
     assert ffn(bad) == 1
     bad = moe.make_params()
     bad.set = 8
+    assert ffn(bad) == 1
+    bad = moe.make_params()
+    bad.ffn_kernel = 3
     assert ffn(bad) == 1
     assert ffn(moe.make_params(), ws_bytes=big - 1) == 3
     assert ffn(moe.make_params(), H=96) == 1

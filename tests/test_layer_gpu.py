@@ -6,7 +6,8 @@ Workloads: the tiny layer, the MiniMind layer (E = 4, 8, 16, top-1, softmax
 over all experts), the GPT-OSS layer (decode n = 1, 8, 64 checked in full;
 prefill n = 2048, 8192 on sampled tokens), the skewed 128-expert prefill
 (n = 16384, sampled tokens), and variants over layouts, activations,
-activation parameters and ragged tile tails."""
+activation parameters and ragged tile tails, each through both grouped-GEMM
+kernels (tokens on the MMA's M side, and weights on it for small batches)."""
 import numpy as np
 import pytest
 import torch
@@ -23,7 +24,7 @@ pytestmark = pytest.mark.gpu
 class Layer:
     """Host inputs of a case plus their device copies and one GPU forward."""
 
-    def __init__(self, case: I.LayerCase, act_kw=None):
+    def __init__(self, case: I.LayerCase, act_kw=None, ffn_kernel: str = "auto"):
         self.case = case
         self.act_kw = act_kw or {}
         self.h = I.layer_inputs(case)
@@ -31,7 +32,8 @@ class Layer:
         self.logits = dev(self.h["logits"])
         self.w13 = dev_bf16(self.h["w13"])
         self.w2 = dev_bf16(self.h["w2"])
-        self.params = moe.make_params(case.gating, case.act, case.layout, **self.act_kw)
+        self.params = moe.make_params(case.gating, case.act, case.layout, **self.act_kw,
+                                      ffn_kernel=ffn_kernel)
 
     def forward(self):
         c = self.case
@@ -144,13 +146,32 @@ VARIANTS = [
 ]
 
 
+@pytest.mark.parametrize("ffn_kernel", ["tiled", "swap"])
 @pytest.mark.parametrize("name,H,E,k,Idim,act,layout,act_kw", VARIANTS,
                          ids=[v[0] for v in VARIANTS])
 @pytest.mark.parametrize("n", [1, 37, 300])
-def test_variants(name, H, E, k, Idim, act, layout, act_kw, n):
+def test_variants(name, H, E, k, Idim, act, layout, act_kw, n, ffn_kernel):
     case = I.LayerCase(f"{name}@n{n}", n=n, H=H, E=E, k=k, I=Idim, act=act, layout=layout,
                        seed=n, w_std=0.1)
-    _check_full(Layer(case, act_kw))
+    _check_full(Layer(case, act_kw, ffn_kernel))
+
+
+def test_swap_kernel_on_many_token_tiles_per_expert():
+    """The swap kernel on 1024 rows per expert (32 token tiles each)."""
+    _check_full(Layer(I.MINIMIND_E4, ffn_kernel="swap"))
+
+
+@pytest.mark.parametrize("n", I.GPTOSS_DECODE_N)
+def test_gptoss_decode_tiled_kernel(n):
+    """Decode through the tiled kernel too (AUTO picks the swap kernel there)."""
+    _check_full(Layer(I.GPTOSS.with_n(n), ffn_kernel="tiled"))
+
+
+def test_auto_kernel_choice_boundary():
+    """n*k on both sides of 32*E: AUTO switches kernels there, both correct."""
+    for n in (64, 65):   # E = 8, k = 4: 256 = 32*8 -> swap, 260 -> tiled
+        case = I.LayerCase(f"boundary@n{n}", n=n, H=128, E=8, k=4, I=192, w_std=0.1, seed=n)
+        _check_full(Layer(case))
 
 
 def test_stages_compose_to_forward():
