@@ -19,6 +19,7 @@
 //   ffn1, packed w13: the gate rows and the up rows of the same h columns go
 //     to two accumulators, so each thread holds its pair.
 //   ffn2: y_flat[col_sorted[m0 + j], f0 + w] = gate_scal[m0 + j] * D[w, j].
+//
 // Warps: 0 TMA producer, 1 TMEM allocation + MMA issue, 2-5 epilogue (warp
 // q reads TMEM lanes 32*(q%4)..). Every mbarrier wait is bounded.
 #include "tc_ptx.cuh"
@@ -190,16 +191,17 @@ __global__ void __launch_bounds__(SW_THREADS, 1)
           tc_fence_after();
           const uint64_t adesc0 = sw128_desc(a_addr(stage, 0));
           const uint64_t bdesc = sw128_desc(b_addr(stage));
+          const bool first = kb == 0;
 #pragma unroll
           for (int kk = 0; kk < SW_BK / SW_UK; ++kk)
             umma_bf16(d_tmem, adesc0 + 2u * kk, bdesc + 2u * kk, kSwIdesc,
-                      (kb | kk) != 0 ? 1u : 0u);
+                      (first && kk == 0) ? 0u : 1u);
           if (DUAL) {
             const uint64_t adesc1 = sw128_desc(a_addr(stage, 1));
 #pragma unroll
             for (int kk = 0; kk < SW_BK / SW_UK; ++kk)
               umma_bf16(d_tmem + SW_N, adesc1 + 2u * kk, bdesc + 2u * kk, kSwIdesc,
-                        (kb | kk) != 0 ? 1u : 0u);
+                        (first && kk == 0) ? 0u : 1u);
           }
           umma_commit(empty_bar(stage));
           if (++stage == C::kStages) {
@@ -214,7 +216,9 @@ __global__ void __launch_bounds__(SW_THREADS, 1)
     }
   } else {
     // ----------------------------------------------------------- epilogue --
-    const int q = warp & 3;  // TMEM lane quarter this warp may read
+    // TMEM is read in 8-column chunks (tokens) up to the tile's valid rows:
+    // decode tiles hold a few tokens, so the work and the code stay small.
+    const int q = warp & 3;       // TMEM lane quarter this warp may read
     const int w = q * 32 + lane;  // weight row within the tile
     int local = 0;
     for (int t = blockIdx.x; t < total; t += gridDim.x, ++local) {
@@ -224,46 +228,46 @@ __global__ void __launch_bounds__(SW_THREADS, 1)
       if (!wait_bounded(tfull_bar(acc), acc_phase, s_abort, args.ctrl, args.timeout_ns)) break;
       tc_fence_after();
       const uint32_t taddr = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * C::kAccCols);
-      uint32_t r0[32];
-      TMEM_LD32(taddr, r0);
-      const int rows = d.m_end - d.m0;  // valid token columns of the tile
-      if (EPI == SW_SCATTER) {
+      const int rows = d.m_end - d.m0;   // valid token columns of the tile
+      const int frow = d.nt * SW_M + w;  // weight row of this thread
+      int dst_mine = 0;
+      float g_mine = 0.f;
+      if (EPI == SW_SCATTER && lane < rows) {  // lane j: token j's destination and weight
+        dst_mine = args.col_sorted[d.m0 + lane];
+        g_mine = bf16_bits_to_float(args.gate_scal[d.m0 + lane]);
+      }
+      for (int c0 = 0; c0 < rows; c0 += 8) {
+        uint32_t r0[8], r1[8];
+        TMEM_LD8(taddr + c0, r0);
+        if (DUAL) TMEM_LD8(taddr + SW_N + c0, r1);
         tmem_wait_ld();
-        // lane j fetches token j's destination row and gate weight
-        const int jp = d.m0 + lane;
-        const int dst_mine = lane < rows ? args.col_sorted[jp] : 0;
-        const float g_mine = lane < rows ? bf16_bits_to_float(args.gate_scal[jp]) : 0.f;
-        const int c = d.nt * SW_M + w;  // output column
+        if (EPI == SW_SCATTER) {
 #pragma unroll
-        for (int j = 0; j < SW_N; ++j) {
-          const int dst = __shfl_sync(0xffffffffu, dst_mine, j);
-          const float g = __shfl_sync(0xffffffffu, g_mine, j);
-          if (j < rows && c < args.H)
-            args.y_out[(size_t)dst * args.H + c] = float_to_bf16_bits(__uint_as_float(r0[j]) * g);
-        }
-      } else if (DUAL) {
-        uint32_t r1[32];
-        TMEM_LD32(taddr + SW_N, r1);
-        tmem_wait_ld();
-        const int c = d.nt * SW_M + w;  // h column
-        if (c < args.I) {
+          for (int i = 0; i < 8; ++i) {
+            const int j = c0 + i;
+            const int dst = __shfl_sync(0xffffffffu, dst_mine, j & 31);
+            const float g = __shfl_sync(0xffffffffu, g_mine, j & 31);
+            if (j < rows && frow < args.H)
+              args.y_out[(size_t)dst * args.H + frow] =
+                  float_to_bf16_bits(__uint_as_float(r0[i]) * g);
+          }
+        } else if (DUAL) {
 #pragma unroll
-          for (int j = 0; j < SW_N; ++j)
-            if (j < rows)
-              args.h_out[(size_t)(d.m0 + j) * args.I + c] = float_to_bf16_bits(
-                  activate(__uint_as_float(r0[j]), __uint_as_float(r1[j]), args.act));
-        }
-      } else {
-        tmem_wait_ld();
-        // weight rows 2i (gate) and 2i+1 (up) sit in lanes 2i, 2i+1
-        const int c = (d.nt * SW_M + w) >> 1;  // h column of this pair
+          for (int i = 0; i < 8; ++i)
+            if (c0 + i < rows && frow < args.I)
+              args.h_out[(size_t)(d.m0 + c0 + i) * args.I + frow] = float_to_bf16_bits(
+                  activate(__uint_as_float(r0[i]), __uint_as_float(r1[i]), args.act));
+        } else {
+          // weight rows 2i (gate) and 2i+1 (up) sit in lanes 2i, 2i+1
+          const int c = frow >> 1;  // h column of this pair
 #pragma unroll
-        for (int j = 0; j < SW_N; ++j) {
-          const float mine = __uint_as_float(r0[j]);
-          const float other = __shfl_xor_sync(0xffffffffu, mine, 1);
-          if ((lane & 1) == 0 && j < rows && c < args.I)
-            args.h_out[(size_t)(d.m0 + j) * args.I + c] =
-                float_to_bf16_bits(activate(mine, other, args.act));
+          for (int i = 0; i < 8; ++i) {
+            const float mine = __uint_as_float(r0[i]);
+            const float other = __shfl_xor_sync(0xffffffffu, mine, 1);
+            if ((lane & 1) == 0 && c0 + i < rows && c < args.I)
+              args.h_out[(size_t)(d.m0 + c0 + i) * args.I + c] =
+                  float_to_bf16_bits(activate(mine, other, args.act));
+          }
         }
       }
       tc_fence_before();

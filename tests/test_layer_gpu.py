@@ -167,6 +167,24 @@ def test_gptoss_decode_tiled_kernel(n):
     _check_full(Layer(I.GPTOSS.with_n(n), ffn_kernel="tiled"))
 
 
+@pytest.mark.parametrize("layout,act", [("packed", "swiglu"), ("interleaved", "swiglu_oai")])
+@pytest.mark.parametrize("n", [1, 5, 40])
+def test_swap_kernel_deep_k(layout, act, n):
+    """The swap kernel with 16 K-blocks per tile in both contractions
+    (H = I = 1024) and 1 .. 32 valid rows per tile (partial 8-column TMEM
+    chunks); the result matches the oracle and repeats bit for bit."""
+    case = I.LayerCase(f"deepk_{layout}@n{n}", n=n, H=1024, E=8, k=2, I=1024, act=act,
+                       layout=layout, w_std=0.03, seed=n)
+    L = Layer(case, ffn_kernel="swap")
+    _check_full(L)
+    c = case
+    ws = moe.workspace(c.n, c.E, c.k, c.H, c.I)
+    outs = [moe.forward(L.x, L.logits, L.w13, L.w2, c.k, L.params, ws).clone() for _ in range(2)]
+    torch.cuda.synchronize()
+    assert moe.read_status(ws) == 0
+    assert torch.equal(outs[0].view(torch.int16), outs[1].view(torch.int16))
+
+
 def test_auto_kernel_choice_boundary():
     """n*k on both sides of 32*E: AUTO switches kernels there, both correct."""
     for n in (64, 65):   # E = 8, k = 4: 256 = 32*8 -> swap, 260 -> tiled
