@@ -184,18 +184,46 @@ class ClockSampler:
 
 
 # ---------------------------------------------------------- algorithmic --
-def stage_work(c: I.LayerCase) -> dict:
-    """Algorithmic FLOPs / bytes of one launch of each stage kernel."""
+def stage_work(c: I.LayerCase, touched: float = None, pk: dict = None) -> dict:
+    """Algorithmic work of one launch of each stage kernel: ("hbm", bytes) or
+    ("tensor", FLOPs). A contraction is bound by whichever of its FLOPs (at
+    the bf16 peak) and its bytes (at the HBM peak) takes longer; its bytes
+    are the weights of the `touched` experts (those that receive a slot)
+    plus its activations in and out."""
     n, E, k, H, Idim = c.n, c.E, c.k, c.H, c.I
     N = n * k
+    touched = E if touched is None else touched
+    ffn1_bytes = touched * 2 * Idim * H * 2 + N * H * 2 + N * Idim * 2
+    ffn2_bytes = touched * H * Idim * 2 + N * Idim * 2 + N * H * 2 + N * (4 + 2)
+    ffn1_flops, ffn2_flops = 2.0 * N * H * 2 * Idim, 2.0 * N * Idim * H
+
+    def contraction(flops, nbytes):
+        if pk is not None and nbytes / (pk["hbm_gbs"] * 1e9) > flops / (pk["bf16_tflops"] * 1e12):
+            return ("hbm", nbytes)
+        return ("tensor", flops)
+
     return {
         "route": ("hbm", n * E * 4 + N * (4 + 2)),
         "metadata": ("hbm", N * (4 + 2) + N * (4 + 4 + 2) + (2 * E + 1) * 4),
         "gather": ("hbm", n * H * 2 + N * H * 2),
-        "ffn1": ("tensor", 2.0 * N * H * 2 * Idim),
-        "ffn2": ("tensor", 2.0 * N * Idim * H),
+        "ffn1": contraction(ffn1_flops, ffn1_bytes),
+        "ffn2": contraction(ffn2_flops, ffn2_bytes),
         "combine": ("hbm", (N * H * 2 + n * H * 2) if k > 1 else 0),
     }
+
+
+def touched_experts(dc) -> float:
+    """Mean number of experts that receive at least one slot over the case's
+    token sets, read back from the library's own routing (untimed)."""
+    import torch
+    import mixture_experts_routing_warp_gb300 as moe
+    c = dc.c
+    counts = []
+    for lg in dc.logits:
+        _, _, meta = moe.route_metadata(lg, c.k, gating=c.gating, ws=dc.ws)
+        counts.append(int((meta["col_sum"] > 0).sum().item()))
+    torch.cuda.synchronize()
+    return float(np.mean(counts))
 
 
 def roofline_entry(bound, work, seconds, pk, source, sustained=False):
@@ -486,10 +514,12 @@ def time_layer_graph(dc, reps, pk, source):
     stage_ms = {name: sum(ev[j].elapsed_time(ev[j + 1]) for ev in events) / reps
                 for j, name in enumerate(moe.STAGES)}
     assert moe.read_status(dc.ws) == 0
-    work = stage_work(c)
+    touched = touched_experts(dc)
+    work = stage_work(c, touched, pk)
     dom = max(stage_ms, key=stage_ms.get)
     roof = roofline_entry(work[dom][0], work[dom][1], stage_ms[dom] * 1e-3, pk, source)
     roof["kernel"] = dom
+    roof["touched_experts"] = touched
     del g
     return {"workload": c.name, "tokens_per_s": round(c.n / (total_ms * 1e-3), 1),
             "ms_per_step": round(total_ms, 4), "timing": f"CUDA-graph replay of {reps} steps",
@@ -613,14 +643,16 @@ def run_ours(args, rank, world, local, pg):
         total_ms = float(t.item())
     ms_per_step = total_ms / args.steps
     value = world * c.n / (ms_per_step * 1e-3)
-    work = stage_work(c)
+    touched = touched_experts(dc)
+    work = stage_work(c, touched, pk)
     dom = max(stage_ms, key=stage_ms.get)
     bound, w = work[dom]
     roof = roofline_entry(bound, w, stage_ms[dom] * 1e-3, pk, source,
                           sustained=total_ms > 100.0)
     roof["kernel"] = dom
+    roof["touched_experts"] = touched
     roof["traffic"] = ncu_traffic(dom, args.workload)
-    kernels_per_step = 5 + (1 if c.k > 1 else 0)
+    kernels_per_step = moe.forward_launch_count(c.n, c.E, c.k, c.H, c.I)
     line = {"metric": METRIC, "value": round(value, 1), "unit": "tokens/s", "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 4),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",

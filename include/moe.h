@@ -286,6 +286,14 @@ moe_status moe_forward_timed(const uint16_t *x, const float *logits, const uint1
                              size_t workspace_bytes, void *const *events, int32_t n_events,
                              moe_stream stream);
 
+/* Number of kernels moe_forward (and moe_forward_timed) enqueues for these
+ * sizes on the current device: route and metadata (one fused kernel when a
+ * CTA's slots fit its shared memory, else two), the gather, the two expert
+ * contractions and, when k > 1, the combine; 0 for n = 0; -1 for sizes
+ * moe_forward rejects. Host-only: launches nothing. No counterpart on the
+ * pages: lets a caller size a CUDA graph or count its launches. */
+int32_t moe_forward_launch_count(int64_t n, int32_t E, int32_t k, int32_t H, int32_t I);
+
 /* DEBUG ONLY -- synchronises `stream`, returns the status word recorded by
  * device-side bounded waits since the last reset (MOE_OK if none). With
  * `reset` non-zero it also zeroes the control block (status word and the

@@ -6,12 +6,14 @@ the C ABI of include/moe.h. This package is the thin Python binding
 (argument marshalling over torch tensors) plus the seeded input generators
 (`inputs`).
 """
-from ._binding import (ACT, GATING, LAYOUT, MoEError, MoeParams, RoutingMeta, build_metadata,
-                       STAGES, combine, empty_meta, forward, forward_timed, grouped_ffn, lib, library_path, make_params,
-                       read_status, route, route_metadata, selftest_wait_timeout, status_string, workspace,
+from ._binding import (ACT, FFN_KERNEL, GATING, LAYOUT, MoEError, MoeParams, RoutingMeta,
+                       STAGES, build_metadata, combine, empty_meta, forward, forward_launch_count,
+                       forward_timed, grouped_ffn, lib, library_path, make_params, read_status,
+                       route, route_metadata, selftest_wait_timeout, status_string, workspace,
                        workspace_size)
 
-__all__ = ["ACT", "GATING", "LAYOUT", "MoEError", "MoeParams", "RoutingMeta", "build_metadata",
-           "STAGES", "combine", "empty_meta", "forward", "forward_timed", "grouped_ffn", "lib", "library_path",
-           "make_params", "read_status", "route", "route_metadata", "selftest_wait_timeout", "status_string",
-           "workspace", "workspace_size"]
+__all__ = ["ACT", "FFN_KERNEL", "GATING", "LAYOUT", "MoEError", "MoeParams", "RoutingMeta",
+           "STAGES", "build_metadata", "combine", "empty_meta", "forward", "forward_launch_count",
+           "forward_timed", "grouped_ffn", "lib", "library_path", "make_params", "read_status",
+           "route", "route_metadata", "selftest_wait_timeout", "status_string", "workspace",
+           "workspace_size"]

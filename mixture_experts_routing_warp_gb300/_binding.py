@@ -71,6 +71,7 @@ SIGNATURES = {
                            _P, _SZ, _P]),
     "moe_forward_timed": (_I32, [_P, _P, _P, _P, _I64, _I32, _I32, _I32, _I32, _PP, _P, _P, _P,
                                  _PM, _P, _SZ, _P, _I32, _P]),
+    "moe_forward_launch_count": (_I32, [_I64, _I32, _I32, _I32, _I32]),
     "moe_read_status": (_I32, [_P, _SZ, _I32, _P]),
     "moe_selftest_wait_timeout": (_I32, [_P, _SZ, _U64, _P]),
 }
@@ -296,6 +297,11 @@ def forward_timed(x: torch.Tensor, logits: torch.Tensor, w13: torch.Tensor, w2: 
                                    ws.numel(), arr, len(events), _stream(x.device)),
            "moe_forward_timed")
     return out
+
+
+def forward_launch_count(n: int, E: int, k: int, H: int, I: int) -> int:
+    """Kernels one moe_forward enqueues for these sizes (-1: invalid sizes)."""
+    return int(lib().moe_forward_launch_count(n, E, k, H, I))
 
 
 def read_status(ws: torch.Tensor, reset: bool = False) -> int:

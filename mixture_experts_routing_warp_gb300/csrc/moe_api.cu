@@ -270,6 +270,13 @@ static moe_status forward_impl(const uint16_t *x, const float *logits, const uin
   return MOE_OK;
 }
 
+int32_t moe_forward_launch_count(int64_t n, int32_t E, int32_t k, int32_t H, int32_t I) {
+  if (check_sizes(n, E, k, H, I, true) != MOE_OK) return -1;
+  if (n == 0) return 0;
+  // the same choice forward_impl makes, then gather, ffn1, ffn2, combine
+  return (route_metadata_fits(n, k) ? 1 : 2) + 3 + (k > 1 ? 1 : 0);
+}
+
 moe_status moe_forward(const uint16_t *x, const float *logits, const uint16_t *w13,
                        const uint16_t *w2, int64_t n, int32_t E, int32_t k, int32_t H, int32_t I,
                        const moe_params *params, uint16_t *out, int32_t *topk_indx,

@@ -83,6 +83,12 @@ def test_route_rejects_before_launch(L):
     assert L.moe_route(None, 0, 8, 2, 0, None, None, None) == 0
 
 
+def test_forward_launch_count_host_rules(L):
+    assert L.moe_forward_launch_count(0, 8, 2, 64, 128) == 0
+    for bad in [(10, 8, 9, 64, 64), (10, 0, 1, 64, 64), (10, 8, 2, 96, 64), (-1, 8, 2, 64, 64)]:
+        assert L.moe_forward_launch_count(*bad) == -1, bad
+
+
 def test_ffn_and_forward_parameter_rules(L):
     good = _p(1 << 20)
     ws = _p(1 << 20)

@@ -78,3 +78,29 @@ def test_bounded_wait_times_out_and_context_survives():
     torch.cuda.synchronize()
     assert moe.read_status(ws) == 0
     assert torch.isfinite(out.float()).all() and out.float().abs().sum() > 0
+
+
+_OUR_KERNELS = ("route", "metadata", "gather_rows", "grouped_gemm", "combine")
+
+
+@pytest.mark.parametrize("case", [
+    I.TINY,                                                           # fused routing, k = 2
+    I.MINIMIND_E4,                                                    # k = 1: no combine
+    I.LayerCase("unfused_n300000", n=300000, H=64, E=8, k=8, I=64),  # route + metadata apart
+], ids=lambda c: c.name)
+def test_forward_launch_count_matches_the_kernels_launched(case):
+    """moe_forward_launch_count equals the kernels one moe_forward launches,
+    as the profiler sees them."""
+    from torch.profiler import ProfilerActivity, profile
+    x, logits, w13, w2, params, ws = _setup(case)
+    moe.forward(x, logits, w13, w2, case.k, params, ws)
+    torch.cuda.synchronize()
+    with profile(activities=[ProfilerActivity.CUDA]) as prof:
+        moe.forward(x, logits, w13, w2, case.k, params, ws)
+        torch.cuda.synchronize()
+    names = [e.name for e in prof.events() if e.device_type.name == "CUDA"]
+    ours = [nm for nm in names if any(kname in nm for kname in _OUR_KERNELS)]
+    if not names:
+        pytest.skip("the profiler recorded no device activity here")
+    assert len(ours) == moe.forward_launch_count(case.n, case.E, case.k, case.H, case.I)
+    assert moe.read_status(ws) == 0
