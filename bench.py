@@ -90,16 +90,45 @@ def parse_args():
 
 
 def dist_setup(args):
+    """One process per GPU under torchrun (RANK / LOCAL_RANK / WORLD_SIZE /
+    MASTER_* from the environment). NCCL for the GPU arm; gloo for the CPU
+    reference arm and wherever no GPU is visible (the multi-rank CPU tests)."""
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     local = int(os.environ.get("LOCAL_RANK", "0"))
     pg = None
     if world > 1:
+        import torch
         import torch.distributed as dist
-        backend = "nccl" if args.impl == "ours" else "gloo"
-        dist.init_process_group(backend=backend)
+        use_nccl = args.impl == "ours" and torch.cuda.is_available()
+        if use_nccl:
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend="nccl" if use_nccl else "gloo")
         pg = dist
     return rank, world, local, pg
+
+
+def max_over_ranks(pg, value: float) -> float:
+    """The slowest rank's value (every rank gets it); value itself when alone."""
+    if pg is None:
+        return value
+    import torch
+    on_gpu = pg.get_backend() == "nccl"
+    t = torch.tensor([value], dtype=torch.float64,
+                     device=torch.device("cuda", torch.cuda.current_device()) if on_gpu else "cpu")
+    pg.all_reduce(t, op=pg.ReduceOp.MAX)
+    return float(t.item())
+
+
+def rank_case(c: I.LayerCase, rank: int, r: int) -> I.LayerCase:
+    """Token set r of rank `rank`: every rank draws its own batches (weak
+    scaling: per-rank work is fixed, ranks never exchange data)."""
+    return dataclasses.replace(c, seed=c.seed + 1000 * rank + r)
+
+
+def job_tokens_per_s(world: int, n: int, ms_per_step: float) -> float:
+    """Whole-job throughput: all ranks' tokens over the slowest rank's step."""
+    return world * n / (ms_per_step * 1e-3)
 
 
 def peaks():
@@ -290,7 +319,7 @@ class DeviceCase:
         self.n_xsets = max(2, min(8, -(-2 * l2_bytes // max(act_bytes, 1))))
         self.x, self.logits, self.host_x, self.host_logits = [], [], [], []
         for r in range(self.n_xsets):
-            cr = dataclasses.replace(c, seed=c.seed + 1000 * rank + r)
+            cr = rank_case(c, rank, r)
             hx = I.layer_x(cr)
             hl = I.layer_logits(cr, hx)
             self.x.append(bf16(hx))
@@ -637,12 +666,9 @@ def run_ours(args, rank, world, local, pg):
     sampler.start()
     total_ms, stage_ms = time_layer(dc, args.steps, args.warmup, pg, sampler)
     sampler.stop()
-    if pg is not None:
-        t = torch.tensor([total_ms], dtype=torch.float64, device=device)
-        pg.all_reduce(t, op=pg.ReduceOp.MAX)
-        total_ms = float(t.item())
+    total_ms = max_over_ranks(pg, total_ms)
     ms_per_step = total_ms / args.steps
-    value = world * c.n / (ms_per_step * 1e-3)
+    value = job_tokens_per_s(world, c.n, ms_per_step)
     touched = touched_experts(dc)
     work = stage_work(c, touched, pk)
     dom = max(stage_ms, key=stage_ms.get)
