@@ -136,9 +136,16 @@ def router_weight(case: LayerCase) -> np.ndarray:
     return normal_bf16((case.E, case.H), case.w_std, case.seed, _TAG_WG, case.E, case.H)
 
 
+def w13_rows(case: LayerCase) -> int:
+    """Rows of one expert's w13: gate and up (2I), or w1 alone (I) for the
+    non-gated ReLU2."""
+    return case.I if case.act == "relu2" else 2 * case.I
+
+
 def expert_w13(case: LayerCase, e: int) -> np.ndarray:
-    """w13 of expert e, [2I, H] bf16 bits, rows in the case's layout."""
-    return normal_bf16((2 * case.I, case.H), case.w_std, case.seed, _TAG_W13, e, case.I, case.H)
+    """w13 of expert e, [2I, H] ([I, H] for ReLU2) bf16 bits, rows in the case's layout."""
+    return normal_bf16((w13_rows(case), case.H), case.w_std, case.seed, _TAG_W13, e, case.I,
+                       case.H)
 
 
 def expert_w2(case: LayerCase, e: int) -> np.ndarray:
@@ -165,7 +172,7 @@ def _per_expert(case: LayerCase, shape, fn) -> np.ndarray:
 
 
 def all_w13(case: LayerCase) -> np.ndarray:
-    return _per_expert(case, (2 * case.I, case.H), expert_w13)
+    return _per_expert(case, (w13_rows(case), case.H), expert_w13)
 
 
 def all_w2(case: LayerCase) -> np.ndarray:

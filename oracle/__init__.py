@@ -37,7 +37,7 @@ import numpy as np
 from . import build as _build
 
 GATING = {"softmax_topk": 0, "softmax_all": 1}
-ACT = {"swiglu": 0, "swiglu_oai": 1}
+ACT = {"swiglu": 0, "swiglu_oai": 1, "relu2": 2}
 LAYOUT = {"packed": 0, "interleaved": 1}
 
 # SwiGLU-OAI defaults ("CuteDSL NVFP4 MoE adds SwiGLU-OAI and ReLU2",
@@ -90,12 +90,17 @@ def _check(rc: int, what: str) -> None:
 def act_params(act: str = "swiglu", layout: str = "packed", alpha: Optional[float] = None,
                beta: Optional[float] = None, limit: Optional[float] = None) -> _ActParams:
     """Resolve activation parameters. Unset values take the activation's own
-    defaults: SwiGLU-OAI 1.702 / 1.0 / 7.0; SwiGLU has no clamp."""
+    defaults: SwiGLU-OAI 1.702 / 1.0 / 7.0; SwiGLU has no clamp unless a
+    limit is given ("SILU + clamp"); ReLU2 takes no parameters."""
     if act == "swiglu_oai":
         a = OAI_ALPHA if alpha is None else alpha
         b = OAI_BETA if beta is None else beta
         lim = OAI_LIMIT if limit is None else limit
+    elif act == "swiglu":
+        a, b, lim = 1.0, 0.0, (math.inf if limit is None else limit)
     else:
+        if limit is not None:
+            raise ValueError("ReLU2 takes no clamp limit")
         a, b, lim = 1.0, 0.0, math.inf
     return _ActParams(ACT[act], LAYOUT[layout], float(a), float(b), float(lim))
 
@@ -148,14 +153,15 @@ def metadata(topk_indx: np.ndarray, topk_vals: np.ndarray, E: int) -> dict:
 
 
 def expert_row(x_row: np.ndarray, w13_e: np.ndarray, w2_e: np.ndarray, **act_kw):
-    """One expert on one row -> (a float64 [2I], h bf16 bits [I], y float64 [H])."""
+    """One expert on one row -> (a float64 [rows], h bf16 bits [I], y float64 [H]);
+    rows = 2I for the gated activations, I for ReLU2."""
     x_row = _c(x_row, np.uint16)
     w13_e = _c(w13_e, np.uint16)
     w2_e = _c(w2_e, np.uint16)
-    I2, H = w13_e.shape
-    I = I2 // 2
+    rows, H = w13_e.shape
+    I = rows if act_kw.get("act") == "relu2" else rows // 2
     assert w2_e.shape == (H, I) and x_row.shape == (H,)
-    a = np.empty(2 * I, dtype=np.float64)
+    a = np.empty(rows, dtype=np.float64)
     h = np.empty(I, dtype=np.uint16)
     y = np.empty(H, dtype=np.float64)
     prm = act_params(**act_kw)
@@ -170,7 +176,7 @@ def ffn(x: np.ndarray, topk_indx: np.ndarray, topk_vals: np.ndarray, w13: np.nda
         **act_kw):
     """Gate-weighted per-expert FFN + combine.
 
-    x [n, H] bf16 bits; w13 [E, 2I, H], w2 [E, H, I] bf16 bits.
+    x [n, H] bf16 bits; w13 [E, 2I, H] (ReLU2: [E, I, H]), w2 [E, H, I] bf16 bits.
     tokens: optional token ids to compute (rows of the result follow it).
     Returns out bf16 bits [n_sel, H]; with want_slots also
     y_slot float64 [n_sel, k, H] (gate-weighted, slot order) and
@@ -181,8 +187,8 @@ def ffn(x: np.ndarray, topk_indx: np.ndarray, topk_vals: np.ndarray, w13: np.nda
     w13 = _c(w13, np.uint16)
     w2 = _c(w2, np.uint16)
     n, H = x.shape
-    E, I2, H2 = w13.shape
-    I = I2 // 2
+    E, rows, H2 = w13.shape
+    I = rows if act_kw.get("act") == "relu2" else rows // 2
     k = indx.shape[1]
     assert H2 == H and w2.shape == (E, H, I) and indx.shape == (n, k) == vals.shape
     toks = None if tokens is None else _c(tokens, np.int64)

@@ -36,7 +36,9 @@
  *    fp32 values (-0.0 ties +0.0); logits must be finite.
  *  - SwiGLU-OAI: gate = min(gate, limit), up = clamp(up, -limit, limit),
  *    h = (gate * sigmoid(alpha * gate)) * (up + beta).
- *  - SwiGLU: h = (gate * sigmoid(gate)) * up.
+ *  - SwiGLU: h = (gate * sigmoid(gate)) * up; with a clamp limit ("SILU +
+ *    clamp") gate and up are clamped as for SwiGLU-OAI first.
+ *  - ReLU2 (non-gated, "RELU2_NO_MUL"): h = max(a, 0)^2 of the single w1 row.
  *  - the router weight multiplies the expert output (after w2).
  *  - combine sums a token's k weighted expert outputs in ascending expert
  *    id, the order of the masked per-expert loop.
@@ -54,6 +56,7 @@
 #define ORC_GATING_SOFTMAX_ALL 1
 #define ORC_ACT_SWIGLU 0
 #define ORC_ACT_SWIGLU_OAI 1
+#define ORC_ACT_RELU2 2 /* non-gated: w13 holds I rows (w1 only) */
 #define ORC_LAYOUT_PACKED 0
 #define ORC_LAYOUT_INTERLEAVED 1
 
@@ -185,26 +188,41 @@ typedef struct {
 
 static double orc_sigmoid(double z) { return 1.0 / (1.0 + exp(-z)); }
 
-/* [R3] 关键源码片段 / 评论区精华 and [R2] Summary: one expert on one row.
- *   a[r] = sum_h w13[r, h] * x[h]                 r in [0, 2I), h ascending
+/* Rows of one expert's w13: gate and up (2I) for the gated activations,
+ * the single w1 projection (I) for ReLU2. */
+static int orc_w13_rows(const orc_act_params *prm, int I) {
+  return prm->act == ORC_ACT_RELU2 ? I : 2 * I;
+}
+
+/* [R3] 实现拆解 / 关键源码片段 / 评论区精华 and [R2] Summary: one expert on
+ * one row.
+ *   a[r] = sum_h w13[r, h] * x[h]                 r in [0, rows), h ascending
  *   packed:      gate_i = a[i],    up_i = a[I + i]
  *   interleaved: gate_i = a[2i],   up_i = a[2i + 1]
- *   SwiGLU:      h_i = (g * sigmoid(g)) * u
+ *   SwiGLU:      g = min(g, limit), u = clamp(u, -limit, limit) (limit +inf
+ *                unless set), h_i = (g * sigmoid(g)) * u
  *   SwiGLU-OAI:  g = min(g, limit), u = clamp(u, -limit, limit),
  *                h_i = (g * sigmoid(alpha * g)) * (u + beta)
+ *   ReLU2:       h_i = max(a[i], 0)^2               (non-gated, rows = I)
  *   h_i stored as bf16
  *   y[c] = sum_i w2[c, i] * h_i                   c in [0, H), i ascending
- * a_out (2I doubles), h_out (I bf16) may be NULL. */
+ * a_out (rows doubles), h_out (I bf16) may be NULL. */
 static int orc_expert_row_impl(const uint16_t *x, const uint16_t *w13, const uint16_t *w2, int H,
                                int I, const orc_act_params *prm, double *a, uint16_t *hb,
                                double *y) {
-  for (int r = 0; r < 2 * I; ++r) {
+  const int rows = orc_w13_rows(prm, I);
+  for (int r = 0; r < rows; ++r) {
     const uint16_t *wr = w13 + (int64_t)r * H;
     double s = 0.0;
     for (int h = 0; h < H; ++h) s += orc_bf16_to_f64(wr[h]) * orc_bf16_to_f64(x[h]);
     a[r] = s;
   }
   for (int i = 0; i < I; ++i) {
+    if (prm->act == ORC_ACT_RELU2) {
+      const double r = a[i] > 0.0 ? a[i] : 0.0;
+      hb[i] = orc_f64_to_bf16(r * r);
+      continue;
+    }
     double g, u;
     if (prm->layout == ORC_LAYOUT_PACKED) {
       g = a[i];
@@ -213,15 +231,14 @@ static int orc_expert_row_impl(const uint16_t *x, const uint16_t *w13, const uin
       g = a[2 * i];
       u = a[2 * i + 1];
     }
+    if (g > prm->limit) g = prm->limit;
+    if (u > prm->limit) u = prm->limit;
+    if (u < -prm->limit) u = -prm->limit;
     double hv;
-    if (prm->act == ORC_ACT_SWIGLU) {
+    if (prm->act == ORC_ACT_SWIGLU)
       hv = (g * orc_sigmoid(g)) * u;
-    } else {
-      if (g > prm->limit) g = prm->limit;
-      if (u > prm->limit) u = prm->limit;
-      if (u < -prm->limit) u = -prm->limit;
+    else
       hv = (g * orc_sigmoid(prm->alpha * g)) * (u + prm->beta);
-    }
     hb[i] = orc_f64_to_bf16(hv);
   }
   for (int c = 0; c < H; ++c) {
@@ -235,7 +252,9 @@ static int orc_expert_row_impl(const uint16_t *x, const uint16_t *w13, const uin
 
 static int orc_check_params(const orc_act_params *p) {
   if (!p) return 0;
-  if (p->act != ORC_ACT_SWIGLU && p->act != ORC_ACT_SWIGLU_OAI) return 0;
+  if (p->act != ORC_ACT_SWIGLU && p->act != ORC_ACT_SWIGLU_OAI && p->act != ORC_ACT_RELU2)
+    return 0;
+  if (isnan(p->limit) || p->limit < 0.0) return 0;
   if (p->layout != ORC_LAYOUT_PACKED && p->layout != ORC_LAYOUT_INTERLEAVED) return 0;
   return 1;
 }
@@ -244,11 +263,12 @@ static int orc_check_params(const orc_act_params *p) {
 int orc_expert_row(const uint16_t *x, const uint16_t *w13, const uint16_t *w2, int H, int I,
                    const orc_act_params *prm, double *a_out, uint16_t *h_out, double *y_out) {
   if (H < 1 || I < 1 || !orc_check_params(prm)) return ORC_BAD_ARG;
-  double *a = (double *)malloc(sizeof(double) * 2 * (size_t)I);
+  const int rows = orc_w13_rows(prm, I);
+  double *a = (double *)malloc(sizeof(double) * (size_t)rows);
   uint16_t *hb = (uint16_t *)malloc(sizeof(uint16_t) * (size_t)I);
   if (!a || !hb) { free(a); free(hb); return ORC_BAD_ARG; }
   orc_expert_row_impl(x, w13, w2, H, I, prm, a, hb, y_out);
-  if (a_out) memcpy(a_out, a, sizeof(double) * 2 * (size_t)I);
+  if (a_out) memcpy(a_out, a, sizeof(double) * (size_t)rows);
   if (h_out) memcpy(h_out, hb, sizeof(uint16_t) * (size_t)I);
   free(a);
   free(hb);
@@ -311,8 +331,8 @@ int orc_ffn(const uint16_t *x, const int32_t *topk_indx, const uint16_t *topk_va
           int j = slot_order[jj];
           int e = topk_indx[t * k + j];
           double wgt = orc_bf16_to_f64(topk_vals[t * k + j]);
-          orc_expert_row_impl(xt, w13 + (int64_t)e * 2 * I * H, w2 + (int64_t)e * H * I, H, I,
-                              prm, a, hb, y);
+          orc_expert_row_impl(xt, w13 + (int64_t)e * orc_w13_rows(prm, I) * H,
+                              w2 + (int64_t)e * H * I, H, I, prm, a, hb, y);
           for (int c = 0; c < H; ++c) acc[c] += y[c] * wgt;
           if (y_slot)
             for (int c = 0; c < H; ++c) y_slot[(s * k + j) * H + c] = y[c] * wgt;

@@ -8,6 +8,11 @@
   report defines them (关键源码片段: interleaved gate = w13[:, 0::2],
   up = w13[:, 1::2]; packed halves [gate; up]);
 * SwiGLU-OAI with alpha=1, beta=0, no clamp equals SwiGLU bit for bit;
+  SwiGLU with a clamp limit ("SILU + clamp", 实现拆解 and 关键源码片段: SiLU
+  forwards only the limit) equals SwiGLU-OAI with alpha=1, beta=0 and that
+  limit, and clamps at hand-worked points;
+* the non-gated ReLU2 ("RELU2_NO_MUL", 实现拆解) at hand-worked points
+  through one-row selectors, and as a dense E = 1 layer against numpy;
 * the combine equals the masked per-expert index_add_ loop of the MiniMind
   issue (Summary) and the sorted dispatch ("It is removable in plain
   PyTorch") bit for bit;
@@ -247,3 +252,106 @@ def test_thread_count_does_not_change_bits(monkeypatch):
         outs.append(subprocess.run([sys.executable, "-c", code], cwd=root, env=env,
                                    capture_output=True, text=True, check=True).stdout)
     assert outs[0] == outs[1]
+
+
+@pytest.mark.parametrize("layout", ["packed", "interleaved"])
+def test_swiglu_clamp_at_worked_points(layout):
+    xs = [10.0, -9.0, 9.0, 2.0, -3.0, 0.5, 1.0, -1.0]
+    x = _b(xs)
+    pairs = [(0, 1), (0, 2), (3, 2), (4, 5), (1, 6), (6, 7)]
+    w13, w2 = _selector_expert(8, len(pairs), [p[0] for p in pairs], [p[1] for p in pairs],
+                               layout)
+    _, h, _ = oracle.expert_row(x, w13, w2, act="swiglu", layout=layout, limit=3.0)
+
+    def silu_clamp(g, u, limit=3.0):
+        g = min(g, limit)
+        u = max(-limit, min(u, limit))
+        return _silu(g) * u
+
+    expected = [silu_clamp(xs[g], xs[u]) for g, u in pairs]
+    np.testing.assert_array_equal(h, oracle.f64_to_bf16(np.array(expected)))
+    # gate 10 -> 3 and up -9 -> -3: silu(3) * -3 = -8.5732 -> bf16 -8.5625
+    assert oracle.bf16_to_f64(h[0]) == -8.5625
+    # gate 10 -> 3 and up 9 -> 3: +8.5625; gate 2 stays, up 9 -> 3: silu(2)*3 = 5.2848 -> 5.28125
+    assert oracle.bf16_to_f64(h[1]) == 8.5625 and oracle.bf16_to_f64(h[2]) == 5.28125
+    # the gate is not clamped from below: silu(-9) * 1 ~ -1.1e-3
+    assert -2e-3 < oracle.bf16_to_f64(h[4]) < -1e-3
+    # without the limit the same inputs differ (the clamp acts)
+    _, h_free, _ = oracle.expert_row(x, w13, w2, act="swiglu", layout=layout)
+    assert not np.array_equal(h, h_free)
+
+
+def test_swiglu_clamp_equals_oai_with_unit_alpha_zero_beta():
+    rng = np.random.default_rng(5)
+    H, Idim = 64, 48
+    x = _b(rng.standard_normal(H) * 3)
+    w13 = _b(rng.standard_normal((2 * Idim, H)) * 0.5)
+    w2 = _b(rng.standard_normal((H, Idim)) * 0.1)
+    for layout in ("packed", "interleaved"):
+        for limit in (0.5, 2.0, 7.0):
+            s = oracle.expert_row(x, w13, w2, act="swiglu", layout=layout, limit=limit)
+            o = oracle.expert_row(x, w13, w2, act="swiglu_oai", layout=layout, alpha=1.0,
+                                  beta=0.0, limit=limit)
+            np.testing.assert_array_equal(s[1], o[1])
+            np.testing.assert_array_equal(s[2], o[2])
+
+
+def test_relu2_at_worked_points():
+    xs = [3.0, -2.0, 0.5, 0.0, -0.25, 1.5, 4.0, -8.0]
+    x = _b(xs)
+    H, Idim = 8, 8
+    w1 = np.zeros((Idim, H), dtype=np.uint16)   # non-gated: I rows, row i picks x[src[i]]
+    src = [0, 1, 2, 3, 4, 5, 6, 7]
+    for i, j in enumerate(src):
+        w1[i, j] = ONE
+    w2 = np.zeros((H, Idim), dtype=np.uint16)
+    for i in range(Idim):
+        w2[i, i] = ONE
+    a, h, y = oracle.expert_row(x, w1, w2, act="relu2")
+    assert a.shape == (Idim,)
+    # max(v, 0)^2, all exact in bf16: 9, 0, 0.25, 0, 0, 2.25, 16, 0
+    assert oracle.bf16_to_f64(h).tolist() == [9.0, 0.0, 0.25, 0.0, 0.0, 2.25, 16.0, 0.0]
+    np.testing.assert_array_equal(oracle.f64_to_bf16(y), h)
+    # two picks summed before the activation: (3 + -2)^2 = 1, (-2 + 0.5) -> 0
+    w1b = np.zeros((2, H), dtype=np.uint16)
+    w1b[0, 0] = w1b[0, 1] = ONE
+    w1b[1, 1] = w1b[1, 2] = ONE
+    _, hb, _ = oracle.expert_row(x, w1b, np.zeros((H, 2), dtype=np.uint16), act="relu2")
+    assert oracle.bf16_to_f64(hb).tolist() == [1.0, 0.0]
+
+
+def test_relu2_rejects_a_clamp_limit():
+    with pytest.raises(ValueError):
+        oracle.act_params(act="relu2", limit=3.0)
+
+
+def test_single_expert_relu2_layer_against_numpy():
+    """E = 1, k = 1, ReLU2: a dense non-gated MLP, bf16(W2 . bf16(max(W1 x, 0)^2))."""
+    case = I.LayerCase("dense_relu2", n=40, H=64, E=1, k=1, I=96, act="relu2")
+    d = I.layer_inputs(case)
+    assert d["w13"].shape == (1, case.I, case.H)
+    indx, vals = oracle.route(d["logits"], 1)
+    out = oracle.bf16_to_f64(oracle.ffn(d["x"], indx, vals, d["w13"], d["w2"], act="relu2"))
+    x = oracle.bf16_to_f64(d["x"])
+    a = x @ oracle.bf16_to_f64(d["w13"][0]).T
+    h = oracle.bf16_to_f64(oracle.f64_to_bf16(np.maximum(a, 0.0) ** 2))
+    ref = h @ oracle.bf16_to_f64(d["w2"][0]).T
+    err = np.abs(out - ref)
+    half_ulp = np.ldexp(1.0, np.frexp(np.abs(ref))[1] - 9)
+    assert np.all(err <= 3 * half_ulp), (err / half_ulp).max()
+    assert (err <= half_ulp * (1 + 1e-9)).mean() > 0.99
+
+
+@pytest.mark.parametrize("k", [1, 2])
+def test_relu2_combine_equals_masked_per_expert_loop(k):
+    case = I.LayerCase("t_relu2", n=33, H=64, E=8, k=k, I=128, act="relu2")
+    d = I.layer_inputs(case)
+    indx, vals = oracle.route(d["logits"], k)
+    out = oracle.ffn(d["x"], indx, vals, d["w13"], d["w2"], act="relu2")
+    acc = np.zeros((case.n, case.H))
+    for e in range(case.E):
+        tok, slot = np.nonzero(indx == e)
+        for t, j in zip(tok, slot):
+            _, _, y = oracle.expert_row(d["x"][t], d["w13"][e], d["w2"][e], act="relu2")
+            acc[t] += y * oracle.bf16_to_f64(vals[t, j])
+    np.testing.assert_array_equal(out, oracle.f64_to_bf16(acc))
