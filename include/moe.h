@@ -79,14 +79,23 @@ typedef enum {
   MOE_GATING_SOFTMAX_ALL = 1   /* softmax over all E logits; keep the k selected, no renormalising */
 } moe_gating;
 
-/* Gated activation [R3] 关键源码片段 (apply). */
+/* Expert activation [R3] 实现拆解 (the five activation cases: SILU, SILU +
+ * clamp, RELU2_NO_MUL, SWIGLUOAI, SWIGLUOAI_UNINTERLEAVE) and 关键源码片段
+ * (apply: SiLU forwards only the clamp limit, SwiGLU-OAI alpha / beta /
+ * limit). The two SwiGLU-OAI cases are MOE_ACT_SWIGLU_OAI with the
+ * interleaved or the packed w13 layout. */
 typedef enum {
-  MOE_ACT_SWIGLU = 0,    /* h = gate * sigmoid(gate) * up */
-  MOE_ACT_SWIGLU_OAI = 1 /* g = min(gate, limit), u = clamp(up, -limit, limit),
-                            h = g * sigmoid(alpha * g) * (u + beta) */
+  MOE_ACT_SWIGLU = 0,     /* h = silu(g) * u; with MOE_SET_LIMIT ("SILU + clamp")
+                             g = min(gate, limit), u = clamp(up, -limit, limit)
+                             first, else g = gate, u = up */
+  MOE_ACT_SWIGLU_OAI = 1, /* g = min(gate, limit), u = clamp(up, -limit, limit),
+                             h = g * sigmoid(alpha * g) * (u + beta) */
+  MOE_ACT_RELU2 = 2       /* non-gated: w13 holds one projection of I rows per
+                             expert ([E, I, H]), h = max(w1 . x, 0)^2;
+                             w13_layout is ignored */
 } moe_activation;
 
-/* Row order of w13 [E, 2I, H] [R3] 关键源码片段 (reorder_w13_to_w31_for_flashinfer_cutedsl). */
+/* Row order of the gated w13 [E, 2I, H] [R3] 关键源码片段 (reorder_w13_to_w31_for_flashinfer_cutedsl). */
 typedef enum {
   MOE_W13_PACKED = 0,     /* rows [gate_0 .. gate_{I-1}, up_0 .. up_{I-1}] */
   MOE_W13_INTERLEAVED = 1 /* rows [gate_0, up_0, gate_1, up_1, ...] (gpt-oss checkpoints) */
@@ -95,7 +104,9 @@ typedef enum {
 /* Flags of moe_params.set: a value whose flag is clear is NOT used; the
  * activation keeps its own default ([R3] 关键源码片段 / 评论区精华: unset
  * parameters must not override the kernel defaults). SwiGLU-OAI defaults:
- * alpha 1.702, beta 1.0, limit 7.0. Plain SwiGLU takes no parameters. */
+ * alpha 1.702, beta 1.0, limit 7.0. SwiGLU takes only a limit (no clamp
+ * when unset; alpha / beta are ignored). ReLU2 takes none (alpha / beta are
+ * ignored, a limit is MOE_ERR_UNSUPPORTED). A limit must be >= 0. */
 #define MOE_SET_ALPHA 1u
 #define MOE_SET_BETA 2u
 #define MOE_SET_LIMIT 4u
@@ -232,7 +243,7 @@ moe_status moe_build_metadata_noalloc(const int32_t *topk_indx, const uint16_t *
  *   x       [n, H] bf16 tokens.
  *   meta    metadata from moe_build_metadata (offs, col_sorted, gate_scal read).
  *   w13     [E, 2I, H] bf16, row-major (each expert's [2I, H] block in
- *           params->w13_layout order).
+ *           params->w13_layout order); [E, I, H] for MOE_ACT_RELU2.
  *   w2      [E, H, I] bf16, row-major.
  *   y_flat  [n*k, H] bf16 out, token-slot order: row f = gate_scal[row_sorted[f]]
  *           * (w2_e . h), e = topk_indx_flat[f], h = act(w13_e . x_t) rounded
@@ -250,8 +261,8 @@ moe_status moe_combine(const uint16_t *y_flat, int64_t n, int32_t k, int32_t H, 
                        moe_stream stream);
 
 /* Stages 1-4 in one call, zero host synchronisations, CUDA-graph friendly.
- *   x [n, H] bf16, logits [n, E] fp32, w13 [E, 2I, H] bf16, w2 [E, H, I] bf16,
- *   out [n, H] bf16.
+ *   x [n, H] bf16, logits [n, E] fp32, w13 [E, 2I, H] bf16 ([E, I, H] for
+ *   MOE_ACT_RELU2), w2 [E, H, I] bf16, out [n, H] bf16.
  *   topk_indx / topk_vals ([n, k]) and meta: optional outputs (NULL = keep
  *   them inside the workspace). When given, all five meta arrays must be
  *   non-NULL. */

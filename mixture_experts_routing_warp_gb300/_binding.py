@@ -18,7 +18,7 @@ import torch
 from . import build as _build
 
 GATING = {"softmax_topk": 0, "softmax_all": 1}
-ACT = {"swiglu": 0, "swiglu_oai": 1}
+ACT = {"swiglu": 0, "swiglu_oai": 1, "relu2": 2}
 LAYOUT = {"packed": 0, "interleaved": 1}
 SET_ALPHA, SET_BETA, SET_LIMIT = 1, 2, 4
 FFN_KERNEL = {"auto": 0, "tiled": 1, "swap": 2}
@@ -222,6 +222,12 @@ def route_metadata(logits: torch.Tensor, k: int, E: Optional[int] = None,
     return indx, vals, m
 
 
+def _intermediate(w13: torch.Tensor, params: MoeParams) -> int:
+    """I from w13's rows: 2I for the gated activations, I for ReLU2."""
+    rows = w13.shape[1]
+    return rows if params.activation == ACT["relu2"] else rows // 2
+
+
 def grouped_ffn(x: torch.Tensor, meta: dict, w13: torch.Tensor, w2: torch.Tensor, k: int,
                 ws: torch.Tensor, params: MoeParams,
                 y_flat: Optional[torch.Tensor] = None) -> torch.Tensor:
@@ -229,12 +235,14 @@ def grouped_ffn(x: torch.Tensor, meta: dict, w13: torch.Tensor, w2: torch.Tensor
     _need(x, "x", torch.bfloat16)
     n, H = x.shape
     _need(w13, "w13", torch.bfloat16)
-    E, I2, _ = w13.shape
-    _need(w2, "w2", torch.bfloat16, (E, H, I2 // 2))
+    E = w13.shape[0]
+    I = _intermediate(w13, params)
+    _need(w13, "w13", torch.bfloat16, (E, w13.shape[1], H))
+    _need(w2, "w2", torch.bfloat16, (E, H, I))
     if y_flat is None:
         y_flat = torch.empty((n * k, H), dtype=torch.bfloat16, device=x.device)
     _check(lib().moe_grouped_ffn(_ptr(x), ctypes.byref(_meta_struct(meta)), _ptr(w13), _ptr(w2),
-                                 n, E, k, H, I2 // 2, ctypes.byref(params), _ptr(y_flat),
+                                 n, E, k, H, I, ctypes.byref(params), _ptr(y_flat),
                                  _ptr(ws), ws.numel(), _stream(x.device)), "moe_grouped_ffn")
     return y_flat
 
@@ -260,8 +268,8 @@ def forward(x: torch.Tensor, logits: torch.Tensor, w13: torch.Tensor, w2: torch.
     _need(logits, "logits", torch.float32)
     E = logits.shape[1]
     _need(w13, "w13", torch.bfloat16)
-    I = w13.shape[1] // 2
-    _need(w13, "w13", torch.bfloat16, (E, 2 * I, H))
+    I = _intermediate(w13, params)
+    _need(w13, "w13", torch.bfloat16, (E, w13.shape[1], H))
     _need(w2, "w2", torch.bfloat16, (E, H, I))
     if out is None:
         out = torch.empty((n, H), dtype=torch.bfloat16, device=x.device)
@@ -283,7 +291,7 @@ def forward_timed(x: torch.Tensor, logits: torch.Tensor, w13: torch.Tensor, w2: 
     the stage kernels (events[i] before stage i, the last after the end)."""
     n, H = x.shape
     E = logits.shape[1]
-    I = w13.shape[1] // 2
+    I = _intermediate(w13, params)
     if out is None:
         out = torch.empty((n, H), dtype=torch.bfloat16, device=x.device)
     if len(events) != len(STAGES) + 1:

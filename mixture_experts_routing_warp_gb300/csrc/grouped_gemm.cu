@@ -13,7 +13,8 @@
 //    PR #45457 report), 关键源码片段: gate_scal in sorted order and the
 //    scatter (row_sorted, col_sorted) back to token-slot order.
 //
-// ffn1:  h[p, :]            = act(w13_e . X_sorted[p])         (EPI_ACT)
+// ffn1:  h[p, :]            = act(w13_e . X_sorted[p])         (EPI_ACT,
+//        gated; EPI_RELU2: h = max(w1_e . X_sorted[p], 0)^2, non-gated)
 // ffn2:  y_flat[col_sorted[p], :] = gate_scal[p] * (w2_e . h[p]) (EPI_SCATTER)
 // for p in expert e's slice [offs[e], offs[e+1]).
 //
@@ -57,7 +58,7 @@ constexpr int kSmemBytes = 1024 /*alignment slack*/ + STAGES * (A_BYTES + B_BYTE
 
 constexpr uint32_t kIdesc = make_idesc_bf16(BM, BN);
 
-enum { EPI_ACT = 0, EPI_SCATTER = 1 };
+enum { EPI_ACT = 0, EPI_SCATTER = 1, EPI_RELU2 = 2 };
 
 struct GemmArgs {
   const int32_t *offs;
@@ -231,7 +232,28 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t tbase = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * BN);
       const int p = d.m0 + row;
       const bool valid = p < d.m_end;
-      if (EPI == EPI_ACT) {
+      if (EPI == EPI_RELU2) {
+        // column j of the tile is h column nt*256 + j
+        uint16_t *hrow = args.h_out + (size_t)p * args.I;
+#pragma unroll 1
+        for (int c = 0; c < 8; ++c) {
+          uint32_t r[32];
+          TMEM_LD32(tbase + c * 32, r);
+          tmem_wait_ld();
+          const int col = d.nt * BN + c * 32;
+          if (valid && col < args.I) {
+            uint32_t o[16];
+#pragma unroll
+            for (int j = 0; j < 16; ++j)
+              o[j] = pack_bf16x2(relu2(__uint_as_float(r[2 * j])),
+                                 relu2(__uint_as_float(r[2 * j + 1])));
+            uint4 *dst = reinterpret_cast<uint4 *>(hrow + col);
+#pragma unroll
+            for (int v = 0; v < 4; ++v)
+              dst[v] = make_uint4(o[4 * v], o[4 * v + 1], o[4 * v + 2], o[4 * v + 3]);
+          }
+        }
+      } else if (EPI == EPI_ACT) {
         uint16_t *hrow = args.h_out + (size_t)p * args.I;
         if (PACKED) {
           // columns [0,128) gate_j, [128,256) up_j -> h columns nt*128 + j
@@ -345,10 +367,12 @@ cudaError_t launch_ffn(const uint16_t *x_sorted, const int32_t *offs, const int3
   if (act.ffn_kernel == MOE_FFN_SWAP || (act.ffn_kernel == MOE_FFN_AUTO && use_swap_ffn(N, E)))
     return launch_ffn_swap(x_sorted, offs, col_sorted, gate_scal, w13, w2, N, E, H, I, act, h_buf,
                            y_flat, ctrl, s, ev_ffn);
-  const bool packed = act.layout == MOE_W13_PACKED;
+  const bool relu2_act = act.act == MOE_ACT_RELU2;
+  const bool packed = !relu2_act && act.layout == MOE_W13_PACKED;
   CUtensorMap ta1, tb1, ta2, tb2;
   if (!map_2d(&ta1, x_sorted, (uint64_t)N, (uint64_t)H, BM) ||
-      !map_3d(&tb1, w13, (uint64_t)E, 2ull * I, (uint64_t)H, packed ? BN / 2 : BN) ||
+      !map_3d(&tb1, w13, (uint64_t)E, (uint64_t)w13_rows(act, I), (uint64_t)H,
+              packed ? BN / 2 : BN) ||
       !map_2d(&ta2, h_buf, (uint64_t)N, (uint64_t)I, BM) ||
       !map_3d(&tb2, w2, (uint64_t)E, (uint64_t)H, (uint64_t)I, BN))
     return cudaErrorInvalidValue;
@@ -368,9 +392,15 @@ cudaError_t launch_ffn(const uint16_t *x_sorted, const int32_t *offs, const int3
 
   if (ev_ffn && record_stage_event(ev_ffn[0], s) != cudaSuccess) return cudaErrorUnknown;
   a.num_kb = H / BK;
-  a.n_tiles = (I + BN / 2 - 1) / (BN / 2);  // each tile yields 128 h columns
-  cudaError_t err = packed ? launch_gemm<EPI_ACT, true>(ta1, tb1, a, s)
-                           : launch_gemm<EPI_ACT, false>(ta1, tb1, a, s);
+  cudaError_t err;
+  if (relu2_act) {
+    a.n_tiles = (I + BN - 1) / BN;  // each tile yields 256 h columns
+    err = launch_gemm<EPI_RELU2, false>(ta1, tb1, a, s);
+  } else {
+    a.n_tiles = (I + BN / 2 - 1) / (BN / 2);  // each tile yields 128 h columns
+    err = packed ? launch_gemm<EPI_ACT, true>(ta1, tb1, a, s)
+                 : launch_gemm<EPI_ACT, false>(ta1, tb1, a, s);
+  }
   if (err != cudaSuccess) return err;
 
   if (ev_ffn && record_stage_event(ev_ffn[1], s) != cudaSuccess) return cudaErrorUnknown;

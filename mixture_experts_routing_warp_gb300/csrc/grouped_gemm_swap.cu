@@ -18,6 +18,7 @@
 //     adjacent TMEM lanes: one shuffle pairs them.
 //   ffn1, packed w13: the gate rows and the up rows of the same h columns go
 //     to two accumulators, so each thread holds its pair.
+//   ffn1, ReLU2 (non-gated): weight row f0 + w is h column f0 + w.
 //   ffn2: y_flat[col_sorted[m0 + j], f0 + w] = gate_scal[m0 + j] * D[w, j].
 //
 // Warps: 0 TMA producer, 1 TMEM allocation + MMA issue, 2-5 epilogue (warp
@@ -39,7 +40,7 @@ constexpr int SW_A_BYTES = SW_M * SW_BK * 2;  // 16 KB of weights
 constexpr int SW_B_BYTES = SW_N * SW_BK * 2;  // 4 KB of token rows
 constexpr uint32_t kSwIdesc = make_idesc_bf16(SW_M, SW_N);
 
-enum { SW_ACT = 0, SW_SCATTER = 1 };
+enum { SW_ACT = 0, SW_SCATTER = 1, SW_RELU2 = 2 };
 
 template <bool DUAL>  // DUAL: gate and up weight tiles in each stage
 struct SwCfg {
@@ -251,6 +252,12 @@ __global__ void __launch_bounds__(SW_THREADS, 1)
               args.y_out[(size_t)dst * args.H + frow] =
                   float_to_bf16_bits(__uint_as_float(r0[i]) * g);
           }
+        } else if (EPI == SW_RELU2) {
+#pragma unroll
+          for (int i = 0; i < 8; ++i)
+            if (c0 + i < rows && frow < args.I)
+              args.h_out[(size_t)(d.m0 + c0 + i) * args.I + frow] =
+                  float_to_bf16_bits(relu2(__uint_as_float(r0[i])));
         } else if (DUAL) {
 #pragma unroll
           for (int i = 0; i < 8; ++i)
@@ -313,9 +320,10 @@ cudaError_t launch_ffn_swap(const uint16_t *x_sorted, const int32_t *offs,
                             int I, const ActParams &act, uint16_t *h_buf, uint16_t *y_flat,
                             uint32_t *ctrl, cudaStream_t s, cudaEvent_t *ev_ffn) {
   if (N == 0) return cudaSuccess;
-  const bool packed = act.layout == MOE_W13_PACKED;
+  const bool relu2_act = act.act == MOE_ACT_RELU2;
+  const bool packed = !relu2_act && act.layout == MOE_W13_PACKED;
   CUtensorMap tw1, tx1, tw2, tx2;
-  if (!map_3d(&tw1, w13, (uint64_t)E, 2ull * I, (uint64_t)H, SW_M) ||
+  if (!map_3d(&tw1, w13, (uint64_t)E, (uint64_t)w13_rows(act, I), (uint64_t)H, SW_M) ||
       !map_2d(&tx1, x_sorted, (uint64_t)N, (uint64_t)H, SW_N) ||
       !map_3d(&tw2, w2, (uint64_t)E, (uint64_t)H, (uint64_t)I, SW_M) ||
       !map_2d(&tx2, h_buf, (uint64_t)N, (uint64_t)I, SW_N))
@@ -335,9 +343,10 @@ cudaError_t launch_ffn_swap(const uint16_t *x_sorted, const int32_t *offs,
 
   if (ev_ffn && record_stage_event(ev_ffn[0], s) != cudaSuccess) return cudaErrorUnknown;
   a.num_kb = H / SW_BK;
-  a.f_tiles = packed ? (I + SW_M - 1) / SW_M : (2 * I + SW_M - 1) / SW_M;
-  cudaError_t err = packed ? launch_swap<SW_ACT, true>(tw1, tx1, a, s)
-                           : launch_swap<SW_ACT, false>(tw1, tx1, a, s);
+  a.f_tiles = (w13_rows(act, I) / (packed ? 2 : 1) + SW_M - 1) / SW_M;
+  cudaError_t err = relu2_act ? launch_swap<SW_RELU2, false>(tw1, tx1, a, s)
+                    : packed  ? launch_swap<SW_ACT, true>(tw1, tx1, a, s)
+                              : launch_swap<SW_ACT, false>(tw1, tx1, a, s);
   if (err != cudaSuccess) return err;
 
   if (ev_ffn && record_stage_event(ev_ffn[1], s) != cudaSuccess) return cudaErrorUnknown;

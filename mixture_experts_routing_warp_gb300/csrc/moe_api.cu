@@ -28,7 +28,8 @@ moe_status resolve_params(const moe_params *p, ActParams &out, int *gating) {
   if (!p) return MOE_ERR_INVALID_ARG;
   if (p->gating != MOE_GATING_SOFTMAX_TOPK && p->gating != MOE_GATING_SOFTMAX_ALL)
     return MOE_ERR_INVALID_ARG;
-  if (p->activation != MOE_ACT_SWIGLU && p->activation != MOE_ACT_SWIGLU_OAI)
+  if (p->activation != MOE_ACT_SWIGLU && p->activation != MOE_ACT_SWIGLU_OAI &&
+      p->activation != MOE_ACT_RELU2)
     return MOE_ERR_INVALID_ARG;
   if (p->w13_layout != MOE_W13_PACKED && p->w13_layout != MOE_W13_INTERLEAVED)
     return MOE_ERR_INVALID_ARG;
@@ -46,9 +47,14 @@ moe_status resolve_params(const moe_params *p, ActParams &out, int *gating) {
     out.limit = (p->set & MOE_SET_LIMIT) ? p->limit : 7.0f;
     if (!isfinite(out.alpha) || !isfinite(out.beta) || isnan(out.limit) || out.limit < 0.f)
       return MOE_ERR_INVALID_ARG;
+  } else if (p->activation == MOE_ACT_SWIGLU) {
+    // SwiGLU takes no alpha / beta; a limit clamps gate and up ("SILU + clamp").
+    out.alpha = 1.f;
+    out.beta = 0.f;
+    out.limit = (p->set & MOE_SET_LIMIT) ? p->limit : INFINITY;
+    if (isnan(out.limit) || out.limit < 0.f) return MOE_ERR_INVALID_ARG;
   } else {
-    // Plain SwiGLU takes no alpha / beta; a clamp limit (SiLU + clamp) is
-    // not implemented.
+    // ReLU2 takes no parameters; a clamp limit is not part of it.
     if (p->set & MOE_SET_LIMIT) return MOE_ERR_UNSUPPORTED;
     out.alpha = 1.f;
     out.beta = 0.f;

@@ -138,16 +138,30 @@ struct ActParams {
   int ffn_kernel;  // moe_ffn_kernel (host-side choice of the GEMM kernel)
 };
 
-// SwiGLU: (g * sigmoid(g)) * u.  SwiGLU-OAI: g = min(g, limit),
-// u = clamp(u, -limit, limit), (g * sigmoid(alpha g)) * (u + beta).
+// Gated activations of (gate, up). SwiGLU: (g * sigmoid(g)) * u, with
+// g = min(g, limit), u = clamp(u, -limit, limit) first when a limit is set.
+// SwiGLU-OAI: the same clamps, then (g * sigmoid(alpha g)) * (u + beta).
 __device__ __forceinline__ float activate(float g, float u, const ActParams &p) {
   if (p.act == MOE_ACT_SWIGLU_OAI) {
     g = fminf(g, p.limit);
     u = fminf(fmaxf(u, -p.limit), p.limit);
     return (g * (1.0f / (1.0f + expf(-p.alpha * g)))) * (u + p.beta);
   }
+  if (p.limit < INFINITY) {
+    g = fminf(g, p.limit);
+    u = fminf(fmaxf(u, -p.limit), p.limit);
+  }
   return (g * (1.0f / (1.0f + expf(-g)))) * u;
 }
+
+// The non-gated ReLU2: max(a, 0)^2.
+__device__ __forceinline__ float relu2(float a) {
+  const float r = fmaxf(a, 0.0f);
+  return r * r;
+}
+
+// Rows of one expert's w13: 2I (gate and up) or I (ReLU2).
+inline int w13_rows(const ActParams &p, int I) { return p.act == MOE_ACT_RELU2 ? I : 2 * I; }
 
 // Stage-timing event record: a plain record on an eager stream, an external
 // record (an event-record node of the graph) while the stream is capturing.

@@ -102,8 +102,14 @@ def test_ffn_and_forward_parameter_rules(L):
                                  a["H"], a["I"], ctypes.byref(params), good, ws, a["ws_bytes"],
                                  None)
 
-    # a clamp limit on plain SwiGLU is not implemented
-    assert ffn(moe.make_params(act="swiglu", limit=7.0)) == 2
+    # SwiGLU takes a clamp limit ("SILU + clamp"), which must be >= 0 and not NaN;
+    # ReLU2 takes none
+    assert ffn(moe.make_params(act="swiglu", limit=-1.0)) == 1
+    assert ffn(moe.make_params(act="swiglu", limit=float("nan"))) == 1
+    assert ffn(moe.make_params(act="relu2", limit=3.0)) == 2
+    bad = moe.make_params()
+    bad.activation = 3
+    assert ffn(bad) == 1
     # alpha / beta are not parameters of plain SwiGLU: ignored, and n = 0 is a no-op
     assert ffn(moe.make_params(act="swiglu", alpha=2.0), n=0) == 0
     assert ffn(moe.make_params(act="swiglu_oai", limit=-1.0)) == 1

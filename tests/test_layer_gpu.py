@@ -143,6 +143,11 @@ VARIANTS = [
      {"alpha": 1.5, "beta": 0.5, "limit": 3.0}),
     ("oai_limit_only", 128, 4, 4, 256, "swiglu_oai", "interleaved", {"limit": 2.0}),
     ("k8_e16", 64, 16, 8, 64, "swiglu", "packed", {}),
+    # SiLU + clamp (a limit on plain SwiGLU) and the non-gated ReLU2
+    ("silu_clamp_packed", 192, 8, 3, 320, "swiglu", "packed", {"limit": 0.5}),
+    ("silu_clamp_interleaved", 128, 6, 2, 192, "swiglu", "interleaved", {"limit": 1.0}),
+    ("relu2", 192, 8, 3, 320, "relu2", "packed", {}),
+    ("relu2_k1", 256, 4, 1, 128, "relu2", "packed", {}),
 ]
 
 
@@ -167,7 +172,8 @@ def test_gptoss_decode_tiled_kernel(n):
     _check_full(Layer(I.GPTOSS.with_n(n), ffn_kernel="tiled"))
 
 
-@pytest.mark.parametrize("layout,act", [("packed", "swiglu"), ("interleaved", "swiglu_oai")])
+@pytest.mark.parametrize("layout,act", [("packed", "swiglu"), ("interleaved", "swiglu_oai"),
+                                        ("packed", "relu2")])
 @pytest.mark.parametrize("n", [1, 5, 40])
 def test_swap_kernel_deep_k(layout, act, n):
     """The swap kernel with 16 K-blocks per tile in both contractions
@@ -192,11 +198,12 @@ def test_auto_kernel_choice_boundary():
         _check_full(Layer(case))
 
 
-def test_stages_compose_to_forward():
+@pytest.mark.parametrize("act,layout", [("swiglu_oai", "interleaved"), ("relu2", "packed")])
+def test_stages_compose_to_forward(act, layout):
     """route -> build_metadata -> grouped_ffn -> combine equals moe_forward bit for bit,
     and the per-slot outputs match the oracle's gate-weighted expert outputs."""
-    case = I.LayerCase("stages", n=200, H=128, E=8, k=3, I=192, act="swiglu_oai",
-                       layout="interleaved", w_std=0.1)
+    case = I.LayerCase("stages", n=200, H=128, E=8, k=3, I=192, act=act, layout=layout,
+                       w_std=0.1)
     L = Layer(case)
     out_fwd = L.forward()[0]
     ws = moe.workspace(case.n, case.E, case.k, case.H, case.I)
