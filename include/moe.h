@@ -116,12 +116,13 @@ typedef enum {
  * rounded to bf16); they tile the work differently, so the last bits of an
  * output may differ between them. No counterpart on the pages: a choice of
  * this implementation.
- *   AUTO   SWAP when n*k <= 32*E (on average at most one 32-row token tile
- *          per expert: decode), else TILED.
+ *   AUTO   = SWAP.
+ *   SWAP   128 weight rows x up to 256 sorted rows per tile (the weights on
+ *          the MMA's M side; 32-row token tiles when n*k <= 32*E, i.e.
+ *          decode). An expert's ragged last token tile runs with the MMA's
+ *          N rounded up to 32, so at most 31 idle columns.
  *   TILED  128 sorted rows x 256 weight rows per tile (the tokens on the
- *          MMA's M side): large per-expert batches.
- *   SWAP   128 weight rows x 32 sorted rows per tile (the weights on the
- *          MMA's M side): small per-expert batches. */
+ *          MMA's M side); ragged tails cost up to 127 idle MMA rows. */
 typedef enum {
   MOE_FFN_AUTO = 0,
   MOE_FFN_TILED = 1,

@@ -364,7 +364,7 @@ cudaError_t launch_ffn(const uint16_t *x_sorted, const int32_t *offs, const int3
                        int64_t N, int E, int H, int I, const ActParams &act, uint16_t *h_buf,
                        uint16_t *y_flat, uint32_t *ctrl, cudaStream_t s, cudaEvent_t *ev_ffn) {
   if (N == 0) return cudaSuccess;
-  if (act.ffn_kernel == MOE_FFN_SWAP || (act.ffn_kernel == MOE_FFN_AUTO && use_swap_ffn(N, E)))
+  if (act.ffn_kernel != MOE_FFN_TILED)  // AUTO: the swap-operand kernel at every size
     return launch_ffn_swap(x_sorted, offs, col_sorted, gate_scal, w13, w2, N, E, H, I, act, h_buf,
                            y_flat, ctrl, s, ev_ffn);
   const bool relu2_act = act.act == MOE_ACT_RELU2;

@@ -1,7 +1,7 @@
-// grouped_gemm_swap.cu -- the expert contractions for small per-expert
-// batches (decode): the same persistent, warp-specialised tcgen05 design as
-// grouped_gemm.cu with the operands swapped, so that the weights fill the
-// MMA's M side and the few token rows its N side.
+// grouped_gemm_swap.cu -- the expert contractions with the operands swapped:
+// the weights fill the MMA's M side (128 weight rows per tile) and the
+// expert-sorted token rows its N side. The same persistent, warp-specialised
+// tcgen05 design as grouped_gemm.cu.
 //
 // Sources (page title, section): as grouped_gemm.cu -- "MoE feed-forward
 // performs ~3xnum_experts device->host syncs per layer, per forward"
@@ -9,17 +9,23 @@
 // adds SwiGLU-OAI and ReLU2" (activations, w13 layouts), "Reuse topk
 // SparseMatrix routing metadata in GPT-OSS MoE forward" (gate_scal, scatter).
 //
-// A tile is (expert e, 32 sorted rows of e's slice, 128 weight rows):
-//   D[w, j] = sum_k W_e[f0 + w, k] * A[m0 + j, k]      (w < 128, j < 32)
-// with tcgen05.mma M=128 (weight rows), N=32 (tokens), fp32 in TMEM. A tile
-// reads its 128 x K weight slice once and the 32 x K token rows, so a decode
-// step streams each touched expert's weights through all SMs.
+// A tile is (expert e, up to NT sorted rows of e's slice, 128 weight rows):
+//   D[w, j] = sum_k W_e[f0 + w, k] * A[m0 + j, k]      (w < 128, j < rows)
+// with tcgen05.mma M=128 (weight rows) and N = rows rounded up to 32 (so an
+// expert's last, ragged token tile costs at most 31 idle columns, not up to
+// 127 idle MMA rows as with tokens on M), fp32 in TMEM.
+//   NT = 32: decode, a handful of tokens per expert; the weights stream
+//     through all SMs.
+//   NT = 256 (128 for the packed gated layout, which needs two
+//     accumulators): prefill; the same MMA shape as tokens-on-M tiles.
+// Epilogues:
 //   ffn1, interleaved w13: weight rows 2i / 2i+1 are gate_i / up_i, in
 //     adjacent TMEM lanes: one shuffle pairs them.
 //   ffn1, packed w13: the gate rows and the up rows of the same h columns go
 //     to two accumulators, so each thread holds its pair.
 //   ffn1, ReLU2 (non-gated): weight row f0 + w is h column f0 + w.
 //   ffn2: y_flat[col_sorted[m0 + j], f0 + w] = gate_scal[m0 + j] * D[w, j].
+// TMEM is read in chunks of 32 (then 8) token columns up to the tile's rows.
 //
 // Warps: 0 TMA producer, 1 TMEM allocation + MMA issue, 2-5 epilogue (warp
 // q reads TMEM lanes 32*(q%4)..). Every mbarrier wait is bounded.
@@ -31,27 +37,31 @@ namespace {
 using namespace tc;
 
 constexpr int SW_M = 128;  // weight rows per tile (UMMA M)
-constexpr int SW_N = 32;   // token rows per tile (UMMA N)
 constexpr int SW_BK = 64;
 constexpr int SW_UK = 16;
-constexpr int SW_EPI_WARPS = 4;
+constexpr int SW_EPI_WARPS = 8;  // two per TMEM lane quarter, splitting the token chunks
 constexpr int SW_THREADS = (2 + SW_EPI_WARPS) * 32;
 constexpr int SW_A_BYTES = SW_M * SW_BK * 2;  // 16 KB of weights
-constexpr int SW_B_BYTES = SW_N * SW_BK * 2;  // 4 KB of token rows
-constexpr uint32_t kSwIdesc = make_idesc_bf16(SW_M, SW_N);
+constexpr int SW_NGRAN = 32;                  // token-column granularity of a tile's MMA N
+constexpr int SW_SMEM_RING = 192 * 1024;      // bytes of stage ring at most
 
 enum { SW_ACT = 0, SW_SCATTER = 1, SW_RELU2 = 2 };
 
-template <bool DUAL>  // DUAL: gate and up weight tiles in each stage
+template <bool DUAL, int NT>  // DUAL: gate and up weight tiles in each stage
 struct SwCfg {
   static constexpr int kA = DUAL ? 2 : 1;
-  static constexpr int kStages = DUAL ? 5 : 8;
-  static constexpr int kStageBytes = kA * SW_A_BYTES + SW_B_BYTES;  // a multiple of 1 KB
-  static constexpr int kAccCols = kA * SW_N;                        // one accumulator buffer
-  static constexpr int kTmemCols = 2 * kAccCols;                    // 64 or 128 (power of 2)
+  static constexpr int kBBytes = NT * SW_BK * 2;  // token rows of one stage
+  static constexpr int kStageBytes = kA * SW_A_BYTES + kBBytes;  // a multiple of 1 KB
+  static constexpr int kStages =
+      SW_SMEM_RING / kStageBytes < 8 ? SW_SMEM_RING / kStageBytes : 8;
+  static constexpr int kAccCols = kA * NT;         // one accumulator buffer
+  static constexpr int kTmemCols = 2 * kAccCols;   // a power of 2 in [64, 512]
   static constexpr int kNumBars = 2 * kStages + 2 + 2 + 1;
   static constexpr int kSmemBytes = 1024 + kStages * kStageBytes + kNumBars * 8 + 16 +
                                     2 * (kMaxExperts + 1) * 4 + 16;
+  static_assert(kTmemCols <= 512 && (kTmemCols & (kTmemCols - 1)) == 0, "TMEM columns");
+  static_assert(NT % SW_NGRAN == 0 && NT <= 256, "token tile");
+  static_assert(kStages >= 4, "pipeline depth");
 };
 
 struct SwArgs {
@@ -69,12 +79,87 @@ struct SwArgs {
   unsigned long long timeout_ns;
 };
 
-template <int EPI, bool PACKED>
+template <int W>
+__device__ __forceinline__ void tmem_ld(uint32_t taddr, uint32_t (&r)[W]) {
+  static_assert(W == 8 || W == 32, "chunk width");
+  if constexpr (W == 32) {
+    TMEM_LD32(taddr, r);
+  } else {
+    TMEM_LD8(taddr, r);
+  }
+}
+
+// Per-warp epilogue state of one tile.
+struct EpiTile {
+  uint32_t taddr;  // this warp's lanes, the tile's accumulator buffer
+  int m0, rows;    // first sorted row, valid token columns
+  int frow;        // weight row of this thread
+  int lane;
+  int dst_base;    // 32-token group whose scatter targets the lanes hold
+  int dst_mine;    // lane l: destination row of token dst_base + l
+  float g_mine;    // lane l: gate weight of token dst_base + l
+};
+
+// Token columns [c0, c0 + W) of the tile: read TMEM, apply the epilogue.
+template <int EPI, bool DUAL, int NT, int W>
+__device__ __forceinline__ void epi_chunk(EpiTile &t, int c0, const SwArgs &args) {
+  uint32_t r0[W], r1[W];
+  tmem_ld<W>(t.taddr + c0, r0);
+  if constexpr (DUAL) tmem_ld<W>(t.taddr + NT + c0, r1);
+  tmem_wait_ld();
+  if constexpr (EPI == SW_SCATTER) {
+    const int base = c0 & ~31;
+    if (base != t.dst_base) {  // warp-uniform: next 32-token group
+      t.dst_base = base;
+      const int j = base + t.lane;
+      t.dst_mine = j < t.rows ? args.col_sorted[t.m0 + j] : 0;
+      t.g_mine = j < t.rows ? bf16_bits_to_float(args.gate_scal[t.m0 + j]) : 0.f;
+    }
+#pragma unroll
+    for (int i = 0; i < W; ++i) {
+      const int j = c0 + i;
+      const int dst = __shfl_sync(0xffffffffu, t.dst_mine, j & 31);
+      const float g = __shfl_sync(0xffffffffu, t.g_mine, j & 31);
+      if (j < t.rows && t.frow < args.H)
+        args.y_out[(size_t)dst * args.H + t.frow] = float_to_bf16_bits(__uint_as_float(r0[i]) * g);
+    }
+  } else if constexpr (EPI == SW_RELU2) {
+#pragma unroll
+    for (int i = 0; i < W; ++i)
+      if (c0 + i < t.rows && t.frow < args.I)
+        args.h_out[(size_t)(t.m0 + c0 + i) * args.I + t.frow] =
+            float_to_bf16_bits(relu2(__uint_as_float(r0[i])));
+  } else if constexpr (DUAL) {
+#pragma unroll
+    for (int i = 0; i < W; ++i)
+      if (c0 + i < t.rows && t.frow < args.I)
+        args.h_out[(size_t)(t.m0 + c0 + i) * args.I + t.frow] = float_to_bf16_bits(
+            activate(__uint_as_float(r0[i]), __uint_as_float(r1[i]), args.act));
+  } else {
+    // Weight rows 2i (gate) and 2i+1 (up) sit in lanes 2i, 2i+1. For each
+    // pair of tokens (j, j+1) the even lane computes token j and the odd
+    // lane token j+1: one shuffle hands over the missing operand.
+    const int c = t.frow >> 1;  // h column of this lane pair
+    const bool odd = t.lane & 1;
+#pragma unroll
+    for (int i = 0; i < W; i += 2) {
+      const float a = __uint_as_float(r0[i]), b = __uint_as_float(r0[i + 1]);
+      const float recv = __shfl_xor_sync(0xffffffffu, odd ? a : b, 1);
+      const int j = c0 + i + (odd ? 1 : 0);
+      const float g = odd ? recv : a;  // even: gate_j (own), up_j (recv)
+      const float u = odd ? b : recv;  // odd: gate_j+1 (recv), up_j+1 (own)
+      if (j < t.rows && c < args.I)
+        args.h_out[(size_t)(t.m0 + j) * args.I + c] = float_to_bf16_bits(activate(g, u, args.act));
+    }
+  }
+}
+
+template <int EPI, bool PACKED, int NT>
 __global__ void __launch_bounds__(SW_THREADS, 1)
     grouped_gemm_swap_kernel(const __grid_constant__ CUtensorMap tmap_w,
                              const __grid_constant__ CUtensorMap tmap_x, const SwArgs args) {
   constexpr bool DUAL = EPI == SW_ACT && PACKED;
-  using C = SwCfg<DUAL>;
+  using C = SwCfg<DUAL, NT>;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_addr = smem_u32(smem_raw);
   uint8_t *smem = smem_raw + ((1024u - (raw_addr & 1023u)) & 1023u);
@@ -124,7 +209,7 @@ __global__ void __launch_bounds__(SW_THREADS, 1)
   }
   for (int i = threadIdx.x; i <= E; i += SW_THREADS) s_offs[i] = args.offs[i];
   __syncthreads();
-  if (warp == 0) row_tile_prefix(s_offs, E, SW_N, s_tstart);
+  if (warp == 0) row_tile_prefix(s_offs, E, NT, s_tstart);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -139,7 +224,7 @@ __global__ void __launch_bounds__(SW_THREADS, 1)
       uint32_t phase = 0, issued = 0;
       bool ok = true;
       for (int t = blockIdx.x; ok && t < total; t += gridDim.x) {
-        const Tile d = decode_tile(t, args.f_tiles, s_tstart, s_offs, E, SW_N);
+        const Tile d = decode_tile(t, args.f_tiles, s_tstart, s_offs, E, NT);
         const int f0 = d.nt * SW_M;  // first weight row of the tile
         for (int kb = 0; kb < num_kb; ++kb) {
           if (!wait_bounded(empty_bar(stage), phase ^ 1u, s_abort, args.ctrl, args.timeout_ns)) {
@@ -178,6 +263,11 @@ __global__ void __launch_bounds__(SW_THREADS, 1)
       bool ok = true;
       int local = 0;
       for (int t = blockIdx.x; ok && t < total; t += gridDim.x, ++local) {
+        const Tile d = decode_tile(t, args.f_tiles, s_tstart, s_offs, E, NT);
+        const int rows = d.m_end - d.m0;
+        // MMA N: the tile's rows rounded up to 32 (a multiple of 16, <= 256)
+        const int n_mma = (rows + SW_NGRAN - 1) / SW_NGRAN * SW_NGRAN;
+        const uint32_t idesc = make_idesc_bf16(SW_M, n_mma);
         const int acc = local & 1;
         const uint32_t acc_phase = (uint32_t)(local >> 1) & 1u;
         if (!wait_bounded(tempty_bar(acc), acc_phase ^ 1u, s_abort, args.ctrl, args.timeout_ns))
@@ -192,17 +282,15 @@ __global__ void __launch_bounds__(SW_THREADS, 1)
           tc_fence_after();
           const uint64_t adesc0 = sw128_desc(a_addr(stage, 0));
           const uint64_t bdesc = sw128_desc(b_addr(stage));
-          const bool first = kb == 0;
 #pragma unroll
           for (int kk = 0; kk < SW_BK / SW_UK; ++kk)
-            umma_bf16(d_tmem, adesc0 + 2u * kk, bdesc + 2u * kk, kSwIdesc,
-                      (first && kk == 0) ? 0u : 1u);
+            umma_bf16(d_tmem, adesc0 + 2u * kk, bdesc + 2u * kk, idesc, (kb | kk) != 0 ? 1u : 0u);
           if (DUAL) {
             const uint64_t adesc1 = sw128_desc(a_addr(stage, 1));
 #pragma unroll
             for (int kk = 0; kk < SW_BK / SW_UK; ++kk)
-              umma_bf16(d_tmem + SW_N, adesc1 + 2u * kk, bdesc + 2u * kk, kSwIdesc,
-                        (first && kk == 0) ? 0u : 1u);
+              umma_bf16(d_tmem + NT, adesc1 + 2u * kk, bdesc + 2u * kk, idesc,
+                        (kb | kk) != 0 ? 1u : 0u);
           }
           umma_commit(empty_bar(stage));
           if (++stage == C::kStages) {
@@ -217,66 +305,33 @@ __global__ void __launch_bounds__(SW_THREADS, 1)
     }
   } else {
     // ----------------------------------------------------------- epilogue --
-    // TMEM is read in 8-column chunks (tokens) up to the tile's valid rows:
-    // decode tiles hold a few tokens, so the work and the code stay small.
-    const int q = warp & 3;       // TMEM lane quarter this warp may read
-    const int w = q * 32 + lane;  // weight row within the tile
+    const int q = warp & 3;             // TMEM lane quarter this warp may read
+    const int half = (warp - 2) >> 2;   // which of the quarter's two warps: chunk parity
     int local = 0;
     for (int t = blockIdx.x; t < total; t += gridDim.x, ++local) {
-      const Tile d = decode_tile(t, args.f_tiles, s_tstart, s_offs, E, SW_N);
+      const Tile d = decode_tile(t, args.f_tiles, s_tstart, s_offs, E, NT);
       const int acc = local & 1;
       const uint32_t acc_phase = (uint32_t)(local >> 1) & 1u;
       if (!wait_bounded(tfull_bar(acc), acc_phase, s_abort, args.ctrl, args.timeout_ns)) break;
       tc_fence_after();
-      const uint32_t taddr = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * C::kAccCols);
-      const int rows = d.m_end - d.m0;   // valid token columns of the tile
-      const int frow = d.nt * SW_M + w;  // weight row of this thread
-      int dst_mine = 0;
-      float g_mine = 0.f;
-      if (EPI == SW_SCATTER && lane < rows) {  // lane j: token j's destination and weight
-        dst_mine = args.col_sorted[d.m0 + lane];
-        g_mine = bf16_bits_to_float(args.gate_scal[d.m0 + lane]);
+      EpiTile et;
+      et.taddr = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * C::kAccCols);
+      et.m0 = d.m0;
+      et.rows = d.m_end - d.m0;
+      et.frow = d.nt * SW_M + q * 32 + lane;
+      et.lane = lane;
+      et.dst_base = -1;
+      et.dst_mine = 0;
+      et.g_mine = 0.f;
+      // chunks of 32 token columns, then of 8; the quarter's two warps take
+      // alternate chunks
+      int c0 = 0;
+      if constexpr (NT > SW_NGRAN) {
+        const int full = et.rows & ~31;
+        for (int c = 32 * half; c < full; c += 64) epi_chunk<EPI, DUAL, NT, 32>(et, c, args);
+        c0 = full;
       }
-      for (int c0 = 0; c0 < rows; c0 += 8) {
-        uint32_t r0[8], r1[8];
-        TMEM_LD8(taddr + c0, r0);
-        if (DUAL) TMEM_LD8(taddr + SW_N + c0, r1);
-        tmem_wait_ld();
-        if (EPI == SW_SCATTER) {
-#pragma unroll
-          for (int i = 0; i < 8; ++i) {
-            const int j = c0 + i;
-            const int dst = __shfl_sync(0xffffffffu, dst_mine, j & 31);
-            const float g = __shfl_sync(0xffffffffu, g_mine, j & 31);
-            if (j < rows && frow < args.H)
-              args.y_out[(size_t)dst * args.H + frow] =
-                  float_to_bf16_bits(__uint_as_float(r0[i]) * g);
-          }
-        } else if (EPI == SW_RELU2) {
-#pragma unroll
-          for (int i = 0; i < 8; ++i)
-            if (c0 + i < rows && frow < args.I)
-              args.h_out[(size_t)(d.m0 + c0 + i) * args.I + frow] =
-                  float_to_bf16_bits(relu2(__uint_as_float(r0[i])));
-        } else if (DUAL) {
-#pragma unroll
-          for (int i = 0; i < 8; ++i)
-            if (c0 + i < rows && frow < args.I)
-              args.h_out[(size_t)(d.m0 + c0 + i) * args.I + frow] = float_to_bf16_bits(
-                  activate(__uint_as_float(r0[i]), __uint_as_float(r1[i]), args.act));
-        } else {
-          // weight rows 2i (gate) and 2i+1 (up) sit in lanes 2i, 2i+1
-          const int c = frow >> 1;  // h column of this pair
-#pragma unroll
-          for (int i = 0; i < 8; ++i) {
-            const float mine = __uint_as_float(r0[i]);
-            const float other = __shfl_xor_sync(0xffffffffu, mine, 1);
-            if ((lane & 1) == 0 && c0 + i < rows && c < args.I)
-              args.h_out[(size_t)(d.m0 + c0 + i) * args.I + c] =
-                  float_to_bf16_bits(activate(mine, other, args.act));
-          }
-        }
-      }
+      for (int c = c0 + 8 * half; c < et.rows; c += 16) epi_chunk<EPI, DUAL, NT, 8>(et, c, args);
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(tempty_bar(acc));
@@ -293,26 +348,53 @@ __global__ void __launch_bounds__(SW_THREADS, 1)
   }
 }
 
-template <int EPI, bool PACKED>
+template <int EPI, bool PACKED, int NT>
 cudaError_t launch_swap(const CUtensorMap &tw, const CUtensorMap &tx, const SwArgs &a,
                         cudaStream_t s) {
-  constexpr bool DUAL = EPI == SW_ACT && PACKED;
-  auto kern = grouped_gemm_swap_kernel<EPI, PACKED>;
+  using C = SwCfg<EPI == SW_ACT && PACKED, NT>;
+  auto kern = grouped_gemm_swap_kernel<EPI, PACKED, NT>;
   static bool attr_set = false;
   if (!attr_set) {
-    cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                           SwCfg<DUAL>::kSmemBytes);
+    cudaError_t err =
+        cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
     if (err != cudaSuccess) return err;
     if ((err = uniform_carveout(kern)) != cudaSuccess) return err;
     attr_set = true;
   }
-  kern<<<device_sm_count(), SW_THREADS, SwCfg<DUAL>::kSmemBytes, s>>>(tw, tx, a);
+  kern<<<device_sm_count(), SW_THREADS, C::kSmemBytes, s>>>(tw, tx, a);
   return cudaGetLastError();
 }
 
-}  // namespace
+// One contraction at token-tile width NT: the tensor maps and the launch.
+template <int NT>
+cudaError_t swap_pair(const uint16_t *x_sorted, const uint16_t *w13, const uint16_t *w2,
+                      int64_t N, int E, int H, int I, const ActParams &act, uint16_t *h_buf,
+                      SwArgs a, cudaStream_t s, cudaEvent_t *ev_ffn) {
+  const bool relu2_act = act.act == MOE_ACT_RELU2;
+  const bool packed = !relu2_act && act.layout == MOE_W13_PACKED;
+  constexpr int NT_DUAL = NT > 128 ? 128 : NT;  // two accumulators per buffer
+  CUtensorMap tw1, tx1, tw2, tx2;
+  if (!map_3d(&tw1, w13, (uint64_t)E, (uint64_t)w13_rows(act, I), (uint64_t)H, SW_M) ||
+      !map_2d(&tx1, x_sorted, (uint64_t)N, (uint64_t)H, packed ? NT_DUAL : NT) ||
+      !map_3d(&tw2, w2, (uint64_t)E, (uint64_t)H, (uint64_t)I, SW_M) ||
+      !map_2d(&tx2, h_buf, (uint64_t)N, (uint64_t)I, NT))
+    return cudaErrorInvalidValue;
 
-bool use_swap_ffn(int64_t N, int E) { return N <= (int64_t)SW_N * E; }
+  if (ev_ffn && record_stage_event(ev_ffn[0], s) != cudaSuccess) return cudaErrorUnknown;
+  a.num_kb = H / SW_BK;
+  a.f_tiles = (w13_rows(act, I) / (packed ? 2 : 1) + SW_M - 1) / SW_M;
+  cudaError_t err = relu2_act ? launch_swap<SW_RELU2, false, NT>(tw1, tx1, a, s)
+                    : packed  ? launch_swap<SW_ACT, true, NT_DUAL>(tw1, tx1, a, s)
+                              : launch_swap<SW_ACT, false, NT>(tw1, tx1, a, s);
+  if (err != cudaSuccess) return err;
+
+  if (ev_ffn && record_stage_event(ev_ffn[1], s) != cudaSuccess) return cudaErrorUnknown;
+  a.num_kb = I / SW_BK;
+  a.f_tiles = (H + SW_M - 1) / SW_M;
+  return launch_swap<SW_SCATTER, false, NT>(tw2, tx2, a, s);
+}
+
+}  // namespace
 
 cudaError_t launch_ffn_swap(const uint16_t *x_sorted, const int32_t *offs,
                             const int32_t *col_sorted, const uint16_t *gate_scal,
@@ -320,14 +402,6 @@ cudaError_t launch_ffn_swap(const uint16_t *x_sorted, const int32_t *offs,
                             int I, const ActParams &act, uint16_t *h_buf, uint16_t *y_flat,
                             uint32_t *ctrl, cudaStream_t s, cudaEvent_t *ev_ffn) {
   if (N == 0) return cudaSuccess;
-  const bool relu2_act = act.act == MOE_ACT_RELU2;
-  const bool packed = !relu2_act && act.layout == MOE_W13_PACKED;
-  CUtensorMap tw1, tx1, tw2, tx2;
-  if (!map_3d(&tw1, w13, (uint64_t)E, (uint64_t)w13_rows(act, I), (uint64_t)H, SW_M) ||
-      !map_2d(&tx1, x_sorted, (uint64_t)N, (uint64_t)H, SW_N) ||
-      !map_3d(&tw2, w2, (uint64_t)E, (uint64_t)H, (uint64_t)I, SW_M) ||
-      !map_2d(&tx2, h_buf, (uint64_t)N, (uint64_t)I, SW_N))
-    return cudaErrorInvalidValue;
   SwArgs a{};
   a.offs = offs;
   a.E = E;
@@ -340,19 +414,10 @@ cudaError_t launch_ffn_swap(const uint16_t *x_sorted, const int32_t *offs,
   a.y_out = y_flat;
   a.ctrl = ctrl;
   a.timeout_ns = kWaitTimeoutNs;
-
-  if (ev_ffn && record_stage_event(ev_ffn[0], s) != cudaSuccess) return cudaErrorUnknown;
-  a.num_kb = H / SW_BK;
-  a.f_tiles = (w13_rows(act, I) / (packed ? 2 : 1) + SW_M - 1) / SW_M;
-  cudaError_t err = relu2_act ? launch_swap<SW_RELU2, false>(tw1, tx1, a, s)
-                    : packed  ? launch_swap<SW_ACT, true>(tw1, tx1, a, s)
-                              : launch_swap<SW_ACT, false>(tw1, tx1, a, s);
-  if (err != cudaSuccess) return err;
-
-  if (ev_ffn && record_stage_event(ev_ffn[1], s) != cudaSuccess) return cudaErrorUnknown;
-  a.num_kb = I / SW_BK;
-  a.f_tiles = (H + SW_M - 1) / SW_M;
-  return launch_swap<SW_SCATTER, false>(tw2, tx2, a, s);
+  // a handful of rows per expert (decode): 32-row token tiles; else 256
+  if (N <= (int64_t)SW_NGRAN * E)
+    return swap_pair<32>(x_sorted, w13, w2, N, E, H, I, act, h_buf, a, s, ev_ffn);
+  return swap_pair<256>(x_sorted, w13, w2, N, E, H, I, act, h_buf, a, s, ev_ffn);
 }
 
 }  // namespace moe

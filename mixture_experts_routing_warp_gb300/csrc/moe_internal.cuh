@@ -218,9 +218,9 @@ cudaError_t launch_ffn(const uint16_t *x_sorted, const int32_t *offs, const int3
                        uint16_t *y_flat, uint32_t *ctrl, cudaStream_t s,
                        cudaEvent_t *ev_ffn = nullptr);
 
-// The swap-operand grouped GEMM (weights on the MMA's M side) for small
-// per-expert batches; launch_ffn hands over to it per act.ffn_kernel.
-bool use_swap_ffn(int64_t N, int E);
+// The swap-operand grouped GEMM (weights on the MMA's M side, token tiles
+// of 32 or 256 rows); launch_ffn hands over to it unless act.ffn_kernel is
+// MOE_FFN_TILED.
 cudaError_t launch_ffn_swap(const uint16_t *x_sorted, const int32_t *offs,
                             const int32_t *col_sorted, const uint16_t *gate_scal,
                             const uint16_t *w13, const uint16_t *w2, int64_t N, int E, int H,

@@ -123,13 +123,15 @@ def test_gptoss_decode(n):
     _check_full(Layer(I.GPTOSS.with_n(n)))
 
 
+@pytest.mark.parametrize("ffn_kernel", ["auto", "tiled"])
 @pytest.mark.parametrize("n", I.GPTOSS_PREFILL_N)
-def test_gptoss_prefill_sampled(n):
-    _check_sampled(Layer(I.GPTOSS.with_n(n)))
+def test_gptoss_prefill_sampled(n, ffn_kernel):
+    _check_sampled(Layer(I.GPTOSS.with_n(n), ffn_kernel=ffn_kernel))
 
 
-def test_skewed_prefill_sampled():
-    L = Layer(I.SKEWED)
+@pytest.mark.parametrize("ffn_kernel", ["auto", "tiled"])
+def test_skewed_prefill_sampled(ffn_kernel):
+    L = Layer(I.SKEWED, ffn_kernel=ffn_kernel)
     stats = _check_sampled(L)
     assert stats["cos"] > 0.99
 
@@ -161,9 +163,10 @@ def test_variants(name, H, E, k, Idim, act, layout, act_kw, n, ffn_kernel):
     _check_full(Layer(case, act_kw, ffn_kernel))
 
 
-def test_swap_kernel_on_many_token_tiles_per_expert():
-    """The swap kernel on 1024 rows per expert (32 token tiles each)."""
-    _check_full(Layer(I.MINIMIND_E4, ffn_kernel="swap"))
+def test_tiled_kernel_on_minimind():
+    """The tiled kernel on 1024 rows per expert (8 token tiles each; the
+    MiniMind test above runs the swap kernel's 256-row token tiles)."""
+    _check_full(Layer(I.MINIMIND_E4, ffn_kernel="tiled"))
 
 
 @pytest.mark.parametrize("n", I.GPTOSS_DECODE_N)
@@ -174,7 +177,7 @@ def test_gptoss_decode_tiled_kernel(n):
 
 @pytest.mark.parametrize("layout,act", [("packed", "swiglu"), ("interleaved", "swiglu_oai"),
                                         ("packed", "relu2")])
-@pytest.mark.parametrize("n", [1, 5, 40])
+@pytest.mark.parametrize("n", [1, 5, 40, 300])
 def test_swap_kernel_deep_k(layout, act, n):
     """The swap kernel with 16 K-blocks per tile in both contractions
     (H = I = 1024) and 1 .. 32 valid rows per tile (partial 8-column TMEM
@@ -192,7 +195,8 @@ def test_swap_kernel_deep_k(layout, act, n):
 
 
 def test_auto_kernel_choice_boundary():
-    """n*k on both sides of 32*E: AUTO switches kernels there, both correct."""
+    """n*k on both sides of 32*E: the swap kernel's token tiles switch from
+    32 to 256 rows there; both widths correct."""
     for n in (64, 65):   # E = 8, k = 4: 256 = 32*8 -> swap, 260 -> tiled
         case = I.LayerCase(f"boundary@n{n}", n=n, H=128, E=8, k=4, I=192, w_std=0.1, seed=n)
         _check_full(Layer(case))
