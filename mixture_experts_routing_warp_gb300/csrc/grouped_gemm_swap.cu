@@ -39,8 +39,6 @@ using namespace tc;
 constexpr int SW_M = 128;  // weight rows per tile (UMMA M)
 constexpr int SW_BK = 64;
 constexpr int SW_UK = 16;
-constexpr int SW_EPI_WARPS = 8;  // two per TMEM lane quarter, splitting the token chunks
-constexpr int SW_THREADS = (2 + SW_EPI_WARPS) * 32;
 constexpr int SW_A_BYTES = SW_M * SW_BK * 2;  // 16 KB of weights
 constexpr int SW_NGRAN = 32;                  // token-column granularity of a tile's MMA N
 constexpr int SW_SMEM_RING = 192 * 1024;      // bytes of stage ring at most
@@ -54,6 +52,10 @@ struct SwCfg {
   static constexpr int kStageBytes = kA * SW_A_BYTES + kBBytes;  // a multiple of 1 KB
   static constexpr int kStages =
       SW_SMEM_RING / kStageBytes < 8 ? SW_SMEM_RING / kStageBytes : 8;
+  // epilogue warps: one per TMEM lane quarter for decode tiles, two (taking
+  // alternate token chunks) for 256-column tiles
+  static constexpr int kEpiWarps = NT > 32 ? 8 : 4;
+  static constexpr int kThreads = (2 + kEpiWarps) * 32;
   static constexpr int kAccCols = kA * NT;         // one accumulator buffer
   static constexpr int kTmemCols = 2 * kAccCols;   // a power of 2 in [64, 512]
   static constexpr int kNumBars = 2 * kStages + 2 + 2 + 1;
@@ -155,7 +157,7 @@ __device__ __forceinline__ void epi_chunk(EpiTile &t, int c0, const SwArgs &args
 }
 
 template <int EPI, bool PACKED, int NT>
-__global__ void __launch_bounds__(SW_THREADS, 1)
+__global__ void __launch_bounds__(SwCfg<EPI == SW_ACT && PACKED, NT>::kThreads, 1)
     grouped_gemm_swap_kernel(const __grid_constant__ CUtensorMap tmap_w,
                              const __grid_constant__ CUtensorMap tmap_x, const SwArgs args) {
   constexpr bool DUAL = EPI == SW_ACT && PACKED;
@@ -189,7 +191,7 @@ __global__ void __launch_bounds__(SW_THREADS, 1)
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(tfull_bar(b), 1);
-      mbar_init(tempty_bar(b), SW_EPI_WARPS);
+      mbar_init(tempty_bar(b), C::kEpiWarps);
     }
     mbar_init(drain_bar, 1);
     *s_abort = 0;
@@ -207,7 +209,7 @@ __global__ void __launch_bounds__(SW_THREADS, 1)
                  : "memory");
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
   }
-  for (int i = threadIdx.x; i <= E; i += SW_THREADS) s_offs[i] = args.offs[i];
+  for (int i = threadIdx.x; i <= E; i += C::kThreads) s_offs[i] = args.offs[i];
   __syncthreads();
   if (warp == 0) row_tile_prefix(s_offs, E, NT, s_tstart);
   tc_fence_before();
@@ -306,7 +308,8 @@ __global__ void __launch_bounds__(SW_THREADS, 1)
   } else {
     // ----------------------------------------------------------- epilogue --
     const int q = warp & 3;             // TMEM lane quarter this warp may read
-    const int half = (warp - 2) >> 2;   // which of the quarter's two warps: chunk parity
+    const int half = (warp - 2) >> 2;   // which of the quarter's warps: chunk parity
+    constexpr int kPer = C::kEpiWarps / 4;  // warps per lane quarter
     int local = 0;
     for (int t = blockIdx.x; t < total; t += gridDim.x, ++local) {
       const Tile d = decode_tile(t, args.f_tiles, s_tstart, s_offs, E, NT);
@@ -328,10 +331,10 @@ __global__ void __launch_bounds__(SW_THREADS, 1)
       int c0 = 0;
       if constexpr (NT > SW_NGRAN) {
         const int full = et.rows & ~31;
-        for (int c = 32 * half; c < full; c += 64) epi_chunk<EPI, DUAL, NT, 32>(et, c, args);
+        for (int c = 32 * half; c < full; c += 32 * kPer) epi_chunk<EPI, DUAL, NT, 32>(et, c, args);
         c0 = full;
       }
-      for (int c = c0 + 8 * half; c < et.rows; c += 16) epi_chunk<EPI, DUAL, NT, 8>(et, c, args);
+      for (int c = c0 + 8 * half; c < et.rows; c += 8 * kPer) epi_chunk<EPI, DUAL, NT, 8>(et, c, args);
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(tempty_bar(acc));
@@ -361,7 +364,7 @@ cudaError_t launch_swap(const CUtensorMap &tw, const CUtensorMap &tx, const SwAr
     if ((err = uniform_carveout(kern)) != cudaSuccess) return err;
     attr_set = true;
   }
-  kern<<<device_sm_count(), SW_THREADS, C::kSmemBytes, s>>>(tw, tx, a);
+  kern<<<device_sm_count(), C::kThreads, C::kSmemBytes, s>>>(tw, tx, a);
   return cudaGetLastError();
 }
 
