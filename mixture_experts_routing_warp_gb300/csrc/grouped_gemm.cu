@@ -101,6 +101,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int E = args.E;
+  pdl_launch_dependents();
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
@@ -127,6 +128,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                  : "memory");
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
   }
+  pdl_wait();  // offs and the operands come from earlier kernels of the stream
   for (int i = threadIdx.x; i <= E; i += kThreads) s_offs[i] = args.offs[i];
   __syncthreads();
   if (warp == 0) row_tile_prefix(s_offs, E, BM, s_tstart);
@@ -353,8 +355,9 @@ cudaError_t launch_gemm(const CUtensorMap &ta, const CUtensorMap &tb, const Gemm
     if ((err = uniform_carveout(kern)) != cudaSuccess) return err;
     attr_set = true;
   }
-  kern<<<device_sm_count(), kThreads, kSmemBytes, s>>>(ta, tb, a);
-  return cudaGetLastError();
+  const cudaError_t err = launch_dependent(kern, dim3(device_sm_count()), dim3(kThreads),
+                                           kSmemBytes, s, ta, tb, a);
+  return err != cudaSuccess ? err : cudaGetLastError();
 }
 
 }  // namespace

@@ -183,6 +183,7 @@ __global__ void __launch_bounds__(SwCfg<EPI == SW_ACT && PACKED, NT>::kThreads, 
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int E = args.E;
+  pdl_launch_dependents();
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < C::kStages; ++s) {
@@ -209,6 +210,7 @@ __global__ void __launch_bounds__(SwCfg<EPI == SW_ACT && PACKED, NT>::kThreads, 
                  : "memory");
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
   }
+  pdl_wait();  // offs and the operands come from earlier kernels of the stream
   for (int i = threadIdx.x; i <= E; i += C::kThreads) s_offs[i] = args.offs[i];
   __syncthreads();
   if (warp == 0) row_tile_prefix(s_offs, E, NT, s_tstart);
@@ -364,8 +366,9 @@ cudaError_t launch_swap(const CUtensorMap &tw, const CUtensorMap &tx, const SwAr
     if ((err = uniform_carveout(kern)) != cudaSuccess) return err;
     attr_set = true;
   }
-  kern<<<device_sm_count(), C::kThreads, C::kSmemBytes, s>>>(tw, tx, a);
-  return cudaGetLastError();
+  const cudaError_t err = launch_dependent(kern, dim3(device_sm_count()), dim3(C::kThreads),
+                                           C::kSmemBytes, s, tw, tx, a);
+  return err != cudaSuccess ? err : cudaGetLastError();
 }
 
 // One contraction at token-tile width NT: the tensor maps and the launch.

@@ -174,6 +174,35 @@ inline cudaError_t record_stage_event(cudaEvent_t ev, cudaStream_t s) {
              : cudaEventRecord(ev, s);
 }
 
+// Programmatic dependent launch. The kernels after the first of a forward
+// (gather, the two expert contractions, combine) are launched with
+// launch_dependent(): they may be scheduled while the previous kernel of the
+// stream still runs, do their set-up (barriers, TMEM, tensor-map prefetch),
+// and call pdl_wait() -- a hardware wait for the previous grid to complete
+// and its writes to be visible -- before reading anything it (or an earlier
+// kernel) wrote. Every kernel calls pdl_launch_dependents() early so that
+// the next one can be scheduled; all of its own CTAs are resident by then.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_dependent(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                                    cudaStream_t s, Args &&...args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, static_cast<Args &&>(args)...);
+}
+
 // Every kernel of the library asks for the same L1 / shared-memory split
 // (all shared: the grouped GEMM needs ~200 KB), so that consecutive kernels
 // never wait for an SM to drain and reconfigure. Call once per kernel

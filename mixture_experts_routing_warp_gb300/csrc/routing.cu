@@ -543,6 +543,7 @@ __global__ void __launch_bounds__(kMetaThreads) metadata_kernel(
   __shared__ MetaShared<kMetaThreads> sh;
   const int tid = threadIdx.x;
   const int b = blockIdx.x;
+  pdl_launch_dependents();  // the gather may be scheduled (it waits for this grid)
   const int lo = (int)min((int64_t)N, (int64_t)b * chunk);
   const int hi = (int)min((int64_t)N, (int64_t)lo + chunk);
 
@@ -641,6 +642,7 @@ __global__ void __launch_bounds__(kFusedThreads, 1) route_metadata_kernel(
   uint16_t *s_slot_v = reinterpret_cast<uint16_t *>(smem_raw + (((size_t)T * K + 15) & ~15ull));
 
   const int tid = threadIdx.x;
+  pdl_launch_dependents();  // the gather may be scheduled (it waits for this grid)
   for (int e = tid; e < E; e += kFusedThreads) sh.base[e] = 0;
   __syncthreads();
 
@@ -830,6 +832,8 @@ constexpr int kChunksPerLane = 4;  // 16-byte chunks in flight per thread
 __global__ void __launch_bounds__(kCopyThreads) gather_rows_kernel(
     const uint4 *__restrict__ x, const int32_t *__restrict__ col_sorted, int64_t N, int k,
     int vec_per_row, int groups_per_row, uint4 *__restrict__ x_sorted) {
+  pdl_launch_dependents();
+  pdl_wait();  // col_sorted comes from the metadata kernel
   const int lane = threadIdx.x & 31;
   const int64_t units = N * groups_per_row;  // (row, group of 32 * kChunksPerLane chunks)
   const int64_t warps = (int64_t)gridDim.x * (kCopyThreads / 32);
@@ -866,10 +870,10 @@ cudaError_t launch_gather_rows(const uint16_t *x, const int32_t *col_sorted, int
   int64_t blocks = (N * gpr + kCopyThreads / 32 - 1) / (kCopyThreads / 32);
   const int64_t cap = (int64_t)device_sm_count() * 16;
   if (blocks > cap) blocks = cap;
-  gather_rows_kernel<<<(unsigned)blocks, kCopyThreads, 0, s>>>(
-      reinterpret_cast<const uint4 *>(x), col_sorted, N, k, vpr, gpr,
-      reinterpret_cast<uint4 *>(x_sorted));
-  return cudaGetLastError();
+  cudaError_t err = launch_dependent(gather_rows_kernel, dim3((unsigned)blocks), dim3(kCopyThreads),
+                                     0, s, reinterpret_cast<const uint4 *>(x), col_sorted, N, k,
+                                     vpr, gpr, reinterpret_cast<uint4 *>(x_sorted));
+  return err != cudaSuccess ? err : cudaGetLastError();
 }
 
 // ============================================================= combine ==
@@ -891,6 +895,8 @@ __global__ void __launch_bounds__(kCopyThreads) combine_kernel(const uint4 *__re
                                                                int groups_per_row,
                                                                uint4 *__restrict__ out) {
   constexpr int CPL = 2;  // chunks per lane: 2*K loads in flight
+  pdl_launch_dependents();
+  pdl_wait();  // y_flat comes from the w2 contraction
   const int lane = threadIdx.x & 31;
   const int64_t units = n * groups_per_row;  // (token, group of 64 chunks) per warp
   const int64_t warps = (int64_t)gridDim.x * (kCopyThreads / 32);
@@ -941,7 +947,11 @@ cudaError_t launch_combine(const uint16_t *y_flat, int64_t n, int k, int H, uint
       if (err != cudaSuccess) return err;                                          \
       configured[K_] = true;                                                       \
     }                                                                              \
-    combine_kernel<K_><<<(unsigned)blocks, kCopyThreads, 0, s>>>(y, n, vpr, gpr, o); \
+    {                                                                              \
+      cudaError_t err = launch_dependent(combine_kernel<K_>, dim3((unsigned)blocks),  \
+                                         dim3(kCopyThreads), 0, s, y, n, vpr, gpr, o); \
+      if (err != cudaSuccess) return err;                                          \
+    }                                                                              \
     break;
     MOE_COMBINE_CASE(1) MOE_COMBINE_CASE(2) MOE_COMBINE_CASE(3) MOE_COMBINE_CASE(4)
     MOE_COMBINE_CASE(5) MOE_COMBINE_CASE(6) MOE_COMBINE_CASE(7) MOE_COMBINE_CASE(8)
