@@ -417,6 +417,67 @@ def time_e2e(dc: DeviceCase, steps, warmup):
     return ms, h2d, d2h
 
 
+def time_e2e_pipelined(dc: DeviceCase, steps, warmup):
+    """The same calls with the copies on their own streams, as a serving
+    loop would run them: step i's H2D (x, logits) on one stream, its forward
+    on a second, its D2H (out) on a third, two device buffer sets, events
+    ordering each step's copies against its forward and the buffer reuse two
+    steps later. Every step still copies its inputs in and its result out
+    inside the timed region; the copies of neighbouring steps overlap the
+    forward. Returns ms per step."""
+    import torch
+    import mixture_experts_routing_warp_gb300 as moe
+    c = dc.c
+    slots = 2
+    xd = [torch.empty_like(dc.x[0]) for _ in range(slots)]
+    ld = [torch.empty_like(dc.logits[0]) for _ in range(slots)]
+    od = [torch.empty_like(dc.out) for _ in range(slots)]
+    host_out = [dc.host_out] + [torch.empty_like(dc.host_out).pin_memory()
+                                for _ in range(slots - 1)]
+    s_in, s_comp, s_out = torch.cuda.Stream(), torch.cuda.Stream(), torch.cuda.Stream()
+    in_done = [torch.cuda.Event() for _ in range(slots)]
+    comp_done = [torch.cuda.Event() for _ in range(slots)]
+    out_done = [torch.cuda.Event() for _ in range(slots)]
+    for e in comp_done + out_done:   # recorded once so that the first waits are no-ops
+        e.record()
+
+    def step(i):
+        b, j = i % slots, i % dc.n_xsets
+        with torch.cuda.stream(s_in):
+            s_in.wait_event(comp_done[b])        # slot b's inputs no longer read
+            xd[b].copy_(dc.host_x[j], non_blocking=True)
+            ld[b].copy_(dc.host_logits[j], non_blocking=True)
+            in_done[b].record(s_in)
+        with torch.cuda.stream(s_comp):
+            s_comp.wait_event(in_done[b])
+            s_comp.wait_event(out_done[b])       # slot b's output already copied out
+            moe.forward(xd[b], ld[b], dc.w13[i % dc.n_wsets], dc.w2[i % dc.n_wsets], c.k,
+                        dc.params, dc.ws, out=od[b])
+            comp_done[b].record(s_comp)
+        with torch.cuda.stream(s_out):
+            s_out.wait_event(comp_done[b])
+            host_out[b].copy_(od[b], non_blocking=True)
+            out_done[b].record(s_out)
+
+    for i in range(warmup):
+        step(i)
+    torch.cuda.synchronize()
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    cur = torch.cuda.current_stream()
+    start.record(cur)
+    for s_ in (s_in, s_comp, s_out):
+        s_.wait_stream(cur)
+    for i in range(steps):
+        step(warmup + i)
+    for s_ in (s_in, s_comp, s_out):
+        cur.wait_stream(s_)
+    end.record(cur)
+    torch.cuda.synchronize()
+    if moe.read_status(dc.ws) != 0:
+        raise RuntimeError("device status after the end-to-end loop")
+    return start.elapsed_time(end) / steps
+
+
 def graph_time_ms(fn, reps: int, replays: int = 5) -> float:
     """Capture reps calls of fn(i) in one CUDA graph, replay it, and return
     the device time per call (median over replays)."""
@@ -694,10 +755,18 @@ def run_ours(args, rank, world, local, pg):
             "gpu_launches": kernels_per_step * args.steps,
             "clocks": sampler.summary()}
     if rank == 0:
-        e2e_ms, h2d, d2h = time_e2e(dc, max(3, min(args.steps, 20)), args.warmup)
-        line["e2e"] = {"value": round(world * c.n / (e2e_ms * 1e-3), 1), "unit": "tokens/s",
-                       "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-                       "ms_per_step": round(e2e_ms, 4)}
+        e2e_steps = max(3, min(args.steps, 50))
+        serial_ms, h2d, d2h = time_e2e(dc, e2e_steps, args.warmup)
+        e2e_ms = time_e2e_pipelined(dc, e2e_steps, args.warmup)
+        line["e2e"] = {"value": round(job_tokens_per_s(world, c.n, e2e_ms), 1),
+                       "unit": "tokens/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                       "ms_per_step": round(e2e_ms, 4), "steps": e2e_steps,
+                       "how": "moe.forward from pinned host buffers: per step H2D x + logits, "
+                              "forward, D2H out; copies on their own streams, overlapping the "
+                              "neighbouring steps' forwards (2 buffer sets)",
+                       "serial": {"value": round(job_tokens_per_s(world, c.n, serial_ms), 1),
+                                  "ms_per_step": round(serial_ms, 4),
+                                  "how": "the same three operations back to back on one stream"}}
         if not args.no_extras:
             also = {"routing_metadata_16k_e128": time_routing(16384, 128, 4, device, l2, pk,
                                                               source),
