@@ -65,6 +65,8 @@ def lib() -> ctypes.CDLL:
         L.orc_expert_row.argtypes = [p, p, p, i32, i32, ctypes.POINTER(_ActParams), p, p, p]
         L.orc_ffn.argtypes = [p, p, p, p, p, i64, i32, i32, i32, i32,
                               ctypes.POINTER(_ActParams), p, i64, p, p, p]
+        L.orc_router_logits.argtypes = [p, p, i64, i32, i32, p]
+        L.orc_router_logits.restype = ctypes.c_int
         L.orc_f64_to_bf16.argtypes = [ctypes.c_double]
         L.orc_f64_to_bf16.restype = ctypes.c_uint16
         L.orc_f64_to_bf16_array.argtypes = [p, i64, p]
@@ -116,6 +118,20 @@ def f64_to_bf16(v) -> np.ndarray:
 def bf16_to_f64(b) -> np.ndarray:
     b = np.asarray(b, dtype=np.uint16)
     return (b.astype(np.uint32) << np.uint32(16)).view(np.float32).astype(np.float64)
+
+
+def router_logits(x: np.ndarray, w_gate: np.ndarray, as_f32: bool = True) -> np.ndarray:
+    """The router matmul: logits[t, e] = sum_h x[t, h] * w_gate[e, h] in float64
+    (h ascending), rounded once to fp32 unless as_f32 is False.
+    x [n, H], w_gate [E, H] bf16 bits."""
+    x = _c(x, np.uint16)
+    w = _c(w_gate, np.uint16)
+    n, H = x.shape
+    E, H2 = w.shape
+    assert H2 == H
+    out = np.empty((n, E), dtype=np.float64)
+    _check(lib().orc_router_logits(_ptr(x), _ptr(w), n, E, H, _ptr(out)), "router_logits")
+    return out.astype(np.float32) if as_f32 else out
 
 
 def route(logits: np.ndarray, k: int, gating: str = "softmax_topk"):

@@ -176,6 +176,28 @@ int orc_metadata(const int32_t *topk_indx, const uint16_t *topk_vals, int64_t n,
   return ORC_OK;
 }
 
+/* ------------------------------------------------------------- router -- */
+
+/* [R1] 功能与动机 (the router / gate matmul that issue #28986 asks to fuse
+ * with expert selection): logits[t, e] = sum_h x[t, h] * w_gate[e, h], in
+ * float64, h ascending; the caller rounds to fp32 where the method stores
+ * fp32 logits. x [n, H], w_gate [E, H] bf16 bits; out [n, E] float64. */
+int orc_router_logits(const uint16_t *x, const uint16_t *w_gate, int64_t n, int E, int H,
+                      double *out) {
+  if (n < 0 || E < 1 || H < 1) return ORC_BAD_ARG;
+#pragma omp parallel for schedule(static)
+  for (int64_t t = 0; t < n; ++t) {
+    const uint16_t *xt = x + t * H;
+    for (int e = 0; e < E; ++e) {
+      const uint16_t *we = w_gate + (int64_t)e * H;
+      double s = 0.0;
+      for (int h = 0; h < H; ++h) s += orc_bf16_to_f64(xt[h]) * orc_bf16_to_f64(we[h]);
+      out[t * E + e] = s;
+    }
+  }
+  return ORC_OK;
+}
+
 /* ------------------------------------------------------------- expert -- */
 
 typedef struct {
