@@ -273,6 +273,35 @@ moe_status moe_forward(const uint16_t *x, const float *logits, const uint16_t *w
                        uint16_t *topk_vals, const moe_routing_meta *meta, void *workspace,
                        size_t workspace_bytes, moe_stream stream);
 
+/* Stage 1 with the router matmul fused in. [R1] 功能与动机 (issue #28986
+ * asks for a fused GPT-OSS router kernel; expert selection is about 3.5 % of
+ * a layer; the PR itself leaves the gate matmul untouched).
+ *   logits[t, e] = sum_h x[t, h] * w_gate[e, h]   (fp32 accumulation of the
+ *   bf16 products), then, in the same kernel, top-k and gate weights
+ *   exactly as moe_route computes them from those logits (ties to the lower
+ *   expert id; softmax over the k selected or over all E).
+ *   x       [n, H] bf16, 16-byte aligned; H a multiple of 64.
+ *   w_gate  [E, H] bf16, 16-byte aligned (E <= 256).
+ *   topk_indx [n, k] int32, topk_vals [n, k] bf16: outputs.
+ *   logits  [n, E] fp32 output, or NULL (then the logits never reach memory).
+ *   workspace: at least the 4 KB control block (status of the bounded
+ *   waits; moe_workspace_init'ed). */
+moe_status moe_route_gemm(const uint16_t *x, const uint16_t *w_gate, int64_t n, int32_t E,
+                          int32_t H, int32_t k, int32_t gating, int32_t *topk_indx,
+                          uint16_t *topk_vals, float *logits, void *workspace,
+                          size_t workspace_bytes, moe_stream stream);
+
+/* moe_forward with the routing computed from x and the gate weights
+ * w_gate [E, H] bf16 (moe_route_gemm's kernel, then the metadata kernel)
+ * instead of from logits; every other argument as moe_forward. Launches one
+ * kernel more than moe_forward when that one fuses route and metadata. */
+moe_status moe_forward_gate(const uint16_t *x, const uint16_t *w_gate, const uint16_t *w13,
+                            const uint16_t *w2, int64_t n, int32_t E, int32_t k, int32_t H,
+                            int32_t I, const moe_params *params, uint16_t *out,
+                            int32_t *topk_indx, uint16_t *topk_vals,
+                            const moe_routing_meta *meta, void *workspace,
+                            size_t workspace_bytes, moe_stream stream);
+
 /* Stage kernels of moe_forward, in launch order (indices of the events of
  * moe_forward_timed). */
 #define MOE_STAGE_ROUTE 0    /* top-k + gate weights                       */

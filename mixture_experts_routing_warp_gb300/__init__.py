@@ -1,19 +1,19 @@
 """GB300-native (sm_103a) Mixture-of-Experts layer forward.
 
-route -> routing metadata -> grouped SwiGLU / SwiGLU-OAI expert FFN ->
-gate-weighted combine, every stage a CUDA kernel in libmoe_gb300.so behind
-the C ABI of include/moe.h. This package is the thin Python binding
+route -> routing metadata -> grouped SwiGLU / SwiGLU-OAI / ReLU2 expert FFN
+-> gate-weighted combine, every stage a CUDA kernel in libmoe_gb300.so
+behind the C ABI of include/moe.h. This package is the thin Python binding
 (argument marshalling over torch tensors) plus the seeded input generators
 (`inputs`).
 """
 from ._binding import (ACT, FFN_KERNEL, GATING, LAYOUT, MoEError, MoeParams, RoutingMeta,
-                       STAGES, build_metadata, combine, empty_meta, forward, forward_launch_count,
-                       forward_timed, grouped_ffn, lib, library_path, make_params, read_status,
-                       route, route_metadata, selftest_wait_timeout, status_string, workspace,
-                       workspace_size)
+                       STAGES, build_metadata, combine, empty_meta, forward, forward_gate,
+                       forward_launch_count, forward_timed, grouped_ffn, lib, library_path,
+                       make_params, read_status, route, route_gemm, route_metadata,
+                       selftest_wait_timeout, status_string, workspace, workspace_size)
 
 __all__ = ["ACT", "FFN_KERNEL", "GATING", "LAYOUT", "MoEError", "MoeParams", "RoutingMeta",
-           "STAGES", "build_metadata", "combine", "empty_meta", "forward", "forward_launch_count",
-           "forward_timed", "grouped_ffn", "lib", "library_path", "make_params", "read_status",
-           "route", "route_metadata", "selftest_wait_timeout", "status_string", "workspace",
-           "workspace_size"]
+           "STAGES", "build_metadata", "combine", "empty_meta", "forward", "forward_gate",
+           "forward_launch_count", "forward_timed", "grouped_ffn", "lib", "library_path",
+           "make_params", "read_status", "route", "route_gemm", "route_metadata",
+           "selftest_wait_timeout", "status_string", "workspace", "workspace_size"]

@@ -71,6 +71,9 @@ SIGNATURES = {
                            _P, _SZ, _P]),
     "moe_forward_timed": (_I32, [_P, _P, _P, _P, _I64, _I32, _I32, _I32, _I32, _PP, _P, _P, _P,
                                  _PM, _P, _SZ, _P, _I32, _P]),
+    "moe_route_gemm": (_I32, [_P, _P, _I64, _I32, _I32, _I32, _I32, _P, _P, _P, _P, _SZ, _P]),
+    "moe_forward_gate": (_I32, [_P, _P, _P, _P, _I64, _I32, _I32, _I32, _I32, _PP, _P, _P, _P,
+                                _PM, _P, _SZ, _P]),
     "moe_forward_launch_count": (_I32, [_I64, _I32, _I32, _I32, _I32]),
     "moe_read_status": (_I32, [_P, _SZ, _I32, _P]),
     "moe_selftest_wait_timeout": (_I32, [_P, _SZ, _U64, _P]),
@@ -278,6 +281,51 @@ def forward(x: torch.Tensor, logits: torch.Tensor, w13: torch.Tensor, w2: torch.
     _check(lib().moe_forward(_ptr(x), _ptr(logits), _ptr(w13), _ptr(w2), n, E, k, H, I,
                              ctypes.byref(params), _ptr(out), _ptr(indx), _ptr(vals), mstruct,
                              _ptr(ws), ws.numel(), _stream(x.device)), "moe_forward")
+    return out
+
+
+def route_gemm(x: torch.Tensor, w_gate: torch.Tensor, k: int, gating: str = "softmax_topk",
+               ws: Optional[torch.Tensor] = None, logits: Optional[torch.Tensor] = None):
+    """Router matmul x . w_gate^T fused with the top-k -> (topk_indx, topk_vals);
+    fills `logits` (fp32 [n, E]) too when given."""
+    _need(x, "x", torch.bfloat16)
+    n, H = x.shape
+    _need(w_gate, "w_gate", torch.bfloat16)
+    E = w_gate.shape[0]
+    _need(w_gate, "w_gate", torch.bfloat16, (E, H))
+    if logits is not None:
+        _need(logits, "logits", torch.float32, (n, E))
+    if ws is None:
+        ws = workspace(max(n, 1), E, k, 64, 64, x.device)
+    indx = torch.empty((n, k), dtype=torch.int32, device=x.device)
+    vals = torch.empty((n, k), dtype=torch.bfloat16, device=x.device)
+    _check(lib().moe_route_gemm(_ptr(x), _ptr(w_gate), n, E, H, k, GATING[gating], _ptr(indx),
+                                _ptr(vals), _ptr(logits), _ptr(ws), ws.numel(),
+                                _stream(x.device)), "moe_route_gemm")
+    return indx, vals
+
+
+def forward_gate(x: torch.Tensor, w_gate: torch.Tensor, w13: torch.Tensor, w2: torch.Tensor,
+                 k: int, params: MoeParams, ws: torch.Tensor, out: Optional[torch.Tensor] = None,
+                 topk: Optional[tuple] = None, meta: Optional[dict] = None) -> torch.Tensor:
+    """forward() with the routing computed from x and the gate weights [E, H]."""
+    _need(x, "x", torch.bfloat16)
+    n, H = x.shape
+    _need(w_gate, "w_gate", torch.bfloat16)
+    E = w_gate.shape[0]
+    _need(w_gate, "w_gate", torch.bfloat16, (E, H))
+    _need(w13, "w13", torch.bfloat16)
+    I = _intermediate(w13, params)
+    _need(w13, "w13", torch.bfloat16, (E, w13.shape[1], H))
+    _need(w2, "w2", torch.bfloat16, (E, H, I))
+    if out is None:
+        out = torch.empty((n, H), dtype=torch.bfloat16, device=x.device)
+    indx, vals = topk if topk is not None else (None, None)
+    mstruct = ctypes.byref(_meta_struct(meta)) if meta is not None else None
+    _check(lib().moe_forward_gate(_ptr(x), _ptr(w_gate), _ptr(w13), _ptr(w2), n, E, k, H, I,
+                                  ctypes.byref(params), _ptr(out), _ptr(indx), _ptr(vals),
+                                  mstruct, _ptr(ws), ws.numel(), _stream(x.device)),
+           "moe_forward_gate")
     return out
 
 

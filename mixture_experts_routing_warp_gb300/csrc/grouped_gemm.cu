@@ -58,7 +58,7 @@ constexpr int kSmemBytes = 1024 /*alignment slack*/ + STAGES * (A_BYTES + B_BYTE
 
 constexpr uint32_t kIdesc = make_idesc_bf16(BM, BN);
 
-enum { EPI_ACT = 0, EPI_SCATTER = 1, EPI_RELU2 = 2 };
+enum { EPI_ACT = 0, EPI_SCATTER = 1, EPI_RELU2 = 2, EPI_ROUTE = 3 };
 
 struct GemmArgs {
   const int32_t *offs;
@@ -71,6 +71,13 @@ struct GemmArgs {
   const int32_t *col_sorted;     // ffn2
   const uint16_t *gate_scal;     // ffn2
   uint16_t *y_out;               // ffn2: y_flat [N or n, H]
+  // router (EPI_ROUTE): one dense group of dense_rows tokens (offs == NULL),
+  // B = the gate weights [n_experts, H]; per token the top-k of its logits
+  int64_t dense_rows;
+  int n_experts, topk, gating;
+  int32_t *topk_indx;
+  uint16_t *topk_vals;
+  float *logits_out;             // [n, n_experts] fp32, or NULL
   uint32_t *ctrl;
   unsigned long long timeout_ns;
 };
@@ -129,7 +136,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
   }
   pdl_wait();  // offs and the operands come from earlier kernels of the stream
-  for (int i = threadIdx.x; i <= E; i += kThreads) s_offs[i] = args.offs[i];
+  if (args.offs) {
+    for (int i = threadIdx.x; i <= E; i += kThreads) s_offs[i] = args.offs[i];
+  } else if (threadIdx.x == 0) {  // one dense group (the router)
+    s_offs[0] = 0;
+    s_offs[1] = (int)args.dense_rows;
+  }
   __syncthreads();
   if (warp == 0) row_tile_prefix(s_offs, E, BM, s_tstart);
   tc_fence_before();
@@ -234,7 +246,60 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t tbase = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * BN);
       const int p = d.m0 + row;
       const bool valid = p < d.m_end;
-      if (EPI == EPI_RELU2) {
+      if (EPI == EPI_ROUTE) {
+        // this thread's row holds token p's logits in columns [0, n_experts):
+        // keep the top 8 by (value descending, expert id ascending), columns
+        // arriving in ascending expert id
+        const int En = args.n_experts;
+        const int nchunk = (En + 31) / 32;
+        float *lrow = (valid && args.logits_out) ? args.logits_out + (size_t)p * En : nullptr;
+        TopK<8> tk;
+        tk.init();
+#pragma unroll 1
+        for (int c = 0; c < nchunk; ++c) {
+          uint32_t r[32];
+          TMEM_LD32(tbase + c * 32, r);
+          tmem_wait_ld();
+#pragma unroll
+          for (int i = 0; i < 32; ++i) {
+            const int e = c * 32 + i;
+            if (e < En) {
+              const float v = __uint_as_float(r[i]);
+              if (lrow) lrow[e] = v;
+              tk.push_ascending(order_key(v), e);
+            }
+          }
+        }
+        const int K = args.topk;
+        const float v0 = key_to_float(tk.key[0]);
+        float ex[8], denom = 0.f;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          ex[j] = j < K ? expf(key_to_float(tk.key[j]) - v0) : 0.f;
+          denom += ex[j];
+        }
+        if (args.gating == MOE_GATING_SOFTMAX_ALL) {  // uniform: every lane reads TMEM
+          float sum = 0.f;
+#pragma unroll 1
+          for (int c = 0; c < nchunk; ++c) {
+            uint32_t r[32];
+            TMEM_LD32(tbase + c * 32, r);
+            tmem_wait_ld();
+#pragma unroll
+            for (int i = 0; i < 32; ++i)
+              if (c * 32 + i < En) sum += expf(__uint_as_float(r[i]) - v0);
+          }
+          denom = sum;
+        }
+        if (valid) {
+#pragma unroll
+          for (int j = 0; j < 8; ++j)
+            if (j < K) {
+              args.topk_indx[(size_t)p * K + j] = tk.e[j];
+              args.topk_vals[(size_t)p * K + j] = float_to_bf16_bits(ex[j] / denom);
+            }
+        }
+      } else if (EPI == EPI_RELU2) {
         // column j of the tile is h column nt*256 + j
         uint16_t *hrow = args.h_out + (size_t)p * args.I;
 #pragma unroll 1
@@ -361,6 +426,34 @@ cudaError_t launch_gemm(const CUtensorMap &ta, const CUtensorMap &tb, const Gemm
 }
 
 }  // namespace
+
+// Router matmul with the top-k in its epilogue: logits = x . w_gate^T
+// (tokens on the MMA's M side, the E <= 256 gate rows on N), then per token
+// the k largest logits (ties to the lower expert id) and their gate weights.
+cudaError_t launch_route_gemm(const uint16_t *x, const uint16_t *w_gate, int64_t n, int E, int H,
+                              int k, int gating, int32_t *topk_indx, uint16_t *topk_vals,
+                              float *logits, uint32_t *ctrl, cudaStream_t s) {
+  if (n == 0) return cudaSuccess;
+  CUtensorMap ta, tb;
+  if (!map_2d(&ta, x, (uint64_t)n, (uint64_t)H, BM) ||
+      !map_3d(&tb, w_gate, 1ull, (uint64_t)E, (uint64_t)H, BN))
+    return cudaErrorInvalidValue;
+  GemmArgs a{};
+  a.offs = nullptr;
+  a.dense_rows = n;
+  a.E = 1;
+  a.num_kb = H / BK;
+  a.n_tiles = 1;  // E <= 256 columns
+  a.n_experts = E;
+  a.topk = k;
+  a.gating = gating;
+  a.topk_indx = topk_indx;
+  a.topk_vals = topk_vals;
+  a.logits_out = logits;
+  a.ctrl = ctrl;
+  a.timeout_ns = kWaitTimeoutNs;
+  return launch_gemm<EPI_ROUTE, false>(ta, tb, a, s);
+}
 
 cudaError_t launch_ffn(const uint16_t *x_sorted, const int32_t *offs, const int32_t *col_sorted,
                        const uint16_t *gate_scal, const uint16_t *w13, const uint16_t *w2,

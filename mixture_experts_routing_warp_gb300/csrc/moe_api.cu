@@ -204,7 +204,10 @@ moe_status moe_combine(const uint16_t *y_flat, int64_t n, int32_t k, int32_t H, 
   return from_cuda(launch_combine(y_flat, n, k, H, out, (cudaStream_t)stream));
 }
 
-static moe_status forward_impl(const uint16_t *x, const float *logits, const uint16_t *w13,
+// Routing comes from `logits`, or, when w_gate is given, from the router
+// matmul x . w_gate^T fused with the top-k.
+static moe_status forward_impl(const uint16_t *x, const float *logits, const uint16_t *w_gate,
+                               const uint16_t *w13,
                                const uint16_t *w2, int64_t n, int32_t E, int32_t k, int32_t H,
                                int32_t I, const moe_params *params, uint16_t *out,
                                int32_t *topk_indx, uint16_t *topk_vals,
@@ -218,10 +221,10 @@ static moe_status forward_impl(const uint16_t *x, const float *logits, const uin
   if (meta && (st = check_meta(meta, n)) != MOE_OK) return st;
   if ((topk_indx == nullptr) != (topk_vals == nullptr)) return MOE_ERR_INVALID_ARG;
   if (n == 0) return MOE_OK;
-  if (!x || !logits || !w13 || !w2 || !out || !workspace) return MOE_ERR_INVALID_ARG;
+  if (!x || (!logits && !w_gate) || !w13 || !w2 || !out || !workspace) return MOE_ERR_INVALID_ARG;
   if (!aligned(x, 16) || !aligned(w13, 16) || !aligned(w2, 16) || !aligned(out, 16) ||
-      !aligned(logits, 4) || !aligned(workspace, kAlign) || !aligned(topk_indx, 4) ||
-      !aligned(topk_vals, 2))
+      !aligned(logits, 4) || !aligned(w_gate, 16) || !aligned(workspace, kAlign) ||
+      !aligned(topk_indx, 4) || !aligned(topk_vals, 2))
     return MOE_ERR_MISALIGNED;
   const WorkspaceLayout L = workspace_layout(n, E, k, H, I);
   if (workspace_bytes < L.total) return MOE_ERR_WORKSPACE_TOO_SMALL;
@@ -249,7 +252,15 @@ static moe_status forward_impl(const uint16_t *x, const float *logits, const uin
   auto mark = [&](int i) { return ev ? record_stage_event(ev[i], s) : cudaSuccess; };
 
   int32_t *hist = ws_at<int32_t>(workspace, L.hist);
-  if (route_metadata_fits(n, k)) {
+  if (w_gate) {
+    // router matmul + top-k in one kernel, then the metadata kernel
+    if (mark(MOE_STAGE_ROUTE) != cudaSuccess ||
+        launch_route_gemm(x, w_gate, n, E, H, k, gating, indx, vals, nullptr, ctrl, s) !=
+            cudaSuccess ||
+        mark(MOE_STAGE_METADATA) != cudaSuccess ||
+        launch_metadata(indx, vals, n, E, k, m, hist, ctrl, s) != cudaSuccess)
+      return MOE_ERR_CUDA;
+  } else if (route_metadata_fits(n, k)) {
     // one cooperative kernel for both stages; the metadata stage time is 0
     if (mark(MOE_STAGE_ROUTE) != cudaSuccess ||
         launch_route_metadata(logits, n, E, k, gating, indx, vals, m, hist, ctrl, s) !=
@@ -288,8 +299,8 @@ moe_status moe_forward(const uint16_t *x, const float *logits, const uint16_t *w
                        const moe_params *params, uint16_t *out, int32_t *topk_indx,
                        uint16_t *topk_vals, const moe_routing_meta *meta, void *workspace,
                        size_t workspace_bytes, moe_stream stream) {
-  return forward_impl(x, logits, w13, w2, n, E, k, H, I, params, out, topk_indx, topk_vals, meta,
-                      workspace, workspace_bytes, (cudaStream_t)stream, nullptr);
+  return forward_impl(x, logits, nullptr, w13, w2, n, E, k, H, I, params, out, topk_indx,
+                      topk_vals, meta, workspace, workspace_bytes, (cudaStream_t)stream, nullptr);
 }
 
 moe_status moe_forward_timed(const uint16_t *x, const float *logits, const uint16_t *w13,
@@ -304,8 +315,37 @@ moe_status moe_forward_timed(const uint16_t *x, const float *logits, const uint1
     if (!events[i]) return MOE_ERR_INVALID_ARG;
   cudaEvent_t ev[MOE_STAGE_COUNT + 1];
   for (int i = 0; i <= MOE_STAGE_COUNT; ++i) ev[i] = (cudaEvent_t)events[i];
-  return forward_impl(x, logits, w13, w2, n, E, k, H, I, params, out, topk_indx, topk_vals, meta,
-                      workspace, workspace_bytes, (cudaStream_t)stream, ev);
+  return forward_impl(x, logits, nullptr, w13, w2, n, E, k, H, I, params, out, topk_indx,
+                      topk_vals, meta, workspace, workspace_bytes, (cudaStream_t)stream, ev);
+}
+
+moe_status moe_forward_gate(const uint16_t *x, const uint16_t *w_gate, const uint16_t *w13,
+                            const uint16_t *w2, int64_t n, int32_t E, int32_t k, int32_t H,
+                            int32_t I, const moe_params *params, uint16_t *out,
+                            int32_t *topk_indx, uint16_t *topk_vals,
+                            const moe_routing_meta *meta, void *workspace,
+                            size_t workspace_bytes, moe_stream stream) {
+  if (n > 0 && !w_gate) return MOE_ERR_INVALID_ARG;
+  return forward_impl(x, nullptr, w_gate, w13, w2, n, E, k, H, I, params, out, topk_indx,
+                      topk_vals, meta, workspace, workspace_bytes, (cudaStream_t)stream, nullptr);
+}
+
+moe_status moe_route_gemm(const uint16_t *x, const uint16_t *w_gate, int64_t n, int32_t E,
+                          int32_t H, int32_t k, int32_t gating, int32_t *topk_indx,
+                          uint16_t *topk_vals, float *logits, void *workspace,
+                          size_t workspace_bytes, moe_stream stream) {
+  moe_status st = check_sizes(n, E, k, H, 64, true);
+  if (st != MOE_OK) return st;
+  if (gating != MOE_GATING_SOFTMAX_TOPK && gating != MOE_GATING_SOFTMAX_ALL)
+    return MOE_ERR_INVALID_ARG;
+  if (n == 0) return MOE_OK;
+  if (!x || !w_gate || !topk_indx || !topk_vals || !workspace) return MOE_ERR_INVALID_ARG;
+  if (!aligned(x, 16) || !aligned(w_gate, 16) || !aligned(topk_indx, 4) ||
+      !aligned(topk_vals, 2) || !aligned(logits, 4) || !aligned(workspace, kAlign))
+    return MOE_ERR_MISALIGNED;
+  if (workspace_bytes < kCtrlBytes) return MOE_ERR_WORKSPACE_TOO_SMALL;
+  return from_cuda(launch_route_gemm(x, w_gate, n, E, H, k, gating, topk_indx, topk_vals, logits,
+                                     ws_at<uint32_t>(workspace, 0), (cudaStream_t)stream));
 }
 
 moe_status moe_read_status(void *workspace, size_t workspace_bytes, int32_t reset,

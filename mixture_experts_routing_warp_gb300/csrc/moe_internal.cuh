@@ -130,6 +130,67 @@ __device__ __forceinline__ uint16_t float_to_bf16_bits(float f) {
   return *reinterpret_cast<uint16_t *>(&h);
 }
 
+// Router top-k keys: an order-preserving 32-bit image of an fp32 logit
+// (-0.0 folded onto +0.0, NaN = 1 below every number, 0 below everything),
+// and a K-entry list kept in (key descending, expert id ascending) order.
+__device__ __forceinline__ uint32_t order_key(float v) {
+  if (v != v) return 1u;                         // NaN: below every number
+  const uint32_t u = __float_as_uint(v + 0.0f);  // -0.0 + 0.0 = +0.0: the two zeros tie
+  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+
+__device__ __forceinline__ float key_to_float(uint32_t key) {
+  return __uint_as_float((key & 0x80000000u) ? (key & 0x7fffffffu) : ~key);
+}
+
+template <int K>
+struct TopK {
+  uint32_t key[K];
+  int e[K];
+  __device__ __forceinline__ void init() {
+#pragma unroll
+    for (int i = 0; i < K; ++i) {
+      key[i] = 0u;  // below every present element
+      e[i] = 0x7fffffff;
+    }
+  }
+  // Elements arriving in ascending id: enter only if strictly larger.
+  __device__ __forceinline__ void push_ascending(uint32_t kv, int ev) {
+    if (kv > key[K - 1]) {
+#pragma unroll
+      for (int i = K - 1; i > 0; --i) {
+        const bool above = kv > key[i - 1];
+        const bool here = kv > key[i];
+        key[i] = above ? key[i - 1] : (here ? kv : key[i]);
+        e[i] = above ? e[i - 1] : (here ? ev : e[i]);
+      }
+      if (kv > key[0]) {
+        key[0] = kv;
+        e[0] = ev;
+      }
+    }
+  }
+  // Any order: (key descending, id ascending).
+  __device__ __forceinline__ static bool before(uint32_t ka, int ea, uint32_t kb, int eb) {
+    return ka > kb || (ka == kb && ea < eb);
+  }
+  __device__ __forceinline__ void push_any(uint32_t kv, int ev) {
+    if (before(kv, ev, key[K - 1], e[K - 1])) {
+#pragma unroll
+      for (int i = K - 1; i > 0; --i) {
+        const bool above = before(kv, ev, key[i - 1], e[i - 1]);
+        const bool here = before(kv, ev, key[i], e[i]);
+        key[i] = above ? key[i - 1] : (here ? kv : key[i]);
+        e[i] = above ? e[i - 1] : (here ? ev : e[i]);
+      }
+      if (before(kv, ev, key[0], e[0])) {
+        key[0] = kv;
+        e[0] = ev;
+      }
+    }
+  }
+};
+
 // Resolved activation parameters handed to the FFN kernels.
 struct ActParams {
   int act;         // moe_activation
@@ -255,6 +316,11 @@ cudaError_t launch_ffn_swap(const uint16_t *x_sorted, const int32_t *offs,
                             const uint16_t *w13, const uint16_t *w2, int64_t N, int E, int H,
                             int I, const ActParams &act, uint16_t *h_buf, uint16_t *y_flat,
                             uint32_t *ctrl, cudaStream_t s, cudaEvent_t *ev_ffn);
+
+// Router matmul fused with the top-k (the tokens-on-M GEMM, EPI_ROUTE).
+cudaError_t launch_route_gemm(const uint16_t *x, const uint16_t *w_gate, int64_t n, int E, int H,
+                              int k, int gating, int32_t *topk_indx, uint16_t *topk_vals,
+                              float *logits, uint32_t *ctrl, cudaStream_t s);
 
 cudaError_t launch_wait_selftest(uint32_t *ctrl, unsigned long long timeout_ns, cudaStream_t s);
 

@@ -47,64 +47,6 @@ constexpr int kRouteThreads = 256;
 constexpr int kFusedThreads = 1024;
 constexpr int kSlotCap = 8192;  // slots a fused CTA keeps in shared memory
 
-__device__ __forceinline__ uint32_t order_key(float v) {
-  if (v != v) return 1u;                         // NaN: below every number
-  const uint32_t u = __float_as_uint(v + 0.0f);  // -0.0 + 0.0 = +0.0: the two zeros tie
-  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
-}
-
-__device__ __forceinline__ float key_to_float(uint32_t key) {
-  return __uint_as_float((key & 0x80000000u) ? (key & 0x7fffffffu) : ~key);
-}
-
-template <int K>
-struct TopK {
-  uint32_t key[K];
-  int e[K];
-  __device__ __forceinline__ void init() {
-#pragma unroll
-    for (int i = 0; i < K; ++i) {
-      key[i] = 0u;  // below every present element
-      e[i] = 0x7fffffff;
-    }
-  }
-  // Elements arriving in ascending id: enter only if strictly larger.
-  __device__ __forceinline__ void push_ascending(uint32_t kv, int ev) {
-    if (kv > key[K - 1]) {
-#pragma unroll
-      for (int i = K - 1; i > 0; --i) {
-        const bool above = kv > key[i - 1];
-        const bool here = kv > key[i];
-        key[i] = above ? key[i - 1] : (here ? kv : key[i]);
-        e[i] = above ? e[i - 1] : (here ? ev : e[i]);
-      }
-      if (kv > key[0]) {
-        key[0] = kv;
-        e[0] = ev;
-      }
-    }
-  }
-  // Any order: (key descending, id ascending).
-  __device__ __forceinline__ static bool before(uint32_t ka, int ea, uint32_t kb, int eb) {
-    return ka > kb || (ka == kb && ea < eb);
-  }
-  __device__ __forceinline__ void push_any(uint32_t kv, int ev) {
-    if (before(kv, ev, key[K - 1], e[K - 1])) {
-#pragma unroll
-      for (int i = K - 1; i > 0; --i) {
-        const bool above = before(kv, ev, key[i - 1], e[i - 1]);
-        const bool here = before(kv, ev, key[i], e[i]);
-        key[i] = above ? key[i - 1] : (here ? kv : key[i]);
-        e[i] = above ? e[i - 1] : (here ? ev : e[i]);
-      }
-      if (before(kv, ev, key[0], e[0])) {
-        key[0] = kv;
-        e[0] = ev;
-      }
-    }
-  }
-};
-
 // Top-K of token row `row` (E fp32) by the G lanes of a group; lane g =
 // lane % G. On return every lane of the group holds the merged list and
 // the K gate weights. `valid` is uniform within a group.
