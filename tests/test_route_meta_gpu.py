@@ -138,11 +138,15 @@ def test_run_to_run_bit_identical():
 
 @pytest.mark.parametrize("n,E,k", [(16384, 128, 4), (4096, 32, 4), (33, 8, 2), (1, 4, 1),
                                    (777, 100, 5), (5000, 7, 3), (3000, 256, 8),
-                                   (600_000, 16, 4)])
+                                   (600_000, 16, 4),
+                                   # decode sizes (n*k <= 32): the one-CTA kernel
+                                   (1, 32, 4), (8, 32, 4), (2, 256, 8), (4, 128, 8),
+                                   (32, 16, 1), (5, 7, 3), (3, 100, 5), (16, 64, 2)])
 @pytest.mark.parametrize("gating", ["softmax_topk", "softmax_all"])
 def test_route_metadata_equals_route_then_build(n, E, k, gating):
-    """The fused call (one cooperative kernel when each SM's slots fit in
-    shared memory, else two kernels) gives the two-call result bit for bit."""
+    """The fused call (one CTA for decode sizes, one cooperative kernel when
+    each SM's slots fit in shared memory, else two kernels) gives the
+    two-call result bit for bit."""
     logits = dev(I.route_logits(n, E, seed=n % 97, tie_heavy=True))
     i1, v1 = moe.route(logits, k, gating)
     ws1 = moe.workspace(n, E, k, 64, 64)
@@ -157,8 +161,11 @@ def test_route_metadata_equals_route_then_build(n, E, k, gating):
             a, b = a.view(torch.int16), b.view(torch.int16)
         assert torch.equal(a, b), key
     if n <= 20000:
-        ref_i, _ = oracle.route(logits.cpu().numpy(), k, gating)
+        ref_i, ref_v = oracle.route(logits.cpu().numpy(), k, gating)
         np.testing.assert_array_equal(i2.cpu().numpy(), ref_i)
+        ref_m = oracle.metadata(ref_i, host_bits(v2), E)
+        for key in ("col_sum", "offs", "col_sorted", "row_sorted"):
+            np.testing.assert_array_equal(m2[key].cpu().numpy(), ref_m[key], err_msg=key)
 
 
 @pytest.mark.parametrize("E,k", [(128, 4), (32, 4), (6, 2)])
