@@ -46,15 +46,25 @@ constexpr int BM = 128;                 // rows per tile (UMMA M)
 constexpr int BN = 256;                 // accumulator columns per tile (UMMA N)
 constexpr int BK = 64;                  // K per stage: 64 bf16 = one 128-byte swizzle row
 constexpr int UK = 16;                  // K per tcgen05.mma (kind::f16)
-constexpr int STAGES = 4;
 constexpr int kEpiWarps = 4;
 constexpr int kThreads = (2 + kEpiWarps) * 32;
 constexpr int A_BYTES = BM * BK * 2;    // 16 KB
-constexpr int B_BYTES = BN * BK * 2;    // 32 KB
-constexpr int kTmemCols = 2 * BN;       // two fp32 accumulators
-constexpr int kNumBars = 2 * STAGES + 2 + 2 + 1;
-constexpr int kSmemBytes = 1024 /*alignment slack*/ + STAGES * (A_BYTES + B_BYTES) +
-                           kNumBars * 8 + 16 + 2 * (kMaxExperts + 1) * 4 + 16;
+
+// Ring configuration by the B rows a stage holds (RB): 256 weight rows for
+// the expert contractions (4 stages of 48 KB); the router's few gate rows
+// leave room for a deeper ring (RB = 32: 9 stages of 20 KB), which is what
+// keeps enough bytes in flight per SM when only n / 128 SMs have a tile.
+template <int RB>
+struct TCfg {
+  static constexpr int kBBytes = RB * BK * 2;
+  static constexpr int kStages =
+      196608 / (A_BYTES + kBBytes) < 12 ? 196608 / (A_BYTES + kBBytes) : 12;
+  static constexpr int kTmemCols = 2 * RB;  // two fp32 accumulators of RB columns
+  static constexpr int kNumBars = 2 * kStages + 2 + 2 + 1;
+  static constexpr int kSmemBytes = 1024 /*alignment slack*/ + kStages * (A_BYTES + kBBytes) +
+                                    kNumBars * 8 + 16 + 2 * (kMaxExperts + 1) * 4 + 16;
+  static_assert(RB == 32 || RB == 64 || RB == 128 || RB == 256, "B rows per stage");
+};
 
 constexpr uint32_t kIdesc = make_idesc_bf16(BM, BN);
 
@@ -74,6 +84,7 @@ struct GemmArgs {
   // router (EPI_ROUTE): one dense group of dense_rows tokens (offs == NULL),
   // B = the gate weights [n_experts, H]; per token the top-k of its logits
   int64_t dense_rows;
+  int b_rows;  // weight rows of a stage's B box and the MMA's N (BN; the router: E to 16)
   int n_experts, topk, gating;
   int32_t *topk_indx;
   uint16_t *topk_vals;
@@ -83,17 +94,20 @@ struct GemmArgs {
 };
 
 // ------------------------------------------------------------------ kernel --
-template <int EPI, bool PACKED>
+template <int EPI, bool PACKED, int RB>
 __global__ void __launch_bounds__(kThreads, 1)
     grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a,
                         const __grid_constant__ CUtensorMap tmap_b, const GemmArgs args) {
+  using C = TCfg<RB>;
+  constexpr int STAGES = C::kStages;
+  constexpr int B_BYTES = C::kBBytes;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_addr = smem_u32(smem_raw);
   uint8_t *smem = smem_raw + ((1024u - (raw_addr & 1023u)) & 1023u);
   uint8_t *sA = smem;
   uint8_t *sB = smem + STAGES * A_BYTES;
   uint64_t *bars = reinterpret_cast<uint64_t *>(sB + STAGES * B_BYTES);
-  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + kNumBars);
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + C::kNumBars);
   volatile int *s_abort = reinterpret_cast<volatile int *>(tmem_slot + 1);
   int *s_offs = reinterpret_cast<int *>(tmem_slot + 4);
   int *s_tstart = s_offs + (kMaxExperts + 1);
@@ -131,7 +145,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 1) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
                      smem_u32(tmem_slot)),
-                 "r"(kTmemCols)
+                 "r"(C::kTmemCols)
                  : "memory");
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
   }
@@ -165,7 +179,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             ok = false;
             break;
           }
-          mbar_arrive_expect_tx(full_bar(stage), A_BYTES + B_BYTES);
+          // B rows past b_rows keep stale data: the MMA's N stops at b_rows
+          mbar_arrive_expect_tx(full_bar(stage), (uint32_t)(A_BYTES + args.b_rows * BK * 2));
           tma_load_2d(sA_addr + stage * A_BYTES, &tmap_a, full_bar(stage), kb * BK, d.m0);
           if (PACKED) {
             tma_load_3d(sB_addr + stage * B_BYTES, &tmap_b, full_bar(stage), kb * BK,
@@ -208,7 +223,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t acc_phase = (uint32_t)(local >> 1) & 1u;
         if (!wait_bounded(tempty_bar(acc), acc_phase ^ 1u, s_abort, args.ctrl, args.timeout_ns)) break;
         tc_fence_after();
-        const uint32_t d_tmem = tmem_base + (uint32_t)(acc * BN);
+        const uint32_t d_tmem = tmem_base + (uint32_t)(acc * RB);
+        const uint32_t idesc = args.b_rows == BN ? kIdesc : make_idesc_bf16(BM, args.b_rows);
         for (int kb = 0; kb < num_kb; ++kb) {
           if (!wait_bounded(full_bar(stage), phase, s_abort, args.ctrl, args.timeout_ns)) {
             ok = false;
@@ -219,7 +235,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint64_t bdesc = sw128_desc(sB_addr + stage * B_BYTES);
 #pragma unroll
           for (int kk = 0; kk < BK / UK; ++kk)  // +32 bytes along K per step = +2 in the descriptor
-            umma_bf16(d_tmem, adesc + 2u * kk, bdesc + 2u * kk, kIdesc, (kb | kk) != 0 ? 1u : 0u);
+            umma_bf16(d_tmem, adesc + 2u * kk, bdesc + 2u * kk, idesc, (kb | kk) != 0 ? 1u : 0u);
           umma_commit(empty_bar(stage));
           if (++stage == STAGES) {
             stage = 0;
@@ -243,7 +259,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t acc_phase = (uint32_t)(local >> 1) & 1u;
       if (!wait_bounded(tfull_bar(acc), acc_phase, s_abort, args.ctrl, args.timeout_ns)) break;
       tc_fence_after();
-      const uint32_t tbase = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * BN);
+      const uint32_t tbase = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * RB);
       const int p = d.m0 + row;
       const bool valid = p < d.m_end;
       if (EPI == EPI_ROUTE) {
@@ -403,25 +419,26 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 1) {
     tc_fence_after();
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_base),
-                 "r"(kTmemCols)
+                 "r"(C::kTmemCols)
                  : "memory");
   }
 }
 
-template <int EPI, bool PACKED>
+template <int EPI, bool PACKED, int RB = BN>
 cudaError_t launch_gemm(const CUtensorMap &ta, const CUtensorMap &tb, const GemmArgs &a,
                         cudaStream_t s) {
-  auto kern = grouped_gemm_kernel<EPI, PACKED>;
+  using C = TCfg<RB>;
+  auto kern = grouped_gemm_kernel<EPI, PACKED, RB>;
   static bool attr_set = false;  // one value for every device of the process
   if (!attr_set) {
     cudaError_t err =
-        cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+        cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
     if (err != cudaSuccess) return err;
     if ((err = uniform_carveout(kern)) != cudaSuccess) return err;
     attr_set = true;
   }
   const cudaError_t err = launch_dependent(kern, dim3(device_sm_count()), dim3(kThreads),
-                                           kSmemBytes, s, ta, tb, a);
+                                           C::kSmemBytes, s, ta, tb, a);
   return err != cudaSuccess ? err : cudaGetLastError();
 }
 
@@ -435,10 +452,12 @@ cudaError_t launch_route_gemm(const uint16_t *x, const uint16_t *w_gate, int64_t
                               float *logits, uint32_t *ctrl, cudaStream_t s) {
   if (n == 0) return cudaSuccess;
   CUtensorMap ta, tb;
+  const int b_rows = (E + 15) / 16 * 16;  // the MMA's N: a multiple of 16
   if (!map_2d(&ta, x, (uint64_t)n, (uint64_t)H, BM) ||
-      !map_3d(&tb, w_gate, 1ull, (uint64_t)E, (uint64_t)H, BN))
+      !map_3d(&tb, w_gate, 1ull, (uint64_t)E, (uint64_t)H, (uint32_t)b_rows))
     return cudaErrorInvalidValue;
   GemmArgs a{};
+  a.b_rows = b_rows;
   a.offs = nullptr;
   a.dense_rows = n;
   a.E = 1;
@@ -452,7 +471,10 @@ cudaError_t launch_route_gemm(const uint16_t *x, const uint16_t *w_gate, int64_t
   a.logits_out = logits;
   a.ctrl = ctrl;
   a.timeout_ns = kWaitTimeoutNs;
-  return launch_gemm<EPI_ROUTE, false>(ta, tb, a, s);
+  if (b_rows <= 32) return launch_gemm<EPI_ROUTE, false, 32>(ta, tb, a, s);
+  if (b_rows <= 64) return launch_gemm<EPI_ROUTE, false, 64>(ta, tb, a, s);
+  if (b_rows <= 128) return launch_gemm<EPI_ROUTE, false, 128>(ta, tb, a, s);
+  return launch_gemm<EPI_ROUTE, false, 256>(ta, tb, a, s);
 }
 
 cudaError_t launch_ffn(const uint16_t *x_sorted, const int32_t *offs, const int32_t *col_sorted,
@@ -474,6 +496,7 @@ cudaError_t launch_ffn(const uint16_t *x_sorted, const int32_t *offs, const int3
     return cudaErrorInvalidValue;
 
   GemmArgs a{};
+  a.b_rows = BN;
   a.offs = offs;
   a.E = E;
   a.I = I;
