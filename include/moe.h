@@ -13,6 +13,11 @@
  *                          scale and scatter back to token-slot order
  *   4. moe_combine         sum of a token's k weighted expert outputs
  *   moe_forward            1 -> 4 in one call
+ * and around them: moe_route_metadata (1 + 2 in one kernel),
+ * moe_build_metadata_noalloc (2 without a workspace), moe_route_gemm (the
+ * router matmul fused with 1), moe_forward_gate (the layer from x and the
+ * gate weights), moe_forward_timed (stage events), moe_forward_launch_count,
+ * the workspace calls, moe_read_status and moe_selftest_wait_timeout.
  *
  * Sources (page title, section):
  *  [R1] "Reuse topk SparseMatrix routing metadata in GPT-OSS MoE forward"
