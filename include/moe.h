@@ -247,7 +247,8 @@ moe_status moe_build_metadata_noalloc(const int32_t *topk_indx, const uint16_t *
  * PyTorch" (each expert runs on its contiguous slice; the weight multiplies
  * the expert output), [R3] 关键源码片段 (activations, w13 layouts).
  *   x       [n, H] bf16 tokens.
- *   meta    metadata from moe_build_metadata (offs, col_sorted, gate_scal read).
+ *   meta    metadata from moe_build_metadata (offs, col_sorted, row_sorted,
+ *           gate_scal read).
  *   w13     [E, 2I, H] bf16, row-major (each expert's [2I, H] block in
  *           params->w13_layout order); [E, I, H] for MOE_ACT_RELU2.
  *   w2      [E, H, I] bf16, row-major.

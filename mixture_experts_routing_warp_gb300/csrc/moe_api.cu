@@ -188,7 +188,7 @@ moe_status moe_grouped_ffn(const uint16_t *x, const moe_routing_meta *meta, cons
   cudaStream_t s = (cudaStream_t)stream;
   const int64_t N = n * k;
   uint16_t *x_sorted = ws_at<uint16_t>(workspace, L.x_sorted);
-  cudaError_t err = launch_gather_rows(x, meta->col_sorted, N, k, H, x_sorted, s);
+  cudaError_t err = launch_gather_rows(x, meta->row_sorted, n, k, H, x_sorted, s);
   if (err != cudaSuccess) return MOE_ERR_CUDA;
   return from_cuda(launch_ffn(x_sorted, meta->offs, meta->col_sorted, meta->gate_scal, w13, w2, N,
                               E, H, I, act, ws_at<uint16_t>(workspace, L.h), y_flat,
@@ -276,7 +276,7 @@ static moe_status forward_impl(const uint16_t *x, const float *logits, const uin
       return MOE_ERR_CUDA;
   }
   if (mark(MOE_STAGE_GATHER) != cudaSuccess ||
-      launch_gather_rows(x, m.col_sorted, N, k, H, x_sorted, s) != cudaSuccess)
+      launch_gather_rows(x, m.row_sorted, n, k, H, x_sorted, s) != cudaSuccess)
     return MOE_ERR_CUDA;
   if (launch_ffn(x_sorted, m.offs, m.col_sorted, m.gate_scal, w13, w2, N, E, H, I, act, h, y_flat,
                  ctrl, s, ev ? ev + MOE_STAGE_FFN1 : nullptr) != cudaSuccess)

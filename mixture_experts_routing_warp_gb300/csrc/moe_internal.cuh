@@ -296,7 +296,8 @@ cudaError_t launch_metadata(const int32_t *topk_indx, const uint16_t *topk_vals,
                             int k, const moe_routing_meta &meta, int32_t *ws_hist,
                             uint32_t *ctrl, cudaStream_t s);
 
-cudaError_t launch_gather_rows(const uint16_t *x, const int32_t *col_sorted, int64_t N, int k,
+// X_sorted[row_sorted[t*k + j]] = x[t] for the n tokens' k slots.
+cudaError_t launch_gather_rows(const uint16_t *x, const int32_t *row_sorted, int64_t n, int k,
                                int H, uint16_t *x_sorted, cudaStream_t s);
 
 cudaError_t launch_combine(const uint16_t *y_flat, int64_t n, int k, int H, uint16_t *out,

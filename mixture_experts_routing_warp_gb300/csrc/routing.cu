@@ -869,44 +869,49 @@ cudaError_t launch_metadata_noalloc(const int32_t *topk_indx, const uint16_t *to
 
 // ======================================================= gather rows ==
 // X_sorted[p] = x[col_sorted[p] / k]: the dispatch index_select of the
-// MiniMind issue ("It is removable in plain PyTorch"). A warp per (row,
-// group of 128 16-byte chunks): up to 4 loads in flight per thread and one
-// memory round trip per unit, so a few rows cost about one round trip.
+// MiniMind issue ("It is removable in plain PyTorch"), done token-major: a
+// warp per (token t, group of 128 16-byte chunks) reads its chunks of x[t]
+// once (up to 4 loads in flight per thread) and writes them to the k sorted
+// positions row_sorted[t*k + j] of the token's slots, so x is read from
+// memory once rather than once per slot.
 constexpr int kCopyThreads = 256;
 
 constexpr int kChunksPerLane = 4;  // 16-byte chunks in flight per thread
 
 __global__ void __launch_bounds__(kCopyThreads) gather_rows_kernel(
-    const uint4 *__restrict__ x, const int32_t *__restrict__ col_sorted, int64_t N, int k,
+    const uint4 *__restrict__ x, const int32_t *__restrict__ row_sorted, int64_t n, int k,
     int vec_per_row, int groups_per_row, uint4 *__restrict__ x_sorted) {
   pdl_launch_dependents();
-  pdl_wait();  // col_sorted comes from the metadata kernel
+  pdl_wait();  // row_sorted comes from the metadata kernel
   const int lane = threadIdx.x & 31;
-  const int64_t units = N * groups_per_row;  // (row, group of 32 * kChunksPerLane chunks)
+  const int64_t N = n * k;
+  const int64_t units = n * groups_per_row;  // (token, group of 32 * kChunksPerLane chunks)
   const int64_t warps = (int64_t)gridDim.x * (kCopyThreads / 32);
   for (int64_t u = (int64_t)blockIdx.x * (kCopyThreads / 32) + (threadIdx.x >> 5); u < units;
        u += warps) {
-    const int64_t p = u / groups_per_row;
-    const int c0 = (int)(u - p * groups_per_row) * 32 * kChunksPerLane + lane;
-    const int32_t f = __ldg(col_sorted + p);
-    // positions whose slot carried an out-of-range expert id are never
-    // written by the metadata kernel (which flags MOE_ERR_INVALID_ARG)
-    if ((uint32_t)f >= (uint32_t)N) continue;
-    const uint4 *src = x + (int64_t)(f / k) * vec_per_row;
-    uint4 *dst = x_sorted + p * vec_per_row;
+    const int64_t t = u / groups_per_row;
+    const int c0 = (int)(u - t * groups_per_row) * 32 * kChunksPerLane + lane;
+    const uint4 *src = x + t * vec_per_row;
     uint4 v[kChunksPerLane];
 #pragma unroll
     for (int q = 0; q < kChunksPerLane; ++q)
-      if (c0 + 32 * q < vec_per_row) v[q] = __ldg(src + c0 + 32 * q);
+      if (c0 + 32 * q < vec_per_row) v[q] = __ldcs(src + c0 + 32 * q);
+    for (int j = 0; j < k; ++j) {
+      const int32_t p = __ldg(row_sorted + t * k + j);
+      // a slot whose expert id was out of range has no position (the metadata
+      // kernel flags MOE_ERR_INVALID_ARG)
+      if ((uint32_t)p >= (uint32_t)N) continue;
+      uint4 *dst = x_sorted + (int64_t)p * vec_per_row;
 #pragma unroll
-    for (int q = 0; q < kChunksPerLane; ++q)
-      if (c0 + 32 * q < vec_per_row) dst[c0 + 32 * q] = v[q];
+      for (int q = 0; q < kChunksPerLane; ++q)
+        if (c0 + 32 * q < vec_per_row) dst[c0 + 32 * q] = v[q];
+    }
   }
 }
 
-cudaError_t launch_gather_rows(const uint16_t *x, const int32_t *col_sorted, int64_t N, int k,
+cudaError_t launch_gather_rows(const uint16_t *x, const int32_t *row_sorted, int64_t n, int k,
                                int H, uint16_t *x_sorted, cudaStream_t s) {
-  if (N == 0) return cudaSuccess;
+  if (n == 0) return cudaSuccess;
   static bool configured = false;
   if (!configured) {
     cudaError_t err = uniform_carveout(gather_rows_kernel);
@@ -914,11 +919,11 @@ cudaError_t launch_gather_rows(const uint16_t *x, const int32_t *col_sorted, int
     configured = true;
   }
   const int vpr = H / 8, gpr = (vpr + 32 * kChunksPerLane - 1) / (32 * kChunksPerLane);
-  int64_t blocks = (N * gpr + kCopyThreads / 32 - 1) / (kCopyThreads / 32);
+  int64_t blocks = (n * gpr + kCopyThreads / 32 - 1) / (kCopyThreads / 32);
   const int64_t cap = (int64_t)device_sm_count() * 16;
   if (blocks > cap) blocks = cap;
   cudaError_t err = launch_dependent(gather_rows_kernel, dim3((unsigned)blocks), dim3(kCopyThreads),
-                                     0, s, reinterpret_cast<const uint4 *>(x), col_sorted, N, k,
+                                     0, s, reinterpret_cast<const uint4 *>(x), row_sorted, n, k,
                                      vpr, gpr, reinterpret_cast<uint4 *>(x_sorted));
   return err != cudaSuccess ? err : cudaGetLastError();
 }
