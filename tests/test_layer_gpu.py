@@ -233,3 +233,49 @@ def test_empty_batch_is_a_noop():
     out = moe.forward(x, logits, L.w13, L.w2, c.k, L.params, ws)
     torch.cuda.synchronize()
     assert out.shape == (0, c.H)
+
+
+def _routed_case(counts, H=128, Idim=192, k=1, seed=0, act="swiglu", layout="packed"):
+    """A layer whose top-1 routing sends exactly counts[e] tokens to expert e
+    (the logits are built on the host so; the k-1 other slots go to the next
+    experts in turn)."""
+    E, n = len(counts), int(sum(counts))
+    case = I.LayerCase(f"counts_{'_'.join(map(str, counts))}", n=n, H=H, E=E, k=k, I=Idim,
+                       act=act, layout=layout, w_std=0.1, seed=seed)
+    h = I.layer_inputs(case)
+    owner = np.repeat(np.arange(E), counts)
+    rng = np.random.default_rng(seed)
+    owner = owner[rng.permutation(n)]
+    logits = np.zeros((n, E), dtype=np.float32)
+    for t in range(n):
+        for j in range(k):
+            logits[t, (owner[t] + j) % E] = float(k - j) + 1.0
+    h["logits"] = logits
+    return case, h
+
+
+@pytest.mark.parametrize("ffn_kernel", ["auto", "tiled"])
+@pytest.mark.parametrize("counts", [(256, 257, 32, 33), (128, 129, 1, 342), (0, 600, 0, 0)])
+def test_tile_boundary_expert_loads(counts, ffn_kernel):
+    """Experts holding exactly one, one-plus-one, or no token tile of either
+    kernel (256 / 32 rows for the swap kernel, 128 for the tiled one)."""
+    case, h = _routed_case(counts)
+    L = Layer(case, ffn_kernel=ffn_kernel)
+    L.h = h
+    L.logits = dev(h["logits"])
+    out, indx, vals, meta = L.forward()
+    np.testing.assert_array_equal(meta["col_sum"].cpu().numpy(), np.array(counts))
+    _check_routing(L, indx, vals, meta)
+    ref = oracle.ffn(h["x"], indx.cpu().numpy(), host_bits(vals), h["w13"], h["w2"],
+                     **L.oracle_kw())
+    assert_layer_close(host_bits(out), ref, case.name)
+
+
+@pytest.mark.parametrize("ffn_kernel", ["auto", "tiled"])
+@pytest.mark.parametrize("E,k", [(1, 1), (4, 4), (8, 8)])
+def test_degenerate_expert_counts(E, k, ffn_kernel):
+    """E = 1 (a dense layer, gate weight 1) and k = E (every token to every
+    expert)."""
+    case = I.LayerCase(f"degenerate_e{E}_k{k}", n=130, H=128, E=E, k=k, I=128, w_std=0.1,
+                       seed=E)
+    _check_full(Layer(case, ffn_kernel=ffn_kernel))
