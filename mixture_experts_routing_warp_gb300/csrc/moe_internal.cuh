@@ -97,6 +97,42 @@ __device__ __forceinline__ long long wait_deadline(unsigned long long timeout_ns
 // without touching shared outputs. After a timeout the counter is off and
 // later barriers on this workspace time out too, until the control block is
 // cleared (moe_read_status with reset).
+// The barrier in two halves, so that a CTA can do work that the other CTAs
+// do not wait for between its arrival and its wait: grid_arrive (every
+// thread; returns thread 0's old counter value) and grid_wait (every thread,
+// with that value).
+__device__ __forceinline__ uint32_t grid_arrive(uint32_t *ctrl) {
+  __syncthreads();
+  uint32_t old = 0;
+  if (threadIdx.x == 0) {
+    const uint32_t inc = blockIdx.x == 0 ? (0x80000000u - (gridDim.x - 1u)) : 1u;
+    old = atom_add_release_gpu(ctrl + kCtrlBarArrive, inc);
+  }
+  return old;
+}
+
+__device__ __forceinline__ bool grid_wait(uint32_t *ctrl, uint32_t old,
+                                          unsigned long long timeout_ns) {
+  __shared__ int s_ok;
+  if (threadIdx.x == 0) {
+    uint32_t *ctr = ctrl + kCtrlBarArrive;
+    int ok = 1;
+    if (((ld_acquire_gpu(ctr) ^ old) & 0x80000000u) == 0u) {
+      const long long deadline = wait_deadline(timeout_ns);
+      while (((ld_acquire_gpu(ctr) ^ old) & 0x80000000u) == 0u) {
+        if (clock64() > deadline) {
+          ok = 0;
+          record_status(ctrl, MOE_ERR_TIMEOUT);
+          break;
+        }
+      }
+    }
+    s_ok = ok;
+  }
+  __syncthreads();
+  return s_ok != 0;
+}
+
 __device__ __forceinline__ bool grid_barrier(uint32_t *ctrl, unsigned long long timeout_ns) {
   __shared__ int s_ok;
   __syncthreads();

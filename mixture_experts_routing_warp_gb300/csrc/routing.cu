@@ -204,9 +204,10 @@ __device__ __forceinline__ void write_token(int64_t t, int64_t t0, const TopK<K>
   for (int j = 0; j < K; ++j) {
     if (j % G != g) continue;
     const uint16_t wb = float_to_bf16_bits(w[j]);
-    topk_indx[t * K + j] = tk.e[j];
-    topk_vals[t * K + j] = wb;
-    if (KEEP) {
+    if (!KEEP) {  // KEEP: the caller writes the outputs from the slots
+      topk_indx[t * K + j] = tk.e[j];
+      topk_vals[t * K + j] = wb;
+    } else {
       const int s = (int)(t - t0) * K + j;
       s_slot_e[s] = (uint8_t)tk.e[j];
       s_slot_v[s] = wb;
@@ -368,16 +369,19 @@ __device__ void meta_scan(int E, MetaShared<THREADS> &sh, int32_t *__restrict__ 
 }
 
 // Publish this CTA's counts (in sh.base[0..E)), pass the grid barrier, read
-// every CTA's and build sh.base = offs + before. Returns false after a
-// timeout.
-template <int THREADS>
+// every CTA's and build sh.base = offs + before. `between` runs (every
+// thread) after this CTA's arrival and before its wait. Returns false after
+// a timeout.
+template <int THREADS, typename Between>
 __device__ bool meta_barrier_prefix(int32_t *__restrict__ ws_hist, int E, MetaShared<THREADS> &sh,
                                     int32_t *__restrict__ col_sum, int32_t *__restrict__ offs,
-                                    uint32_t *ctrl, unsigned long long timeout_ns) {
+                                    uint32_t *ctrl, unsigned long long timeout_ns,
+                                    Between between) {
   const int tid = threadIdx.x;
   const int b = blockIdx.x, B = gridDim.x;
   const int stride = hist_stride(E), E4 = stride / 4;
   if (B == 1) {  // one CTA holds every slot: no exchange, no barrier
+    between();
     for (int e = tid; e < E; e += THREADS) {
       sh.tot[e] = sh.base[e];
       sh.pre[e] = 0;
@@ -388,7 +392,9 @@ __device__ bool meta_barrier_prefix(int32_t *__restrict__ ws_hist, int E, MetaSh
   }
   int32_t *row = ws_hist + (size_t)b * stride;
   for (int e = tid; e < stride; e += THREADS) row[e] = e < E ? sh.base[e] : 0;
-  if (!grid_barrier(ctrl, timeout_ns)) return false;
+  const uint32_t arrived = grid_arrive(ctrl);
+  between();
+  if (!grid_wait(ctrl, arrived, timeout_ns)) return false;
 
   const int parts = prefix_parts(THREADS, stride);
   if (tid < parts * E4) {
@@ -500,7 +506,7 @@ __global__ void __launch_bounds__(kMetaThreads) metadata_kernel(
   __syncthreads();
   if (sh.bad && tid == 0) record_status(ctrl, MOE_ERR_INVALID_ARG);
 
-  if (!meta_barrier_prefix(ws_hist, E, sh, col_sum, offs, ctrl, timeout_ns)) return;
+  if (!meta_barrier_prefix(ws_hist, E, sh, col_sum, offs, ctrl, timeout_ns, [] {})) return;
   meta_scatter(
       lo, hi - lo, E, sh,
       [&](int i, int &e, uint16_t &w) {
@@ -601,7 +607,15 @@ __global__ void __launch_bounds__(kFusedThreads, 1) route_metadata_kernel(
       write_token<K, G, true>(t, t0, tk, w, topk_indx, topk_vals, s_slot_e, s_slot_v, sh.base);
   }
   __syncthreads();
-  if (!meta_barrier_prefix(ws_hist, E, sh, col_sum, offs, ctrl, timeout_ns)) return;
+  // the CTA's top-k outputs leave shared memory while the other CTAs arrive
+  const int nslots = (int)(t1 - t0) * K;
+  auto write_topk = [&] {
+    for (int i = tid; i < nslots; i += kFusedThreads) {
+      topk_indx[t0 * K + i] = s_slot_e[i];
+      topk_vals[t0 * K + i] = s_slot_v[i];
+    }
+  };
+  if (!meta_barrier_prefix(ws_hist, E, sh, col_sum, offs, ctrl, timeout_ns, write_topk)) return;
   meta_scatter(
       t0 * K, (int)(t1 - t0) * K, E, sh,
       [&](int i, int &e, uint16_t &w) {
