@@ -16,8 +16,10 @@
 // 127 idle MMA rows as with tokens on M), fp32 in TMEM.
 //   NT = 32: decode, a handful of tokens per expert; the weights stream
 //     through all SMs.
-//   NT = 256 (128 for the packed gated layout, which needs two
-//     accumulators): prefill; the same MMA shape as tokens-on-M tiles.
+//   NT = 32 .. 256 (at most 128 for the packed gated layout, which needs
+//     two accumulators): prefill; per contraction the NT with the least
+//     estimated time (waves x per-tile cost; 256: the same MMA shape as
+//     tokens-on-M tiles).
 // Epilogues:
 //   ffn1, interleaved w13: weight rows 2i / 2i+1 are gate_i / up_i, in
 //     adjacent TMEM lanes: one shuffle pairs them.
@@ -371,33 +373,60 @@ cudaError_t launch_swap(const CUtensorMap &tw, const CUtensorMap &tx, const SwAr
   return err != cudaSuccess ? err : cudaGetLastError();
 }
 
-// One contraction at token-tile width NT: the tensor maps and the launch.
+// The w13 contraction at token-tile width NT (NT <= 128 for the packed
+// gated layout, whose two accumulators must fit TMEM twice).
 template <int NT>
-cudaError_t swap_pair(const uint16_t *x_sorted, const uint16_t *w13, const uint16_t *w2,
-                      int64_t N, int E, int H, int I, const ActParams &act, uint16_t *h_buf,
-                      SwArgs a, cudaStream_t s, cudaEvent_t *ev_ffn) {
+cudaError_t swap_ffn1(const uint16_t *x_sorted, const uint16_t *w13, int64_t N, int E, int H,
+                      int I, const ActParams &act, SwArgs a, cudaStream_t s) {
   const bool relu2_act = act.act == MOE_ACT_RELU2;
   const bool packed = !relu2_act && act.layout == MOE_W13_PACKED;
-  constexpr int NT_DUAL = NT > 128 ? 128 : NT;  // two accumulators per buffer
-  CUtensorMap tw1, tx1, tw2, tx2;
-  if (!map_3d(&tw1, w13, (uint64_t)E, (uint64_t)w13_rows(act, I), (uint64_t)H, SW_M) ||
-      !map_2d(&tx1, x_sorted, (uint64_t)N, (uint64_t)H, packed ? NT_DUAL : NT) ||
-      !map_3d(&tw2, w2, (uint64_t)E, (uint64_t)H, (uint64_t)I, SW_M) ||
-      !map_2d(&tx2, h_buf, (uint64_t)N, (uint64_t)I, NT))
+  constexpr int NT_DUAL = NT > 128 ? 128 : NT;
+  CUtensorMap tw, tx;
+  if (!map_3d(&tw, w13, (uint64_t)E, (uint64_t)w13_rows(act, I), (uint64_t)H, SW_M) ||
+      !map_2d(&tx, x_sorted, (uint64_t)N, (uint64_t)H, packed ? NT_DUAL : NT))
     return cudaErrorInvalidValue;
-
-  if (ev_ffn && record_stage_event(ev_ffn[0], s) != cudaSuccess) return cudaErrorUnknown;
   a.num_kb = H / SW_BK;
   a.f_tiles = (w13_rows(act, I) / (packed ? 2 : 1) + SW_M - 1) / SW_M;
-  cudaError_t err = relu2_act ? launch_swap<SW_RELU2, false, NT>(tw1, tx1, a, s)
-                    : packed  ? launch_swap<SW_ACT, true, NT_DUAL>(tw1, tx1, a, s)
-                              : launch_swap<SW_ACT, false, NT>(tw1, tx1, a, s);
-  if (err != cudaSuccess) return err;
+  return relu2_act ? launch_swap<SW_RELU2, false, NT>(tw, tx, a, s)
+         : packed  ? launch_swap<SW_ACT, true, NT_DUAL>(tw, tx, a, s)
+                   : launch_swap<SW_ACT, false, NT>(tw, tx, a, s);
+}
 
-  if (ev_ffn && record_stage_event(ev_ffn[1], s) != cudaSuccess) return cudaErrorUnknown;
+// The w2 contraction (gate scale + scatter) at token-tile width NT.
+template <int NT>
+cudaError_t swap_ffn2(const uint16_t *h_buf, const uint16_t *w2, int64_t N, int E, int H, int I,
+                      SwArgs a, cudaStream_t s) {
+  CUtensorMap tw, tx;
+  if (!map_3d(&tw, w2, (uint64_t)E, (uint64_t)H, (uint64_t)I, SW_M) ||
+      !map_2d(&tx, h_buf, (uint64_t)N, (uint64_t)I, NT))
+    return cudaErrorInvalidValue;
   a.num_kb = I / SW_BK;
   a.f_tiles = (H + SW_M - 1) / SW_M;
-  return launch_swap<SW_SCATTER, false, NT>(tw2, tx2, a, s);
+  return launch_swap<SW_SCATTER, false, NT>(tw, tx, a, s);
+}
+
+// Token-tile width of a contraction with f_tiles weight tiles per expert:
+// the NT that minimises waves * (cycles per K step of one tile). A tile's K
+// step reads kA weight tiles (16 KB each) and NT token rows (128 B each) from
+// shared memory at ~128 B per cycle, and issues MMAs worth ~1.45 cycles per
+// token column per weight tile: narrow tiles are bound by the shared-memory
+// reads, so more of them is not always faster. Tiles are estimated as
+// (ceil(N / NT) + min(E, N)) * f_tiles (each expert's ragged last tile).
+int pick_token_tile(int64_t N, int E, int f_tiles, bool dual) {
+  const int64_t sms = device_sm_count();
+  const int kA = dual ? 2 : 1;
+  int best = 32;
+  double best_t = 1e300;
+  for (int nt = dual ? 128 : 256; nt >= 32; nt /= 2) {
+    const int64_t tiles = ((N + nt - 1) / nt + (N < E ? N : E)) * (int64_t)f_tiles;
+    const double smem = 128.0 * kA + nt, mma = 1.45 * kA * nt;
+    const double t = (double)((tiles + sms - 1) / sms) * (smem > mma ? smem : mma);
+    if (t < best_t) {
+      best_t = t;
+      best = nt;
+    }
+  }
+  return best;
 }
 
 }  // namespace
@@ -420,10 +449,30 @@ cudaError_t launch_ffn_swap(const uint16_t *x_sorted, const int32_t *offs,
   a.y_out = y_flat;
   a.ctrl = ctrl;
   a.timeout_ns = kWaitTimeoutNs;
-  // a handful of rows per expert (decode): 32-row token tiles; else 256
-  if (N <= (int64_t)SW_NGRAN * E)
-    return swap_pair<32>(x_sorted, w13, w2, N, E, H, I, act, h_buf, a, s, ev_ffn);
-  return swap_pair<256>(x_sorted, w13, w2, N, E, H, I, act, h_buf, a, s, ev_ffn);
+  // a handful of rows per expert (decode): 32-row token tiles for both
+  int nt1 = 32, nt2 = 32;
+  if (N > (int64_t)SW_NGRAN * E) {
+    const bool packed = act.act != MOE_ACT_RELU2 && act.layout == MOE_W13_PACKED;
+    const int f1 = (w13_rows(act, I) / (packed ? 2 : 1) + SW_M - 1) / SW_M;
+    nt1 = pick_token_tile(N, E, f1, packed);
+    nt2 = pick_token_tile(N, E, (H + SW_M - 1) / SW_M, false);
+  }
+  if (ev_ffn && record_stage_event(ev_ffn[0], s) != cudaSuccess) return cudaErrorUnknown;
+  cudaError_t err;
+  switch (nt1) {
+    case 32: err = swap_ffn1<32>(x_sorted, w13, N, E, H, I, act, a, s); break;
+    case 64: err = swap_ffn1<64>(x_sorted, w13, N, E, H, I, act, a, s); break;
+    case 128: err = swap_ffn1<128>(x_sorted, w13, N, E, H, I, act, a, s); break;
+    default: err = swap_ffn1<256>(x_sorted, w13, N, E, H, I, act, a, s); break;
+  }
+  if (err != cudaSuccess) return err;
+  if (ev_ffn && record_stage_event(ev_ffn[1], s) != cudaSuccess) return cudaErrorUnknown;
+  switch (nt2) {
+    case 32: return swap_ffn2<32>(h_buf, w2, N, E, H, I, a, s);
+    case 64: return swap_ffn2<64>(h_buf, w2, N, E, H, I, a, s);
+    case 128: return swap_ffn2<128>(h_buf, w2, N, E, H, I, a, s);
+    default: return swap_ffn2<256>(h_buf, w2, N, E, H, I, a, s);
+  }
 }
 
 }  // namespace moe

@@ -279,3 +279,16 @@ def test_degenerate_expert_counts(E, k, ffn_kernel):
     case = I.LayerCase(f"degenerate_e{E}_k{k}", n=130, H=128, E=E, k=k, I=128, w_std=0.1,
                        seed=E)
     _check_full(Layer(case, ffn_kernel=ffn_kernel))
+
+
+@pytest.mark.parametrize("act,layout,Idim", [("swiglu_oai", "interleaved", 256),
+                                             ("relu2", "packed", 512), ("swiglu", "packed", 512)])
+def test_token_tile_widths(act, layout, Idim):
+    """Sizes at which the swap kernel's width choice (least waves x per-tile
+    cost) lands on 64-row token tiles for both contractions: n*k = 1200 rows
+    over 8 experts with 4 weight tiles per expert on each side (32-row tiles
+    would need two waves, 64-row ones fit one). The MiniMind tests cover the
+    128-row choice."""
+    case = I.LayerCase(f"ntw_{act}_{layout}", n=300, H=512, E=8, k=4, I=Idim, act=act,
+                       layout=layout, w_std=0.05, seed=21)
+    _check_full(Layer(case))
