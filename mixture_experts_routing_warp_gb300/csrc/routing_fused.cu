@@ -1,0 +1,146 @@
+// routing_fused.cu -- router top-k and routing metadata in one cooperative
+// kernel (one CTA per SM; a single CTA with no exchange when the batch fits
+// one pass), and the entry that picks it or the decode-size kernel.
+//
+// Sources (page title, section): as routing.cu.
+#include "routing_common.cuh"
+
+namespace moe {
+
+// ================================================= fused route + metadata ==
+//
+// moe_route_metadata / moe_forward's first two stages in one cooperative
+// kernel, one CTA per SM: CTA b routes tokens [b*T, b*T + T) (G lanes per
+// token as above), keeping its slots and histogram in shared memory, then
+// publishes, gathers and scatters its slots from shared memory.
+template <int K, int G, int NQ>
+__global__ void __launch_bounds__(kFusedThreads, 1) route_metadata_kernel(
+    const float *__restrict__ logits, int64_t n, int E, int gating, int T, int vec4,
+    int32_t *__restrict__ topk_indx, uint16_t *__restrict__ topk_vals,
+    int32_t *__restrict__ col_sum, int32_t *__restrict__ offs, int32_t *__restrict__ col_sorted,
+    int32_t *__restrict__ row_sorted, uint16_t *__restrict__ gate_scal,
+    int32_t *__restrict__ ws_hist, uint32_t *ctrl, unsigned long long timeout_ns) {
+  extern __shared__ uint8_t smem_raw[];
+  __shared__ MetaShared<kFusedThreads> sh;
+  uint8_t *s_slot_e = smem_raw;
+  uint16_t *s_slot_v = reinterpret_cast<uint16_t *>(smem_raw + (((size_t)T * K + 15) & ~15ull));
+
+  const int tid = threadIdx.x;
+  pdl_launch_dependents();  // the gather may be scheduled (it waits for this grid)
+  for (int e = tid; e < E; e += kFusedThreads) sh.base[e] = 0;
+  __syncthreads();
+
+  const int64_t t0 = min(n, (int64_t)blockIdx.x * T);
+  const int64_t t1 = min(n, t0 + T);
+  constexpr int per_pass = kFusedThreads / G;
+  for (int64_t tb = t0; tb < t1; tb += per_pass) {  // uniform over the block
+    const int64_t t = tb + tid / G;
+    const bool valid = t < t1;
+    TopK<K> tk;
+    float w[K];
+    topk_group<K, G, NQ>(logits + (valid ? t : 0) * E, valid, E, gating, vec4 != 0, tk, w);
+    if (valid)
+      write_token<K, G, true>(t, t0, tk, w, topk_indx, topk_vals, s_slot_e, s_slot_v, sh.base);
+  }
+  __syncthreads();
+  // the CTA's top-k outputs leave shared memory while the other CTAs arrive
+  const int nslots = (int)(t1 - t0) * K;
+  auto write_topk = [&] {
+    for (int i = tid; i < nslots; i += kFusedThreads) {
+      topk_indx[t0 * K + i] = s_slot_e[i];
+      topk_vals[t0 * K + i] = s_slot_v[i];
+    }
+  };
+  if (!meta_barrier_prefix(ws_hist, E, sh, col_sum, offs, ctrl, timeout_ns, write_topk)) return;
+  meta_scatter(
+      t0 * K, (int)(t1 - t0) * K, E, sh,
+      [&](int i, int &e, uint16_t &w) {
+        e = s_slot_e[i];
+        w = s_slot_v[i];
+      },
+      col_sorted, row_sorted, gate_scal);
+}
+
+// Tokens per CTA of the fused kernel: spread over the SMs, a multiple of 4;
+// a batch that one pass of one CTA covers (1024 / G tokens) gets one CTA,
+// which skips the cross-CTA exchange.
+int64_t fused_tokens_per_cta(int64_t n, int per_pass) {
+  if (n <= per_pass) return (n + 3) / 4 * 4;
+  const int sms = device_sm_count();
+  int64_t T = (n + sms - 1) / sms;
+  if (T < 4) T = 4;
+  return (T + 3) / 4 * 4;
+}
+
+struct RouteMetaLaunch {
+  const float *logits;
+  int64_t n;
+  int E, gating;
+  int32_t *indx;
+  uint16_t *vals;
+  const moe_routing_meta *meta;
+  int32_t *ws_hist;
+  uint32_t *ctrl;
+  cudaStream_t s;
+  template <int K, int G, int NQ>
+  cudaError_t go() {
+    const int64_t T = fused_tokens_per_cta(n, kFusedThreads / G);
+    const int64_t B = (n + T - 1) / T;
+    const size_t slots = (size_t)T * K;
+    const size_t smem = ((slots + 15) & ~(size_t)15) + slots * 2;
+    auto kern = route_metadata_kernel<K, G, NQ>;
+    static bool configured = false;
+    if (!configured) {
+      const int max_smem = kSlotCap * 3 + 16;
+      cudaError_t e1 =
+          cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, max_smem);
+      if (e1 != cudaSuccess) return e1;
+      if ((e1 = uniform_carveout(kern)) != cudaSuccess) return e1;
+      configured = true;
+    }
+    cudaError_t err = cudaSuccess;
+    int Ti = (int)T;
+    int64_t nn = n;
+    int E_ = E, g_ = gating;
+    int vec4 = (E % 4) == 0 && ((uintptr_t)logits % 16) == 0;
+    unsigned long long timeout = kWaitTimeoutNs;
+    void *args[] = {(void *)&logits, (void *)&nn, (void *)&E_, (void *)&g_, (void *)&Ti,
+                    (void *)&vec4, (void *)&indx, (void *)&vals, (void *)&meta->col_sum, (void *)&meta->offs,
+                    (void *)&meta->col_sorted, (void *)&meta->row_sorted,
+                    (void *)&meta->gate_scal, (void *)&ws_hist, (void *)&ctrl,
+                    (void *)&timeout};
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)B);
+    cfg.blockDim = dim3(kFusedThreads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeCooperative;
+    attr[0].val.cooperative = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = B > 1 ? 1 : 0;  // one CTA needs no co-residency guarantee
+    err = cudaLaunchKernelExC(&cfg, (const void *)kern, args);
+    if (err != cudaSuccess) return err;
+    return cudaGetLastError();
+  }
+};
+
+// True when the fused kernel can take (n, k): each CTA's slots fit in
+// shared memory. Otherwise the two kernels run.
+bool route_metadata_fits(int64_t n, int k) {
+  return fused_tokens_per_cta(n, 0) * k <= kSlotCap;  // the larger of the two T
+}
+
+cudaError_t launch_route_metadata(const float *logits, int64_t n, int E, int k, int gating,
+                                  int32_t *topk_indx, uint16_t *topk_vals,
+                                  const moe_routing_meta &meta, int32_t *ws_hist,
+                                  uint32_t *ctrl, cudaStream_t s) {
+  // every G (<= 8) lanes take a token: n <= 32 tokens fit one 256-thread CTA
+  if (n * k <= kSmallSlots)
+    return launch_route_metadata_small(logits, (int)n, E, k, gating, topk_indx, topk_vals, meta,
+                                       s);
+  return dispatch_kg(k, E, RouteMetaLaunch{logits, n, E, gating, topk_indx, topk_vals, &meta,
+                                           ws_hist, ctrl, s});
+}
+
+}  // namespace moe
