@@ -29,6 +29,14 @@
 //   ffn2: y_flat[col_sorted[m0 + j], f0 + w] = gate_scal[m0 + j] * D[w, j].
 // TMEM is read in chunks of 32 (then 8) token columns up to the tile's rows.
 //
+// Between the contractions: the w13 kernel counts, per expert, the tiles
+// whose h rows are stored; the w2 kernel waits for those counts instead of
+// for the whole w13 grid, so its tiles of finished experts run on the SMs
+// that w13 CTAs leave in their last wave. One SM streams a weight tile at
+// roughly 70 GB/s at most, so a decode w13 contraction with fewer than two
+// waves of tiles splits its (tile, K step) units evenly over the grid
+// (stream-K) instead of leaving most SMs idle behind a few whole tiles.
+//
 // Warps: 0 TMA producer, 1 TMEM allocation + MMA issue, 2-5 epilogue (warp
 // q reads TMEM lanes 32*(q%4)..). Every mbarrier wait is bounded.
 #include "tc_ptx.cuh"
@@ -47,6 +55,10 @@ constexpr int SW_SMEM_RING = 192 * 1024;      // bytes of stage ring at most
 
 enum { SW_ACT = 0, SW_SCATTER = 1, SW_RELU2 = 2 };
 
+// epilogue warps: one per TMEM lane quarter for decode tiles, two (taking
+// alternate token chunks) for wider tiles
+constexpr int sw_epi_warps(int nt) { return nt > SW_NGRAN ? 8 : 4; }
+
 template <bool DUAL, int NT>  // DUAL: gate and up weight tiles in each stage
 struct SwCfg {
   static constexpr int kA = DUAL ? 2 : 1;
@@ -54,9 +66,7 @@ struct SwCfg {
   static constexpr int kStageBytes = kA * SW_A_BYTES + kBBytes;  // a multiple of 1 KB
   static constexpr int kStages =
       SW_SMEM_RING / kStageBytes < 8 ? SW_SMEM_RING / kStageBytes : 8;
-  // epilogue warps: one per TMEM lane quarter for decode tiles, two (taking
-  // alternate token chunks) for 256-column tiles
-  static constexpr int kEpiWarps = NT > 32 ? 8 : 4;
+  static constexpr int kEpiWarps = sw_epi_warps(NT);
   static constexpr int kThreads = (2 + kEpiWarps) * 32;
   static constexpr int kAccCols = kA * NT;         // one accumulator buffer
   static constexpr int kTmemCols = 2 * kAccCols;   // a power of 2 in [64, 512]
@@ -81,7 +91,114 @@ struct SwArgs {
   uint16_t *y_out;
   uint32_t *ctrl;
   unsigned long long timeout_ns;
+  // Expert handoff between the two contractions. The w13 kernel adds one to
+  // ready_out[e] per epilogue warp and tile of expert e once the tile's h
+  // rows are stored; the w2 kernel loads expert e's h rows once ready_in[e]
+  // reaches ceil(rows_e / ready_nt) * ready_per_tile, and meanwhile streams
+  // the tile's weight rows (w, w_rows per expert) into L2.
+  uint32_t *ready_out;
+  const uint32_t *ready_in;
+  int ready_nt, ready_per_tile;
+  const uint16_t *w;
+  int w_rows;
+  // Decode stream-K (NT = 32, the w13 contraction when it has fewer than two
+  // waves of tiles): CTA c owns the (tile, K step) units
+  // [c * U / G, (c + 1) * U / G) of U = tiles * num_kb. A tile cut by a CTA
+  // boundary is computed in pieces; each piece stores its fp32 partial sums
+  // in its CTA's slot of sk_part, and the last piece to arrive on the tile's
+  // counters (sk_cnt, per first CTA and TMEM lane quarter) adds them up in
+  // piece order and applies the epilogue: no CTA waits for another.
+  int stream_k;
+  uint32_t *sk_cnt;
+  float *sk_part;
 };
+
+// ------------------------------------------------------------- stream-K --
+__device__ __forceinline__ int64_t sk_lo(int64_t c, int64_t U, int G) { return c * U / G; }
+// CTA owning unit u: the largest c with sk_lo(c) <= u
+__device__ __forceinline__ int sk_cta(int64_t u, int64_t U, int G) {
+  return (int)(((u + 1) * G + U - 1) / U - 1);
+}
+// Pieces of the tile whose units start at u0: the CTAs c_first..c_last that
+// own at least one of its units (with fewer units than CTAs, some CTAs in
+// between own none).
+__device__ __forceinline__ int sk_pieces(int c_first, int c_last, int64_t U, int G) {
+  int pieces = 0;
+  for (int c = c_first; c <= c_last; ++c) pieces += sk_lo(c, U, G) < sk_lo(c + 1, U, G);
+  return pieces;
+}
+
+// One unit of a CTA's work: K steps [k_lo, k_hi) of tile t.
+struct Work {
+  int t, k_lo, k_hi;
+};
+
+// The CTA's work items in order: whole tiles t = blockIdx.x + i * gridDim.x,
+// or (stream-K) the pieces of its unit range. Every role walks the same list.
+struct WorkIter {
+  int64_t u, hi;
+  int t, total, kb;
+  bool sk;
+  __device__ WorkIter(bool stream_k, int total_tiles, int num_kb)
+      : u(0), hi(0), t(blockIdx.x), total(total_tiles), kb(num_kb), sk(stream_k) {
+    if (sk) {
+      const int64_t U = (int64_t)total * kb;
+      u = sk_lo(blockIdx.x, U, gridDim.x);
+      hi = sk_lo(blockIdx.x + 1, U, gridDim.x);
+    }
+  }
+  __device__ bool next(Work &w) {
+    if (sk) {
+      if (u >= hi) return false;
+      w.t = (int)(u / kb);
+      const int64_t base = (int64_t)w.t * kb, end = base + kb < hi ? base + kb : hi;
+      w.k_lo = (int)(u - base);
+      w.k_hi = (int)(end - base);
+      u = end;
+      return true;
+    }
+    if (t >= total) return false;
+    w.t = t;
+    w.k_lo = 0;
+    w.k_hi = kb;
+    t += gridDim.x;
+    return true;
+  }
+};
+
+// Producer side of the handoff for tile (e, weight rows f0..): true once
+// expert e's h rows are complete and visible to this thread's TMA loads.
+__device__ __forceinline__ bool wait_expert_ready(const SwArgs &args, int e, int f0,
+                                                  const int *s_offs, volatile int *abort_flag) {
+  const int rows = s_offs[e + 1] - s_offs[e];
+  const uint32_t need =
+      (uint32_t)((rows + args.ready_nt - 1) / args.ready_nt) * (uint32_t)args.ready_per_tile;
+  const uint32_t *p = args.ready_in + e;
+  if (ld_acquire_gpu(p) < need) {
+    // the tile's weight rows are contiguous: W[e, f0 .. f0 + wr, 0 .. K)
+    const int K = args.num_kb * SW_BK;
+    const int wr = args.w_rows - f0 < SW_M ? args.w_rows - f0 : SW_M;
+    const char *base = reinterpret_cast<const char *>(args.w + ((size_t)e * args.w_rows + f0) * K);
+    const uint32_t bytes = (uint32_t)wr * (uint32_t)K * 2u;
+    for (uint32_t o = 0; o < bytes; o += 65536u)
+      prefetch_l2(base + o, bytes - o < 65536u ? bytes - o : 65536u);
+    const long long deadline = wait_deadline(args.timeout_ns);
+    uint32_t spins = 0;
+    while (ld_acquire_gpu(p) < need) {
+      __nanosleep(64);
+      if ((++spins & 15u) == 0) {
+        if (*abort_flag) return false;
+        if (clock64() > deadline) {
+          *abort_flag = 1;
+          record_status(args.ctrl, MOE_ERR_TIMEOUT);
+          return false;
+        }
+      }
+    }
+  }
+  fence_proxy_async_global();
+  return true;
+}
 
 template <int W>
 __device__ __forceinline__ void tmem_ld(uint32_t taddr, uint32_t (&r)[W]) {
@@ -104,13 +221,11 @@ struct EpiTile {
   float g_mine;    // lane l: gate weight of token dst_base + l
 };
 
-// Token columns [c0, c0 + W) of the tile: read TMEM, apply the epilogue.
+// Token columns [c0, c0 + W) of the tile, accumulators r0 (and r1: the up
+// rows of the packed layout) as fp32 bits: apply the epilogue.
 template <int EPI, bool DUAL, int NT, int W>
-__device__ __forceinline__ void epi_chunk(EpiTile &t, int c0, const SwArgs &args) {
-  uint32_t r0[W], r1[W];
-  tmem_ld<W>(t.taddr + c0, r0);
-  if constexpr (DUAL) tmem_ld<W>(t.taddr + NT + c0, r1);
-  tmem_wait_ld();
+__device__ __forceinline__ void epi_apply(EpiTile &t, int c0, const uint32_t (&r0)[W],
+                                          const uint32_t (&r1)[W], const SwArgs &args) {
   if constexpr (EPI == SW_SCATTER) {
     const int base = c0 & ~31;
     if (base != t.dst_base) {  // warp-uniform: next 32-token group
@@ -158,6 +273,93 @@ __device__ __forceinline__ void epi_chunk(EpiTile &t, int c0, const SwArgs &args
   }
 }
 
+// Token columns [c0, c0 + W) of the tile: read TMEM, apply the epilogue.
+template <int EPI, bool DUAL, int NT, int W>
+__device__ __forceinline__ void epi_chunk(EpiTile &t, int c0, const SwArgs &args) {
+  uint32_t r0[W], r1[W];
+  tmem_ld<W>(t.taddr + c0, r0);
+  if constexpr (DUAL) tmem_ld<W>(t.taddr + NT + c0, r1);
+  tmem_wait_ld();
+  epi_apply<EPI, DUAL, NT, W>(t, c0, r0, r1, args);
+}
+
+// The w13 epilogue's handoff: this warp's h rows of a tile of expert e are
+// stored; count them for the w2 kernel (the warp barrier orders every lane's
+// stores before lane 0's release).
+__device__ __forceinline__ void publish_ready(const SwArgs &args, int e, int lane) {
+  fence_proxy_async_global();  // h rows -> the w2 kernel's TMA loads
+  __syncwarp();
+  if (lane == 0) atom_add_release_gpu(args.ready_out + e, 1u);
+}
+
+// A piece of a split tile (decode stream-K). The warp stores its partial
+// sums (32 weight rows x the tile's token columns, per accumulator) in this
+// CTA's slot -- slot 0 for the piece that starts the CTA's unit range, 1 for
+// the one that ends it --, releases the accumulator buffer and counts the
+// piece. The warp that counts the tile's last piece of its lane quarter adds
+// the pieces' partials in piece order (a fixed order: the result does not
+// depend on which piece finishes last) and applies the epilogue.
+template <int EPI, bool DUAL, int NT>
+__device__ __forceinline__ void sk_piece(EpiTile &et, const SwArgs &args, int64_t u0,
+                                         int c_first, int c_last, int pieces, int k_lo,
+                                         int64_t U, int G, int q, int e, uint32_t tempty) {
+  constexpr size_t kSlot = kSkPartFloats / 2;
+  static_assert(2 * SW_M * NT <= (int)kSlot, "partial slot");
+  const int w_row = q * 32 + et.lane;
+  const int my_slot = u0 + k_lo == sk_lo(blockIdx.x, U, G) ? 0 : 1;
+  float *mine = args.sk_part + ((size_t)blockIdx.x * 2 + my_slot) * kSlot;
+  for (int c = 0; c < et.rows; c += 8) {
+    uint32_t r0[8], r1[8];
+    tmem_ld<8>(et.taddr + c, r0);
+    if constexpr (DUAL) tmem_ld<8>(et.taddr + NT + c, r1);
+    tmem_wait_ld();
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+      if (c + i < et.rows) {
+        mine[(size_t)(c + i) * SW_M + w_row] = __uint_as_float(r0[i]);
+        if constexpr (DUAL) mine[(size_t)(NT + c + i) * SW_M + w_row] = __uint_as_float(r1[i]);
+      }
+  }
+  tc_fence_before();
+  __syncwarp();
+  // the warp barrier orders every lane's partial stores before lane 0's
+  // release; lane 0's acquire and the next warp barrier order the last
+  // piece's reads of the other partials after their stores
+  uint32_t old = 0;
+  if (et.lane == 0) {
+    mbar_arrive(tempty);
+    old = atom_add_acq_rel_gpu(args.sk_cnt + (size_t)c_first * 4 + q, 1u);
+  }
+  old = __shfl_sync(0xffffffffu, old, 0);
+  if (old != (uint32_t)pieces - 1) return;
+  __syncwarp();
+  for (int c = 0; c < et.rows; c += 8) {
+    float s0[8], s1[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) s0[i] = s1[i] = 0.f;
+    for (int cta = c_first; cta <= c_last; ++cta) {
+      const int64_t lo = sk_lo(cta, U, G);
+      if (lo == sk_lo(cta + 1, U, G)) continue;  // owns no unit
+      const int slot = (u0 > lo ? u0 : lo) == lo ? 0 : 1;
+      const float *part = args.sk_part + ((size_t)cta * 2 + slot) * kSlot;
+#pragma unroll
+      for (int i = 0; i < 8; ++i)
+        if (c + i < et.rows) {
+          s0[i] += __ldcg(part + (size_t)(c + i) * SW_M + w_row);
+          if constexpr (DUAL) s1[i] += __ldcg(part + (size_t)(NT + c + i) * SW_M + w_row);
+        }
+    }
+    uint32_t r0[8], r1[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      r0[i] = __float_as_uint(s0[i]);
+      r1[i] = __float_as_uint(s1[i]);
+    }
+    epi_apply<EPI, DUAL, NT, 8>(et, c, r0, r1, args);
+  }
+  if (args.ready_out) publish_ready(args, e, et.lane);
+}
+
 template <int EPI, bool PACKED, int NT>
 __global__ void __launch_bounds__(SwCfg<EPI == SW_ACT && PACKED, NT>::kThreads, 1)
     grouped_gemm_swap_kernel(const __grid_constant__ CUtensorMap tmap_w,
@@ -185,7 +387,7 @@ __global__ void __launch_bounds__(SwCfg<EPI == SW_ACT && PACKED, NT>::kThreads, 
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int E = args.E;
-  pdl_launch_dependents();
+  if (!args.ready_out) pdl_launch_dependents();
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < C::kStages; ++s) {
@@ -212,7 +414,12 @@ __global__ void __launch_bounds__(SwCfg<EPI == SW_ACT && PACKED, NT>::kThreads, 
                  : "memory");
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
   }
-  pdl_wait();  // offs and the operands come from earlier kernels of the stream
+  // offs and the operands come from earlier kernels of the stream. The w2
+  // kernel of a handoff skips the grid-wide wait: the w13 kernel triggered it
+  // only after its own pdl_wait, so everything but h is complete, and h is
+  // waited for per expert.
+  if (!args.ready_in) pdl_wait();
+  if (args.ready_out) pdl_launch_dependents();
   for (int i = threadIdx.x; i <= E; i += C::kThreads) s_offs[i] = args.offs[i];
   __syncthreads();
   if (warp == 0) row_tile_prefix(s_offs, E, NT, s_tstart);
@@ -222,6 +429,9 @@ __global__ void __launch_bounds__(SwCfg<EPI == SW_ACT && PACKED, NT>::kThreads, 
   const uint32_t tmem_base = *tmem_slot;
   const int total = s_tstart[E] * args.f_tiles;
   const int num_kb = args.num_kb;
+  // stream-K pays only where whole tiles leave a large last wave idle; with
+  // two or more waves, CTAs that finish early start the next contraction
+  const bool sk = NT == SW_NGRAN && args.stream_k && total < 2 * (int)gridDim.x;
 
   if (warp == 0) {
     // ------------------------------------------------------ TMA producer --
@@ -229,10 +439,20 @@ __global__ void __launch_bounds__(SwCfg<EPI == SW_ACT && PACKED, NT>::kThreads, 
       int stage = 0;
       uint32_t phase = 0, issued = 0;
       bool ok = true;
-      for (int t = blockIdx.x; ok && t < total; t += gridDim.x) {
-        const Tile d = decode_tile(t, args.f_tiles, s_tstart, s_offs, E, NT);
+      int ready_e = -1;  // expert whose h rows this thread has seen complete
+      WorkIter it(sk, total, num_kb);
+      Work w;
+      while (ok && it.next(w)) {
+        const Tile d = decode_tile(w.t, args.f_tiles, s_tstart, s_offs, E, NT);
         const int f0 = d.nt * SW_M;  // first weight row of the tile
-        for (int kb = 0; kb < num_kb; ++kb) {
+        if (args.ready_in && d.e != ready_e) {
+          if (!wait_expert_ready(args, d.e, f0, s_offs, s_abort)) {
+            ok = false;
+            break;
+          }
+          ready_e = d.e;
+        }
+        for (int kb = w.k_lo; kb < w.k_hi; ++kb) {
           if (!wait_bounded(empty_bar(stage), phase ^ 1u, s_abort, args.ctrl, args.timeout_ns)) {
             ok = false;
             break;
@@ -268,8 +488,10 @@ __global__ void __launch_bounds__(SwCfg<EPI == SW_ACT && PACKED, NT>::kThreads, 
       uint32_t phase = 0;
       bool ok = true;
       int local = 0;
-      for (int t = blockIdx.x; ok && t < total; t += gridDim.x, ++local) {
-        const Tile d = decode_tile(t, args.f_tiles, s_tstart, s_offs, E, NT);
+      WorkIter it(sk, total, num_kb);
+      Work w;
+      for (; ok && it.next(w); ++local) {
+        const Tile d = decode_tile(w.t, args.f_tiles, s_tstart, s_offs, E, NT);
         const int rows = d.m_end - d.m0;
         // MMA N: the tile's rows rounded up to 32 (a multiple of 16, <= 256)
         const int n_mma = (rows + SW_NGRAN - 1) / SW_NGRAN * SW_NGRAN;
@@ -280,23 +502,24 @@ __global__ void __launch_bounds__(SwCfg<EPI == SW_ACT && PACKED, NT>::kThreads, 
           break;
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + (uint32_t)(acc * C::kAccCols);
-        for (int kb = 0; kb < num_kb; ++kb) {
+        for (int kb = w.k_lo; kb < w.k_hi; ++kb) {
           if (!wait_bounded(full_bar(stage), phase, s_abort, args.ctrl, args.timeout_ns)) {
             ok = false;
             break;
           }
+          const uint32_t acc_k0 = kb != w.k_lo ? 1u : 0u;  // first K step: overwrite
           tc_fence_after();
           const uint64_t adesc0 = sw128_desc(a_addr(stage, 0));
           const uint64_t bdesc = sw128_desc(b_addr(stage));
 #pragma unroll
           for (int kk = 0; kk < SW_BK / SW_UK; ++kk)
-            umma_bf16(d_tmem, adesc0 + 2u * kk, bdesc + 2u * kk, idesc, (kb | kk) != 0 ? 1u : 0u);
+            umma_bf16(d_tmem, adesc0 + 2u * kk, bdesc + 2u * kk, idesc, acc_k0 | (kk != 0));
           if (DUAL) {
             const uint64_t adesc1 = sw128_desc(a_addr(stage, 1));
 #pragma unroll
             for (int kk = 0; kk < SW_BK / SW_UK; ++kk)
               umma_bf16(d_tmem + NT, adesc1 + 2u * kk, bdesc + 2u * kk, idesc,
-                        (kb | kk) != 0 ? 1u : 0u);
+                        acc_k0 | (kk != 0));
           }
           umma_commit(empty_bar(stage));
           if (++stage == C::kStages) {
@@ -315,8 +538,12 @@ __global__ void __launch_bounds__(SwCfg<EPI == SW_ACT && PACKED, NT>::kThreads, 
     const int half = (warp - 2) >> 2;   // which of the quarter's warps: chunk parity
     constexpr int kPer = C::kEpiWarps / 4;  // warps per lane quarter
     int local = 0;
-    for (int t = blockIdx.x; t < total; t += gridDim.x, ++local) {
-      const Tile d = decode_tile(t, args.f_tiles, s_tstart, s_offs, E, NT);
+    WorkIter it(sk, total, num_kb);
+    Work w;
+    const int64_t U = (int64_t)total * num_kb;
+    const int G = (int)gridDim.x;
+    for (; it.next(w); ++local) {
+      const Tile d = decode_tile(w.t, args.f_tiles, s_tstart, s_offs, E, NT);
       const int acc = local & 1;
       const uint32_t acc_phase = (uint32_t)(local >> 1) & 1u;
       if (!wait_bounded(tfull_bar(acc), acc_phase, s_abort, args.ctrl, args.timeout_ns)) break;
@@ -330,6 +557,18 @@ __global__ void __launch_bounds__(SwCfg<EPI == SW_ACT && PACKED, NT>::kThreads, 
       et.dst_base = -1;
       et.dst_mine = 0;
       et.g_mine = 0.f;
+      if constexpr (NT == SW_NGRAN) {
+        if (sk) {
+          const int64_t u0 = (int64_t)w.t * num_kb;
+          const int c_first = sk_cta(u0, U, G), c_last = sk_cta(u0 + num_kb - 1, U, G);
+          if (c_last > c_first) {
+            sk_piece<EPI, DUAL, NT>(et, args, u0, c_first, c_last,
+                                    sk_pieces(c_first, c_last, U, G), w.k_lo, U, G, q, d.e,
+                                    tempty_bar(acc));
+            continue;  // the piece released its accumulator buffer
+          }
+        }
+      }
       // chunks of 32 token columns, then of 8; the quarter's two warps take
       // alternate chunks
       int c0 = 0;
@@ -342,6 +581,7 @@ __global__ void __launch_bounds__(SwCfg<EPI == SW_ACT && PACKED, NT>::kThreads, 
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(tempty_bar(acc));
+      if (args.ready_out) publish_ready(args, d.e, lane);
     }
   }
 
@@ -435,7 +675,7 @@ cudaError_t launch_ffn_swap(const uint16_t *x_sorted, const int32_t *offs,
                             const int32_t *col_sorted, const uint16_t *gate_scal,
                             const uint16_t *w13, const uint16_t *w2, int64_t N, int E, int H,
                             int I, const ActParams &act, uint16_t *h_buf, uint16_t *y_flat,
-                            uint32_t *ctrl, cudaStream_t s, cudaEvent_t *ev_ffn) {
+                            const FfnScratch &scr, cudaStream_t s, cudaEvent_t *ev_ffn) {
   if (N == 0) return cudaSuccess;
   SwArgs a{};
   a.offs = offs;
@@ -447,17 +687,28 @@ cudaError_t launch_ffn_swap(const uint16_t *x_sorted, const int32_t *offs,
   a.col_sorted = col_sorted;
   a.gate_scal = gate_scal;
   a.y_out = y_flat;
-  a.ctrl = ctrl;
+  a.ctrl = scr.ctrl;
   a.timeout_ns = kWaitTimeoutNs;
-  // a handful of rows per expert (decode): 32-row token tiles for both
+  const bool packed = act.act != MOE_ACT_RELU2 && act.layout == MOE_W13_PACKED;
+  const int f_tiles1 = (w13_rows(act, I) / (packed ? 2 : 1) + SW_M - 1) / SW_M;
+  // a handful of rows per expert (decode): 32-row token tiles for both, the
+  // (tile, K step) units split evenly over the grid
   int nt1 = 32, nt2 = 32;
-  if (N > (int64_t)SW_NGRAN * E) {
-    const bool packed = act.act != MOE_ACT_RELU2 && act.layout == MOE_W13_PACKED;
-    const int f1 = (w13_rows(act, I) / (packed ? 2 : 1) + SW_M - 1) / SW_M;
-    nt1 = pick_token_tile(N, E, f1, packed);
+  const bool decode = N <= (int64_t)kDecodeRowsPerExpert * E;
+  a.stream_k = decode && scr.sync && scr.sk_part && device_sm_count() <= kSkMaxCtas;
+  if (!decode) {
+    nt1 = pick_token_tile(N, E, f_tiles1, packed);
     nt2 = pick_token_tile(N, E, (H + SW_M - 1) / SW_M, false);
   }
   if (ev_ffn && record_stage_event(ev_ffn[0], s) != cudaSuccess) return cudaErrorUnknown;
+  // the w13 kernel publishes per-expert completion; the w2 kernel waits on it
+  const int nt1_eff = packed && nt1 > 128 ? 128 : nt1;  // swap_ffn1's NT_DUAL
+  uint32_t *ready = scr.sync ? scr.sync + kSyncReady : nullptr;
+  a.ready_out = ready;
+  if (a.stream_k) {
+    a.sk_cnt = scr.sync + kSyncSk;
+    a.sk_part = scr.sk_part;
+  }
   cudaError_t err;
   switch (nt1) {
     case 32: err = swap_ffn1<32>(x_sorted, w13, N, E, H, I, act, a, s); break;
@@ -467,6 +718,13 @@ cudaError_t launch_ffn_swap(const uint16_t *x_sorted, const int32_t *offs,
   }
   if (err != cudaSuccess) return err;
   if (ev_ffn && record_stage_event(ev_ffn[1], s) != cudaSuccess) return cudaErrorUnknown;
+  a.ready_out = nullptr;
+  a.ready_in = ready;
+  a.ready_nt = nt1_eff;
+  a.ready_per_tile = f_tiles1 * sw_epi_warps(nt1_eff);
+  a.w = w2;
+  a.w_rows = H;
+  a.stream_k = 0;  // whole w2 tiles: they start as soon as w13 CTAs leave SMs free
   switch (nt2) {
     case 32: return swap_ffn2<32>(h_buf, w2, N, E, H, I, a, s);
     case 64: return swap_ffn2<64>(h_buf, w2, N, E, H, I, a, s);

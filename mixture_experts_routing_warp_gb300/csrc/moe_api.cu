@@ -81,6 +81,11 @@ T *ws_at(void *ws, size_t off) {
   return reinterpret_cast<T *>(static_cast<char *>(ws) + off);
 }
 
+FfnScratch ffn_scratch(void *ws, const WorkspaceLayout &L) {
+  return {ws_at<uint32_t>(ws, L.ctrl), ws_at<uint32_t>(ws, L.sync),
+          L.x_sorted > L.sk_part ? ws_at<float>(ws, L.sk_part) : nullptr};
+}
+
 }  // namespace
 
 extern "C" {
@@ -188,11 +193,11 @@ moe_status moe_grouped_ffn(const uint16_t *x, const moe_routing_meta *meta, cons
   cudaStream_t s = (cudaStream_t)stream;
   const int64_t N = n * k;
   uint16_t *x_sorted = ws_at<uint16_t>(workspace, L.x_sorted);
-  cudaError_t err = launch_gather_rows(x, meta->row_sorted, n, k, H, x_sorted, s);
+  const FfnScratch scr = ffn_scratch(workspace, L);
+  cudaError_t err = launch_gather_rows(x, meta->row_sorted, n, k, H, x_sorted, scr.sync, s);
   if (err != cudaSuccess) return MOE_ERR_CUDA;
   return from_cuda(launch_ffn(x_sorted, meta->offs, meta->col_sorted, meta->gate_scal, w13, w2, N,
-                              E, H, I, act, ws_at<uint16_t>(workspace, L.h), y_flat,
-                              ws_at<uint32_t>(workspace, L.ctrl), s));
+                              E, H, I, act, ws_at<uint16_t>(workspace, L.h), y_flat, scr, s));
 }
 
 moe_status moe_combine(const uint16_t *y_flat, int64_t n, int32_t k, int32_t H, uint16_t *out,
@@ -247,6 +252,7 @@ static moe_status forward_impl(const uint16_t *x, const float *logits, const uin
   uint16_t *y_flat = k == 1 ? out : ws_at<uint16_t>(workspace, L.y_flat);
   uint16_t *x_sorted = ws_at<uint16_t>(workspace, L.x_sorted);
   uint16_t *h = ws_at<uint16_t>(workspace, L.h);
+  const FfnScratch scr = ffn_scratch(workspace, L);
   // Inside a stream capture the records become event-record nodes, so stage
   // timing works for graph replays too.
   auto mark = [&](int i) { return ev ? record_stage_event(ev[i], s) : cudaSuccess; };
@@ -276,10 +282,10 @@ static moe_status forward_impl(const uint16_t *x, const float *logits, const uin
       return MOE_ERR_CUDA;
   }
   if (mark(MOE_STAGE_GATHER) != cudaSuccess ||
-      launch_gather_rows(x, m.row_sorted, n, k, H, x_sorted, s) != cudaSuccess)
+      launch_gather_rows(x, m.row_sorted, n, k, H, x_sorted, scr.sync, s) != cudaSuccess)
     return MOE_ERR_CUDA;
   if (launch_ffn(x_sorted, m.offs, m.col_sorted, m.gate_scal, w13, w2, N, E, H, I, act, h, y_flat,
-                 ctrl, s, ev ? ev + MOE_STAGE_FFN1 : nullptr) != cudaSuccess)
+                 scr, s, ev ? ev + MOE_STAGE_FFN1 : nullptr) != cudaSuccess)
     return MOE_ERR_CUDA;
   if (mark(MOE_STAGE_COMBINE) != cudaSuccess) return MOE_ERR_CUDA;
   if (k > 1 && launch_combine(y_flat, n, k, H, out, s) != cudaSuccess) return MOE_ERR_CUDA;

@@ -22,21 +22,49 @@ constexpr int kCtrlStatus = 0;           // sticky moe_status from device-side w
 constexpr int kCtrlBarArrive = 32;       // grid barrier counter (top bit flips per barrier)
 constexpr int kCtrlNeverSet = 96;        // a word no kernel writes (bounded-wait self-test)
 
+// Per-forward synchronisation words of the expert contractions, zeroed by the
+// dispatch gather of each forward (grouped_gemm_swap.cu):
+//   [kSyncReady, +kMaxExperts): per-expert completion counts of the w13
+//     contraction; the w2 contraction starts an expert's tiles once complete;
+//   [kSyncSk, +4 * kSkMaxCtas): arrival counters (per first CTA of a split
+//     tile and TMEM lane quarter) of the w13 contraction's decode stream-K
+//     partition.
+constexpr int kSkMaxCtas = 256;
+constexpr int kSyncReady = 0;
+constexpr int kSyncSk = kMaxExperts;
+constexpr int kSyncWords = kMaxExperts + 4 * kSkMaxCtas;
+// Decode tiling (32-row token tiles, stream-K) applies when n*k <= 32 * E.
+constexpr int kDecodeRowsPerExpert = 32;
+// fp32 partial sums per stream-K CTA: 2 slots (the CTA's first and last
+// piece) x up to 2 accumulators x 128 weight rows x 32 token columns.
+constexpr size_t kSkPartFloats = 2 * 2 * 128 * 32;
+
 // Default limit of a device-side wait (ns). Legitimate waits last microseconds.
 constexpr unsigned long long kWaitTimeoutNs = 1000000000ull;
 
 // ------------------------------------------------------ workspace layout --
 struct WorkspaceLayout {
   size_t ctrl, hist, topk_indx, topk_vals, col_sum, offs, col_sorted, row_sorted, gate_scal;
-  size_t x_sorted, h, y_flat, total;
+  size_t sync, sk_part, x_sorted, h, y_flat, total;
+};
+
+// What the expert contractions use besides their operands: the control
+// block (status word), the per-forward sync words, the stream-K partials
+// (null when the workspace has none: n*k > 32 * E).
+struct FfnScratch {
+  uint32_t *ctrl;
+  uint32_t *sync;
+  float *sk_part;
 };
 
 inline size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
 // Regions: control block; per-CTA histograms of the metadata kernel; the
 // routing result and metadata used when moe_forward's caller keeps them
-// internal; the expert-sorted activations X_sorted [N, H]; the intermediate
-// h [N, I]; the per-slot outputs y_flat [N, H] (k > 1 only). N = n * k.
+// internal; the sync words of the expert contractions; the decode stream-K
+// partial sums (n*k <= 32 * E only); the expert-sorted activations X_sorted
+// [N, H]; the intermediate h [N, I]; the per-slot outputs y_flat [N, H]
+// (k > 1 only). N = n * k.
 inline WorkspaceLayout workspace_layout(int64_t n, int E, int k, int H, int I) {
   WorkspaceLayout L{};
   const size_t N = (size_t)n * (size_t)k;
@@ -51,6 +79,10 @@ inline WorkspaceLayout workspace_layout(int64_t n, int E, int k, int H, int I) {
   L.col_sorted = take(N * 4);
   L.row_sorted = take(N * 4);
   L.gate_scal = take(N * 2);
+  L.sync = take((size_t)kSyncWords * 4);
+  L.sk_part = take(N <= (size_t)kDecodeRowsPerExpert * (size_t)E
+                       ? (size_t)kSkMaxCtas * kSkPartFloats * 4
+                       : 0);
   L.x_sorted = take(N * (size_t)H * 2);
   L.h = take(N * (size_t)I * 2);
   L.y_flat = take(k > 1 ? N * (size_t)H * 2 : 0);
@@ -63,6 +95,13 @@ __device__ __forceinline__ uint32_t ld_acquire_gpu(const uint32_t *p) {
   uint32_t v;
   asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
   return v;
+}
+
+__device__ __forceinline__ uint32_t atom_add_acq_rel_gpu(uint32_t *p, uint32_t v) {
+  uint32_t old;
+  asm volatile("atom.add.acq_rel.gpu.global.u32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v)
+               : "memory");
+  return old;
 }
 
 __device__ __forceinline__ uint32_t atom_add_release_gpu(uint32_t *p, uint32_t v) {
@@ -279,6 +318,10 @@ inline cudaError_t record_stage_event(cudaEvent_t ev, cudaStream_t s) {
 // and its writes to be visible -- before reading anything it (or an earlier
 // kernel) wrote. Every kernel calls pdl_launch_dependents() early so that
 // the next one can be scheduled; all of its own CTAs are resident by then.
+// One exception: the swap-operand w13 kernel triggers after its pdl_wait, and
+// the w2 kernel that follows does not pdl_wait; it waits per expert on the
+// w13 kernel's completion counters instead (everything older than the w13
+// kernel is complete once the w13 kernel has passed its own pdl_wait).
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 __device__ __forceinline__ void pdl_launch_dependents() {
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
@@ -333,8 +376,9 @@ cudaError_t launch_metadata(const int32_t *topk_indx, const uint16_t *topk_vals,
                             uint32_t *ctrl, cudaStream_t s);
 
 // X_sorted[row_sorted[t*k + j]] = x[t] for the n tokens' k slots.
+// sync (may be null): the kSyncWords sync words the gather zeroes
 cudaError_t launch_gather_rows(const uint16_t *x, const int32_t *row_sorted, int64_t n, int k,
-                               int H, uint16_t *x_sorted, cudaStream_t s);
+                               int H, uint16_t *x_sorted, uint32_t *sync, cudaStream_t s);
 
 cudaError_t launch_combine(const uint16_t *y_flat, int64_t n, int k, int H, uint16_t *out,
                            cudaStream_t s);
@@ -342,7 +386,7 @@ cudaError_t launch_combine(const uint16_t *y_flat, int64_t n, int k, int H, uint
 cudaError_t launch_ffn(const uint16_t *x_sorted, const int32_t *offs, const int32_t *col_sorted,
                        const uint16_t *gate_scal, const uint16_t *w13, const uint16_t *w2,
                        int64_t N, int E, int H, int I, const ActParams &act, uint16_t *h_buf,
-                       uint16_t *y_flat, uint32_t *ctrl, cudaStream_t s,
+                       uint16_t *y_flat, const FfnScratch &scr, cudaStream_t s,
                        cudaEvent_t *ev_ffn = nullptr);
 
 // The swap-operand grouped GEMM (weights on the MMA's M side, token tiles
@@ -352,7 +396,7 @@ cudaError_t launch_ffn_swap(const uint16_t *x_sorted, const int32_t *offs,
                             const int32_t *col_sorted, const uint16_t *gate_scal,
                             const uint16_t *w13, const uint16_t *w2, int64_t N, int E, int H,
                             int I, const ActParams &act, uint16_t *h_buf, uint16_t *y_flat,
-                            uint32_t *ctrl, cudaStream_t s, cudaEvent_t *ev_ffn);
+                            const FfnScratch &scr, cudaStream_t s, cudaEvent_t *ev_ffn);
 
 // Router matmul fused with the top-k (the tokens-on-M GEMM, EPI_ROUTE).
 cudaError_t launch_route_gemm(const uint16_t *x, const uint16_t *w_gate, int64_t n, int E, int H,

@@ -246,16 +246,19 @@ cudaError_t launch_metadata_noalloc(const int32_t *topk_indx, const uint16_t *to
 // warp per (token t, group of 128 16-byte chunks) reads its chunks of x[t]
 // once (up to 4 loads in flight per thread) and writes them to the k sorted
 // positions row_sorted[t*k + j] of the token's slots, so x is read from
-// memory once rather than once per slot.
+// memory once rather than once per slot. Block 0 also zeroes the sync words
+// of this forward's expert contractions.
 constexpr int kCopyThreads = 256;
 
 constexpr int kChunksPerLane = 4;  // 16-byte chunks in flight per thread
 
 __global__ void __launch_bounds__(kCopyThreads) gather_rows_kernel(
     const uint4 *__restrict__ x, const int32_t *__restrict__ row_sorted, int64_t n, int k,
-    int vec_per_row, int groups_per_row, uint4 *__restrict__ x_sorted) {
+    int vec_per_row, int groups_per_row, uint4 *__restrict__ x_sorted, uint32_t *sync) {
   pdl_launch_dependents();
   pdl_wait();  // row_sorted comes from the metadata kernel
+  if (sync && blockIdx.x == 0)
+    for (int i = threadIdx.x; i < kSyncWords; i += kCopyThreads) sync[i] = 0;
   const int lane = threadIdx.x & 31;
   const int64_t N = n * k;
   const int64_t units = n * groups_per_row;  // (token, group of 32 * kChunksPerLane chunks)
@@ -283,7 +286,7 @@ __global__ void __launch_bounds__(kCopyThreads) gather_rows_kernel(
 }
 
 cudaError_t launch_gather_rows(const uint16_t *x, const int32_t *row_sorted, int64_t n, int k,
-                               int H, uint16_t *x_sorted, cudaStream_t s) {
+                               int H, uint16_t *x_sorted, uint32_t *sync, cudaStream_t s) {
   if (n == 0) return cudaSuccess;
   static bool configured = false;
   if (!configured) {
@@ -297,7 +300,7 @@ cudaError_t launch_gather_rows(const uint16_t *x, const int32_t *row_sorted, int
   if (blocks > cap) blocks = cap;
   cudaError_t err = launch_dependent(gather_rows_kernel, dim3((unsigned)blocks), dim3(kCopyThreads),
                                      0, s, reinterpret_cast<const uint4 *>(x), row_sorted, n, k,
-                                     vpr, gpr, reinterpret_cast<uint4 *>(x_sorted));
+                                     vpr, gpr, reinterpret_cast<uint4 *>(x_sorted), sync);
   return err != cudaSuccess ? err : cudaGetLastError();
 }
 

@@ -155,6 +155,19 @@ __device__ __forceinline__ void wait_drain(uint32_t bar, uint32_t parity,
     if (clock64() > deadline) return;
 }
 
+// Bulk prefetch of [p, p + bytes) into L2 (p and bytes multiples of 16).
+__device__ __forceinline__ void prefetch_l2(const void *p, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"((uint64_t)p), "r"(bytes)
+               : "memory");
+}
+
+// Orders this thread's generic-proxy global accesses with async-proxy (TMA)
+// accesses: after stores that another CTA's TMA will read, and after the
+// acquire that precedes such a TMA load.
+__device__ __forceinline__ void fence_proxy_async_global() {
+  asm volatile("fence.proxy.async.global;" ::: "memory");
+}
+
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   return (uint32_t)float_to_bf16_bits(lo) | ((uint32_t)float_to_bf16_bits(hi) << 16);
 }

@@ -66,6 +66,43 @@ def test_repeated_runs_bit_identical():
         assert torch.equal(first.view(torch.int16), again.view(torch.int16))
 
 
+@pytest.mark.parametrize("case", [
+    I.GPTOSS.with_n(1),      # decode: w2 tiles start beside the w13 kernel's last wave
+    I.GPTOSS.with_n(8),
+    I.GPTOSS.with_n(300),    # 64..256-row token tiles, ragged experts
+    I.MINIMIND_E4,           # k = 1: the w2 kernel writes out directly
+], ids=lambda c: c.name)
+def test_expert_handoff_replays_alternating_inputs(case):
+    """The w2 kernel starts an expert's tiles once the w13 kernel has counted
+    that expert's h rows complete (no grid-wide wait between the two). Graph
+    replays alternate between two token batches under the same routing, so a
+    w2 tile that read h before it was complete would see the other batch's
+    values: every replay must equal the eager result of its own batch."""
+    x, logits, w13, w2, params, ws = _setup(case)
+    x_b = torch.flip(x, dims=[1]).contiguous()  # same routing, other activations
+    ref = [moe.forward(x, logits, w13, w2, case.k, params, ws),
+           moe.forward(x_b, logits, w13, w2, case.k, params, ws)]
+    assert not torch.equal(ref[0], ref[1])
+    x_in = x.clone()
+    out = torch.empty_like(ref[0])
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        moe.forward(x_in, logits, w13, w2, case.k, params, ws, out=out)
+    torch.cuda.current_stream().wait_stream(s)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        moe.forward(x_in, logits, w13, w2, case.k, params, ws, out=out)
+    bad = torch.zeros((), dtype=torch.int64, device=x.device)
+    for i in range(40):
+        x_in.copy_(x if i % 2 == 0 else x_b)
+        g.replay()
+        bad += (out.view(torch.int16) != ref[i % 2].view(torch.int16)).sum()
+    torch.cuda.synchronize()
+    assert int(bad) == 0
+    assert moe.read_status(ws) == 0
+
+
 def test_bounded_wait_times_out_and_context_survives():
     case = I.TINY
     x, logits, w13, w2, params, ws = _setup(case)
