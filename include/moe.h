@@ -171,9 +171,12 @@ int32_t moe_abi_version(void);
 const char *moe_status_string(moe_status status);
 
 /* Bytes of workspace that moe_build_metadata, moe_grouped_ffn and
- * moe_forward need for these sizes (a few KB of control data plus, for the
- * FFN, the expert-sorted activations, the intermediate h and, when k > 1,
- * the per-slot outputs). Returns 0 for invalid sizes. */
+ * moe_forward need for these sizes (a few KB of control and sync data plus,
+ * for the FFN, the expert-sorted activations, the intermediate h and, when
+ * k > 1, the per-slot outputs; for decode sizes, n*k <= 32*E, also 16 MB of
+ * fp32 partial sums of the w13 contraction's even split of its work over
+ * the SMs). The sync words are rewritten by every FFN call, so one
+ * workspace serves one stream at a time. Returns 0 for invalid sizes. */
 size_t moe_workspace_size(int64_t n, int32_t E, int32_t k, int32_t H, int32_t I);
 
 /* Prepare a freshly allocated workspace: zero its control block (the first
