@@ -50,6 +50,7 @@ METRIC = "MoE-layer tokens/s and routing-metadata µs/call on 1 GB300; % of roof
 WORKLOADS = {
     "gptoss_prefill_n8192": I.GPTOSS.with_n(8192),
     "gptoss_prefill_n2048": I.GPTOSS.with_n(2048),
+    "gptoss_prefill_n4096": I.GPTOSS.with_n(4096),
     "minimind_e4": I.MINIMIND_E4,
     "minimind_e8": I.MINIMIND_E8,
     "minimind_e16": I.MINIMIND_E16,

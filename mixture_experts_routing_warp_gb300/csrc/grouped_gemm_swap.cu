@@ -59,10 +59,13 @@ enum { SW_ACT = 0, SW_SCATTER = 1, SW_RELU2 = 2 };
 // alternate token chunks) for wider tiles
 constexpr int sw_epi_warps(int nt) { return nt > SW_NGRAN ? 8 : 4; }
 
-template <bool DUAL, int NT>  // DUAL: gate and up weight tiles in each stage
+// DUAL: gate and up weight tiles in each stage. PAIR: a CTA pair runs one
+// MMA of M = 256 (cta_group::2); each CTA's stage holds its 128 weight rows
+// and half of the tile's token rows.
+template <bool DUAL, int NT, bool PAIR = false>
 struct SwCfg {
   static constexpr int kA = DUAL ? 2 : 1;
-  static constexpr int kBBytes = NT * SW_BK * 2;  // token rows of one stage
+  static constexpr int kBBytes = (PAIR ? NT / 2 : NT) * SW_BK * 2;  // token rows of one stage
   static constexpr int kStageBytes = kA * SW_A_BYTES + kBBytes;  // a multiple of 1 KB
   static constexpr int kStages =
       SW_SMEM_RING / kStageBytes < 8 ? SW_SMEM_RING / kStageBytes : 8;
@@ -76,6 +79,7 @@ struct SwCfg {
   static_assert(kTmemCols <= 512 && (kTmemCols & (kTmemCols - 1)) == 0, "TMEM columns");
   static_assert(NT % SW_NGRAN == 0 && NT <= 256, "token tile");
   static_assert(kStages >= 4, "pipeline depth");
+  static_assert(!PAIR || (!DUAL && NT > SW_NGRAN), "CTA pairs: one accumulator, wide tiles");
 };
 
 struct SwArgs {
@@ -133,18 +137,20 @@ struct Work {
   int t, k_lo, k_hi;
 };
 
-// The CTA's work items in order: whole tiles t = blockIdx.x + i * gridDim.x,
-// or (stream-K) the pieces of its unit range. Every role walks the same list.
+// The CTA's work items in order: whole tiles t = first + i * step, or
+// (stream-K) the pieces of its unit range. Every role walks the same list.
 struct WorkIter {
   int64_t u, hi;
   int t, total, kb;
   bool sk;
-  __device__ WorkIter(bool stream_k, int total_tiles, int num_kb)
-      : u(0), hi(0), t(blockIdx.x), total(total_tiles), kb(num_kb), sk(stream_k) {
+  int step;
+  // first, step: this CTA's (or CTA pair's) index and the number of them
+  __device__ WorkIter(bool stream_k, int total_tiles, int num_kb, int first, int step_)
+      : u(0), hi(0), t(first), total(total_tiles), kb(num_kb), sk(stream_k), step(step_) {
     if (sk) {
       const int64_t U = (int64_t)total * kb;
-      u = sk_lo(blockIdx.x, U, gridDim.x);
-      hi = sk_lo(blockIdx.x + 1, U, gridDim.x);
+      u = sk_lo(first, U, step);
+      hi = sk_lo(first + 1, U, step);
     }
   }
   __device__ bool next(Work &w) {
@@ -161,7 +167,7 @@ struct WorkIter {
     w.t = t;
     w.k_lo = 0;
     w.k_hi = kb;
-    t += gridDim.x;
+    t += step;
     return true;
   }
 };
@@ -360,12 +366,14 @@ __device__ __forceinline__ void sk_piece(EpiTile &et, const SwArgs &args, int64_
   if (args.ready_out) publish_ready(args, e, et.lane);
 }
 
-template <int EPI, bool PACKED, int NT>
-__global__ void __launch_bounds__(SwCfg<EPI == SW_ACT && PACKED, NT>::kThreads, 1)
+template <int EPI, bool PACKED, int NT, bool PAIR>
+__global__ void __launch_bounds__(SwCfg<EPI == SW_ACT && PACKED, NT, PAIR>::kThreads, 1)
     grouped_gemm_swap_kernel(const __grid_constant__ CUtensorMap tmap_w,
                              const __grid_constant__ CUtensorMap tmap_x, const SwArgs args) {
   constexpr bool DUAL = EPI == SW_ACT && PACKED;
-  using C = SwCfg<DUAL, NT>;
+  using C = SwCfg<DUAL, NT, PAIR>;
+  // PAIR: tiles of 256 weight rows; this CTA's half starts at row `rank` * 128
+  constexpr int kTileRows = PAIR ? 2 * SW_M : SW_M;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_addr = smem_u32(smem_raw);
   uint8_t *smem = smem_raw + ((1024u - (raw_addr & 1023u)) & 1023u);
@@ -387,6 +395,10 @@ __global__ void __launch_bounds__(SwCfg<EPI == SW_ACT && PACKED, NT>::kThreads, 
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int E = args.E;
+  const uint32_t rank = PAIR ? cluster_rank() : 0u;
+  const bool leader = rank == 0;
+  const int first = PAIR ? (int)(blockIdx.x >> 1) : (int)blockIdx.x;
+  const int step = PAIR ? (int)(gridDim.x >> 1) : (int)gridDim.x;
   if (!args.ready_out) pdl_launch_dependents();
 
   if (threadIdx.x == 0) {
@@ -396,7 +408,7 @@ __global__ void __launch_bounds__(SwCfg<EPI == SW_ACT && PACKED, NT>::kThreads, 
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(tfull_bar(b), 1);
-      mbar_init(tempty_bar(b), C::kEpiWarps);
+      mbar_init(tempty_bar(b), C::kEpiWarps * (PAIR ? 2 : 1));  // the leader's counts both CTAs
     }
     mbar_init(drain_bar, 1);
     *s_abort = 0;
@@ -408,11 +420,19 @@ __global__ void __launch_bounds__(SwCfg<EPI == SW_ACT && PACKED, NT>::kThreads, 
     prefetch_tmap(&tmap_x);
   }
   if (warp == 1) {
-    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
-                     smem_u32(tmem_slot)),
-                 "r"(C::kTmemCols)
-                 : "memory");
-    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    if constexpr (PAIR) {  // one warp of each CTA of the pair, collectively
+      asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                       smem_u32(tmem_slot)),
+                   "r"(C::kTmemCols)
+                   : "memory");
+      asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+    } else {
+      asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                       smem_u32(tmem_slot)),
+                   "r"(C::kTmemCols)
+                   : "memory");
+      asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    }
   }
   // offs and the operands come from earlier kernels of the stream. The w2
   // kernel of a handoff skips the grid-wide wait: the w13 kernel triggered it
@@ -424,7 +444,11 @@ __global__ void __launch_bounds__(SwCfg<EPI == SW_ACT && PACKED, NT>::kThreads, 
   __syncthreads();
   if (warp == 0) row_tile_prefix(s_offs, E, NT, s_tstart);
   tc_fence_before();
-  __syncthreads();
+  if constexpr (PAIR) {
+    cluster_sync();  // both CTAs' barriers and TMEM exist before any cross-CTA use
+  } else {
+    __syncthreads();
+  }
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
   const int total = s_tstart[E] * args.f_tiles;
@@ -440,11 +464,15 @@ __global__ void __launch_bounds__(SwCfg<EPI == SW_ACT && PACKED, NT>::kThreads, 
       uint32_t phase = 0, issued = 0;
       bool ok = true;
       int ready_e = -1;  // expert whose h rows this thread has seen complete
-      WorkIter it(sk, total, num_kb);
+      WorkIter it(sk, total, num_kb, first, step);
       Work w;
       while (ok && it.next(w)) {
         const Tile d = decode_tile(w.t, args.f_tiles, s_tstart, s_offs, E, NT);
-        const int f0 = d.nt * SW_M;  // first weight row of the tile
+        const int f0 = d.nt * kTileRows + (int)rank * SW_M;  // first weight row of this CTA
+        // PAIR: the MMA reads its first n_mma / 2 token rows from the leader
+        // and the rest from the peer
+        const int rows = d.m_end - d.m0;
+        const int m_b = d.m0 + (int)rank * ((rows + SW_NGRAN - 1) / SW_NGRAN * SW_NGRAN / 2);
         if (args.ready_in && d.e != ready_e) {
           if (!wait_expert_ready(args, d.e, f0, s_offs, s_abort)) {
             ok = false;
@@ -457,11 +485,20 @@ __global__ void __launch_bounds__(SwCfg<EPI == SW_ACT && PACKED, NT>::kThreads, 
             ok = false;
             break;
           }
-          mbar_arrive_expect_tx(full_bar(stage), C::kStageBytes);
-          tma_load_3d(a_addr(stage, 0), &tmap_w, full_bar(stage), kb * SW_BK, f0, d.e);
-          if (DUAL)
-            tma_load_3d(a_addr(stage, 1), &tmap_w, full_bar(stage), kb * SW_BK, args.I + f0, d.e);
-          tma_load_2d(b_addr(stage), &tmap_x, full_bar(stage), kb * SW_BK, d.m0);
+          if constexpr (PAIR) {
+            // both CTAs' copies complete on the leader's full barrier
+            if (leader) mbar_arrive_expect_tx(full_bar(stage), 2 * C::kStageBytes);
+            const uint32_t fb = map_to_rank(full_bar(stage), 0);
+            tma_load_3d_pair(a_addr(stage, 0), &tmap_w, fb, kb * SW_BK, f0, d.e);
+            tma_load_2d_pair(b_addr(stage), &tmap_x, fb, kb * SW_BK, m_b);
+          } else {
+            mbar_arrive_expect_tx(full_bar(stage), C::kStageBytes);
+            tma_load_3d(a_addr(stage, 0), &tmap_w, full_bar(stage), kb * SW_BK, f0, d.e);
+            if (DUAL)
+              tma_load_3d(a_addr(stage, 1), &tmap_w, full_bar(stage), kb * SW_BK, args.I + f0,
+                          d.e);
+            tma_load_2d(b_addr(stage), &tmap_x, full_bar(stage), kb * SW_BK, d.m0);
+          }
           issued = issued < (uint32_t)C::kStages ? issued + 1 : (uint32_t)C::kStages;
           if (++stage == C::kStages) {
             stage = 0;
@@ -469,7 +506,9 @@ __global__ void __launch_bounds__(SwCfg<EPI == SW_ACT && PACKED, NT>::kThreads, 
           }
         }
       }
-      if (!ok) {
+      // a pair's copies complete on the leader's barriers: the leader drains
+      // (the peer stays resident until the final cluster barrier)
+      if (!ok && leader) {
         for (uint32_t i = 0; i < issued; ++i) {
           int s = stage - 1 - (int)i;
           uint32_t ph = phase;
@@ -482,20 +521,20 @@ __global__ void __launch_bounds__(SwCfg<EPI == SW_ACT && PACKED, NT>::kThreads, 
       }
     }
   } else if (warp == 1) {
-    // --------------------------------------------------------- MMA issuer --
-    if (lane == 0) {
+    // ------------------------------------- MMA issuer (a pair's leader) --
+    if (lane == 0 && leader) {
       int stage = 0;
       uint32_t phase = 0;
       bool ok = true;
       int local = 0;
-      WorkIter it(sk, total, num_kb);
+      WorkIter it(sk, total, num_kb, first, step);
       Work w;
       for (; ok && it.next(w); ++local) {
         const Tile d = decode_tile(w.t, args.f_tiles, s_tstart, s_offs, E, NT);
         const int rows = d.m_end - d.m0;
         // MMA N: the tile's rows rounded up to 32 (a multiple of 16, <= 256)
         const int n_mma = (rows + SW_NGRAN - 1) / SW_NGRAN * SW_NGRAN;
-        const uint32_t idesc = make_idesc_bf16(SW_M, n_mma);
+        const uint32_t idesc = make_idesc_bf16(kTileRows, n_mma);
         const int acc = local & 1;
         const uint32_t acc_phase = (uint32_t)(local >> 1) & 1u;
         if (!wait_bounded(tempty_bar(acc), acc_phase ^ 1u, s_abort, args.ctrl, args.timeout_ns))
@@ -512,8 +551,12 @@ __global__ void __launch_bounds__(SwCfg<EPI == SW_ACT && PACKED, NT>::kThreads, 
           const uint64_t adesc0 = sw128_desc(a_addr(stage, 0));
           const uint64_t bdesc = sw128_desc(b_addr(stage));
 #pragma unroll
-          for (int kk = 0; kk < SW_BK / SW_UK; ++kk)
-            umma_bf16(d_tmem, adesc0 + 2u * kk, bdesc + 2u * kk, idesc, acc_k0 | (kk != 0));
+          for (int kk = 0; kk < SW_BK / SW_UK; ++kk) {
+            if constexpr (PAIR)
+              umma_bf16_pair(d_tmem, adesc0 + 2u * kk, bdesc + 2u * kk, idesc, acc_k0 | (kk != 0));
+            else
+              umma_bf16(d_tmem, adesc0 + 2u * kk, bdesc + 2u * kk, idesc, acc_k0 | (kk != 0));
+          }
           if (DUAL) {
             const uint64_t adesc1 = sw128_desc(a_addr(stage, 1));
 #pragma unroll
@@ -521,15 +564,26 @@ __global__ void __launch_bounds__(SwCfg<EPI == SW_ACT && PACKED, NT>::kThreads, 
               umma_bf16(d_tmem + NT, adesc1 + 2u * kk, bdesc + 2u * kk, idesc,
                         acc_k0 | (kk != 0));
           }
-          umma_commit(empty_bar(stage));
+          if constexpr (PAIR)
+            umma_commit_pair(empty_bar(stage), 0x3);
+          else
+            umma_commit(empty_bar(stage));
           if (++stage == C::kStages) {
             stage = 0;
             phase ^= 1u;
           }
         }
-        if (ok) umma_commit(tfull_bar(acc));
+        if (ok) {
+          if constexpr (PAIR)
+            umma_commit_pair(tfull_bar(acc), 0x3);
+          else
+            umma_commit(tfull_bar(acc));
+        }
       }
-      umma_commit(drain_bar);
+      if constexpr (PAIR)
+        umma_commit_pair(drain_bar, 0x1);
+      else
+        umma_commit(drain_bar);
       wait_drain(drain_bar, 0, 100000000ull);
     }
   } else {
@@ -538,7 +592,7 @@ __global__ void __launch_bounds__(SwCfg<EPI == SW_ACT && PACKED, NT>::kThreads, 
     const int half = (warp - 2) >> 2;   // which of the quarter's warps: chunk parity
     constexpr int kPer = C::kEpiWarps / 4;  // warps per lane quarter
     int local = 0;
-    WorkIter it(sk, total, num_kb);
+    WorkIter it(sk, total, num_kb, first, step);
     Work w;
     const int64_t U = (int64_t)total * num_kb;
     const int G = (int)gridDim.x;
@@ -552,7 +606,7 @@ __global__ void __launch_bounds__(SwCfg<EPI == SW_ACT && PACKED, NT>::kThreads, 
       et.taddr = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * C::kAccCols);
       et.m0 = d.m0;
       et.rows = d.m_end - d.m0;
-      et.frow = d.nt * SW_M + q * 32 + lane;
+      et.frow = d.nt * kTileRows + (int)rank * SW_M + q * 32 + lane;
       et.lane = lane;
       et.dst_base = -1;
       et.dst_mine = 0;
@@ -580,26 +634,40 @@ __global__ void __launch_bounds__(SwCfg<EPI == SW_ACT && PACKED, NT>::kThreads, 
       for (int c = c0 + 8 * half; c < et.rows; c += 8 * kPer) epi_chunk<EPI, DUAL, NT, 8>(et, c, args);
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(tempty_bar(acc));
+      if (lane == 0) {
+        if (PAIR && !leader)
+          mbar_arrive_cluster(map_to_rank(tempty_bar(acc), 0));
+        else
+          mbar_arrive(tempty_bar(acc));
+      }
       if (args.ready_out) publish_ready(args, d.e, lane);
     }
   }
 
   tc_fence_before();
-  __syncthreads();
+  if constexpr (PAIR) {
+    cluster_sync();  // the leader's MMAs into the peer's TMEM are complete
+  } else {
+    __syncthreads();
+  }
   if (warp == 1) {
     tc_fence_after();
-    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_base),
-                 "r"(C::kTmemCols)
-                 : "memory");
+    if constexpr (PAIR)
+      asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(tmem_base),
+                   "r"(C::kTmemCols)
+                   : "memory");
+    else
+      asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_base),
+                   "r"(C::kTmemCols)
+                   : "memory");
   }
 }
 
-template <int EPI, bool PACKED, int NT>
+template <int EPI, bool PACKED, int NT, bool PAIR = false>
 cudaError_t launch_swap(const CUtensorMap &tw, const CUtensorMap &tx, const SwArgs &a,
                         cudaStream_t s) {
-  using C = SwCfg<EPI == SW_ACT && PACKED, NT>;
-  auto kern = grouped_gemm_swap_kernel<EPI, PACKED, NT>;
+  using C = SwCfg<EPI == SW_ACT && PACKED, NT, PAIR>;
+  auto kern = grouped_gemm_swap_kernel<EPI, PACKED, NT, PAIR>;
   static bool attr_set = false;
   if (!attr_set) {
     cudaError_t err =
@@ -608,10 +676,28 @@ cudaError_t launch_swap(const CUtensorMap &tw, const CUtensorMap &tx, const SwAr
     if ((err = uniform_carveout(kern)) != cudaSuccess) return err;
     attr_set = true;
   }
-  const cudaError_t err = launch_dependent(kern, dim3(device_sm_count()), dim3(C::kThreads),
-                                           C::kSmemBytes, s, tw, tx, a);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(PAIR ? device_sm_count() & ~1 : device_sm_count());
+  cfg.blockDim = dim3(C::kThreads);
+  cfg.dynamicSmemBytes = C::kSmemBytes;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  attr[1].id = cudaLaunchAttributeClusterDimension;  // PAIR: two CTAs per cluster
+  attr[1].val.clusterDim.x = PAIR ? 2 : 1;
+  attr[1].val.clusterDim.y = 1;
+  attr[1].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = PAIR ? 2 : 1;
+  const cudaError_t err = cudaLaunchKernelEx(&cfg, kern, tw, tx, a);
   return err != cudaSuccess ? err : cudaGetLastError();
 }
+
+// CTA pairs (M = 256 per MMA) for one-accumulator contractions with 256-row
+// token tiles: each SM then reads 32 KB per K step instead of 48 KB, so the
+// same shared memory keeps 6 K steps in flight instead of 4.
+constexpr bool use_pair(int nt, bool dual) { return nt == 256 && !dual; }
 
 // The w13 contraction at token-tile width NT (NT <= 128 for the packed
 // gated layout, whose two accumulators must fit TMEM twice).
@@ -621,28 +707,33 @@ cudaError_t swap_ffn1(const uint16_t *x_sorted, const uint16_t *w13, int64_t N, 
   const bool relu2_act = act.act == MOE_ACT_RELU2;
   const bool packed = !relu2_act && act.layout == MOE_W13_PACKED;
   constexpr int NT_DUAL = NT > 128 ? 128 : NT;
+  constexpr bool PAIR = use_pair(NT, false);
+  const int tile_rows = !packed && PAIR ? 2 * SW_M : SW_M;
   CUtensorMap tw, tx;
   if (!map_3d(&tw, w13, (uint64_t)E, (uint64_t)w13_rows(act, I), (uint64_t)H, SW_M) ||
-      !map_2d(&tx, x_sorted, (uint64_t)N, (uint64_t)H, packed ? NT_DUAL : NT))
+      !map_2d(&tx, x_sorted, (uint64_t)N, (uint64_t)H,
+              packed ? NT_DUAL : (PAIR ? NT / 2 : NT)))
     return cudaErrorInvalidValue;
   a.num_kb = H / SW_BK;
-  a.f_tiles = (w13_rows(act, I) / (packed ? 2 : 1) + SW_M - 1) / SW_M;
-  return relu2_act ? launch_swap<SW_RELU2, false, NT>(tw, tx, a, s)
+  a.f_tiles = (w13_rows(act, I) / (packed ? 2 : 1) + tile_rows - 1) / tile_rows;
+  return relu2_act ? launch_swap<SW_RELU2, false, NT, PAIR>(tw, tx, a, s)
          : packed  ? launch_swap<SW_ACT, true, NT_DUAL>(tw, tx, a, s)
-                   : launch_swap<SW_ACT, false, NT>(tw, tx, a, s);
+                   : launch_swap<SW_ACT, false, NT, PAIR>(tw, tx, a, s);
 }
 
 // The w2 contraction (gate scale + scatter) at token-tile width NT.
 template <int NT>
 cudaError_t swap_ffn2(const uint16_t *h_buf, const uint16_t *w2, int64_t N, int E, int H, int I,
                       SwArgs a, cudaStream_t s) {
+  constexpr bool PAIR = use_pair(NT, false);
+  const int tile_rows = PAIR ? 2 * SW_M : SW_M;
   CUtensorMap tw, tx;
   if (!map_3d(&tw, w2, (uint64_t)E, (uint64_t)H, (uint64_t)I, SW_M) ||
-      !map_2d(&tx, h_buf, (uint64_t)N, (uint64_t)I, NT))
+      !map_2d(&tx, h_buf, (uint64_t)N, (uint64_t)I, PAIR ? NT / 2 : NT))
     return cudaErrorInvalidValue;
   a.num_kb = I / SW_BK;
-  a.f_tiles = (H + SW_M - 1) / SW_M;
-  return launch_swap<SW_SCATTER, false, NT>(tw, tx, a, s);
+  a.f_tiles = (H + tile_rows - 1) / tile_rows;
+  return launch_swap<SW_SCATTER, false, NT, PAIR>(tw, tx, a, s);
 }
 
 // Token-tile width of a contraction with f_tiles weight tiles per expert:
@@ -659,7 +750,7 @@ int pick_token_tile(int64_t N, int E, int f_tiles, bool dual) {
   double best_t = 1e300;
   for (int nt = dual ? 128 : 256; nt >= 32; nt /= 2) {
     const int64_t tiles = ((N + nt - 1) / nt + (N < E ? N : E)) * (int64_t)f_tiles;
-    const double smem = 128.0 * kA + nt, mma = 1.45 * kA * nt;
+    const double smem = 128.0 * kA + (use_pair(nt, dual) ? nt / 2 : nt), mma = 1.45 * kA * nt;
     const double t = (double)((tiles + sms - 1) / sms) * (smem > mma ? smem : mma);
     if (t < best_t) {
       best_t = t;
@@ -721,7 +812,10 @@ cudaError_t launch_ffn_swap(const uint16_t *x_sorted, const int32_t *offs,
   a.ready_out = nullptr;
   a.ready_in = ready;
   a.ready_nt = nt1_eff;
-  a.ready_per_tile = f_tiles1 * sw_epi_warps(nt1_eff);
+  // arrivals per token tile: every epilogue warp of every weight tile (a
+  // CTA pair's tile covers 256 weight rows with both CTAs' warps)
+  const bool pair1 = !packed && use_pair(nt1_eff, false);
+  a.ready_per_tile = (pair1 ? (f_tiles1 + 1) / 2 * 2 : f_tiles1) * sw_epi_warps(nt1_eff);
   a.w = w2;
   a.w_rows = H;
   a.stream_k = 0;  // whole w2 tiles: they start as soon as w13 CTAs leave SMs free
