@@ -67,15 +67,18 @@ struct SwCfg {
   static constexpr int kA = DUAL ? 2 : 1;
   static constexpr int kBBytes = (PAIR ? NT / 2 : NT) * SW_BK * 2;  // token rows of one stage
   static constexpr int kStageBytes = kA * SW_A_BYTES + kBBytes;  // a multiple of 1 KB
-  static constexpr int kStages =
-      SW_SMEM_RING / kStageBytes < 8 ? SW_SMEM_RING / kStageBytes : 8;
+  // pairs: 7 stages of 32 KB, which fit only without the 1 KB alignment slack
+  static constexpr int kRing = PAIR ? 7 * 32 * 1024 : SW_SMEM_RING;
+  static constexpr int kStages = kRing / kStageBytes < 8 ? kRing / kStageBytes : 8;
+  static constexpr int kSlack = PAIR ? 0 : 1024;  // PAIR: the base must be 1024-aligned
   static constexpr int kEpiWarps = sw_epi_warps(NT);
   static constexpr int kThreads = (2 + kEpiWarps) * 32;
   static constexpr int kAccCols = kA * NT;         // one accumulator buffer
   static constexpr int kTmemCols = 2 * kAccCols;   // a power of 2 in [64, 512]
   static constexpr int kNumBars = 2 * kStages + 2 + 2 + 1;
-  static constexpr int kSmemBytes = 1024 + kStages * kStageBytes + kNumBars * 8 + 16 +
+  static constexpr int kSmemBytes = kSlack + kStages * kStageBytes + kNumBars * 8 + 16 +
                                     2 * (kMaxExperts + 1) * 4 + 16;
+  static_assert(kSmemBytes <= 227 * 1024, "shared memory per CTA");
   static_assert(kTmemCols <= 512 && (kTmemCols & (kTmemCols - 1)) == 0, "TMEM columns");
   static_assert(NT % SW_NGRAN == 0 && NT <= 256, "token tile");
   static_assert(kStages >= 4, "pipeline depth");
@@ -376,6 +379,12 @@ __global__ void __launch_bounds__(SwCfg<EPI == SW_ACT && PACKED, NT, PAIR>::kThr
   constexpr int kTileRows = PAIR ? 2 * SW_M : SW_M;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_addr = smem_u32(smem_raw);
+  if (C::kSlack == 0 && (raw_addr & 1023u) != 0) {
+    // no room to align the stages (128-byte swizzle needs 1024): refuse, in
+    // every CTA alike (the same address in both CTAs of a pair)
+    if (threadIdx.x == 0) record_status(args.ctrl, MOE_ERR_UNSUPPORTED);
+    return;
+  }
   uint8_t *smem = smem_raw + ((1024u - (raw_addr & 1023u)) & 1023u);
   uint64_t *bars = reinterpret_cast<uint64_t *>(smem + C::kStages * C::kStageBytes);
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + C::kNumBars);
