@@ -17,6 +17,7 @@
  * moe_build_metadata_noalloc (2 without a workspace), moe_route_gemm (the
  * router matmul fused with 1), moe_forward_gate (the layer from x and the
  * gate weights), moe_forward_timed (stage events), moe_forward_launch_count,
+ * moe_ffn_plan,
  * the workspace calls, moe_read_status and moe_selftest_wait_timeout.
  *
  * Sources (page title, section):
@@ -343,6 +344,19 @@ moe_status moe_forward_timed(const uint16_t *x, const float *logits, const uint1
  * moe_forward rejects. Host-only: launches nothing. No counterpart on the
  * pages: lets a caller size a CUDA graph or count its launches. */
 int32_t moe_forward_launch_count(int64_t n, int32_t E, int32_t k, int32_t H, int32_t I);
+
+/* How moe_grouped_ffn / moe_forward tile the two expert contractions for these
+ * sizes and params (no launch; the current device's SM count enters the
+ * choice). Writes plan[0..4]: token rows per tile of the w13 and of the w2
+ * contraction; 1 if the w13 / the w2 contraction runs on CTA pairs (one
+ * M = 256 MMA over two SMs), else 0; 1 for the decode tiling (32-row tiles,
+ * the w13 units split evenly over the SMs when they make under two waves).
+ * With params->ffn_kernel = MOE_FFN_TILED: 128, 128, 0, 0, 0. Returns the
+ * validation status of moe_forward for the same arguments (MOE_ERR_INVALID_ARG
+ * for a null plan). No counterpart on the pages: introspection for callers
+ * and tests. */
+moe_status moe_ffn_plan(int64_t n, int32_t E, int32_t k, int32_t H, int32_t I,
+                        const moe_params *params, int32_t *plan);
 
 /* DEBUG ONLY -- synchronises `stream`, returns the status word recorded by
  * device-side bounded waits since the last reset (MOE_OK if none). With

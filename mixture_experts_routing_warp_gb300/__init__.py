@@ -8,12 +8,12 @@ behind the C ABI of include/moe.h. This package is the thin Python binding
 """
 from ._binding import (ACT, FFN_KERNEL, GATING, LAYOUT, MoEError, MoeParams, RoutingMeta,
                        STAGES, build_metadata, combine, empty_meta, forward, forward_gate,
-                       forward_launch_count, forward_timed, grouped_ffn, lib, library_path,
+                       ffn_plan, forward_launch_count, forward_timed, grouped_ffn, lib, library_path,
                        make_params, read_status, route, route_gemm, route_metadata,
                        selftest_wait_timeout, status_string, workspace, workspace_size)
 
 __all__ = ["ACT", "FFN_KERNEL", "GATING", "LAYOUT", "MoEError", "MoeParams", "RoutingMeta",
            "STAGES", "build_metadata", "combine", "empty_meta", "forward", "forward_gate",
-           "forward_launch_count", "forward_timed", "grouped_ffn", "lib", "library_path",
+           "ffn_plan", "forward_launch_count", "forward_timed", "grouped_ffn", "lib", "library_path",
            "make_params", "read_status", "route", "route_gemm", "route_metadata",
            "selftest_wait_timeout", "status_string", "workspace", "workspace_size"]

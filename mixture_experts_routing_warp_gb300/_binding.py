@@ -75,6 +75,7 @@ SIGNATURES = {
     "moe_forward_gate": (_I32, [_P, _P, _P, _P, _I64, _I32, _I32, _I32, _I32, _PP, _P, _P, _P,
                                 _PM, _P, _SZ, _P]),
     "moe_forward_launch_count": (_I32, [_I64, _I32, _I32, _I32, _I32]),
+    "moe_ffn_plan": (_I32, [_I64, _I32, _I32, _I32, _I32, _P, _P]),
     "moe_read_status": (_I32, [_P, _SZ, _I32, _P]),
     "moe_selftest_wait_timeout": (_I32, [_P, _SZ, _U64, _P]),
 }
@@ -358,6 +359,16 @@ def forward_timed(x: torch.Tensor, logits: torch.Tensor, w13: torch.Tensor, w2: 
 def forward_launch_count(n: int, E: int, k: int, H: int, I: int) -> int:
     """Kernels one moe_forward enqueues for these sizes (-1: invalid sizes)."""
     return int(lib().moe_forward_launch_count(n, E, k, H, I))
+
+
+def ffn_plan(n: int, E: int, k: int, H: int, I: int, params: MoeParams) -> dict:
+    """How the two expert contractions are tiled for these sizes (no launch):
+    token rows per tile of each, whether each runs on CTA pairs, and whether
+    the decode tiling applies."""
+    plan = (ctypes.c_int32 * 5)()
+    _check(lib().moe_ffn_plan(n, E, k, H, I, ctypes.byref(params), plan), "moe_ffn_plan")
+    return {"token_tile_w13": plan[0], "token_tile_w2": plan[1], "pair_w13": bool(plan[2]),
+            "pair_w2": bool(plan[3]), "decode": bool(plan[4])}
 
 
 def read_status(ws: torch.Tensor, reset: bool = False) -> int:

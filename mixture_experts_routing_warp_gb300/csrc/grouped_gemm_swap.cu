@@ -771,6 +771,24 @@ int pick_token_tile(int64_t N, int E, int f_tiles, bool dual) {
 
 }  // namespace
 
+SwapPlan plan_ffn_swap(int64_t N, int E, int H, int I, const ActParams &act) {
+  SwapPlan p{};
+  p.packed = act.act != MOE_ACT_RELU2 && act.layout == MOE_W13_PACKED;
+  p.f_tiles1 = (w13_rows(act, I) / (p.packed ? 2 : 1) + SW_M - 1) / SW_M;
+  // a handful of rows per expert (decode): 32-row token tiles for both, the
+  // w13 (tile, K step) units split evenly over the grid when short
+  p.nt1 = p.nt2 = SW_NGRAN;
+  p.decode = N <= (int64_t)kDecodeRowsPerExpert * E;
+  if (!p.decode) {
+    p.nt1 = pick_token_tile(N, E, p.f_tiles1, p.packed);
+    p.nt2 = pick_token_tile(N, E, (H + SW_M - 1) / SW_M, false);
+  }
+  p.nt1_eff = p.packed && p.nt1 > 128 ? 128 : p.nt1;  // swap_ffn1's NT_DUAL
+  p.pair1 = !p.packed && use_pair(p.nt1_eff, false);
+  p.pair2 = use_pair(p.nt2, false);
+  return p;
+}
+
 cudaError_t launch_ffn_swap(const uint16_t *x_sorted, const int32_t *offs,
                             const int32_t *col_sorted, const uint16_t *gate_scal,
                             const uint16_t *w13, const uint16_t *w2, int64_t N, int E, int H,
@@ -789,20 +807,11 @@ cudaError_t launch_ffn_swap(const uint16_t *x_sorted, const int32_t *offs,
   a.y_out = y_flat;
   a.ctrl = scr.ctrl;
   a.timeout_ns = kWaitTimeoutNs;
-  const bool packed = act.act != MOE_ACT_RELU2 && act.layout == MOE_W13_PACKED;
-  const int f_tiles1 = (w13_rows(act, I) / (packed ? 2 : 1) + SW_M - 1) / SW_M;
-  // a handful of rows per expert (decode): 32-row token tiles for both, the
-  // (tile, K step) units split evenly over the grid
-  int nt1 = 32, nt2 = 32;
-  const bool decode = N <= (int64_t)kDecodeRowsPerExpert * E;
-  a.stream_k = decode && scr.sync && scr.sk_part && device_sm_count() <= kSkMaxCtas;
-  if (!decode) {
-    nt1 = pick_token_tile(N, E, f_tiles1, packed);
-    nt2 = pick_token_tile(N, E, (H + SW_M - 1) / SW_M, false);
-  }
+  const SwapPlan plan = plan_ffn_swap(N, E, H, I, act);
+  const int f_tiles1 = plan.f_tiles1, nt1 = plan.nt1, nt2 = plan.nt2, nt1_eff = plan.nt1_eff;
+  a.stream_k = plan.decode && scr.sync && scr.sk_part && device_sm_count() <= kSkMaxCtas;
   if (ev_ffn && record_stage_event(ev_ffn[0], s) != cudaSuccess) return cudaErrorUnknown;
   // the w13 kernel publishes per-expert completion; the w2 kernel waits on it
-  const int nt1_eff = packed && nt1 > 128 ? 128 : nt1;  // swap_ffn1's NT_DUAL
   uint32_t *ready = scr.sync ? scr.sync + kSyncReady : nullptr;
   a.ready_out = ready;
   if (a.stream_k) {
@@ -823,8 +832,7 @@ cudaError_t launch_ffn_swap(const uint16_t *x_sorted, const int32_t *offs,
   a.ready_nt = nt1_eff;
   // arrivals per token tile: every epilogue warp of every weight tile (a
   // CTA pair's tile covers 256 weight rows with both CTAs' warps)
-  const bool pair1 = !packed && use_pair(nt1_eff, false);
-  a.ready_per_tile = (pair1 ? (f_tiles1 + 1) / 2 * 2 : f_tiles1) * sw_epi_warps(nt1_eff);
+  a.ready_per_tile = (plan.pair1 ? (f_tiles1 + 1) / 2 * 2 : f_tiles1) * sw_epi_warps(nt1_eff);
   a.w = w2;
   a.w_rows = H;
   a.stream_k = 0;  // whole w2 tiles: they start as soon as w13 CTAs leave SMs free

@@ -293,6 +293,27 @@ static moe_status forward_impl(const uint16_t *x, const float *logits, const uin
   return MOE_OK;
 }
 
+moe_status moe_ffn_plan(int64_t n, int32_t E, int32_t k, int32_t H, int32_t I,
+                        const moe_params *params, int32_t *plan) {
+  moe_status st = check_sizes(n, E, k, H, I, true);
+  if (st != MOE_OK) return st;
+  ActParams act;
+  if ((st = resolve_params(params, act, nullptr)) != MOE_OK) return st;
+  if (!plan) return MOE_ERR_INVALID_ARG;
+  if (act.ffn_kernel == MOE_FFN_TILED) {
+    plan[0] = plan[1] = 128;  // BM: token rows per tile of the tokens-on-M kernel
+    plan[2] = plan[3] = plan[4] = 0;
+    return MOE_OK;
+  }
+  const SwapPlan p = plan_ffn_swap(n * k, E, H, I, act);
+  plan[0] = p.nt1_eff;
+  plan[1] = p.nt2;
+  plan[2] = p.pair1;
+  plan[3] = p.pair2;
+  plan[4] = p.decode;
+  return MOE_OK;
+}
+
 int32_t moe_forward_launch_count(int64_t n, int32_t E, int32_t k, int32_t H, int32_t I) {
   if (check_sizes(n, E, k, H, I, true) != MOE_OK) return -1;
   if (n == 0) return 0;

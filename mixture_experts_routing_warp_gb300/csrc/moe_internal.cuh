@@ -389,6 +389,16 @@ cudaError_t launch_ffn(const uint16_t *x_sorted, const int32_t *offs, const int3
                        uint16_t *y_flat, const FfnScratch &scr, cudaStream_t s,
                        cudaEvent_t *ev_ffn = nullptr);
 
+// Tiling of the swap-operand contractions for N rows (host only): token-tile
+// rows of each (nt1_eff: the w13 kernel's, at most 128 for the packed gated
+// layout), CTA pairs, decode tiling (32-row tiles; the w13 kernel may then
+// split its units evenly over the grid).
+struct SwapPlan {
+  int nt1, nt2, nt1_eff, f_tiles1;
+  bool packed, decode, pair1, pair2;
+};
+SwapPlan plan_ffn_swap(int64_t N, int E, int H, int I, const ActParams &act);
+
 // The swap-operand grouped GEMM (weights on the MMA's M side, token tiles
 // of 32 or 256 rows); launch_ffn hands over to it unless act.ffn_kernel is
 // MOE_FFN_TILED.

@@ -89,6 +89,26 @@ def test_forward_launch_count_host_rules(L):
         assert L.moe_forward_launch_count(*bad) == -1, bad
 
 
+def test_ffn_plan_host_rules(L):
+    """moe_ffn_plan validates like moe_forward, reports the tokens-on-M
+    kernel's fixed tiling, and flags the decode tiling (n*k <= 32 E) on the
+    host alone."""
+    plan = (ctypes.c_int32 * 5)()
+    p = ctypes.byref(moe.make_params())
+    assert L.moe_ffn_plan(8, 0, 1, 128, 128, p, plan) == 1      # E < 1
+    assert L.moe_ffn_plan(8, 4, 2, 96, 128, p, plan) == 1       # H not a multiple of 64
+    assert L.moe_ffn_plan(8, 4, 2, 128, 128, p, None) == 1      # no output
+    assert L.moe_ffn_plan(8, 4, 2, 128, 128, ctypes.byref(moe.make_params(ffn_kernel="tiled")),
+                          plan) == 0
+    assert list(plan) == [128, 128, 0, 0, 0]
+    assert L.moe_ffn_plan(1, 32, 4, 2880, 2880, p, plan) == 0
+    assert plan[4] == 1 and plan[0] == plan[1] == 32 and plan[2] == plan[3] == 0
+    assert L.moe_ffn_plan(256, 32, 4, 2880, 2880, p, plan) == 0  # n*k = 32 E: still decode
+    assert plan[4] == 1
+    assert L.moe_ffn_plan(257, 32, 4, 2880, 2880, p, plan) == 0
+    assert plan[4] == 0
+
+
 def test_ffn_and_forward_parameter_rules(L):
     good = _p(1 << 20)
     ws = _p(1 << 20)

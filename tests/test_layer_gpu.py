@@ -120,7 +120,11 @@ def test_minimind_layer(case):
 
 @pytest.mark.parametrize("n", I.GPTOSS_DECODE_N)
 def test_gptoss_decode(n):
-    _check_full(Layer(I.GPTOSS.with_n(n)))
+    L = Layer(I.GPTOSS.with_n(n))
+    c = L.case
+    plan = moe.ffn_plan(c.n, c.E, c.k, c.H, c.I, L.params)
+    assert plan["decode"] == (c.n * c.k <= 32 * c.E)
+    _check_full(L)
 
 
 @pytest.mark.parametrize("ffn_kernel", ["auto", "tiled"])
@@ -291,4 +295,42 @@ def test_token_tile_widths(act, layout, Idim):
     128-row choice."""
     case = I.LayerCase(f"ntw_{act}_{layout}", n=300, H=512, E=8, k=4, I=Idim, act=act,
                        layout=layout, w_std=0.05, seed=21)
-    _check_full(Layer(case))
+    L = Layer(case)
+    plan = moe.ffn_plan(case.n, case.E, case.k, case.H, case.I, L.params)
+    assert (plan["token_tile_w13"], plan["token_tile_w2"]) == (64, 64)
+    assert not (plan["pair_w13"] or plan["pair_w2"] or plan["decode"])
+    _check_full(L)
+
+
+@pytest.mark.parametrize("act,layout", [("swiglu_oai", "interleaved"), ("relu2", "packed")])
+def test_cta_pair_tiles(act, layout):
+    """Both contractions on CTA pairs (one M = 256 MMA over two SMs): 256-row
+    token tiles in two waves. 384 weight rows per expert on each side, so the
+    last pair tile's second CTA holds only rows past the end (zero-filled
+    copies, skipped by the epilogue)."""
+    Idim = 192 if act == "swiglu_oai" else 384  # w13 rows: 2I or I = 384
+    case = I.LayerCase(f"pairs_{act}", n=2048, H=384, E=8, k=4, I=Idim, act=act,
+                       layout=layout, w_std=0.05, seed=31)
+    L = Layer(case)
+    plan = moe.ffn_plan(case.n, case.E, case.k, case.H, case.I, L.params)
+    assert plan["token_tile_w13"] == 256 and plan["pair_w13"] and plan["pair_w2"]
+    _check_full(L)
+
+
+def test_cta_pair_ragged_expert_loads():
+    """The pair MMA reads its first n_mma/2 token rows from the leader CTA and
+    the rest from the peer: expert loads that leave last tiles of 1, 33, 164,
+    20 and 255 rows move that split (16, 32, 96, 16, 128 rows)."""
+    counts = (513, 1, 255, 257, 33, 0, 1700, 1300)
+    case, h = _routed_case(counts, H=384, Idim=1536, act="swiglu_oai", layout="interleaved")
+    L = Layer(case)
+    L.h = h
+    L.logits = dev(h["logits"])
+    plan = moe.ffn_plan(case.n, case.E, case.k, case.H, case.I, L.params)
+    assert plan["token_tile_w13"] == 256 and plan["pair_w13"]
+    out, indx, vals, meta = L.forward()
+    np.testing.assert_array_equal(meta["col_sum"].cpu().numpy(), np.array(counts))
+    _check_routing(L, indx, vals, meta)
+    ref = oracle.ffn(h["x"], indx.cpu().numpy(), host_bits(vals), h["w13"], h["w2"],
+                     **L.oracle_kw())
+    assert_layer_close(host_bits(out), ref, case.name)
