@@ -231,10 +231,13 @@ struct EpiTile {
 };
 
 // Token columns [c0, c0 + W) of the tile, accumulators r0 (and r1: the up
-// rows of the packed layout) as fp32 bits: apply the epilogue.
-template <int EPI, bool DUAL, int NT, int W>
+// rows of the packed layout) as fp32 bits: apply the epilogue. FULL: every
+// column of the chunk is a valid token row (no per-column bounds test).
+// Stores walk a row pointer instead of recomputing 64-bit offsets.
+template <int EPI, bool DUAL, int NT, int W, bool FULL = false>
 __device__ __forceinline__ void epi_apply(EpiTile &t, int c0, const uint32_t (&r0)[W],
                                           const uint32_t (&r1)[W], const SwArgs &args) {
+  const int nvalid = t.rows - c0;  // columns of this chunk holding tokens
   if constexpr (EPI == SW_SCATTER) {
     const int base = c0 & ~31;
     if (base != t.dst_base) {  // warp-uniform: next 32-token group
@@ -243,53 +246,61 @@ __device__ __forceinline__ void epi_apply(EpiTile &t, int c0, const uint32_t (&r
       t.dst_mine = j < t.rows ? args.col_sorted[t.m0 + j] : 0;
       t.g_mine = j < t.rows ? bf16_bits_to_float(args.gate_scal[t.m0 + j]) : 0.f;
     }
+    if (t.frow < args.H) {
+      uint16_t *col = args.y_out + t.frow;
 #pragma unroll
-    for (int i = 0; i < W; ++i) {
-      const int j = c0 + i;
-      const int dst = __shfl_sync(0xffffffffu, t.dst_mine, j & 31);
-      const float g = __shfl_sync(0xffffffffu, t.g_mine, j & 31);
-      if (j < t.rows && t.frow < args.H)
-        args.y_out[(size_t)dst * args.H + t.frow] = float_to_bf16_bits(__uint_as_float(r0[i]) * g);
+      for (int i = 0; i < W; ++i) {
+        const int j = c0 + i;
+        const int dst = __shfl_sync(0xffffffffu, t.dst_mine, j & 31);
+        const float g = __shfl_sync(0xffffffffu, t.g_mine, j & 31);
+        if (FULL || i < nvalid)
+          col[(size_t)dst * args.H] = float_to_bf16_bits(__uint_as_float(r0[i]) * g);
+      }
     }
   } else if constexpr (EPI == SW_RELU2) {
+    if (t.frow < args.I) {
+      uint16_t *dst = args.h_out + (size_t)(t.m0 + c0) * args.I + t.frow;
 #pragma unroll
-    for (int i = 0; i < W; ++i)
-      if (c0 + i < t.rows && t.frow < args.I)
-        args.h_out[(size_t)(t.m0 + c0 + i) * args.I + t.frow] =
-            float_to_bf16_bits(relu2(__uint_as_float(r0[i])));
+      for (int i = 0; i < W; ++i, dst += args.I)
+        if (FULL || i < nvalid) *dst = float_to_bf16_bits(relu2(__uint_as_float(r0[i])));
+    }
   } else if constexpr (DUAL) {
+    if (t.frow < args.I) {
+      uint16_t *dst = args.h_out + (size_t)(t.m0 + c0) * args.I + t.frow;
 #pragma unroll
-    for (int i = 0; i < W; ++i)
-      if (c0 + i < t.rows && t.frow < args.I)
-        args.h_out[(size_t)(t.m0 + c0 + i) * args.I + t.frow] = float_to_bf16_bits(
-            activate(__uint_as_float(r0[i]), __uint_as_float(r1[i]), args.act));
+      for (int i = 0; i < W; ++i, dst += args.I)
+        if (FULL || i < nvalid)
+          *dst = float_to_bf16_bits(
+              activate(__uint_as_float(r0[i]), __uint_as_float(r1[i]), args.act));
+    }
   } else {
     // Weight rows 2i (gate) and 2i+1 (up) sit in lanes 2i, 2i+1. For each
     // pair of tokens (j, j+1) the even lane computes token j and the odd
     // lane token j+1: one shuffle hands over the missing operand.
     const int c = t.frow >> 1;  // h column of this lane pair
-    const bool odd = t.lane & 1;
+    const int odd = t.lane & 1;
+    const bool col_ok = c < args.I;
+    uint16_t *dst = args.h_out + (size_t)(t.m0 + c0 + odd) * args.I + c;
+    const size_t step = 2 * (size_t)args.I;
 #pragma unroll
-    for (int i = 0; i < W; i += 2) {
+    for (int i = 0; i < W; i += 2, dst += step) {
       const float a = __uint_as_float(r0[i]), b = __uint_as_float(r0[i + 1]);
       const float recv = __shfl_xor_sync(0xffffffffu, odd ? a : b, 1);
-      const int j = c0 + i + (odd ? 1 : 0);
       const float g = odd ? recv : a;  // even: gate_j (own), up_j (recv)
       const float u = odd ? b : recv;  // odd: gate_j+1 (recv), up_j+1 (own)
-      if (j < t.rows && c < args.I)
-        args.h_out[(size_t)(t.m0 + j) * args.I + c] = float_to_bf16_bits(activate(g, u, args.act));
+      if (col_ok && (FULL || i + odd < nvalid)) *dst = float_to_bf16_bits(activate(g, u, args.act));
     }
   }
 }
 
 // Token columns [c0, c0 + W) of the tile: read TMEM, apply the epilogue.
-template <int EPI, bool DUAL, int NT, int W>
+template <int EPI, bool DUAL, int NT, int W, bool FULL = false>
 __device__ __forceinline__ void epi_chunk(EpiTile &t, int c0, const SwArgs &args) {
   uint32_t r0[W], r1[W];
   tmem_ld<W>(t.taddr + c0, r0);
   if constexpr (DUAL) tmem_ld<W>(t.taddr + NT + c0, r1);
   tmem_wait_ld();
-  epi_apply<EPI, DUAL, NT, W>(t, c0, r0, r1, args);
+  epi_apply<EPI, DUAL, NT, W, FULL>(t, c0, r0, r1, args);
 }
 
 // The w13 epilogue's handoff: this warp's h rows of a tile of expert e are
@@ -637,7 +648,8 @@ __global__ void __launch_bounds__(SwCfg<EPI == SW_ACT && PACKED, NT, PAIR>::kThr
       int c0 = 0;
       if constexpr (NT > SW_NGRAN) {
         const int full = et.rows & ~31;
-        for (int c = 32 * half; c < full; c += 32 * kPer) epi_chunk<EPI, DUAL, NT, 32>(et, c, args);
+        for (int c = 32 * half; c < full; c += 32 * kPer)
+          epi_chunk<EPI, DUAL, NT, 32, true>(et, c, args);
         c0 = full;
       }
       for (int c = c0 + 8 * half; c < et.rows; c += 8 * kPer) epi_chunk<EPI, DUAL, NT, 8>(et, c, args);

@@ -274,6 +274,19 @@ struct ActParams {
   int ffn_kernel;  // moe_ffn_kernel (host-side choice of the GEMM kernel)
 };
 
+// Logistic sigmoid 1 / (1 + e^-x) = 1 / (1 + 2^(-x log2 e)) on the special
+// function unit: one ex2.approx and one rcp.approx (each within a few fp32
+// ulp; subnormals flushed), far below the bf16 rounding of h that follows.
+// The short-K epilogues are instruction-bound, and this is a fraction of the
+// instructions of expf and an IEEE division. x -> -inf: 2^(+inf) = +inf and
+// its reciprocal 0; x -> +inf: 2^(-inf) = 0 and the result 1.
+__device__ __forceinline__ float sigmoid_fast(float x) {
+  float e, r;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(e) : "f"(x * -1.4426950408889634f));
+  asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(1.0f + e));
+  return r;
+}
+
 // Gated activations of (gate, up). SwiGLU: (g * sigmoid(g)) * u, with
 // g = min(g, limit), u = clamp(u, -limit, limit) first when a limit is set.
 // SwiGLU-OAI: the same clamps, then (g * sigmoid(alpha g)) * (u + beta).
@@ -281,13 +294,13 @@ __device__ __forceinline__ float activate(float g, float u, const ActParams &p) 
   if (p.act == MOE_ACT_SWIGLU_OAI) {
     g = fminf(g, p.limit);
     u = fminf(fmaxf(u, -p.limit), p.limit);
-    return (g * (1.0f / (1.0f + expf(-p.alpha * g)))) * (u + p.beta);
+    return (g * sigmoid_fast(p.alpha * g)) * (u + p.beta);
   }
   if (p.limit < INFINITY) {
     g = fminf(g, p.limit);
     u = fminf(fmaxf(u, -p.limit), p.limit);
   }
-  return (g * (1.0f / (1.0f + expf(-g)))) * u;
+  return (g * sigmoid_fast(g)) * u;
 }
 
 // The non-gated ReLU2: max(a, 0)^2.
