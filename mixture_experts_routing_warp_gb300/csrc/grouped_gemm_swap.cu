@@ -16,15 +16,15 @@
 // 127 idle MMA rows as with tokens on M), fp32 in TMEM.
 //   NT = 32: decode, a handful of tokens per expert; the weights stream
 //     through all SMs.
-//   NT = 32 .. 256 (at most 128 for the packed gated layout, which needs
-//     two accumulators): prefill; per contraction the NT with the least
+//   NT = 32 .. 256: prefill; per contraction the NT with the least
 //     estimated time (waves x per-tile cost; 256: the same MMA shape as
-//     tokens-on-M tiles).
+//     tokens-on-M tiles, on a CTA pair).
 // Epilogues:
 //   ffn1, interleaved w13: weight rows 2i / 2i+1 are gate_i / up_i, in
 //     adjacent TMEM lanes: one shuffle pairs them.
-//   ffn1, packed w13: the gate rows and the up rows of the same h columns go
-//     to two accumulators, so each thread holds its pair.
+//   ffn1, packed w13: loaded through a 4-D tensor map that interleaves the
+//     gate and up rows of the same h columns on the way into shared memory,
+//     so the tile is the interleaved layout's and so is the epilogue.
 //   ffn1, ReLU2 (non-gated): weight row f0 + w is h column f0 + w.
 //   ffn2: y_flat[col_sorted[m0 + j], f0 + w] = gate_scal[m0 + j] * D[w, j].
 // TMEM is read in chunks of 32 (then 8) token columns up to the tile's rows.
@@ -59,21 +59,19 @@ enum { SW_ACT = 0, SW_SCATTER = 1, SW_RELU2 = 2 };
 // alternate token chunks) for wider tiles
 constexpr int sw_epi_warps(int nt) { return nt > SW_NGRAN ? 8 : 4; }
 
-// DUAL: gate and up weight tiles in each stage. PAIR: a CTA pair runs one
-// MMA of M = 256 (cta_group::2); each CTA's stage holds its 128 weight rows
-// and half of the tile's token rows.
-template <bool DUAL, int NT, bool PAIR = false>
+// PAIR: a CTA pair runs one MMA of M = 256 (cta_group::2); each CTA's stage
+// holds its 128 weight rows and half of the tile's token rows.
+template <int NT, bool PAIR = false>
 struct SwCfg {
-  static constexpr int kA = DUAL ? 2 : 1;
   static constexpr int kBBytes = (PAIR ? NT / 2 : NT) * SW_BK * 2;  // token rows of one stage
-  static constexpr int kStageBytes = kA * SW_A_BYTES + kBBytes;  // a multiple of 1 KB
+  static constexpr int kStageBytes = SW_A_BYTES + kBBytes;  // a multiple of 1 KB
   // pairs: 7 stages of 32 KB, which fit only without the 1 KB alignment slack
   static constexpr int kRing = PAIR ? 7 * 32 * 1024 : SW_SMEM_RING;
   static constexpr int kStages = kRing / kStageBytes < 8 ? kRing / kStageBytes : 8;
   static constexpr int kSlack = PAIR ? 0 : 1024;  // PAIR: the base must be 1024-aligned
   static constexpr int kEpiWarps = sw_epi_warps(NT);
   static constexpr int kThreads = (2 + kEpiWarps) * 32;
-  static constexpr int kAccCols = kA * NT;         // one accumulator buffer
+  static constexpr int kAccCols = NT;              // one accumulator buffer
   static constexpr int kTmemCols = 2 * kAccCols;   // a power of 2 in [64, 512]
   static constexpr int kNumBars = 2 * kStages + 2 + 2 + 1;
   static constexpr int kSmemBytes = kSlack + kStages * kStageBytes + kNumBars * 8 + 16 +
@@ -82,7 +80,7 @@ struct SwCfg {
   static_assert(kTmemCols <= 512 && (kTmemCols & (kTmemCols - 1)) == 0, "TMEM columns");
   static_assert(NT % SW_NGRAN == 0 && NT <= 256, "token tile");
   static_assert(kStages >= 4, "pipeline depth");
-  static_assert(!PAIR || (!DUAL && NT > SW_NGRAN), "CTA pairs: one accumulator, wide tiles");
+  static_assert(!PAIR || NT > SW_NGRAN, "CTA pairs: wide token tiles");
 };
 
 struct SwArgs {
@@ -230,13 +228,13 @@ struct EpiTile {
   float g_mine;    // lane l: gate weight of token dst_base + l
 };
 
-// Token columns [c0, c0 + W) of the tile, accumulators r0 (and r1: the up
-// rows of the packed layout) as fp32 bits: apply the epilogue. FULL: every
-// column of the chunk is a valid token row (no per-column bounds test).
-// Stores walk a row pointer instead of recomputing 64-bit offsets.
-template <int EPI, bool DUAL, int NT, int W, bool FULL = false>
+// Token columns [c0, c0 + W) of the tile, accumulators r0 as fp32 bits:
+// apply the epilogue. FULL: every column of the chunk is a valid token row
+// (no per-column bounds test). Stores walk a row pointer instead of
+// recomputing 64-bit offsets.
+template <int EPI, int W, bool FULL = false>
 __device__ __forceinline__ void epi_apply(EpiTile &t, int c0, const uint32_t (&r0)[W],
-                                          const uint32_t (&r1)[W], const SwArgs &args) {
+                                          const SwArgs &args) {
   const int nvalid = t.rows - c0;  // columns of this chunk holding tokens
   if constexpr (EPI == SW_SCATTER) {
     const int base = c0 & ~31;
@@ -264,17 +262,9 @@ __device__ __forceinline__ void epi_apply(EpiTile &t, int c0, const uint32_t (&r
       for (int i = 0; i < W; ++i, dst += args.I)
         if (FULL || i < nvalid) *dst = float_to_bf16_bits(relu2(__uint_as_float(r0[i])));
     }
-  } else if constexpr (DUAL) {
-    if (t.frow < args.I) {
-      uint16_t *dst = args.h_out + (size_t)(t.m0 + c0) * args.I + t.frow;
-#pragma unroll
-      for (int i = 0; i < W; ++i, dst += args.I)
-        if (FULL || i < nvalid)
-          *dst = float_to_bf16_bits(
-              activate(__uint_as_float(r0[i]), __uint_as_float(r1[i]), args.act));
-    }
   } else {
-    // Weight rows 2i (gate) and 2i+1 (up) sit in lanes 2i, 2i+1. For each
+    // Weight rows 2i (gate) and 2i+1 (up) sit in lanes 2i, 2i+1 (either
+    // layout: the packed one is interleaved by its tensor map). For each
     // pair of tokens (j, j+1) the even lane computes token j and the odd
     // lane token j+1: one shuffle hands over the missing operand.
     const int c = t.frow >> 1;  // h column of this lane pair
@@ -294,13 +284,12 @@ __device__ __forceinline__ void epi_apply(EpiTile &t, int c0, const uint32_t (&r
 }
 
 // Token columns [c0, c0 + W) of the tile: read TMEM, apply the epilogue.
-template <int EPI, bool DUAL, int NT, int W, bool FULL = false>
+template <int EPI, int W, bool FULL = false>
 __device__ __forceinline__ void epi_chunk(EpiTile &t, int c0, const SwArgs &args) {
-  uint32_t r0[W], r1[W];
+  uint32_t r0[W];
   tmem_ld<W>(t.taddr + c0, r0);
-  if constexpr (DUAL) tmem_ld<W>(t.taddr + NT + c0, r1);
   tmem_wait_ld();
-  epi_apply<EPI, DUAL, NT, W, FULL>(t, c0, r0, r1, args);
+  epi_apply<EPI, W, FULL>(t, c0, r0, args);
 }
 
 // The w13 epilogue's handoff: this warp's h rows of a tile of expert e are
@@ -313,32 +302,28 @@ __device__ __forceinline__ void publish_ready(const SwArgs &args, int e, int lan
 }
 
 // A piece of a split tile (decode stream-K). The warp stores its partial
-// sums (32 weight rows x the tile's token columns, per accumulator) in this
+// sums (32 weight rows x the tile's token columns) in this
 // CTA's slot -- slot 0 for the piece that starts the CTA's unit range, 1 for
 // the one that ends it --, releases the accumulator buffer and counts the
 // piece. The warp that counts the tile's last piece of its lane quarter adds
 // the pieces' partials in piece order (a fixed order: the result does not
 // depend on which piece finishes last) and applies the epilogue.
-template <int EPI, bool DUAL, int NT>
+template <int EPI, int NT>
 __device__ __forceinline__ void sk_piece(EpiTile &et, const SwArgs &args, int64_t u0,
                                          int c_first, int c_last, int pieces, int k_lo,
                                          int64_t U, int G, int q, int e, uint32_t tempty) {
   constexpr size_t kSlot = kSkPartFloats / 2;
-  static_assert(2 * SW_M * NT <= (int)kSlot, "partial slot");
+  static_assert(SW_M * NT <= (int)kSlot, "partial slot");
   const int w_row = q * 32 + et.lane;
   const int my_slot = u0 + k_lo == sk_lo(blockIdx.x, U, G) ? 0 : 1;
   float *mine = args.sk_part + ((size_t)blockIdx.x * 2 + my_slot) * kSlot;
   for (int c = 0; c < et.rows; c += 8) {
-    uint32_t r0[8], r1[8];
+    uint32_t r0[8];
     tmem_ld<8>(et.taddr + c, r0);
-    if constexpr (DUAL) tmem_ld<8>(et.taddr + NT + c, r1);
     tmem_wait_ld();
 #pragma unroll
     for (int i = 0; i < 8; ++i)
-      if (c + i < et.rows) {
-        mine[(size_t)(c + i) * SW_M + w_row] = __uint_as_float(r0[i]);
-        if constexpr (DUAL) mine[(size_t)(NT + c + i) * SW_M + w_row] = __uint_as_float(r1[i]);
-      }
+      if (c + i < et.rows) mine[(size_t)(c + i) * SW_M + w_row] = __uint_as_float(r0[i]);
   }
   tc_fence_before();
   __syncwarp();
@@ -354,9 +339,9 @@ __device__ __forceinline__ void sk_piece(EpiTile &et, const SwArgs &args, int64_
   if (old != (uint32_t)pieces - 1) return;
   __syncwarp();
   for (int c = 0; c < et.rows; c += 8) {
-    float s0[8], s1[8];
+    float s0[8];
 #pragma unroll
-    for (int i = 0; i < 8; ++i) s0[i] = s1[i] = 0.f;
+    for (int i = 0; i < 8; ++i) s0[i] = 0.f;
     for (int cta = c_first; cta <= c_last; ++cta) {
       const int64_t lo = sk_lo(cta, U, G);
       if (lo == sk_lo(cta + 1, U, G)) continue;  // owns no unit
@@ -364,28 +349,24 @@ __device__ __forceinline__ void sk_piece(EpiTile &et, const SwArgs &args, int64_
       const float *part = args.sk_part + ((size_t)cta * 2 + slot) * kSlot;
 #pragma unroll
       for (int i = 0; i < 8; ++i)
-        if (c + i < et.rows) {
-          s0[i] += __ldcg(part + (size_t)(c + i) * SW_M + w_row);
-          if constexpr (DUAL) s1[i] += __ldcg(part + (size_t)(NT + c + i) * SW_M + w_row);
-        }
+        if (c + i < et.rows) s0[i] += __ldcg(part + (size_t)(c + i) * SW_M + w_row);
     }
-    uint32_t r0[8], r1[8];
+    uint32_t r0[8];
 #pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      r0[i] = __float_as_uint(s0[i]);
-      r1[i] = __float_as_uint(s1[i]);
-    }
-    epi_apply<EPI, DUAL, NT, 8>(et, c, r0, r1, args);
+    for (int i = 0; i < 8; ++i) r0[i] = __float_as_uint(s0[i]);
+    epi_apply<EPI, 8>(et, c, r0, args);
   }
   if (args.ready_out) publish_ready(args, e, et.lane);
 }
 
+// PACKED: the weights are a packed gated w13, read through the 4-D map that
+// interleaves gate and up rows (box coordinates: column, 0, pair, expert).
 template <int EPI, bool PACKED, int NT, bool PAIR>
-__global__ void __launch_bounds__(SwCfg<EPI == SW_ACT && PACKED, NT, PAIR>::kThreads, 1)
+__global__ void __launch_bounds__(SwCfg<NT, PAIR>::kThreads, 1)
     grouped_gemm_swap_kernel(const __grid_constant__ CUtensorMap tmap_w,
                              const __grid_constant__ CUtensorMap tmap_x, const SwArgs args) {
-  constexpr bool DUAL = EPI == SW_ACT && PACKED;
-  using C = SwCfg<DUAL, NT, PAIR>;
+  static_assert(!PACKED || EPI == SW_ACT, "the packed layout is a gated w13");
+  using C = SwCfg<NT, PAIR>;
   // PAIR: tiles of 256 weight rows; this CTA's half starts at row `rank` * 128
   constexpr int kTileRows = PAIR ? 2 * SW_M : SW_M;
   extern __shared__ uint8_t smem_raw[];
@@ -410,8 +391,8 @@ __global__ void __launch_bounds__(SwCfg<EPI == SW_ACT && PACKED, NT, PAIR>::kThr
   auto tfull_bar = [&](int b) { return full0 + 8u * (2 * C::kStages + b); };
   auto tempty_bar = [&](int b) { return full0 + 8u * (2 * C::kStages + 2 + b); };
   const uint32_t drain_bar = full0 + 8u * (2 * C::kStages + 4);
-  auto a_addr = [&](int s, int which) { return stage0 + s * C::kStageBytes + which * SW_A_BYTES; };
-  auto b_addr = [&](int s) { return stage0 + s * C::kStageBytes + C::kA * SW_A_BYTES; };
+  auto a_addr = [&](int s) { return stage0 + s * C::kStageBytes; };
+  auto b_addr = [&](int s) { return stage0 + s * C::kStageBytes + SW_A_BYTES; };
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int E = args.E;
@@ -509,14 +490,17 @@ __global__ void __launch_bounds__(SwCfg<EPI == SW_ACT && PACKED, NT, PAIR>::kThr
             // both CTAs' copies complete on the leader's full barrier
             if (leader) mbar_arrive_expect_tx(full_bar(stage), 2 * C::kStageBytes);
             const uint32_t fb = map_to_rank(full_bar(stage), 0);
-            tma_load_3d_pair(a_addr(stage, 0), &tmap_w, fb, kb * SW_BK, f0, d.e);
+            if constexpr (PACKED)
+              tma_load_4d_pair(a_addr(stage), &tmap_w, fb, kb * SW_BK, 0, f0 / 2, d.e);
+            else
+              tma_load_3d_pair(a_addr(stage), &tmap_w, fb, kb * SW_BK, f0, d.e);
             tma_load_2d_pair(b_addr(stage), &tmap_x, fb, kb * SW_BK, m_b);
           } else {
             mbar_arrive_expect_tx(full_bar(stage), C::kStageBytes);
-            tma_load_3d(a_addr(stage, 0), &tmap_w, full_bar(stage), kb * SW_BK, f0, d.e);
-            if (DUAL)
-              tma_load_3d(a_addr(stage, 1), &tmap_w, full_bar(stage), kb * SW_BK, args.I + f0,
-                          d.e);
+            if constexpr (PACKED)
+              tma_load_4d(a_addr(stage), &tmap_w, full_bar(stage), kb * SW_BK, 0, f0 / 2, d.e);
+            else
+              tma_load_3d(a_addr(stage), &tmap_w, full_bar(stage), kb * SW_BK, f0, d.e);
             tma_load_2d(b_addr(stage), &tmap_x, full_bar(stage), kb * SW_BK, d.m0);
           }
           issued = issued < (uint32_t)C::kStages ? issued + 1 : (uint32_t)C::kStages;
@@ -568,7 +552,7 @@ __global__ void __launch_bounds__(SwCfg<EPI == SW_ACT && PACKED, NT, PAIR>::kThr
           }
           const uint32_t acc_k0 = kb != w.k_lo ? 1u : 0u;  // first K step: overwrite
           tc_fence_after();
-          const uint64_t adesc0 = sw128_desc(a_addr(stage, 0));
+          const uint64_t adesc0 = sw128_desc(a_addr(stage));
           const uint64_t bdesc = sw128_desc(b_addr(stage));
 #pragma unroll
           for (int kk = 0; kk < SW_BK / SW_UK; ++kk) {
@@ -576,13 +560,6 @@ __global__ void __launch_bounds__(SwCfg<EPI == SW_ACT && PACKED, NT, PAIR>::kThr
               umma_bf16_pair(d_tmem, adesc0 + 2u * kk, bdesc + 2u * kk, idesc, acc_k0 | (kk != 0));
             else
               umma_bf16(d_tmem, adesc0 + 2u * kk, bdesc + 2u * kk, idesc, acc_k0 | (kk != 0));
-          }
-          if (DUAL) {
-            const uint64_t adesc1 = sw128_desc(a_addr(stage, 1));
-#pragma unroll
-            for (int kk = 0; kk < SW_BK / SW_UK; ++kk)
-              umma_bf16(d_tmem + NT, adesc1 + 2u * kk, bdesc + 2u * kk, idesc,
-                        acc_k0 | (kk != 0));
           }
           if constexpr (PAIR)
             umma_commit_pair(empty_bar(stage), 0x3);
@@ -636,7 +613,7 @@ __global__ void __launch_bounds__(SwCfg<EPI == SW_ACT && PACKED, NT, PAIR>::kThr
           const int64_t u0 = (int64_t)w.t * num_kb;
           const int c_first = sk_cta(u0, U, G), c_last = sk_cta(u0 + num_kb - 1, U, G);
           if (c_last > c_first) {
-            sk_piece<EPI, DUAL, NT>(et, args, u0, c_first, c_last,
+            sk_piece<EPI, NT>(et, args, u0, c_first, c_last,
                                     sk_pieces(c_first, c_last, U, G), w.k_lo, U, G, q, d.e,
                                     tempty_bar(acc));
             continue;  // the piece released its accumulator buffer
@@ -649,10 +626,10 @@ __global__ void __launch_bounds__(SwCfg<EPI == SW_ACT && PACKED, NT, PAIR>::kThr
       if constexpr (NT > SW_NGRAN) {
         const int full = et.rows & ~31;
         for (int c = 32 * half; c < full; c += 32 * kPer)
-          epi_chunk<EPI, DUAL, NT, 32, true>(et, c, args);
+          epi_chunk<EPI, 32, true>(et, c, args);
         c0 = full;
       }
-      for (int c = c0 + 8 * half; c < et.rows; c += 8 * kPer) epi_chunk<EPI, DUAL, NT, 8>(et, c, args);
+      for (int c = c0 + 8 * half; c < et.rows; c += 8 * kPer) epi_chunk<EPI, 8>(et, c, args);
       tc_fence_before();
       __syncwarp();
       if (lane == 0) {
@@ -687,7 +664,7 @@ __global__ void __launch_bounds__(SwCfg<EPI == SW_ACT && PACKED, NT, PAIR>::kThr
 template <int EPI, bool PACKED, int NT, bool PAIR = false>
 cudaError_t launch_swap(const CUtensorMap &tw, const CUtensorMap &tx, const SwArgs &a,
                         cudaStream_t s) {
-  using C = SwCfg<EPI == SW_ACT && PACKED, NT, PAIR>;
+  using C = SwCfg<NT, PAIR>;
   auto kern = grouped_gemm_swap_kernel<EPI, PACKED, NT, PAIR>;
   static bool attr_set = false;
   if (!attr_set) {
@@ -715,30 +692,30 @@ cudaError_t launch_swap(const CUtensorMap &tw, const CUtensorMap &tx, const SwAr
   return err != cudaSuccess ? err : cudaGetLastError();
 }
 
-// CTA pairs (M = 256 per MMA) for one-accumulator contractions with 256-row
-// token tiles: each SM then reads 32 KB per K step instead of 48 KB, so the
-// same shared memory keeps 6 K steps in flight instead of 4.
-constexpr bool use_pair(int nt, bool dual) { return nt == 256 && !dual; }
+// CTA pairs (M = 256 per MMA) for 256-row token tiles: each SM then reads
+// 32 KB per K step instead of 48 KB, so the same shared memory keeps 7 K
+// steps in flight instead of 4.
+constexpr bool use_pair(int nt) { return nt == 256; }
 
-// The w13 contraction at token-tile width NT (NT <= 128 for the packed
-// gated layout, whose two accumulators must fit TMEM twice).
+// The w13 contraction at token-tile width NT. A packed gated w13 goes
+// through the interleaving 4-D map: the kernel sees the interleaved layout.
 template <int NT>
 cudaError_t swap_ffn1(const uint16_t *x_sorted, const uint16_t *w13, int64_t N, int E, int H,
                       int I, const ActParams &act, SwArgs a, cudaStream_t s) {
   const bool relu2_act = act.act == MOE_ACT_RELU2;
   const bool packed = !relu2_act && act.layout == MOE_W13_PACKED;
-  constexpr int NT_DUAL = NT > 128 ? 128 : NT;
-  constexpr bool PAIR = use_pair(NT, false);
-  const int tile_rows = !packed && PAIR ? 2 * SW_M : SW_M;
+  constexpr bool PAIR = use_pair(NT);
+  constexpr int tile_rows = PAIR ? 2 * SW_M : SW_M;
   CUtensorMap tw, tx;
-  if (!map_3d(&tw, w13, (uint64_t)E, (uint64_t)w13_rows(act, I), (uint64_t)H, SW_M) ||
-      !map_2d(&tx, x_sorted, (uint64_t)N, (uint64_t)H,
-              packed ? NT_DUAL : (PAIR ? NT / 2 : NT)))
+  const bool w_ok =
+      packed ? map_w13_packed_interleaved(&tw, w13, (uint64_t)E, (uint64_t)I, (uint64_t)H, SW_M / 2)
+             : map_3d(&tw, w13, (uint64_t)E, (uint64_t)w13_rows(act, I), (uint64_t)H, SW_M);
+  if (!w_ok || !map_2d(&tx, x_sorted, (uint64_t)N, (uint64_t)H, PAIR ? NT / 2 : NT))
     return cudaErrorInvalidValue;
   a.num_kb = H / SW_BK;
-  a.f_tiles = (w13_rows(act, I) / (packed ? 2 : 1) + tile_rows - 1) / tile_rows;
+  a.f_tiles = (w13_rows(act, I) + tile_rows - 1) / tile_rows;
   return relu2_act ? launch_swap<SW_RELU2, false, NT, PAIR>(tw, tx, a, s)
-         : packed  ? launch_swap<SW_ACT, true, NT_DUAL>(tw, tx, a, s)
+         : packed  ? launch_swap<SW_ACT, true, NT, PAIR>(tw, tx, a, s)
                    : launch_swap<SW_ACT, false, NT, PAIR>(tw, tx, a, s);
 }
 
@@ -746,7 +723,7 @@ cudaError_t swap_ffn1(const uint16_t *x_sorted, const uint16_t *w13, int64_t N, 
 template <int NT>
 cudaError_t swap_ffn2(const uint16_t *h_buf, const uint16_t *w2, int64_t N, int E, int H, int I,
                       SwArgs a, cudaStream_t s) {
-  constexpr bool PAIR = use_pair(NT, false);
+  constexpr bool PAIR = use_pair(NT);
   const int tile_rows = PAIR ? 2 * SW_M : SW_M;
   CUtensorMap tw, tx;
   if (!map_3d(&tw, w2, (uint64_t)E, (uint64_t)H, (uint64_t)I, SW_M) ||
@@ -757,22 +734,26 @@ cudaError_t swap_ffn2(const uint16_t *h_buf, const uint16_t *w2, int64_t N, int 
   return launch_swap<SW_SCATTER, false, NT, PAIR>(tw, tx, a, s);
 }
 
-// Token-tile width of a contraction with f_tiles weight tiles per expert:
-// the NT that minimises waves * (cycles per K step of one tile). A tile's K
-// step reads kA weight tiles (16 KB each) and NT token rows (128 B each) from
-// shared memory at ~128 B per cycle, and issues MMAs worth ~1.45 cycles per
-// token column per weight tile: narrow tiles are bound by the shared-memory
-// reads, so more of them is not always faster. Tiles are estimated as
-// (ceil(N / NT) + min(E, N)) * f_tiles (each expert's ragged last tile).
-int pick_token_tile(int64_t N, int E, int f_tiles, bool dual) {
+// Token-tile width of a contraction with f_tiles weight tiles per expert and
+// num_kb K steps: the NT that minimises waves * (per-tile cost + num_kb *
+// cost of one K step). A K step reads a 16 KB weight tile and NT token rows
+// (128 B each; half of them per CTA of a pair) from shared memory at ~128 B
+// per cycle, and issues MMAs worth ~1.45 cycles per token column: narrow
+// tiles are bound by the shared-memory reads. A tile also costs a fixed
+// ~1450 of these units (start-up and hand-over between tiles, measured at
+// K = 512: 8 K steps took the time of ~12), so short contractions favour
+// fewer, wider tiles. Tiles are estimated as (ceil(N / NT) + min(E, N)) *
+// f_tiles (each expert's ragged last tile).
+int pick_token_tile(int64_t N, int E, int f_tiles, int num_kb) {
+  constexpr double kTileCost = 1450.0;
   const int64_t sms = device_sm_count();
-  const int kA = dual ? 2 : 1;
   int best = 32;
   double best_t = 1e300;
-  for (int nt = dual ? 128 : 256; nt >= 32; nt /= 2) {
+  for (int nt = 256; nt >= 32; nt /= 2) {
     const int64_t tiles = ((N + nt - 1) / nt + (N < E ? N : E)) * (int64_t)f_tiles;
-    const double smem = 128.0 * kA + (use_pair(nt, dual) ? nt / 2 : nt), mma = 1.45 * kA * nt;
-    const double t = (double)((tiles + sms - 1) / sms) * (smem > mma ? smem : mma);
+    const double smem = 128.0 + (use_pair(nt) ? nt / 2 : nt), mma = 1.45 * nt;
+    const double t = (double)((tiles + sms - 1) / sms) *
+                     (kTileCost + (double)num_kb * (smem > mma ? smem : mma));
     if (t < best_t) {
       best_t = t;
       best = nt;
@@ -785,19 +766,17 @@ int pick_token_tile(int64_t N, int E, int f_tiles, bool dual) {
 
 SwapPlan plan_ffn_swap(int64_t N, int E, int H, int I, const ActParams &act) {
   SwapPlan p{};
-  p.packed = act.act != MOE_ACT_RELU2 && act.layout == MOE_W13_PACKED;
-  p.f_tiles1 = (w13_rows(act, I) / (p.packed ? 2 : 1) + SW_M - 1) / SW_M;
+  p.f_tiles1 = (w13_rows(act, I) + SW_M - 1) / SW_M;
   // a handful of rows per expert (decode): 32-row token tiles for both, the
   // w13 (tile, K step) units split evenly over the grid when short
   p.nt1 = p.nt2 = SW_NGRAN;
   p.decode = N <= (int64_t)kDecodeRowsPerExpert * E;
   if (!p.decode) {
-    p.nt1 = pick_token_tile(N, E, p.f_tiles1, p.packed);
-    p.nt2 = pick_token_tile(N, E, (H + SW_M - 1) / SW_M, false);
+    p.nt1 = pick_token_tile(N, E, p.f_tiles1, H / SW_BK);
+    p.nt2 = pick_token_tile(N, E, (H + SW_M - 1) / SW_M, I / SW_BK);
   }
-  p.nt1_eff = p.packed && p.nt1 > 128 ? 128 : p.nt1;  // swap_ffn1's NT_DUAL
-  p.pair1 = !p.packed && use_pair(p.nt1_eff, false);
-  p.pair2 = use_pair(p.nt2, false);
+  p.pair1 = use_pair(p.nt1);
+  p.pair2 = use_pair(p.nt2);
   return p;
 }
 
@@ -820,7 +799,7 @@ cudaError_t launch_ffn_swap(const uint16_t *x_sorted, const int32_t *offs,
   a.ctrl = scr.ctrl;
   a.timeout_ns = kWaitTimeoutNs;
   const SwapPlan plan = plan_ffn_swap(N, E, H, I, act);
-  const int f_tiles1 = plan.f_tiles1, nt1 = plan.nt1, nt2 = plan.nt2, nt1_eff = plan.nt1_eff;
+  const int f_tiles1 = plan.f_tiles1, nt1 = plan.nt1, nt2 = plan.nt2;
   a.stream_k = plan.decode && scr.sync && scr.sk_part && device_sm_count() <= kSkMaxCtas;
   if (ev_ffn && record_stage_event(ev_ffn[0], s) != cudaSuccess) return cudaErrorUnknown;
   // the w13 kernel publishes per-expert completion; the w2 kernel waits on it
@@ -841,10 +820,10 @@ cudaError_t launch_ffn_swap(const uint16_t *x_sorted, const int32_t *offs,
   if (ev_ffn && record_stage_event(ev_ffn[1], s) != cudaSuccess) return cudaErrorUnknown;
   a.ready_out = nullptr;
   a.ready_in = ready;
-  a.ready_nt = nt1_eff;
+  a.ready_nt = nt1;
   // arrivals per token tile: every epilogue warp of every weight tile (a
   // CTA pair's tile covers 256 weight rows with both CTAs' warps)
-  a.ready_per_tile = (plan.pair1 ? (f_tiles1 + 1) / 2 * 2 : f_tiles1) * sw_epi_warps(nt1_eff);
+  a.ready_per_tile = (plan.pair1 ? (f_tiles1 + 1) / 2 * 2 : f_tiles1) * sw_epi_warps(nt1);
   a.w = w2;
   a.w_rows = H;
   a.stream_k = 0;  // whole w2 tiles: they start as soon as w13 CTAs leave SMs free

@@ -306,7 +306,7 @@ moe_status moe_ffn_plan(int64_t n, int32_t E, int32_t k, int32_t H, int32_t I,
     return MOE_OK;
   }
   const SwapPlan p = plan_ffn_swap(n * k, E, H, I, act);
-  plan[0] = p.nt1_eff;
+  plan[0] = p.nt1;
   plan[1] = p.nt2;
   plan[2] = p.pair1;
   plan[3] = p.pair2;

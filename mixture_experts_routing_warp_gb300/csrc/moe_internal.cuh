@@ -403,12 +403,12 @@ cudaError_t launch_ffn(const uint16_t *x_sorted, const int32_t *offs, const int3
                        cudaEvent_t *ev_ffn = nullptr);
 
 // Tiling of the swap-operand contractions for N rows (host only): token-tile
-// rows of each (nt1_eff: the w13 kernel's, at most 128 for the packed gated
-// layout), CTA pairs, decode tiling (32-row tiles; the w13 kernel may then
-// split its units evenly over the grid).
+// rows of each, weight tiles per expert of the w13 one, CTA pairs, decode
+// tiling (32-row tiles; the w13 kernel may then split its units evenly over
+// the grid).
 struct SwapPlan {
-  int nt1, nt2, nt1_eff, f_tiles1;
-  bool packed, decode, pair1, pair2;
+  int nt1, nt2, f_tiles1;
+  bool decode, pair1, pair2;
 };
 SwapPlan plan_ffn_swap(int64_t N, int E, int H, int I, const ActParams &act);
 

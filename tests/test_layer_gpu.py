@@ -286,7 +286,7 @@ def test_degenerate_expert_counts(E, k, ffn_kernel):
 
 
 @pytest.mark.parametrize("act,layout,Idim", [("swiglu_oai", "interleaved", 256),
-                                             ("relu2", "packed", 512), ("swiglu", "packed", 512)])
+                                             ("relu2", "packed", 512), ("swiglu", "packed", 256)])
 def test_token_tile_widths(act, layout, Idim):
     """Sizes at which the swap kernel's width choice (least waves x per-tile
     cost) lands on 64-row token tiles for both contractions: n*k = 1200 rows
@@ -302,13 +302,16 @@ def test_token_tile_widths(act, layout, Idim):
     _check_full(L)
 
 
-@pytest.mark.parametrize("act,layout", [("swiglu_oai", "interleaved"), ("relu2", "packed")])
+@pytest.mark.parametrize("act,layout", [("swiglu_oai", "interleaved"), ("relu2", "packed"),
+                                        ("swiglu", "packed")])
 def test_cta_pair_tiles(act, layout):
     """Both contractions on CTA pairs (one M = 256 MMA over two SMs): 256-row
     token tiles in two waves. 384 weight rows per expert on each side, so the
     last pair tile's second CTA holds only rows past the end (zero-filled
-    copies, skipped by the epilogue)."""
-    Idim = 192 if act == "swiglu_oai" else 384  # w13 rows: 2I or I = 384
+    copies, skipped by the epilogue). The packed gated w13 reaches the kernel
+    interleaved by its tensor map; there the past-the-end rows are gate/up
+    pairs beyond I."""
+    Idim = 384 if act == "relu2" else 192  # w13 rows: I or 2I = 384
     case = I.LayerCase(f"pairs_{act}", n=2048, H=384, E=8, k=4, I=Idim, act=act,
                        layout=layout, w_std=0.05, seed=31)
     L = Layer(case)
