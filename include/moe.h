@@ -274,6 +274,10 @@ moe_status moe_combine(const uint16_t *y_flat, int64_t n, int32_t k, int32_t H, 
 /* Stages 1-4 in one call, zero host synchronisations, CUDA-graph friendly.
  *   x [n, H] bf16, logits [n, E] fp32, w13 [E, 2I, H] bf16 ([E, I, H] for
  *   MOE_ACT_RELU2), w2 [E, H, I] bf16, out [n, H] bf16.
+ *   With n*k <= 2E slots and the swap-operand kernel, the w13 contraction
+ *   fetches its token rows from x itself (the dispatch gather fused into its
+ *   loads, "It is removable in plain PyTorch": x[tok], tok = order // k);
+ *   otherwise a gather kernel first copies them into expert-sorted order.
  *   topk_indx / topk_vals ([n, k]) and meta: optional outputs (NULL = keep
  *   them inside the workspace). When given, all five meta arrays must be
  *   non-NULL. */
@@ -338,11 +342,13 @@ moe_status moe_forward_timed(const uint16_t *x, const float *logits, const uint1
                              moe_stream stream);
 
 /* Number of kernels moe_forward (and moe_forward_timed) enqueues for these
- * sizes on the current device: route and metadata (one fused kernel when a
- * CTA's slots fit its shared memory, else two), the gather, the two expert
- * contractions and, when k > 1, the combine; 0 for n = 0; -1 for sizes
- * moe_forward rejects. Host-only: launches nothing. No counterpart on the
- * pages: lets a caller size a CUDA graph or count its launches. */
+ * sizes on the current device with the default grouped-GEMM kernel
+ * (MOE_FFN_AUTO): route and metadata (one fused kernel when a CTA's slots
+ * fit its shared memory, else two), the gather (none when n*k <= 2E: the
+ * w13 contraction gathers), the two expert contractions and, when k > 1,
+ * the combine; 0 for n = 0; -1 for sizes moe_forward rejects. Host-only:
+ * launches nothing. No counterpart on the pages: lets a caller size a CUDA
+ * graph or count its launches. */
 int32_t moe_forward_launch_count(int64_t n, int32_t E, int32_t k, int32_t H, int32_t I);
 
 /* How moe_grouped_ffn / moe_forward tile the two expert contractions for these

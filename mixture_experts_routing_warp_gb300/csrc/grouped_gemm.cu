@@ -481,11 +481,12 @@ cudaError_t launch_ffn(const uint16_t *x_sorted, const int32_t *offs, const int3
                        const uint16_t *gate_scal, const uint16_t *w13, const uint16_t *w2,
                        int64_t N, int E, int H, int I, const ActParams &act, uint16_t *h_buf,
                        uint16_t *y_flat, const FfnScratch &scr, cudaStream_t s,
-                       cudaEvent_t *ev_ffn) {
+                       cudaEvent_t *ev_ffn, const GatherSrc *gather) {
   if (N == 0) return cudaSuccess;
   if (act.ffn_kernel != MOE_FFN_TILED)  // AUTO: the swap-operand kernel at every size
     return launch_ffn_swap(x_sorted, offs, col_sorted, gate_scal, w13, w2, N, E, H, I, act, h_buf,
-                           y_flat, scr, s, ev_ffn);
+                           y_flat, scr, s, ev_ffn, gather);
+  if (gather) return cudaErrorInvalidValue;  // the tokens-on-M kernel reads x_sorted
   uint32_t *ctrl = scr.ctrl;
   const bool relu2_act = act.act == MOE_ACT_RELU2;
   const bool packed = !relu2_act && act.layout == MOE_W13_PACKED;

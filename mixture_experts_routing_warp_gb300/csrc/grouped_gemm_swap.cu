@@ -81,6 +81,7 @@ struct SwCfg {
   static_assert(NT % SW_NGRAN == 0 && NT <= 256, "token tile");
   static_assert(kStages >= 4, "pipeline depth");
   static_assert(!PAIR || NT > SW_NGRAN, "CTA pairs: wide token tiles");
+  static_assert((PAIR ? NT / 2 : NT) <= 4 * 32, "a gathering lane fetches 4 token rows");
 };
 
 struct SwArgs {
@@ -106,6 +107,12 @@ struct SwArgs {
   int ready_nt, ready_per_tile;
   const uint16_t *w;
   int w_rows;
+  // Dispatch gather fused into the token-operand loads (w13 contraction):
+  // with gather_rows set, sorted row p is token gather_rows[p] / gather_k of
+  // the unsorted tokens that tmap_x maps with one-row boxes, and the producer
+  // warp fetches each tile's rows with tile::gather4 (one lane per 4 rows).
+  const int32_t *gather_rows;
+  int gather_k;
   // Decode stream-K (NT = 32, the w13 contraction when it has fewer than two
   // waves of tiles): CTA c owns the (tile, K step) units
   // [c * U / G, (c + 1) * U / G) of U = tiles * num_kb. A tile cut by a CTA
@@ -460,68 +467,100 @@ __global__ void __launch_bounds__(SwCfg<NT, PAIR>::kThreads, 1)
 
   if (warp == 0) {
     // ------------------------------------------------------ TMA producer --
-    if (lane == 0) {
-      int stage = 0;
-      uint32_t phase = 0, issued = 0;
-      bool ok = true;
-      int ready_e = -1;  // expert whose h rows this thread has seen complete
-      WorkIter it(sk, total, num_kb, first, step);
-      Work w;
-      while (ok && it.next(w)) {
-        const Tile d = decode_tile(w.t, args.f_tiles, s_tstart, s_offs, E, NT);
-        const int f0 = d.nt * kTileRows + (int)rank * SW_M;  // first weight row of this CTA
-        // PAIR: the MMA reads its first n_mma / 2 token rows from the leader
-        // and the rest from the peer
-        const int rows = d.m_end - d.m0;
-        const int m_b = d.m0 + (int)rank * ((rows + SW_NGRAN - 1) / SW_NGRAN * SW_NGRAN / 2);
-        if (args.ready_in && d.e != ready_e) {
-          if (!wait_expert_ready(args, d.e, f0, s_offs, s_abort)) {
-            ok = false;
-            break;
-          }
-          ready_e = d.e;
-        }
-        for (int kb = w.k_lo; kb < w.k_hi; ++kb) {
-          if (!wait_bounded(empty_bar(stage), phase ^ 1u, s_abort, args.ctrl, args.timeout_ns)) {
-            ok = false;
-            break;
-          }
-          if constexpr (PAIR) {
-            // both CTAs' copies complete on the leader's full barrier
-            if (leader) mbar_arrive_expect_tx(full_bar(stage), 2 * C::kStageBytes);
-            const uint32_t fb = map_to_rank(full_bar(stage), 0);
+    // Lane 0 waits for free stages and issues the weight (and plain token)
+    // copies; with the fused gather every lane then fetches four token rows.
+    const bool gather = args.gather_rows != nullptr;
+    int stage = 0;
+    uint32_t phase = 0, issued = 0;
+    bool ok = true;
+    int ready_e = -1;  // expert whose h rows this warp has seen complete
+    WorkIter it(sk, total, num_kb, first, step);
+    Work w;
+    while (ok && it.next(w)) {
+      const Tile d = decode_tile(w.t, args.f_tiles, s_tstart, s_offs, E, NT);
+      const int f0 = d.nt * kTileRows + (int)rank * SW_M;  // first weight row of this CTA
+      // PAIR: the MMA reads its first n_mma / 2 token rows from the leader
+      // and the rest from the peer
+      const int rows = d.m_end - d.m0;
+      const int n_mma = (rows + SW_NGRAN - 1) / SW_NGRAN * SW_NGRAN;
+      const int m_b = d.m0 + (int)rank * (n_mma / 2);
+      // Token rows a CTA gathers: only the tile's own, in groups of 4 (a
+      // group's padding reads row 0). The MMA's padding rows up to n_mma keep
+      // stale data: they feed only columns the epilogue discards.
+      const int half = n_mma / 2;
+      const int n_lead = PAIR ? (rows < half ? rows : half) : rows;
+      const int n_peer = PAIR && rows > half ? rows - half : 0;
+      const int n_cta = rank ? n_peer : n_lead;
+      int g0 = 0, g1 = 0, g2 = 0, g3 = 0;  // this lane's 4 token rows
+      if (gather && 4 * lane < n_cta) {
+        const int p = m_b + 4 * lane;
+        g0 = p < d.m_end ? args.gather_rows[p] / args.gather_k : 0;
+        g1 = p + 1 < d.m_end ? args.gather_rows[p + 1] / args.gather_k : 0;
+        g2 = p + 2 < d.m_end ? args.gather_rows[p + 2] / args.gather_k : 0;
+        g3 = p + 3 < d.m_end ? args.gather_rows[p + 3] / args.gather_k : 0;
+      }
+      // stage bytes: weights, then the token rows (the gathered groups of
+      // both CTAs of a pair; a plain box always its full height)
+      const uint32_t b_bytes = gather ? 512u * (uint32_t)((n_lead + 3) / 4 + (n_peer + 3) / 4)
+                                      : (uint32_t)(PAIR ? 2 : 1) * C::kBBytes;
+      const uint32_t tx_bytes = (uint32_t)(PAIR ? 2 : 1) * SW_A_BYTES + b_bytes;
+      if (args.ready_in && d.e != ready_e) {
+        if (lane == 0) ok = wait_expert_ready(args, d.e, f0, s_offs, s_abort);
+        ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+        if (!ok) break;
+        ready_e = d.e;
+      }
+      for (int kb = w.k_lo; kb < w.k_hi; ++kb) {
+        if (lane == 0)
+          ok = wait_bounded(empty_bar(stage), phase ^ 1u, s_abort, args.ctrl, args.timeout_ns);
+        ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+        if (!ok) break;
+        if constexpr (PAIR) {
+          // both CTAs' copies complete on the leader's full barrier
+          const uint32_t fb = map_to_rank(full_bar(stage), 0);
+          if (lane == 0) {
+            if (leader) mbar_arrive_expect_tx(full_bar(stage), tx_bytes);
             if constexpr (PACKED)
               tma_load_4d_pair(a_addr(stage), &tmap_w, fb, kb * SW_BK, 0, f0 / 2, d.e);
             else
               tma_load_3d_pair(a_addr(stage), &tmap_w, fb, kb * SW_BK, f0, d.e);
-            tma_load_2d_pair(b_addr(stage), &tmap_x, fb, kb * SW_BK, m_b);
-          } else {
-            mbar_arrive_expect_tx(full_bar(stage), C::kStageBytes);
+            if (!gather) tma_load_2d_pair(b_addr(stage), &tmap_x, fb, kb * SW_BK, m_b);
+          }
+          __syncwarp();
+          if (gather && 4 * lane < n_cta)
+            tma_gather4_pair(b_addr(stage) + 512u * lane, &tmap_x, fb, kb * SW_BK, g0, g1, g2, g3);
+        } else {
+          if (lane == 0) {
+            mbar_arrive_expect_tx(full_bar(stage), tx_bytes);
             if constexpr (PACKED)
               tma_load_4d(a_addr(stage), &tmap_w, full_bar(stage), kb * SW_BK, 0, f0 / 2, d.e);
             else
               tma_load_3d(a_addr(stage), &tmap_w, full_bar(stage), kb * SW_BK, f0, d.e);
-            tma_load_2d(b_addr(stage), &tmap_x, full_bar(stage), kb * SW_BK, d.m0);
+            if (!gather) tma_load_2d(b_addr(stage), &tmap_x, full_bar(stage), kb * SW_BK, d.m0);
           }
-          issued = issued < (uint32_t)C::kStages ? issued + 1 : (uint32_t)C::kStages;
-          if (++stage == C::kStages) {
-            stage = 0;
-            phase ^= 1u;
-          }
+          __syncwarp();  // the expected bytes are posted before any gathered row lands
+          if (gather && 4 * lane < n_cta)
+            tma_gather4(b_addr(stage) + 512u * lane, &tmap_x, full_bar(stage), kb * SW_BK, g0, g1,
+                        g2, g3);
+        }
+        issued = issued < (uint32_t)C::kStages ? issued + 1 : (uint32_t)C::kStages;
+        if (++stage == C::kStages) {
+          stage = 0;
+          phase ^= 1u;
         }
       }
-      // a pair's copies complete on the leader's barriers: the leader drains
-      // (the peer stays resident until the final cluster barrier)
-      if (!ok && leader) {
-        for (uint32_t i = 0; i < issued; ++i) {
-          int s = stage - 1 - (int)i;
-          uint32_t ph = phase;
-          if (s < 0) {
-            s += C::kStages;
-            ph ^= 1u;
-          }
-          wait_drain(full_bar(s), ph, 100000000ull);
+    }
+    // a pair's copies complete on the leader's barriers: the leader drains
+    // (the peer stays resident until the final cluster barrier)
+    if (!ok && leader && lane == 0) {
+      for (uint32_t i = 0; i < issued; ++i) {
+        int s = stage - 1 - (int)i;
+        uint32_t ph = phase;
+        if (s < 0) {
+          s += C::kStages;
+          ph ^= 1u;
         }
+        wait_drain(full_bar(s), ph, 100000000ull);
       }
     }
   } else if (warp == 1) {
@@ -699,9 +738,11 @@ constexpr bool use_pair(int nt) { return nt == 256; }
 
 // The w13 contraction at token-tile width NT. A packed gated w13 goes
 // through the interleaving 4-D map: the kernel sees the interleaved layout.
+// With `gather` the token rows come from the unsorted x (one-row boxes).
 template <int NT>
 cudaError_t swap_ffn1(const uint16_t *x_sorted, const uint16_t *w13, int64_t N, int E, int H,
-                      int I, const ActParams &act, SwArgs a, cudaStream_t s) {
+                      int I, const ActParams &act, SwArgs a, cudaStream_t s,
+                      const GatherSrc *gather) {
   const bool relu2_act = act.act == MOE_ACT_RELU2;
   const bool packed = !relu2_act && act.layout == MOE_W13_PACKED;
   constexpr bool PAIR = use_pair(NT);
@@ -710,8 +751,13 @@ cudaError_t swap_ffn1(const uint16_t *x_sorted, const uint16_t *w13, int64_t N, 
   const bool w_ok =
       packed ? map_w13_packed_interleaved(&tw, w13, (uint64_t)E, (uint64_t)I, (uint64_t)H, SW_M / 2)
              : map_3d(&tw, w13, (uint64_t)E, (uint64_t)w13_rows(act, I), (uint64_t)H, SW_M);
-  if (!w_ok || !map_2d(&tx, x_sorted, (uint64_t)N, (uint64_t)H, PAIR ? NT / 2 : NT))
-    return cudaErrorInvalidValue;
+  const bool x_ok = gather ? map_2d_rows(&tx, gather->x, (uint64_t)gather->n, (uint64_t)H)
+                           : map_2d(&tx, x_sorted, (uint64_t)N, (uint64_t)H, PAIR ? NT / 2 : NT);
+  if (!w_ok || !x_ok) return cudaErrorInvalidValue;
+  if (gather) {
+    a.gather_rows = a.col_sorted;
+    a.gather_k = gather->k;
+  }
   a.num_kb = H / SW_BK;
   a.f_tiles = (w13_rows(act, I) + tile_rows - 1) / tile_rows;
   return relu2_act ? launch_swap<SW_RELU2, false, NT, PAIR>(tw, tx, a, s)
@@ -784,7 +830,8 @@ cudaError_t launch_ffn_swap(const uint16_t *x_sorted, const int32_t *offs,
                             const int32_t *col_sorted, const uint16_t *gate_scal,
                             const uint16_t *w13, const uint16_t *w2, int64_t N, int E, int H,
                             int I, const ActParams &act, uint16_t *h_buf, uint16_t *y_flat,
-                            const FfnScratch &scr, cudaStream_t s, cudaEvent_t *ev_ffn) {
+                            const FfnScratch &scr, cudaStream_t s, cudaEvent_t *ev_ffn,
+                            const GatherSrc *gather) {
   if (N == 0) return cudaSuccess;
   SwArgs a{};
   a.offs = offs;
@@ -811,10 +858,10 @@ cudaError_t launch_ffn_swap(const uint16_t *x_sorted, const int32_t *offs,
   }
   cudaError_t err;
   switch (nt1) {
-    case 32: err = swap_ffn1<32>(x_sorted, w13, N, E, H, I, act, a, s); break;
-    case 64: err = swap_ffn1<64>(x_sorted, w13, N, E, H, I, act, a, s); break;
-    case 128: err = swap_ffn1<128>(x_sorted, w13, N, E, H, I, act, a, s); break;
-    default: err = swap_ffn1<256>(x_sorted, w13, N, E, H, I, act, a, s); break;
+    case 32: err = swap_ffn1<32>(x_sorted, w13, N, E, H, I, act, a, s, gather); break;
+    case 64: err = swap_ffn1<64>(x_sorted, w13, N, E, H, I, act, a, s, gather); break;
+    case 128: err = swap_ffn1<128>(x_sorted, w13, N, E, H, I, act, a, s, gather); break;
+    default: err = swap_ffn1<256>(x_sorted, w13, N, E, H, I, act, a, s, gather); break;
   }
   if (err != cudaSuccess) return err;
   if (ev_ffn && record_stage_event(ev_ffn[1], s) != cudaSuccess) return cudaErrorUnknown;

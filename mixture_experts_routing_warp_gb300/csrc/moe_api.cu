@@ -64,6 +64,15 @@ moe_status resolve_params(const moe_params *p, ActParams &out, int *gating) {
   return MOE_OK;
 }
 
+// True when moe_forward's w13 contraction gathers its own token rows (no
+// gather kernel): the swap-operand kernel with at most 2 slots per expert on
+// average, where a tile's rows take one tile::gather4 per K step. Measured on
+// GPT-OSS decode (32 experts, top-4): 1 token 53.7 -> 52.1 us, 8 tokens equal,
+// 64 tokens (~8 rows per expert) 254 -> 256 us.
+static bool fused_gather_rows(int64_t n, int32_t E, int32_t k, int ffn_kernel) {
+  return ffn_kernel != MOE_FFN_TILED && n * k <= 2 * (int64_t)E;
+}
+
 // The per-slot arrays may be NULL when there are no slots (n = 0).
 moe_status check_meta(const moe_routing_meta *m, int64_t n) {
   if (!m || !m->col_sum || !m->offs) return MOE_ERR_INVALID_ARG;
@@ -264,12 +273,12 @@ static moe_status forward_impl(const uint16_t *x, const float *logits, const uin
         launch_route_gemm(x, w_gate, n, E, H, k, gating, indx, vals, nullptr, ctrl, s) !=
             cudaSuccess ||
         mark(MOE_STAGE_METADATA) != cudaSuccess ||
-        launch_metadata(indx, vals, n, E, k, m, hist, ctrl, s) != cudaSuccess)
+        launch_metadata(indx, vals, n, E, k, m, hist, ctrl, s, scr.sync) != cudaSuccess)
       return MOE_ERR_CUDA;
   } else if (route_metadata_fits(n, k)) {
     // one cooperative kernel for both stages; the metadata stage time is 0
     if (mark(MOE_STAGE_ROUTE) != cudaSuccess ||
-        launch_route_metadata(logits, n, E, k, gating, indx, vals, m, hist, ctrl, s) !=
+        launch_route_metadata(logits, n, E, k, gating, indx, vals, m, hist, ctrl, s, scr.sync) !=
             cudaSuccess ||
         mark(MOE_STAGE_METADATA) != cudaSuccess)
       return MOE_ERR_CUDA;
@@ -278,14 +287,23 @@ static moe_status forward_impl(const uint16_t *x, const float *logits, const uin
         launch_route(logits, n, E, k, gating, indx, vals, ctrl, s) != cudaSuccess)
       return MOE_ERR_CUDA;
     if (mark(MOE_STAGE_METADATA) != cudaSuccess ||
-        launch_metadata(indx, vals, n, E, k, m, hist, ctrl, s) != cudaSuccess)
+        launch_metadata(indx, vals, n, E, k, m, hist, ctrl, s, scr.sync) != cudaSuccess)
       return MOE_ERR_CUDA;
   }
+  // A row or two per expert: the swap-operand kernel gathers its token rows
+  // from x itself (tile::gather4, one instruction per 4 rows). Otherwise they
+  // come from X_sorted, materialised by the gather kernel: a gather4 costs
+  // about as much TMA time as a whole 2-D box, so 128 rows per K step as 32
+  // gathers ran w13 3.4x slower at prefill.
+  const bool fused_gather = fused_gather_rows(n, E, k, act.ffn_kernel);
+  const GatherSrc src{x, n, k};
   if (mark(MOE_STAGE_GATHER) != cudaSuccess ||
-      launch_gather_rows(x, m.row_sorted, n, k, H, x_sorted, scr.sync, s) != cudaSuccess)
+      (!fused_gather &&
+       launch_gather_rows(x, m.row_sorted, n, k, H, x_sorted, scr.sync, s) != cudaSuccess))
     return MOE_ERR_CUDA;
   if (launch_ffn(x_sorted, m.offs, m.col_sorted, m.gate_scal, w13, w2, N, E, H, I, act, h, y_flat,
-                 scr, s, ev ? ev + MOE_STAGE_FFN1 : nullptr) != cudaSuccess)
+                 scr, s, ev ? ev + MOE_STAGE_FFN1 : nullptr,
+                 fused_gather ? &src : nullptr) != cudaSuccess)
     return MOE_ERR_CUDA;
   if (mark(MOE_STAGE_COMBINE) != cudaSuccess) return MOE_ERR_CUDA;
   if (k > 1 && launch_combine(y_flat, n, k, H, out, s) != cudaSuccess) return MOE_ERR_CUDA;
@@ -317,8 +335,10 @@ moe_status moe_ffn_plan(int64_t n, int32_t E, int32_t k, int32_t H, int32_t I,
 int32_t moe_forward_launch_count(int64_t n, int32_t E, int32_t k, int32_t H, int32_t I) {
   if (check_sizes(n, E, k, H, I, true) != MOE_OK) return -1;
   if (n == 0) return 0;
-  // the same choice forward_impl makes, then gather, ffn1, ffn2, combine
-  return (route_metadata_fits(n, k) ? 1 : 2) + 3 + (k > 1 ? 1 : 0);
+  // the same choices forward_impl makes (default kernel: the swap-operand
+  // one), then the gather unless w13 gathers its rows, ffn1, ffn2, combine
+  return (route_metadata_fits(n, k) ? 1 : 2) + (fused_gather_rows(n, E, k, MOE_FFN_AUTO) ? 0 : 1) +
+         2 + (k > 1 ? 1 : 0);
 }
 
 moe_status moe_forward(const uint16_t *x, const float *logits, const uint16_t *w13,

@@ -382,11 +382,13 @@ bool route_metadata_fits(int64_t n, int k);
 cudaError_t launch_route_metadata(const float *logits, int64_t n, int E, int k, int gating,
                                   int32_t *topk_indx, uint16_t *topk_vals,
                                   const moe_routing_meta &meta, int32_t *ws_hist,
-                                  uint32_t *ctrl, cudaStream_t s);
+                                  uint32_t *ctrl, cudaStream_t s, uint32_t *sync = nullptr);
 
+// sync (may be null): the kSyncWords per-forward sync words of the expert
+// contractions, zeroed by these kernels (and by the gather)
 cudaError_t launch_metadata(const int32_t *topk_indx, const uint16_t *topk_vals, int64_t n, int E,
                             int k, const moe_routing_meta &meta, int32_t *ws_hist,
-                            uint32_t *ctrl, cudaStream_t s);
+                            uint32_t *ctrl, cudaStream_t s, uint32_t *sync = nullptr);
 
 // X_sorted[row_sorted[t*k + j]] = x[t] for the n tokens' k slots.
 // sync (may be null): the kSyncWords sync words the gather zeroes
@@ -396,11 +398,22 @@ cudaError_t launch_gather_rows(const uint16_t *x, const int32_t *row_sorted, int
 cudaError_t launch_combine(const uint16_t *y_flat, int64_t n, int k, int H, uint16_t *out,
                            cudaStream_t s);
 
+// The unsorted tokens x [n, H] and k, for the w13 contraction's fused
+// dispatch gather: sorted row p is x[col_sorted[p] / k].
+struct GatherSrc {
+  const uint16_t *x;
+  int64_t n;
+  int k;
+};
+
+// The two expert contractions. The w13 one reads its token rows from
+// x_sorted, or, with `gather` (swap-operand kernel only), straight from the
+// unsorted tokens.
 cudaError_t launch_ffn(const uint16_t *x_sorted, const int32_t *offs, const int32_t *col_sorted,
                        const uint16_t *gate_scal, const uint16_t *w13, const uint16_t *w2,
                        int64_t N, int E, int H, int I, const ActParams &act, uint16_t *h_buf,
                        uint16_t *y_flat, const FfnScratch &scr, cudaStream_t s,
-                       cudaEvent_t *ev_ffn = nullptr);
+                       cudaEvent_t *ev_ffn = nullptr, const GatherSrc *gather = nullptr);
 
 // Tiling of the swap-operand contractions for N rows (host only): token-tile
 // rows of each, weight tiles per expert of the w13 one, CTA pairs, decode
@@ -419,7 +432,8 @@ cudaError_t launch_ffn_swap(const uint16_t *x_sorted, const int32_t *offs,
                             const int32_t *col_sorted, const uint16_t *gate_scal,
                             const uint16_t *w13, const uint16_t *w2, int64_t N, int E, int H,
                             int I, const ActParams &act, uint16_t *h_buf, uint16_t *y_flat,
-                            const FfnScratch &scr, cudaStream_t s, cudaEvent_t *ev_ffn);
+                            const FfnScratch &scr, cudaStream_t s, cudaEvent_t *ev_ffn,
+                            const GatherSrc *gather);
 
 // Router matmul fused with the top-k (the tokens-on-M GEMM, EPI_ROUTE).
 cudaError_t launch_route_gemm(const uint16_t *x, const uint16_t *w_gate, int64_t n, int E, int H,

@@ -83,11 +83,12 @@ __global__ void __launch_bounds__(kMetaThreads) metadata_kernel(
     int chunk, int32_t *__restrict__ col_sum, int32_t *__restrict__ offs,
     int32_t *__restrict__ col_sorted, int32_t *__restrict__ row_sorted,
     uint16_t *__restrict__ gate_scal, int32_t *__restrict__ ws_hist, uint32_t *ctrl,
-    unsigned long long timeout_ns) {
+    unsigned long long timeout_ns, uint32_t *sync) {
   __shared__ MetaShared<kMetaThreads> sh;
   const int tid = threadIdx.x;
   const int b = blockIdx.x;
-  pdl_launch_dependents();  // the gather may be scheduled (it waits for this grid)
+  pdl_launch_dependents();  // the next kernel may be scheduled (it waits for this grid)
+  zero_sync_words(sync);
   const int lo = (int)min((int64_t)N, (int64_t)b * chunk);
   const int hi = (int)min((int64_t)N, (int64_t)lo + chunk);
 
@@ -127,7 +128,8 @@ int metadata_ctas_per_sm() {
 
 cudaError_t launch_metadata_kernel(const int32_t *topk_indx, const uint16_t *topk_vals, int N,
                                    int E, const moe_routing_meta &meta, int32_t *ws_hist,
-                                   uint32_t *ctrl, int max_ctas, cudaStream_t s) {
+                                   uint32_t *ctrl, int max_ctas, cudaStream_t s,
+                                   uint32_t *sync = nullptr) {
   static bool configured = false;
   if (!configured) {
     cudaError_t err = uniform_carveout(metadata_kernel);
@@ -145,7 +147,7 @@ cudaError_t launch_metadata_kernel(const int32_t *topk_indx, const uint16_t *top
   void *args[] = {(void *)&topk_indx, (void *)&topk_vals, (void *)&N, (void *)&E,
                   (void *)&chunk, (void *)&meta.col_sum, (void *)&meta.offs,
                   (void *)&meta.col_sorted, (void *)&meta.row_sorted, (void *)&meta.gate_scal,
-                  (void *)&ws_hist, (void *)&ctrl, (void *)&timeout};
+                  (void *)&ws_hist, (void *)&ctrl, (void *)&timeout, (void *)&sync};
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)B);
   cfg.blockDim = dim3(kMetaThreads);
@@ -162,9 +164,9 @@ cudaError_t launch_metadata_kernel(const int32_t *topk_indx, const uint16_t *top
 
 cudaError_t launch_metadata(const int32_t *topk_indx, const uint16_t *topk_vals, int64_t n, int E,
                             int k, const moe_routing_meta &meta, int32_t *ws_hist,
-                            uint32_t *ctrl, cudaStream_t s) {
+                            uint32_t *ctrl, cudaStream_t s, uint32_t *sync) {
   return launch_metadata_kernel(topk_indx, topk_vals, (int)(n * k), E, meta, ws_hist, ctrl,
-                                kMetaMaxCtas, s);
+                                kMetaMaxCtas, s, sync);
 }
 
 // ======================================== metadata without a workspace ==

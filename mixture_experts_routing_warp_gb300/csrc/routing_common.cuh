@@ -28,6 +28,16 @@ namespace moe {
 // softmax in fp32 over the K selected (or over all E), rounded to bf16.
 
 constexpr int kRouteThreads = 256;
+
+// The kernels that build the routing metadata also zero the per-forward sync
+// words of the expert contractions (block 0; `sync` may be null): the w13
+// contraction reads them only after these grids have completed
+// (griddepcontrol.wait), and the previous forward's contractions have
+// completed before these grids start (they are not dependent launches).
+__device__ __forceinline__ void zero_sync_words(uint32_t *sync) {
+  if (sync && blockIdx.x == 0)
+    for (int i = threadIdx.x; i < kSyncWords; i += blockDim.x) sync[i] = 0;
+}
 constexpr int kFusedThreads = 1024;
 constexpr int kSlotCap = 8192;  // slots a fused CTA keeps in shared memory
 
@@ -421,6 +431,7 @@ __device__ void meta_scatter(int64_t f_lo, int count, int E, MetaShared<THREADS>
 constexpr int kSmallSlots = 32;
 cudaError_t launch_route_metadata_small(const float *logits, int n, int E, int k, int gating,
                                         int32_t *topk_indx, uint16_t *topk_vals,
-                                        const moe_routing_meta &meta, cudaStream_t s);
+                                        const moe_routing_meta &meta, uint32_t *sync,
+                                        cudaStream_t s);
 
 }  // namespace moe

@@ -19,14 +19,16 @@ __global__ void __launch_bounds__(kFusedThreads, 1) route_metadata_kernel(
     int32_t *__restrict__ topk_indx, uint16_t *__restrict__ topk_vals,
     int32_t *__restrict__ col_sum, int32_t *__restrict__ offs, int32_t *__restrict__ col_sorted,
     int32_t *__restrict__ row_sorted, uint16_t *__restrict__ gate_scal,
-    int32_t *__restrict__ ws_hist, uint32_t *ctrl, unsigned long long timeout_ns) {
+    int32_t *__restrict__ ws_hist, uint32_t *ctrl, unsigned long long timeout_ns,
+    uint32_t *sync) {
   extern __shared__ uint8_t smem_raw[];
   __shared__ MetaShared<kFusedThreads> sh;
   uint8_t *s_slot_e = smem_raw;
   uint16_t *s_slot_v = reinterpret_cast<uint16_t *>(smem_raw + (((size_t)T * K + 15) & ~15ull));
 
   const int tid = threadIdx.x;
-  pdl_launch_dependents();  // the gather may be scheduled (it waits for this grid)
+  pdl_launch_dependents();  // the next kernel may be scheduled (it waits for this grid)
+  zero_sync_words(sync);
   for (int e = tid; e < E; e += kFusedThreads) sh.base[e] = 0;
   __syncthreads();
 
@@ -81,6 +83,7 @@ struct RouteMetaLaunch {
   const moe_routing_meta *meta;
   int32_t *ws_hist;
   uint32_t *ctrl;
+  uint32_t *sync;
   cudaStream_t s;
   template <int K, int G, int NQ>
   cudaError_t go() {
@@ -108,7 +111,7 @@ struct RouteMetaLaunch {
                     (void *)&vec4, (void *)&indx, (void *)&vals, (void *)&meta->col_sum, (void *)&meta->offs,
                     (void *)&meta->col_sorted, (void *)&meta->row_sorted,
                     (void *)&meta->gate_scal, (void *)&ws_hist, (void *)&ctrl,
-                    (void *)&timeout};
+                    (void *)&timeout, (void *)&sync};
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)B);
     cfg.blockDim = dim3(kFusedThreads);
@@ -134,13 +137,13 @@ bool route_metadata_fits(int64_t n, int k) {
 cudaError_t launch_route_metadata(const float *logits, int64_t n, int E, int k, int gating,
                                   int32_t *topk_indx, uint16_t *topk_vals,
                                   const moe_routing_meta &meta, int32_t *ws_hist,
-                                  uint32_t *ctrl, cudaStream_t s) {
+                                  uint32_t *ctrl, cudaStream_t s, uint32_t *sync) {
   // every G (<= 8) lanes take a token: n <= 32 tokens fit one 256-thread CTA
   if (n * k <= kSmallSlots)
     return launch_route_metadata_small(logits, (int)n, E, k, gating, topk_indx, topk_vals, meta,
-                                       s);
+                                       sync, s);
   return dispatch_kg(k, E, RouteMetaLaunch{logits, n, E, gating, topk_indx, topk_vals, &meta,
-                                           ws_hist, ctrl, s});
+                                           ws_hist, ctrl, sync, s});
 }
 
 }  // namespace moe

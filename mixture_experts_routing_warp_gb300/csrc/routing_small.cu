@@ -20,12 +20,13 @@ __global__ void __launch_bounds__(kSmallThreads) route_metadata_small_kernel(
     const float *__restrict__ logits, int n, int E, int gating, int vec4,
     int32_t *__restrict__ topk_indx, uint16_t *__restrict__ topk_vals,
     int32_t *__restrict__ col_sum, int32_t *__restrict__ offs, int32_t *__restrict__ col_sorted,
-    int32_t *__restrict__ row_sorted, uint16_t *__restrict__ gate_scal) {
+    int32_t *__restrict__ row_sorted, uint16_t *__restrict__ gate_scal, uint32_t *sync) {
   __shared__ int s_cnt[kMaxExperts];
   __shared__ int s_e[kSmallSlots];
   __shared__ uint16_t s_w[kSmallSlots];
   const int tid = threadIdx.x, lane = tid & 31;
-  pdl_launch_dependents();  // the gather may be scheduled (it waits for this grid)
+  pdl_launch_dependents();  // the next kernel may be scheduled (it waits for this grid)
+  zero_sync_words(sync);
   for (int e = tid; e < E; e += kSmallThreads) s_cnt[e] = 0;
   __syncthreads();
   {
@@ -88,6 +89,7 @@ struct RouteMetaSmallLaunch {
   int32_t *indx;
   uint16_t *vals;
   const moe_routing_meta *meta;
+  uint32_t *sync;
   cudaStream_t s;
   template <int K, int G, int NQ>
   cudaError_t go() {
@@ -101,16 +103,17 @@ struct RouteMetaSmallLaunch {
     const int vec4 = (E % 4) == 0 && ((uintptr_t)logits % 16) == 0;
     kern<<<1, kSmallThreads, 0, s>>>(logits, n, E, gating, vec4, indx, vals, meta->col_sum,
                                       meta->offs, meta->col_sorted, meta->row_sorted,
-                                      meta->gate_scal);
+                                      meta->gate_scal, sync);
     return cudaGetLastError();
   }
 };
 
 cudaError_t launch_route_metadata_small(const float *logits, int n, int E, int k, int gating,
                                         int32_t *topk_indx, uint16_t *topk_vals,
-                                        const moe_routing_meta &meta, cudaStream_t s) {
+                                        const moe_routing_meta &meta, uint32_t *sync,
+                                        cudaStream_t s) {
   return dispatch_kg(k, E, RouteMetaSmallLaunch{logits, n, E, gating, topk_indx, topk_vals,
-                                                &meta, s});
+                                                &meta, sync, s});
 }
 
 }  // namespace moe

@@ -228,6 +228,34 @@ def test_stages_compose_to_forward(act, layout):
     assert_layer_close(host_bits(out), ref_out, "out")
 
 
+@pytest.mark.parametrize("n,E,k,H,I_,act,layout", [
+    (3, 32, 4, 256, 128, "swiglu_oai", "interleaved"),   # ~1 row per tile, stream-K w13
+    (16, 32, 4, 256, 128, "swiglu", "packed"),           # n*k = 2 E
+    (5, 5, 2, 128, 192, "swiglu_oai", "interleaved"),    # ragged groups of 4 rows
+    (16, 8, 1, 128, 256, "relu2", "packed"),             # k = 1: w2 writes the output
+])
+def test_fused_gather_matches_materialised_rows(n, E, k, H, I_, act, layout):
+    """With at most 2 slots per expert, moe_forward's w13 contraction fetches
+    each tile's token rows from x (tile::gather4 of rows col_sorted[p] / k,
+    only the tile's own rows); the stage path reads the rows the gather
+    kernel materialised in X_sorted. Same arithmetic on the same rows: the
+    outputs agree bit for bit. The forward launches no gather kernel there."""
+    assert moe.ffn_plan(n, E, k, H, I_, moe.make_params())["decode"]
+    assert moe.forward_launch_count(n, E, k, H, I_) == 3 + (k > 1)
+    case = I.LayerCase(f"fused_gather_n{n}", n=n, H=H, E=E, k=k, I=I_, act=act, layout=layout,
+                       w_std=0.05, seed=n + E)
+    L = Layer(case)
+    out_fwd = L.forward()[0]
+    ws = moe.workspace(case.n, case.E, case.k, case.H, case.I)
+    indx, vals = moe.route(L.logits, case.k, case.gating)
+    meta = moe.build_metadata(indx, vals, case.E, ws)
+    y_flat = moe.grouped_ffn(L.x, meta, L.w13, L.w2, case.k, ws, L.params)
+    out = y_flat if k == 1 else moe.combine(y_flat, case.n, case.k)
+    torch.cuda.synchronize()
+    assert torch.equal(out.view(torch.int16), out_fwd.view(torch.int16))
+    _check_full(L)
+
+
 def test_empty_batch_is_a_noop():
     c = I.TINY
     L = Layer(c)
