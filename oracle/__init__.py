@@ -18,6 +18,10 @@ Functions, each following the pages (page title, section):
                issue, Summary; activations and w13 layouts of "CuteDSL NVFP4 MoE
                adds SwiGLU-OAI and ReLU2", 关键源码片段 and 评论区精华).
   forward   -- route -> metadata -> ffn.
+  metadata and ffn take an optional expert map (expert parallelism: the
+  rank's local id of each global expert, -1 for another rank's), under which
+  slots of other ranks' experts are dropped; first report, 功能与动机 and
+  风险与影响 (the -1 slots of an expert-parallel routing).
 
 Pinning: `tests/test_oracle_*.py` check these against brute force on tiny
 inputs, library routines (numpy stable argsort, bincount, argmax, float64
@@ -61,9 +65,9 @@ def lib() -> ctypes.CDLL:
         p = ctypes.c_void_p
         i64, i32 = ctypes.c_int64, ctypes.c_int
         L.orc_route.argtypes = [p, i64, i32, i32, i32, p, p]
-        L.orc_metadata.argtypes = [p, p, i64, i32, i32, p, p, p, p, p]
+        L.orc_metadata.argtypes = [p, p, i64, i32, i32, p, i32, p, p, p, p, p]
         L.orc_expert_row.argtypes = [p, p, p, i32, i32, ctypes.POINTER(_ActParams), p, p, p]
-        L.orc_ffn.argtypes = [p, p, p, p, p, i64, i32, i32, i32, i32,
+        L.orc_ffn.argtypes = [p, p, p, p, p, i64, i32, i32, i32, i32, p, i32,
                               ctypes.POINTER(_ActParams), p, i64, p, p, p]
         L.orc_router_logits.argtypes = [p, p, i64, i32, i32, p]
         L.orc_router_logits.restype = ctypes.c_int
@@ -145,21 +149,38 @@ def route(logits: np.ndarray, k: int, gating: str = "softmax_topk"):
     return indx, vals
 
 
-def metadata(topk_indx: np.ndarray, topk_vals: np.ndarray, E: int) -> dict:
+def _expert_map(expert_map, E: int, n_local: Optional[int]):
+    if expert_map is None:
+        return None, E
+    m = _c(expert_map, np.int32)
+    assert m.shape == (E,) and n_local is not None
+    return m, int(n_local)
+
+
+def metadata(topk_indx: np.ndarray, topk_vals: np.ndarray, E: int, expert_map=None,
+             n_local: Optional[int] = None) -> dict:
     """-> dict(col_sum [E], offs [E+1], col_sorted [n*k], row_sorted [n*k],
-    gate_scal [n*k] bf16 bits, gather_src, gather_dst, scatter_src, scatter_dst)."""
+    gate_scal [n*k] bf16 bits, gather_src, gather_dst, scatter_src, scatter_dst).
+
+    expert_map [E] (expert parallelism): local id in [0, n_local) of each
+    global expert, or -1 (expert on another rank). Then col_sum / offs cover
+    the n_local local experts, col_sorted / gate_scal hold the offs[-1] kept
+    slots, and row_sorted is -1 at dropped slots."""
     indx = _c(topk_indx, np.int32)
     vals = _c(topk_vals, np.uint16)
     n, k = indx.shape
     N = n * k
-    col_sum = np.empty(E, dtype=np.int32)
-    offs = np.empty(E + 1, dtype=np.int32)
+    emap, E_loc = _expert_map(expert_map, E, n_local)
+    col_sum = np.empty(E_loc, dtype=np.int32)
+    offs = np.empty(E_loc + 1, dtype=np.int32)
     col_sorted = np.empty(N, dtype=np.int32)
     row_sorted = np.empty(N, dtype=np.int32)
     gate_scal = np.empty(N, dtype=np.uint16)
-    rc = lib().orc_metadata(_ptr(indx), _ptr(vals), n, E, k, _ptr(col_sum), _ptr(offs),
-                            _ptr(col_sorted), _ptr(row_sorted), _ptr(gate_scal))
+    rc = lib().orc_metadata(_ptr(indx), _ptr(vals), n, E, k, _ptr(emap), E_loc, _ptr(col_sum),
+                            _ptr(offs), _ptr(col_sorted), _ptr(row_sorted), _ptr(gate_scal))
     _check(rc, "metadata")
+    kept = int(offs[-1])
+    col_sorted, gate_scal = col_sorted[:kept], gate_scal[:kept]
     return {"col_sum": col_sum, "offs": offs, "col_sorted": col_sorted,
             "row_sorted": row_sorted, "gate_scal": gate_scal,
             # GatherIndx(src=combine_indx, dst=dispatch_indx),
@@ -189,11 +210,14 @@ def expert_row(x_row: np.ndarray, w13_e: np.ndarray, w2_e: np.ndarray, **act_kw)
 
 def ffn(x: np.ndarray, topk_indx: np.ndarray, topk_vals: np.ndarray, w13: np.ndarray,
         w2: np.ndarray, tokens: Optional[np.ndarray] = None, want_slots: bool = False,
-        **act_kw):
+        expert_map=None, n_experts: Optional[int] = None, **act_kw):
     """Gate-weighted per-expert FFN + combine.
 
     x [n, H] bf16 bits; w13 [E, 2I, H] (ReLU2: [E, I, H]), w2 [E, H, I] bf16 bits.
     tokens: optional token ids to compute (rows of the result follow it).
+    expert_map [n_experts] (expert parallelism): w13 / w2 then hold the local
+    experts, slot j uses local expert expert_map[topk_indx[t, j]], and slots
+    mapped to -1 add nothing (zero y_slot / h_slot entries).
     Returns out bf16 bits [n_sel, H]; with want_slots also
     y_slot float64 [n_sel, k, H] (gate-weighted, slot order) and
     h_slot bf16 bits [n_sel, k, I]."""
@@ -203,10 +227,12 @@ def ffn(x: np.ndarray, topk_indx: np.ndarray, topk_vals: np.ndarray, w13: np.nda
     w13 = _c(w13, np.uint16)
     w2 = _c(w2, np.uint16)
     n, H = x.shape
-    E, rows, H2 = w13.shape
+    E_loc, rows, H2 = w13.shape
     I = rows if act_kw.get("act") == "relu2" else rows // 2
     k = indx.shape[1]
-    assert H2 == H and w2.shape == (E, H, I) and indx.shape == (n, k) == vals.shape
+    assert H2 == H and w2.shape == (E_loc, H, I) and indx.shape == (n, k) == vals.shape
+    E = E_loc if expert_map is None else int(n_experts)
+    emap, E_loc = _expert_map(expert_map, E, E_loc)
     toks = None if tokens is None else _c(tokens, np.int64)
     n_sel = n if toks is None else toks.size
     out = np.empty((n_sel, H), dtype=np.uint16)
@@ -214,8 +240,8 @@ def ffn(x: np.ndarray, topk_indx: np.ndarray, topk_vals: np.ndarray, w13: np.nda
     h_slot = np.empty((n_sel, k, I), dtype=np.uint16) if want_slots else None
     prm = act_params(**act_kw)
     rc = lib().orc_ffn(_ptr(x), _ptr(indx), _ptr(vals), _ptr(w13), _ptr(w2), n, E, k, H, I,
-                       ctypes.byref(prm), _ptr(toks), n_sel, _ptr(out), _ptr(y_slot),
-                       _ptr(h_slot))
+                       _ptr(emap), E_loc, ctypes.byref(prm), _ptr(toks), n_sel, _ptr(out),
+                       _ptr(y_slot), _ptr(h_slot))
     _check(rc, "ffn")
     if want_slots:
         return out, y_slot, h_slot

@@ -142,8 +142,21 @@ int orc_route(const float *logits, int64_t n, int E, int k, int gating,
   return ORC_OK;
 }
 
+/* Expert map (expert parallelism; [R1] 功能与动机 and 风险与影响: the
+ * routing of a rank that holds a subset of the experts, where a slot whose
+ * expert lives elsewhere is marked -1): expert_map[e] is the local id in
+ * [0, E_loc) of global expert e, or -1. A slot f keeps local expert
+ * map[indx[f]]; a -1 slot is dropped (it is listed nowhere and contributes
+ * nothing to this rank's output). expert_map = NULL: the identity, E_loc = E.
+ * Returns the local id of slot f, -1 if dropped, -2 for an invalid map entry. */
+static int orc_local(const int32_t *expert_map, int E_loc, int32_t e) {
+  if (!expert_map) return e;
+  int32_t v = expert_map[e];
+  return (v >= -1 && v < E_loc) ? v : -2;
+}
+
 /* [R1] 关键源码片段 (routing_data_from_sparse_topk): with f = t*k + j the
- * flat slot index,
+ * flat slot index and e(f) its (local) expert,
  *   col_sum[e]        = #{ f : indx[f] = e }                   (histogram)
  *   offs[0] = 0, offs[e+1] = offs[e] + col_sum[e]               (ragged offsets)
  *   col_sorted[p]     = slots listed expert by expert, ascending f within
@@ -152,27 +165,34 @@ int orc_route(const float *logits, int64_t n, int E, int k, int gating,
  *   row_sorted[f]     = p such that col_sorted[p] = f           (dispatch_indx)
  *   gate_scal[p]      = vals_flat[col_sorted[p]]
  * Gather = (src col_sorted, dst row_sorted); scatter = (src row_sorted,
- * dst col_sorted): the same two arrays. */
+ * dst col_sorted): the same two arrays. With an expert map the histogram
+ * and offsets run over the E_loc local experts, col_sorted / gate_scal list
+ * the offs[E_loc] kept slots, and row_sorted[f] = -1 for a dropped slot. */
 int orc_metadata(const int32_t *topk_indx, const uint16_t *topk_vals, int64_t n, int E, int k,
-                 int32_t *col_sum, int32_t *offs, int32_t *col_sorted, int32_t *row_sorted,
-                 uint16_t *gate_scal) {
+                 const int32_t *expert_map, int E_loc, int32_t *col_sum, int32_t *offs,
+                 int32_t *col_sorted, int32_t *row_sorted, uint16_t *gate_scal) {
   if (n < 0 || E < 1 || k < 1) return ORC_BAD_ARG;
+  if (!expert_map) E_loc = E;
+  if (E_loc < 1 || E_loc > E) return ORC_BAD_ARG;
+  for (int e = 0; expert_map && e < E; ++e)
+    if (orc_local(expert_map, E_loc, e) < -1) return ORC_BAD_ARG;
   int64_t N = n * (int64_t)k;
   for (int64_t f = 0; f < N; ++f)
     if (topk_indx[f] < 0 || topk_indx[f] >= E) return ORC_BAD_ARG;
-  for (int e = 0; e < E; ++e) {
+  for (int e = 0; e < E_loc; ++e) {
     int32_t c = 0;
-    for (int64_t f = 0; f < N; ++f) c += (topk_indx[f] == e);
+    for (int64_t f = 0; f < N; ++f) c += (orc_local(expert_map, E_loc, topk_indx[f]) == e);
     col_sum[e] = c;
   }
   offs[0] = 0;
-  for (int e = 0; e < E; ++e) offs[e + 1] = offs[e] + col_sum[e];
+  for (int e = 0; e < E_loc; ++e) offs[e + 1] = offs[e] + col_sum[e];
   int64_t p = 0;
-  for (int e = 0; e < E; ++e)
+  for (int e = 0; e < E_loc; ++e)
     for (int64_t f = 0; f < N; ++f)
-      if (topk_indx[f] == e) col_sorted[p++] = (int32_t)f;
-  for (int64_t q = 0; q < N; ++q) row_sorted[col_sorted[q]] = (int32_t)q;
-  for (int64_t q = 0; q < N; ++q) gate_scal[q] = topk_vals[col_sorted[q]];
+      if (orc_local(expert_map, E_loc, topk_indx[f]) == e) col_sorted[p++] = (int32_t)f;
+  for (int64_t f = 0; f < N; ++f) row_sorted[f] = -1;
+  for (int64_t q = 0; q < p; ++q) row_sorted[col_sorted[q]] = (int32_t)q;
+  for (int64_t q = 0; q < p; ++q) gate_scal[q] = topk_vals[col_sorted[q]];
   return ORC_OK;
 }
 
@@ -303,7 +323,9 @@ int orc_expert_row(const uint16_t *x, const uint16_t *w13, const uint16_t *w2, i
  * written per token: for each requested token t, its k (expert, weight)
  * pairs are taken in ascending expert id; each expert output y_e(x_t) is
  * multiplied by the bf16 gate weight and summed in float64; the sum is
- * rounded once to bf16.
+ * rounded once to bf16. With an expert map, w13 / w2 hold the E_loc local
+ * experts, slot j uses local expert map[e_j], and dropped slots add nothing
+ * (their y_slot / h_slot entries are zero).
  *
  * tokens: list of n_sel token ids to compute (NULL = all n, in order).
  * out [n_sel, H] bf16 bits, row s for token tokens[s].
@@ -312,10 +334,15 @@ int orc_expert_row(const uint16_t *x, const uint16_t *w13, const uint16_t *w2, i
  * h_slot (optional, [n_sel, k, I] bf16): the intermediate of slot j. */
 int orc_ffn(const uint16_t *x, const int32_t *topk_indx, const uint16_t *topk_vals,
             const uint16_t *w13, const uint16_t *w2, int64_t n, int E, int k, int H, int I,
-            const orc_act_params *prm, const int64_t *tokens, int64_t n_sel, uint16_t *out,
-            double *y_slot, uint16_t *h_slot) {
+            const int32_t *expert_map, int E_loc, const orc_act_params *prm,
+            const int64_t *tokens, int64_t n_sel, uint16_t *out, double *y_slot,
+            uint16_t *h_slot) {
   if (n < 0 || E < 1 || k < 1 || k > E || k > 64 || H < 1 || I < 1 || !orc_check_params(prm))
     return ORC_BAD_ARG;
+  if (!expert_map) E_loc = E;
+  if (E_loc < 1 || E_loc > E) return ORC_BAD_ARG;
+  for (int e = 0; expert_map && e < E; ++e)
+    if (orc_local(expert_map, E_loc, e) < -1) return ORC_BAD_ARG;
   if (!tokens) n_sel = n;
   for (int64_t s = 0; s < n_sel; ++s) {
     int64_t t = tokens ? tokens[s] : s;
@@ -351,7 +378,13 @@ int orc_ffn(const uint16_t *x, const int32_t *topk_indx, const uint16_t *topk_va
         }
         for (int jj = 0; jj < k; ++jj) {
           int j = slot_order[jj];
-          int e = topk_indx[t * k + j];
+          int e = orc_local(expert_map, E_loc, topk_indx[t * k + j]);
+          if (e < 0) { /* dropped: another rank's expert */
+            if (y_slot)
+              for (int c = 0; c < H; ++c) y_slot[(s * k + j) * H + c] = 0.0;
+            if (h_slot) memset(h_slot + (s * k + j) * I, 0, sizeof(uint16_t) * (size_t)I);
+            continue;
+          }
           double wgt = orc_bf16_to_f64(topk_vals[t * k + j]);
           orc_expert_row_impl(xt, w13 + (int64_t)e * orc_w13_rows(prm, I) * H,
                               w2 + (int64_t)e * H * I, H, I, prm, a, hb, y);
