@@ -65,7 +65,7 @@
 extern "C" {
 #endif
 
-#define MOE_ABI_VERSION 2
+#define MOE_ABI_VERSION 3
 
 typedef void *moe_stream;  /* a cudaStream_t */
 
@@ -142,6 +142,24 @@ typedef struct {
   uint32_t set;       /* MOE_SET_* bits */
   float alpha, beta, limit;
   int32_t ffn_kernel; /* moe_ffn_kernel; 0 = AUTO */
+  /* Expert parallelism [R1] 功能与动机 (expert-parallel routing) and 风险与影响
+   * (its -1 slots): this rank holds n_local_experts of the E experts.
+   * expert_map: device int32 [E], 4-byte aligned, the local id in
+   * [0, n_local_experts) of each global expert or -1 for an expert on another
+   * rank; NULL = every expert local (n_local_experts is then ignored).
+   * Used by moe_forward, moe_forward_gate and moe_forward_timed: top-k runs
+   * over the E global logits (topk_indx holds global ids); the metadata
+   * covers the local experts (col_sum [n_local_experts], offs
+   * [n_local_experts + 1]; the offs[n_local_experts] kept slots are listed in
+   * col_sorted / gate_scal; row_sorted is -1 at a dropped slot); w13 / w2
+   * hold the n_local_experts local experts; out[t] sums only the token's
+   * slots on local experts (a zero row when it has none): this rank's share
+   * of the layer output. Entries outside [-1, n_local_experts) count as -1
+   * and record MOE_ERR_INVALID_ARG in the status word. The stage entry
+   * points ignore the map: moe_grouped_ffn takes E = n_local_experts and the
+   * metadata of moe_forward's meta output; moe_combine adds every slot. */
+  const int32_t *expert_map;
+  int32_t n_local_experts;
 } moe_params;
 
 /* Routing metadata [R1] 关键源码片段 (routing_data_from_sparse_topk),
@@ -173,8 +191,8 @@ const char *moe_status_string(moe_status status);
 
 /* Bytes of workspace that moe_build_metadata, moe_grouped_ffn and
  * moe_forward need for these sizes (a few KB of control and sync data plus,
- * for the FFN, the expert-sorted activations, the intermediate h and, when
- * k > 1, the per-slot outputs; for decode sizes, n*k <= 32*E, also 16 MB of
+ * for the FFN, the expert-sorted activations, the intermediate h and the
+ * per-slot outputs; for decode sizes, n*k <= 32*E, also 16 MB of
  * fp32 partial sums of the w13 contraction's even split of its work over
  * the SMs). The sync words are rewritten by every FFN call, so one
  * workspace serves one stream at a time. Returns 0 for invalid sizes. */
@@ -343,7 +361,7 @@ moe_status moe_forward_timed(const uint16_t *x, const float *logits, const uint1
 
 /* Number of kernels moe_forward (and moe_forward_timed) enqueues for these
  * sizes on the current device with the default grouped-GEMM kernel
- * (MOE_FFN_AUTO): route and metadata (one fused kernel when a CTA's slots
+ * (MOE_FFN_AUTO) and no expert map: route and metadata (one fused kernel when a CTA's slots
  * fit its shared memory, else two), the gather (none when n*k <= 2E: the
  * w13 contraction gathers), the two expert contractions and, when k > 1,
  * the combine; 0 for n = 0; -1 for sizes moe_forward rejects. Host-only:

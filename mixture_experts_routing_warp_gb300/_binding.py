@@ -22,7 +22,7 @@ ACT = {"swiglu": 0, "swiglu_oai": 1, "relu2": 2}
 LAYOUT = {"packed": 0, "interleaved": 1}
 SET_ALPHA, SET_BETA, SET_LIMIT = 1, 2, 4
 FFN_KERNEL = {"auto": 0, "tiled": 1, "swap": 2}
-ABI_VERSION = 2
+ABI_VERSION = 3
 
 STATUS = {0: "MOE_OK", 1: "MOE_ERR_INVALID_ARG", 2: "MOE_ERR_UNSUPPORTED",
           3: "MOE_ERR_WORKSPACE_TOO_SMALL", 4: "MOE_ERR_CUDA", 5: "MOE_ERR_TIMEOUT",
@@ -39,7 +39,8 @@ class MoeParams(ctypes.Structure):
     _fields_ = [("gating", ctypes.c_int32), ("activation", ctypes.c_int32),
                 ("w13_layout", ctypes.c_int32), ("set", ctypes.c_uint32),
                 ("alpha", ctypes.c_float), ("beta", ctypes.c_float), ("limit", ctypes.c_float),
-                ("ffn_kernel", ctypes.c_int32)]
+                ("ffn_kernel", ctypes.c_int32), ("expert_map", ctypes.c_void_p),
+                ("n_local_experts", ctypes.c_int32)]
 
 
 class RoutingMeta(ctypes.Structure):
@@ -131,13 +132,24 @@ def _ptr(t: Optional[torch.Tensor]) -> ctypes.c_void_p:
 
 def make_params(gating: str = "softmax_topk", act: str = "swiglu", layout: str = "packed",
                 alpha: Optional[float] = None, beta: Optional[float] = None,
-                limit: Optional[float] = None, ffn_kernel: str = "auto") -> MoeParams:
+                limit: Optional[float] = None, ffn_kernel: str = "auto",
+                expert_map: Optional[torch.Tensor] = None,
+                n_local_experts: Optional[int] = None) -> MoeParams:
     """moe_params with the `set` bits of the values that are not None, so
     unset parameters keep the activation's defaults. ffn_kernel picks the
     grouped-GEMM kernel: "auto", "tiled" (large per-expert batches) or
-    "swap" (small ones)."""
+    "swap" (small ones). expert_map (int32 [E] on the device: local expert id
+    or -1) and n_local_experts make moe_forward compute an expert-parallel
+    rank's share; the params keep a reference to the map tensor."""
     p = MoeParams(GATING[gating], ACT[act], LAYOUT[layout], 0, 0.0, 0.0, 0.0,
-                  FFN_KERNEL[ffn_kernel])
+                  FFN_KERNEL[ffn_kernel], None, 0)
+    if expert_map is not None:
+        _need(expert_map, "expert_map", torch.int32)
+        if n_local_experts is None:
+            raise ValueError("an expert map needs n_local_experts")
+        p.expert_map = expert_map.data_ptr()
+        p.n_local_experts = int(n_local_experts)
+        p._map_tensor = expert_map
     if alpha is not None:
         p.set |= SET_ALPHA
         p.alpha = float(alpha)
@@ -271,10 +283,11 @@ def forward(x: torch.Tensor, logits: torch.Tensor, w13: torch.Tensor, w2: torch.
     n, H = x.shape
     _need(logits, "logits", torch.float32)
     E = logits.shape[1]
+    E_w = params.n_local_experts if params.expert_map else E  # experts held in w13 / w2
     _need(w13, "w13", torch.bfloat16)
     I = _intermediate(w13, params)
-    _need(w13, "w13", torch.bfloat16, (E, w13.shape[1], H))
-    _need(w2, "w2", torch.bfloat16, (E, H, I))
+    _need(w13, "w13", torch.bfloat16, (E_w, w13.shape[1], H))
+    _need(w2, "w2", torch.bfloat16, (E_w, H, I))
     if out is None:
         out = torch.empty((n, H), dtype=torch.bfloat16, device=x.device)
     indx, vals = topk if topk is not None else (None, None)
@@ -315,10 +328,11 @@ def forward_gate(x: torch.Tensor, w_gate: torch.Tensor, w13: torch.Tensor, w2: t
     _need(w_gate, "w_gate", torch.bfloat16)
     E = w_gate.shape[0]
     _need(w_gate, "w_gate", torch.bfloat16, (E, H))
+    E_w = params.n_local_experts if params.expert_map else E  # experts held in w13 / w2
     _need(w13, "w13", torch.bfloat16)
     I = _intermediate(w13, params)
-    _need(w13, "w13", torch.bfloat16, (E, w13.shape[1], H))
-    _need(w2, "w2", torch.bfloat16, (E, H, I))
+    _need(w13, "w13", torch.bfloat16, (E_w, w13.shape[1], H))
+    _need(w2, "w2", torch.bfloat16, (E_w, H, I))
     if out is None:
         out = torch.empty((n, H), dtype=torch.bfloat16, device=x.device)
     indx, vals = topk if topk is not None else (None, None)

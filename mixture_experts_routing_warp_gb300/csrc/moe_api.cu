@@ -234,6 +234,12 @@ static moe_status forward_impl(const uint16_t *x, const float *logits, const uin
   if ((st = resolve_params(params, act, &gating)) != MOE_OK) return st;
   if (meta && (st = check_meta(meta, n)) != MOE_OK) return st;
   if ((topk_indx == nullptr) != (topk_vals == nullptr)) return MOE_ERR_INVALID_ARG;
+  // expert parallelism: routing over the E global experts, the metadata and
+  // the contractions over the E_loc local ones
+  const int32_t *emap = params->expert_map;
+  const int32_t E_loc = emap ? params->n_local_experts : E;
+  if (E_loc < 1 || E_loc > E) return MOE_ERR_INVALID_ARG;
+  if (!aligned(emap, 4)) return MOE_ERR_MISALIGNED;
   if (n == 0) return MOE_OK;
   if (!x || (!logits && !w_gate) || !w13 || !w2 || !out || !workspace) return MOE_ERR_INVALID_ARG;
   if (!aligned(x, 16) || !aligned(w13, 16) || !aligned(w2, 16) || !aligned(out, 16) ||
@@ -257,8 +263,11 @@ static moe_status forward_impl(const uint16_t *x, const float *logits, const uin
   }
   uint32_t *ctrl = ws_at<uint32_t>(workspace, L.ctrl);
   const int64_t N = n * k;
-  // k = 1: slot f is token t, so the w2 epilogue writes the output directly.
-  uint16_t *y_flat = k == 1 ? out : ws_at<uint16_t>(workspace, L.y_flat);
+  // k = 1: slot f is token t, so the w2 epilogue writes the output directly
+  // (not with an expert map: a token without a local slot needs a zero row,
+  // which the combine writes).
+  const bool direct = k == 1 && !emap;
+  uint16_t *y_flat = direct ? out : ws_at<uint16_t>(workspace, L.y_flat);
   uint16_t *x_sorted = ws_at<uint16_t>(workspace, L.x_sorted);
   uint16_t *h = ws_at<uint16_t>(workspace, L.h);
   const FfnScratch scr = ffn_scratch(workspace, L);
@@ -273,13 +282,14 @@ static moe_status forward_impl(const uint16_t *x, const float *logits, const uin
         launch_route_gemm(x, w_gate, n, E, H, k, gating, indx, vals, nullptr, ctrl, s) !=
             cudaSuccess ||
         mark(MOE_STAGE_METADATA) != cudaSuccess ||
-        launch_metadata(indx, vals, n, E, k, m, hist, ctrl, s, scr.sync) != cudaSuccess)
+        launch_metadata(indx, vals, n, E, k, m, hist, ctrl, s, scr.sync, emap, E_loc) !=
+            cudaSuccess)
       return MOE_ERR_CUDA;
   } else if (route_metadata_fits(n, k)) {
     // one cooperative kernel for both stages; the metadata stage time is 0
     if (mark(MOE_STAGE_ROUTE) != cudaSuccess ||
-        launch_route_metadata(logits, n, E, k, gating, indx, vals, m, hist, ctrl, s, scr.sync) !=
-            cudaSuccess ||
+        launch_route_metadata(logits, n, E, k, gating, indx, vals, m, hist, ctrl, s, scr.sync,
+                              emap, E_loc) != cudaSuccess ||
         mark(MOE_STAGE_METADATA) != cudaSuccess)
       return MOE_ERR_CUDA;
   } else {
@@ -287,7 +297,8 @@ static moe_status forward_impl(const uint16_t *x, const float *logits, const uin
         launch_route(logits, n, E, k, gating, indx, vals, ctrl, s) != cudaSuccess)
       return MOE_ERR_CUDA;
     if (mark(MOE_STAGE_METADATA) != cudaSuccess ||
-        launch_metadata(indx, vals, n, E, k, m, hist, ctrl, s, scr.sync) != cudaSuccess)
+        launch_metadata(indx, vals, n, E, k, m, hist, ctrl, s, scr.sync, emap, E_loc) !=
+            cudaSuccess)
       return MOE_ERR_CUDA;
   }
   // A row or two per expert: the swap-operand kernel gathers its token rows
@@ -295,18 +306,20 @@ static moe_status forward_impl(const uint16_t *x, const float *logits, const uin
   // come from X_sorted, materialised by the gather kernel: a gather4 costs
   // about as much TMA time as a whole 2-D box, so 128 rows per K step as 32
   // gathers ran w13 3.4x slower at prefill.
-  const bool fused_gather = fused_gather_rows(n, E, k, act.ffn_kernel);
+  const bool fused_gather = fused_gather_rows(n, E_loc, k, act.ffn_kernel);
   const GatherSrc src{x, n, k};
   if (mark(MOE_STAGE_GATHER) != cudaSuccess ||
       (!fused_gather &&
        launch_gather_rows(x, m.row_sorted, n, k, H, x_sorted, scr.sync, s) != cudaSuccess))
     return MOE_ERR_CUDA;
-  if (launch_ffn(x_sorted, m.offs, m.col_sorted, m.gate_scal, w13, w2, N, E, H, I, act, h, y_flat,
-                 scr, s, ev ? ev + MOE_STAGE_FFN1 : nullptr,
+  if (launch_ffn(x_sorted, m.offs, m.col_sorted, m.gate_scal, w13, w2, N, E_loc, H, I, act, h,
+                 y_flat, scr, s, ev ? ev + MOE_STAGE_FFN1 : nullptr,
                  fused_gather ? &src : nullptr) != cudaSuccess)
     return MOE_ERR_CUDA;
   if (mark(MOE_STAGE_COMBINE) != cudaSuccess) return MOE_ERR_CUDA;
-  if (k > 1 && launch_combine(y_flat, n, k, H, out, s) != cudaSuccess) return MOE_ERR_CUDA;
+  if (!direct &&
+      launch_combine(y_flat, n, k, H, out, s, emap ? m.row_sorted : nullptr) != cudaSuccess)
+    return MOE_ERR_CUDA;
   if (mark(MOE_STAGE_COUNT) != cudaSuccess) return MOE_ERR_CUDA;
   return MOE_OK;
 }

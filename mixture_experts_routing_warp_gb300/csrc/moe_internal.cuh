@@ -64,7 +64,8 @@ inline size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 // internal; the sync words of the expert contractions; the decode stream-K
 // partial sums (n*k <= 32 * E only); the expert-sorted activations X_sorted
 // [N, H]; the intermediate h [N, I]; the per-slot outputs y_flat [N, H]
-// (k > 1 only). N = n * k.
+// (at k = 1 used only with an expert map, where the combine writes the zero
+// rows of tokens without a local slot). N = n * k.
 inline WorkspaceLayout workspace_layout(int64_t n, int E, int k, int H, int I) {
   WorkspaceLayout L{};
   const size_t N = (size_t)n * (size_t)k;
@@ -85,7 +86,7 @@ inline WorkspaceLayout workspace_layout(int64_t n, int E, int k, int H, int I) {
                        : 0);
   L.x_sorted = take(N * (size_t)H * 2);
   L.h = take(N * (size_t)I * 2);
-  L.y_flat = take(k > 1 ? N * (size_t)H * 2 : 0);
+  L.y_flat = take(N * (size_t)H * 2);
   L.total = o;
   return L;
 }
@@ -382,21 +383,24 @@ bool route_metadata_fits(int64_t n, int k);
 cudaError_t launch_route_metadata(const float *logits, int64_t n, int E, int k, int gating,
                                   int32_t *topk_indx, uint16_t *topk_vals,
                                   const moe_routing_meta &meta, int32_t *ws_hist,
-                                  uint32_t *ctrl, cudaStream_t s, uint32_t *sync = nullptr);
+                                  uint32_t *ctrl, cudaStream_t s, uint32_t *sync = nullptr,
+                                  const int32_t *expert_map = nullptr, int E_loc = 0);
 
 // sync (may be null): the kSyncWords per-forward sync words of the expert
 // contractions, zeroed by these kernels (and by the gather)
 cudaError_t launch_metadata(const int32_t *topk_indx, const uint16_t *topk_vals, int64_t n, int E,
                             int k, const moe_routing_meta &meta, int32_t *ws_hist,
-                            uint32_t *ctrl, cudaStream_t s, uint32_t *sync = nullptr);
+                            uint32_t *ctrl, cudaStream_t s, uint32_t *sync = nullptr,
+                            const int32_t *expert_map = nullptr, int E_loc = 0);
 
 // X_sorted[row_sorted[t*k + j]] = x[t] for the n tokens' k slots.
 // sync (may be null): the kSyncWords sync words the gather zeroes
 cudaError_t launch_gather_rows(const uint16_t *x, const int32_t *row_sorted, int64_t n, int k,
                                int H, uint16_t *x_sorted, uint32_t *sync, cudaStream_t s);
 
+// row_sorted (may be null): leave out the slots whose row_sorted is -1
 cudaError_t launch_combine(const uint16_t *y_flat, int64_t n, int k, int H, uint16_t *out,
-                           cudaStream_t s);
+                           cudaStream_t s, const int32_t *row_sorted = nullptr);
 
 // The unsorted tokens x [n, H] and k, for the w13 contraction's fused
 // dispatch gather: sorted row p is x[col_sorted[p] / k].

@@ -77,38 +77,44 @@ cudaError_t launch_route(const float *logits, int64_t n, int E, int k, int gatin
   return dispatch_kg(k, E, RouteLaunch{logits, n, E, gating, topk_indx, topk_vals, s});
 }
 
-// Metadata from a top-k result in global memory (moe_build_metadata).
+// Metadata from a top-k result in global memory (moe_build_metadata). With
+// an expert map, over the E_loc local experts; other ranks' slots dropped.
 __global__ void __launch_bounds__(kMetaThreads) metadata_kernel(
     const int32_t *__restrict__ topk_indx, const uint16_t *__restrict__ topk_vals, int N, int E,
     int chunk, int32_t *__restrict__ col_sum, int32_t *__restrict__ offs,
     int32_t *__restrict__ col_sorted, int32_t *__restrict__ row_sorted,
     uint16_t *__restrict__ gate_scal, int32_t *__restrict__ ws_hist, uint32_t *ctrl,
-    unsigned long long timeout_ns, uint32_t *sync) {
+    unsigned long long timeout_ns, uint32_t *sync, const int32_t *__restrict__ expert_map,
+    int E_loc) {
   __shared__ MetaShared<kMetaThreads> sh;
+  __shared__ int s_map_buf[kMaxExperts];
   const int tid = threadIdx.x;
   const int b = blockIdx.x;
   pdl_launch_dependents();  // the next kernel may be scheduled (it waits for this grid)
   zero_sync_words(sync);
+  const int *s_map = load_expert_map(expert_map, E, E_loc, s_map_buf, ctrl);
   const int lo = (int)min((int64_t)N, (int64_t)b * chunk);
   const int hi = (int)min((int64_t)N, (int64_t)lo + chunk);
+  // local expert of a slot: -1 when dropped (another rank's) or invalid
+  auto local = [&](int e) { return (unsigned)e < (unsigned)E ? (s_map ? s_map[e] : e) : -1; };
 
-  for (int e = tid; e < E; e += kMetaThreads) sh.base[e] = 0;
+  for (int e = tid; e < E_loc; e += kMetaThreads) sh.base[e] = 0;
   if (tid == 0) sh.bad = 0;
   __syncthreads();
   for (int f = lo + tid; f < hi; f += kMetaThreads) {
     const int e = __ldg(topk_indx + f);
-    if ((unsigned)e < (unsigned)E) atomicAdd(&sh.base[e], 1);
-    else sh.bad = 1;
+    if ((unsigned)e >= (unsigned)E) sh.bad = 1;
+    const int le = local(e);
+    if (le >= 0) atomicAdd(&sh.base[le], 1);
   }
   __syncthreads();
   if (sh.bad && tid == 0) record_status(ctrl, MOE_ERR_INVALID_ARG);
 
-  if (!meta_barrier_prefix(ws_hist, E, sh, col_sum, offs, ctrl, timeout_ns, [] {})) return;
+  if (!meta_barrier_prefix(ws_hist, E_loc, sh, col_sum, offs, ctrl, timeout_ns, [] {})) return;
   meta_scatter(
-      lo, hi - lo, E, sh,
+      lo, hi - lo, E_loc, sh,
       [&](int i, int &e, uint16_t &w) {
-        e = __ldg(topk_indx + lo + i);
-        if ((unsigned)e >= (unsigned)E) e = -1;
+        e = local(__ldg(topk_indx + lo + i));
         w = __ldg(topk_vals + lo + i);
       },
       col_sorted, row_sorted, gate_scal);
@@ -129,7 +135,9 @@ int metadata_ctas_per_sm() {
 cudaError_t launch_metadata_kernel(const int32_t *topk_indx, const uint16_t *topk_vals, int N,
                                    int E, const moe_routing_meta &meta, int32_t *ws_hist,
                                    uint32_t *ctrl, int max_ctas, cudaStream_t s,
-                                   uint32_t *sync = nullptr) {
+                                   uint32_t *sync = nullptr, const int32_t *expert_map = nullptr,
+                                   int E_loc = 0) {
+  if (!expert_map) E_loc = E;
   static bool configured = false;
   if (!configured) {
     cudaError_t err = uniform_carveout(metadata_kernel);
@@ -147,7 +155,8 @@ cudaError_t launch_metadata_kernel(const int32_t *topk_indx, const uint16_t *top
   void *args[] = {(void *)&topk_indx, (void *)&topk_vals, (void *)&N, (void *)&E,
                   (void *)&chunk, (void *)&meta.col_sum, (void *)&meta.offs,
                   (void *)&meta.col_sorted, (void *)&meta.row_sorted, (void *)&meta.gate_scal,
-                  (void *)&ws_hist, (void *)&ctrl, (void *)&timeout, (void *)&sync};
+                  (void *)&ws_hist, (void *)&ctrl, (void *)&timeout, (void *)&sync,
+                  (void *)&expert_map, (void *)&E_loc};
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)B);
   cfg.blockDim = dim3(kMetaThreads);
@@ -164,9 +173,10 @@ cudaError_t launch_metadata_kernel(const int32_t *topk_indx, const uint16_t *top
 
 cudaError_t launch_metadata(const int32_t *topk_indx, const uint16_t *topk_vals, int64_t n, int E,
                             int k, const moe_routing_meta &meta, int32_t *ws_hist,
-                            uint32_t *ctrl, cudaStream_t s, uint32_t *sync) {
+                            uint32_t *ctrl, cudaStream_t s, uint32_t *sync,
+                            const int32_t *expert_map, int E_loc) {
   return launch_metadata_kernel(topk_indx, topk_vals, (int)(n * k), E, meta, ws_hist, ctrl,
-                                kMetaMaxCtas, s, sync);
+                                kMetaMaxCtas, s, sync, expert_map, E_loc);
 }
 
 // ======================================== metadata without a workspace ==
@@ -309,7 +319,9 @@ cudaError_t launch_gather_rows(const uint16_t *x, const int32_t *row_sorted, int
 // ============================================================= combine ==
 // out[t] = sum_{j<k} y_flat[t*k + j] in fp32, j ascending, one bf16 rounding.
 // A warp per (token, group of 64 16-byte chunks), 2 chunks x k slots in
-// flight per thread.
+// flight per thread. With row_sorted (an expert map in use), slots without a
+// sorted position (another rank's expert: row_sorted -1) are left out; their
+// y_flat rows were never written.
 __device__ __forceinline__ void add_bf16x8(float (&acc)[8], const uint4 &v) {
   const uint32_t w[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
@@ -323,7 +335,8 @@ template <int K>
 __global__ void __launch_bounds__(kCopyThreads) combine_kernel(const uint4 *__restrict__ y_flat,
                                                                int64_t n, int vec_per_row,
                                                                int groups_per_row,
-                                                               uint4 *__restrict__ out) {
+                                                               uint4 *__restrict__ out,
+                                                               const int32_t *row_sorted) {
   constexpr int CPL = 2;  // chunks per lane: 2*K loads in flight
   pdl_launch_dependents();
   pdl_wait();  // y_flat comes from the w2 contraction
@@ -335,13 +348,17 @@ __global__ void __launch_bounds__(kCopyThreads) combine_kernel(const uint4 *__re
     const int64_t t = u / groups_per_row;
     const int c0 = (int)(u - t * groups_per_row) * 32 * CPL + lane;
     const uint4 *src = y_flat + t * K * vec_per_row;
+    bool kept[K];
+#pragma unroll
+    for (int j = 0; j < K; ++j) kept[j] = !row_sorted || __ldg(row_sorted + t * K + j) >= 0;
     uint4 v[CPL][K];
 #pragma unroll
     for (int q = 0; q < CPL; ++q)
 #pragma unroll
       for (int j = 0; j < K; ++j)
-        if (c0 + 32 * q < vec_per_row)
-          v[q][j] = __ldcs(src + (int64_t)j * vec_per_row + c0 + 32 * q);
+        v[q][j] = c0 + 32 * q < vec_per_row && kept[j]
+                      ? __ldcs(src + (int64_t)j * vec_per_row + c0 + 32 * q)
+                      : make_uint4(0u, 0u, 0u, 0u);
 #pragma unroll
     for (int q = 0; q < CPL; ++q) {
       const int c = c0 + 32 * q;
@@ -360,7 +377,7 @@ __global__ void __launch_bounds__(kCopyThreads) combine_kernel(const uint4 *__re
 }
 
 cudaError_t launch_combine(const uint16_t *y_flat, int64_t n, int k, int H, uint16_t *out,
-                           cudaStream_t s) {
+                           cudaStream_t s, const int32_t *row_sorted) {
   if (n == 0) return cudaSuccess;
   const int vpr = H / 8, gpr = (vpr + 63) / 64;
   int64_t blocks = (n * gpr + kCopyThreads / 32 - 1) / (kCopyThreads / 32);
@@ -379,7 +396,8 @@ cudaError_t launch_combine(const uint16_t *y_flat, int64_t n, int k, int H, uint
     }                                                                              \
     {                                                                              \
       cudaError_t err = launch_dependent(combine_kernel<K_>, dim3((unsigned)blocks),  \
-                                         dim3(kCopyThreads), 0, s, y, n, vpr, gpr, o); \
+                                         dim3(kCopyThreads), 0, s, y, n, vpr, gpr, o,  \
+                                         row_sorted);                              \
       if (err != cudaSuccess) return err;                                          \
     }                                                                              \
     break;

@@ -188,11 +188,15 @@ __device__ __forceinline__ void topk_group(const float *__restrict__ row, bool v
 }
 
 // Outputs of one token: lane g of the group writes entries j = g, g+G, ...
+// KEEP: the slots stay in shared memory (global expert ids) and are counted
+// per local expert (s_map: local id of each global expert or -1, null for
+// the identity; a -1 slot is not counted).
 template <int K, int G, bool KEEP>
 __device__ __forceinline__ void write_token(int64_t t, int64_t t0, const TopK<K> &tk,
                                             const float (&w)[K], int32_t *__restrict__ topk_indx,
                                             uint16_t *__restrict__ topk_vals, uint8_t *s_slot_e,
-                                            uint16_t *s_slot_v, int *s_hist) {
+                                            uint16_t *s_slot_v, int *s_hist,
+                                            const int *s_map = nullptr) {
   const int g = (threadIdx.x & 31) % G;
 #pragma unroll
   for (int j = 0; j < K; ++j) {
@@ -205,7 +209,8 @@ __device__ __forceinline__ void write_token(int64_t t, int64_t t0, const TopK<K>
       const int s = (int)(t - t0) * K + j;
       s_slot_e[s] = (uint8_t)tk.e[j];
       s_slot_v[s] = wb;
-      atomicAdd(&s_hist[tk.e[j]], 1);
+      const int le = s_map ? s_map[tk.e[j]] : tk.e[j];
+      if (le >= 0) atomicAdd(&s_hist[le], 1);
     }
   }
 }
@@ -398,7 +403,12 @@ __device__ void meta_scatter(int64_t f_lo, int count, int E, MetaShared<THREADS>
     const int i = r0 + tid;
     int e = -1;
     uint16_t w = 0;
-    if (i < count) get(i, e, w);
+    if (i < count) {
+      get(i, e, w);
+      // a dropped slot (expert on another rank, or an invalid id) has no
+      // sorted position
+      if (e < 0) row_sorted[f_lo + i] = -1;
+    }
     const unsigned peers = __match_any_sync(0xffffffffu, e);
     const int rank = __popc(peers & lt_mask);
     if (e >= 0 && rank == 0) sh.cnt[warp][e] = __popc(peers);
@@ -426,12 +436,29 @@ __device__ void meta_scatter(int64_t f_lo, int count, int E, MetaShared<THREADS>
   }
 }
 
+// Expert map (expert parallelism): the local id of each of the E global
+// experts, or -1 for an expert on another rank, copied to shared memory.
+// An entry outside [-1, E_loc) is treated as -1 and flags
+// MOE_ERR_INVALID_ARG. Returns the table, or null (identity) without a map.
+__device__ __forceinline__ const int *load_expert_map(const int32_t *expert_map, int E, int E_loc,
+                                                      int *s_map, uint32_t *ctrl) {
+  if (!expert_map) return nullptr;
+  for (int e = threadIdx.x; e < E; e += blockDim.x) {
+    const int v = expert_map[e];
+    const bool ok = v >= -1 && v < E_loc;
+    if (!ok && ctrl) record_status(ctrl, MOE_ERR_INVALID_ARG);
+    s_map[e] = ok ? v : -1;
+  }
+  return s_map;
+}
+
 // Decode sizes (n*k <= kSmallSlots): route + metadata in one CTA
 // (routing_small.cu).
 constexpr int kSmallSlots = 32;
 cudaError_t launch_route_metadata_small(const float *logits, int n, int E, int k, int gating,
                                         int32_t *topk_indx, uint16_t *topk_vals,
                                         const moe_routing_meta &meta, uint32_t *sync,
+                                        const int32_t *expert_map, int E_loc, uint32_t *ctrl,
                                         cudaStream_t s);
 
 }  // namespace moe

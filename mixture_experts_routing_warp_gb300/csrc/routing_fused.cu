@@ -12,7 +12,9 @@ namespace moe {
 // moe_route_metadata / moe_forward's first two stages in one cooperative
 // kernel, one CTA per SM: CTA b routes tokens [b*T, b*T + T) (G lanes per
 // token as above), keeping its slots and histogram in shared memory, then
-// publishes, gathers and scatters its slots from shared memory.
+// publishes, gathers and scatters its slots from shared memory. With an
+// expert map the metadata covers the E_loc local experts and drops the slots
+// of other ranks' experts.
 template <int K, int G, int NQ>
 __global__ void __launch_bounds__(kFusedThreads, 1) route_metadata_kernel(
     const float *__restrict__ logits, int64_t n, int E, int gating, int T, int vec4,
@@ -20,16 +22,18 @@ __global__ void __launch_bounds__(kFusedThreads, 1) route_metadata_kernel(
     int32_t *__restrict__ col_sum, int32_t *__restrict__ offs, int32_t *__restrict__ col_sorted,
     int32_t *__restrict__ row_sorted, uint16_t *__restrict__ gate_scal,
     int32_t *__restrict__ ws_hist, uint32_t *ctrl, unsigned long long timeout_ns,
-    uint32_t *sync) {
+    uint32_t *sync, const int32_t *__restrict__ expert_map, int E_loc) {
   extern __shared__ uint8_t smem_raw[];
   __shared__ MetaShared<kFusedThreads> sh;
+  __shared__ int s_map_buf[kMaxExperts];
   uint8_t *s_slot_e = smem_raw;
   uint16_t *s_slot_v = reinterpret_cast<uint16_t *>(smem_raw + (((size_t)T * K + 15) & ~15ull));
 
   const int tid = threadIdx.x;
   pdl_launch_dependents();  // the next kernel may be scheduled (it waits for this grid)
   zero_sync_words(sync);
-  for (int e = tid; e < E; e += kFusedThreads) sh.base[e] = 0;
+  const int *s_map = load_expert_map(expert_map, E, E_loc, s_map_buf, ctrl);
+  for (int e = tid; e < E_loc; e += kFusedThreads) sh.base[e] = 0;
   __syncthreads();
 
   const int64_t t0 = min(n, (int64_t)blockIdx.x * T);
@@ -42,7 +46,8 @@ __global__ void __launch_bounds__(kFusedThreads, 1) route_metadata_kernel(
     float w[K];
     topk_group<K, G, NQ>(logits + (valid ? t : 0) * E, valid, E, gating, vec4 != 0, tk, w);
     if (valid)
-      write_token<K, G, true>(t, t0, tk, w, topk_indx, topk_vals, s_slot_e, s_slot_v, sh.base);
+      write_token<K, G, true>(t, t0, tk, w, topk_indx, topk_vals, s_slot_e, s_slot_v, sh.base,
+                              s_map);
   }
   __syncthreads();
   // the CTA's top-k outputs leave shared memory while the other CTAs arrive
@@ -53,11 +58,12 @@ __global__ void __launch_bounds__(kFusedThreads, 1) route_metadata_kernel(
       topk_vals[t0 * K + i] = s_slot_v[i];
     }
   };
-  if (!meta_barrier_prefix(ws_hist, E, sh, col_sum, offs, ctrl, timeout_ns, write_topk)) return;
+  if (!meta_barrier_prefix(ws_hist, E_loc, sh, col_sum, offs, ctrl, timeout_ns, write_topk))
+    return;
   meta_scatter(
-      t0 * K, (int)(t1 - t0) * K, E, sh,
+      t0 * K, (int)(t1 - t0) * K, E_loc, sh,
       [&](int i, int &e, uint16_t &w) {
-        e = s_slot_e[i];
+        e = s_map ? s_map[s_slot_e[i]] : s_slot_e[i];
         w = s_slot_v[i];
       },
       col_sorted, row_sorted, gate_scal);
@@ -84,6 +90,8 @@ struct RouteMetaLaunch {
   int32_t *ws_hist;
   uint32_t *ctrl;
   uint32_t *sync;
+  const int32_t *expert_map;
+  int E_loc;
   cudaStream_t s;
   template <int K, int G, int NQ>
   cudaError_t go() {
@@ -111,7 +119,7 @@ struct RouteMetaLaunch {
                     (void *)&vec4, (void *)&indx, (void *)&vals, (void *)&meta->col_sum, (void *)&meta->offs,
                     (void *)&meta->col_sorted, (void *)&meta->row_sorted,
                     (void *)&meta->gate_scal, (void *)&ws_hist, (void *)&ctrl,
-                    (void *)&timeout, (void *)&sync};
+                    (void *)&timeout, (void *)&sync, (void *)&expert_map, (void *)&E_loc};
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)B);
     cfg.blockDim = dim3(kFusedThreads);
@@ -137,13 +145,15 @@ bool route_metadata_fits(int64_t n, int k) {
 cudaError_t launch_route_metadata(const float *logits, int64_t n, int E, int k, int gating,
                                   int32_t *topk_indx, uint16_t *topk_vals,
                                   const moe_routing_meta &meta, int32_t *ws_hist,
-                                  uint32_t *ctrl, cudaStream_t s, uint32_t *sync) {
+                                  uint32_t *ctrl, cudaStream_t s, uint32_t *sync,
+                                  const int32_t *expert_map, int E_loc) {
+  if (!expert_map) E_loc = E;
   // every G (<= 8) lanes take a token: n <= 32 tokens fit one 256-thread CTA
   if (n * k <= kSmallSlots)
     return launch_route_metadata_small(logits, (int)n, E, k, gating, topk_indx, topk_vals, meta,
-                                       sync, s);
+                                       sync, expert_map, E_loc, ctrl, s);
   return dispatch_kg(k, E, RouteMetaLaunch{logits, n, E, gating, topk_indx, topk_vals, &meta,
-                                           ws_hist, ctrl, sync, s});
+                                           ws_hist, ctrl, sync, expert_map, E_loc, s});
 }
 
 }  // namespace moe

@@ -45,7 +45,7 @@ def test_exports_every_declared_function(L):
 
 
 def test_abi_and_status_strings(L):
-    assert L.moe_abi_version() == 2
+    assert L.moe_abi_version() == 3
     for code in range(7):
         s = moe.status_string(code)
         assert s.startswith("MOE_"), s
@@ -153,6 +153,19 @@ def test_ffn_and_forward_parameter_rules(L):
     assert L.moe_forward(good, good, good, good, 8, 4, 2, 64, 64,
                          ctypes.byref(moe.make_params()), good, good, None, None, ws, big,
                          None) == 1
+    # expert map: n_local_experts in [1, E], a 4-byte aligned map (checked
+    # before the n = 0 shortcut, so no launch is needed to see it)
+    def fwd(params, n=0):
+        return L.moe_forward(good, good, good, good, n, 4, 2, 64, 64, ctypes.byref(params), good,
+                             None, None, None, ws, big, None)
+
+    emap = moe.make_params()
+    emap.expert_map = 1 << 20
+    for n_local, rc in ((0, 1), (5, 1), (1, 0), (4, 0)):
+        emap.n_local_experts = n_local
+        assert fwd(emap) == rc, n_local
+    emap.expert_map = (1 << 20) + 2
+    assert fwd(emap) == 6
     assert L.moe_combine(good, 8, 2, 100, good, None) == 1
     assert L.moe_combine(None, 0, 2, 64, None, None) == 0
     assert L.moe_read_status(None, 0, 0, None) == 1
