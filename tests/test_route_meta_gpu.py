@@ -186,3 +186,45 @@ def test_logits_base_only_4_byte_aligned(E, k):
     assert torch.equal(v1.view(torch.int16), v2.view(torch.int16))
     ref_i, _ = oracle.route(host, k)
     np.testing.assert_array_equal(i1.cpu().numpy(), ref_i)
+
+
+def _near_tie_logits(n, E, k, seed):
+    """N(0,1) logits where, per token, an unselected expert (or one of the
+    selected) is moved to within 1..300 ulps of the k-th largest value, above
+    or below it, or onto it exactly: the selection then hinges on the low bits
+    of the fp32 values, below the resolution of the kernels' 32-bit
+    selection keys (which then fall back to exact 64-bit keys)."""
+    rng = np.random.default_rng(seed)
+    logits = rng.standard_normal((n, E)).astype(np.float32)
+    order = np.argsort(-logits, axis=1, kind="stable")
+    bits = logits.view(np.uint32)
+    for t in range(n):
+        kth = order[t, k - 1]
+        other = order[t, rng.integers(k, E)] if rng.random() < 0.7 else order[t, rng.integers(0, k)]
+        if other == kth:
+            continue
+        step = int(rng.integers(-300, 301))
+        v = np.int64(bits[t, kth])
+        # move by `step` ulps in magnitude, staying on the same side of zero
+        bits[t, other] = np.uint32(max(1, min(0x7F7FFFFF, (v & 0x7FFFFFFF) + step)) | (v & 0x80000000))
+    return logits
+
+
+@pytest.mark.parametrize("E,k", [(32, 4), (128, 4), (16, 2), (256, 4), (6, 3)])
+def test_near_ties_below_the_selection_key_resolution(E, k):
+    """Bit-exact top-k (ties to the lower id) when candidates differ only in
+    the lowest mantissa bits, through the route kernel and the fused route +
+    metadata kernel."""
+    n = 4096
+    logits = _near_tie_logits(n, E, k, seed=E * 10 + k)
+    ref_i, ref_v = oracle.route(logits, k)
+    indx, vals = _gpu_route(logits, k)
+    np.testing.assert_array_equal(indx.cpu().numpy(), ref_i)
+    _check_vals(host_bits(vals), ref_v)
+    i2, v2, m2 = moe.route_metadata(dev(logits), k)
+    torch.cuda.synchronize()
+    np.testing.assert_array_equal(i2.cpu().numpy(), ref_i)
+    _check_vals(host_bits(v2), ref_v)
+    ref_m = oracle.metadata(ref_i, host_bits(v2), E)
+    for key in ("col_sum", "offs", "col_sorted", "row_sorted"):
+        np.testing.assert_array_equal(m2[key].cpu().numpy(), ref_m[key], err_msg=key)
