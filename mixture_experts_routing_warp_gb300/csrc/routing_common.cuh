@@ -83,6 +83,13 @@ __device__ __forceinline__ void topk_group(const float *__restrict__ row, bool v
                                            int gating, bool vec4, TopK<K> &tk, float (&w)[K]) {
   const int lane = threadIdx.x & 31, g = lane % G;
   tk.init();
+  // a warp without a token (the tail of a CTA's range) has nothing to rank;
+  // the test is warp-uniform, so the shuffles below stay warp-complete
+  if (!__any_sync(0xffffffffu, valid)) {
+#pragma unroll
+    for (int j = 0; j < K; ++j) w[j] = 0.f;
+    return;
+  }
   const int nq = (E + 3) >> 2;  // chunks of 4 elements in the row
   float4 x[NQ];
   if (vec4) {
@@ -111,6 +118,7 @@ __device__ __forceinline__ void topk_group(const float *__restrict__ row, bool v
     unsigned long long top[4];
 #pragma unroll
     for (int i = 0; i < NQ; ++i) {
+      if (i > 0 && i * G * 4 >= E) break;  // uniform: no lane's chunk holds an expert
       const int e0 = (i * G + g) * 4;
       unsigned long long c[4];
       c[0] = e0 < E ? pack_key(order_key(x[i].x), e0) : 0ull;

@@ -57,6 +57,47 @@ def test_forward_captures_in_a_cuda_graph(case):
         assert _page_sync_counts()[case.E] == 3 * case.E  # the page's masked-loop count
 
 
+@pytest.mark.parametrize("variant", ["expert_map", "fused_gather"])
+def test_rank_and_decode_paths_capture_in_a_cuda_graph(variant):
+    """The expert-map forward (a rank's share, k = 1 through the combine) and
+    the decode forward whose w13 kernel gathers its own rows also run with
+    no host synchronisation: captured, replayed, equal to eager bit for bit."""
+    if variant == "expert_map":
+        case = I.LayerCase("graph_ep", n=600, H=128, E=8, k=1, I=256, gating="softmax_all",
+                           act="swiglu", layout="packed", w_std=0.05, seed=9)
+        h = I.layer_inputs(case)
+        m = np.array([-1, 0, -1, 1, 2, -1, 3, -1], dtype=np.int32)
+        inv = np.array([1, 3, 4, 6])
+        emap = dev(m)
+        params = moe.make_params(case.gating, case.act, case.layout, expert_map=emap,
+                                 n_local_experts=4)
+        w13, w2 = dev_bf16(h["w13"][inv]), dev_bf16(h["w2"][inv])
+    else:
+        case = I.LayerCase("graph_dec", n=3, H=256, E=32, k=4, I=128, act="swiglu_oai",
+                           layout="interleaved", w_std=0.05, seed=4)
+        h = I.layer_inputs(case)
+        params = moe.make_params(case.gating, case.act, case.layout)
+        w13, w2 = dev_bf16(h["w13"]), dev_bf16(h["w2"])
+        assert moe.forward_launch_count(case.n, case.E, case.k, case.H, case.I) == 4
+    x, logits = dev_bf16(h["x"]), dev(h["logits"])
+    ws = moe.workspace(case.n, case.E, case.k, case.H, case.I)
+    eager = moe.forward(x, logits, w13, w2, case.k, params, ws)
+    out = torch.empty_like(eager)
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        moe.forward(x, logits, w13, w2, case.k, params, ws, out=out)
+    torch.cuda.current_stream().wait_stream(s)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        moe.forward(x, logits, w13, w2, case.k, params, ws, out=out)
+    out.fill_(1.0)
+    g.replay()
+    torch.cuda.synchronize()
+    assert torch.equal(out.view(torch.int16), eager.view(torch.int16))
+    assert moe.read_status(ws) == 0
+
+
 def test_repeated_runs_bit_identical():
     case = I.GPTOSS.with_n(512)
     x, logits, w13, w2, params, ws = _setup(case)
