@@ -29,6 +29,12 @@
 //   ffn2: y_flat[col_sorted[m0 + j], f0 + w] = gate_scal[m0 + j] * D[w, j].
 // TMEM is read in chunks of 32 (then 8) token columns up to the tile's rows.
 //
+// Token rows come from X_sorted (the gather kernel's expert-sorted copy) as
+// 2-D boxes, or, with at most 2 slots per expert, straight from the unsorted
+// x: the producer warp reads the tile's rows col_sorted[p] / k and each lane
+// fetches 4 of them per K step with tile::gather4 (one-row boxes). A gather4
+// costs about as much TMA time as a whole box, so wide tiles keep X_sorted.
+//
 // Between the contractions: the w13 kernel counts, per expert, the tiles
 // whose h rows are stored; the w2 kernel waits for those counts instead of
 // for the whole w13 grid, so its tiles of finished experts run on the SMs

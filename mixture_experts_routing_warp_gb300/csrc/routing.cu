@@ -286,8 +286,9 @@ __global__ void __launch_bounds__(kCopyThreads) gather_rows_kernel(
       if (c0 + 32 * q < vec_per_row) v[q] = __ldcs(src + c0 + 32 * q);
     for (int j = 0; j < k; ++j) {
       const int32_t p = __ldg(row_sorted + t * k + j);
-      // a slot whose expert id was out of range has no position (the metadata
-      // kernel flags MOE_ERR_INVALID_ARG)
+      // a slot without a position: another rank's expert under an expert map,
+      // or an out-of-range expert id (the metadata kernel flags
+      // MOE_ERR_INVALID_ARG)
       if ((uint32_t)p >= (uint32_t)N) continue;
       uint4 *dst = x_sorted + (int64_t)p * vec_per_row;
 #pragma unroll

@@ -35,7 +35,7 @@ def _rank_map(E, ranks, r, permute=False):
     return m, inv
 
 
-def _run(case, m, inv, gate=False):
+def _run(case, m, inv, gate=False, ffn_kernel="auto"):
     h = I.layer_inputs(case)
     if gate:  # routing from the router matmul: the oracle routes the GPU's logits
         w_gate = I.router_weight(case)
@@ -43,7 +43,7 @@ def _run(case, m, inv, gate=False):
     E_loc = inv.size
     emap = dev(m)
     params = moe.make_params(case.gating, case.act, case.layout, expert_map=emap,
-                             n_local_experts=E_loc)
+                             n_local_experts=E_loc, ffn_kernel=ffn_kernel)
     x = dev_bf16(h["x"])
     w13 = dev_bf16(h["w13"][inv])
     w2 = dev_bf16(h["w2"][inv])
@@ -91,6 +91,15 @@ def test_gptoss_shaped_rank(n, E, k, ranks, r):
     m, inv = _rank_map(E, ranks, r)
     ref_m, none_local = _run(case, m, inv)
     assert ref_m["offs"][-1] > 0 and (ref_m["row_sorted"] == -1).any()
+
+
+def test_rank_on_the_tokens_on_m_kernel():
+    """The same contract through the tokens-on-M grouped GEMM (X_sorted from
+    the gather kernel, which skips dropped slots)."""
+    case = I.LayerCase("ep_tiled", n=700, H=256, E=16, k=4, I=128, act="swiglu_oai",
+                       layout="interleaved", w_std=0.05, seed=17)
+    m, inv = _rank_map(16, 2, 1, permute=True)
+    _run(case, m, inv, ffn_kernel="tiled")
 
 
 def test_top1_rank_through_the_combine():
