@@ -275,7 +275,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int c = 0; c < nchunk; ++c) {
           uint32_t r[32];
           TMEM_LD32(tbase + c * 32, r);
-          tmem_wait_ld();
+          tmem_wait_ld(r);
 #pragma unroll
           for (int i = 0; i < 32; ++i) {
             const int e = c * 32 + i;
@@ -300,7 +300,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int c = 0; c < nchunk; ++c) {
             uint32_t r[32];
             TMEM_LD32(tbase + c * 32, r);
-            tmem_wait_ld();
+            tmem_wait_ld(r);
 #pragma unroll
             for (int i = 0; i < 32; ++i)
               if (c * 32 + i < En) sum += expf(__uint_as_float(r[i]) - v0);
@@ -322,7 +322,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int c = 0; c < 8; ++c) {
           uint32_t r[32];
           TMEM_LD32(tbase + c * 32, r);
-          tmem_wait_ld();
+          tmem_wait_ld(r);
           const int col = d.nt * BN + c * 32;
           if (valid && col < args.I) {
             uint32_t o[16];
@@ -345,7 +345,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             uint32_t g[32], u[32];
             TMEM_LD32(tbase + c * 32, g);
             TMEM_LD32(tbase + 128 + c * 32, u);
-            tmem_wait_ld();
+            tmem_wait_ld(g, u);
             const int col = d.nt * 128 + c * 32;
             if (valid && col < args.I) {
               uint32_t o[16];
@@ -367,7 +367,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int c = 0; c < 8; ++c) {
             uint32_t r[32];
             TMEM_LD32(tbase + c * 32, r);
-            tmem_wait_ld();
+            tmem_wait_ld(r);
             const int col = d.nt * 128 + c * 16;
             if (valid && col < args.I) {
               uint32_t o[8];
@@ -394,7 +394,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int c = 0; c < 8; ++c) {
           uint32_t r[32];
           TMEM_LD32(tbase + c * 32, r);
-          tmem_wait_ld();
+          tmem_wait_ld(r);
           const int col = d.nt * BN + c * 32;
           if (valid && col < args.H) {
             uint32_t o[16];

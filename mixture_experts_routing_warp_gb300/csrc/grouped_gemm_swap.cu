@@ -301,7 +301,7 @@ template <int EPI, int W, bool FULL = false>
 __device__ __forceinline__ void epi_chunk(EpiTile &t, int c0, const SwArgs &args) {
   uint32_t r0[W];
   tmem_ld<W>(t.taddr + c0, r0);
-  tmem_wait_ld();
+  tmem_wait_ld(r0);
   epi_apply<EPI, W, FULL>(t, c0, r0, args);
 }
 
@@ -333,7 +333,7 @@ __device__ __forceinline__ void sk_piece(EpiTile &et, const SwArgs &args, int64_
   for (int c = 0; c < et.rows; c += 8) {
     uint32_t r0[8];
     tmem_ld<8>(et.taddr + c, r0);
-    tmem_wait_ld();
+    tmem_wait_ld(r0);
 #pragma unroll
     for (int i = 0; i < 8; ++i)
       if (c + i < et.rows) mine[(size_t)(c + i) * SW_M + w_row] = __uint_as_float(r0[i]);

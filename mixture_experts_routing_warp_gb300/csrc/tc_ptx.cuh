@@ -239,6 +239,23 @@ __device__ __forceinline__ void tmem_wait_ld() {
   asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }
 
+// The same wait, with the destination registers of the tcgen05.ld it waits
+// for tied to it: the empty asm statements redefine them after the wait, so
+// no use of a loaded value can be scheduled above it.
+template <int W>
+__device__ __forceinline__ void tmem_wait_ld(uint32_t (&r)[W]) {
+  tmem_wait_ld();
+#pragma unroll
+  for (int i = 0; i < W; ++i) asm volatile("" : "+r"(r[i]));
+}
+
+template <int W>
+__device__ __forceinline__ void tmem_wait_ld(uint32_t (&r0)[W], uint32_t (&r1)[W]) {
+  tmem_wait_ld();
+#pragma unroll
+  for (int i = 0; i < W; ++i) asm volatile("" : "+r"(r0[i]), "+r"(r1[i]));
+}
+
 // Bounded mbarrier wait. Returns false when this wait gave up (records
 // MOE_ERR_TIMEOUT and raises the CTA's abort flag) or another role already
 // aborted.

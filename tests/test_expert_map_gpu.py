@@ -149,3 +149,34 @@ def test_ranks_add_up_to_the_full_layer():
         total += part.float()
     torch.cuda.synchronize()
     assert_layer_close(host_bits(total.to(torch.bfloat16)), host_bits(full), "sum of ranks")
+
+
+@pytest.mark.parametrize("n", [3, 600])  # the one-CTA decode kernel, the cooperative one
+def test_map_entries_outside_the_local_range_flag_invalid_arg(n):
+    """An entry outside [-1, n_local) counts as -1 (its slots are dropped) and
+    records MOE_ERR_INVALID_ARG in the workspace status word; the metadata
+    is the oracle's with that entry set to -1."""
+    case = I.LayerCase(f"ep_bad_n{n}", n=n, H=128, E=8, k=2, I=128, act="swiglu",
+                       layout="interleaved", w_std=0.05, seed=n)
+    h = I.layer_inputs(case)
+    m, inv = _rank_map(8, 2, 0)              # experts 0..3 local
+    ref_i, ref_v = oracle.route(h["logits"], case.k)
+    bad_e = int(ref_i[0, 0])                 # an expert that receives a slot
+    m_bad = m.copy()
+    m_bad[bad_e] = inv.size                  # one past the local range
+    m_ref = m.copy()
+    m_ref[bad_e] = -1
+    emap = dev(m_bad)
+    params = moe.make_params(case.gating, case.act, case.layout, expert_map=emap,
+                             n_local_experts=inv.size)
+    ws = moe.workspace(n, case.E, case.k, case.H, case.I)
+    indx = torch.empty((n, case.k), dtype=torch.int32, device="cuda")
+    vals = torch.empty((n, case.k), dtype=torch.bfloat16, device="cuda")
+    meta = moe.empty_meta(n * case.k, inv.size, "cuda")
+    moe.forward(dev_bf16(h["x"]), dev(h["logits"]), dev_bf16(h["w13"][inv]),
+                dev_bf16(h["w2"][inv]), case.k, params, ws, topk=(indx, vals), meta=meta)
+    assert moe.read_status(ws, reset=True) == 1  # MOE_ERR_INVALID_ARG
+    ref_m = oracle.metadata(indx.cpu().numpy(), host_bits(vals), case.E, expert_map=m_ref,
+                            n_local=inv.size)
+    for key in ("col_sum", "offs", "row_sorted"):
+        np.testing.assert_array_equal(meta[key].cpu().numpy(), ref_m[key], err_msg=key)
