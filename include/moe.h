@@ -292,10 +292,12 @@ moe_status moe_combine(const uint16_t *y_flat, int64_t n, int32_t k, int32_t H, 
 /* Stages 1-4 in one call, zero host synchronisations, CUDA-graph friendly.
  *   x [n, H] bf16, logits [n, E] fp32, w13 [E, 2I, H] bf16 ([E, I, H] for
  *   MOE_ACT_RELU2), w2 [E, H, I] bf16, out [n, H] bf16.
- *   With n*k <= 2E slots and the swap-operand kernel, the w13 contraction
- *   fetches its token rows from x itself (the dispatch gather fused into its
- *   loads, "It is removable in plain PyTorch": x[tok], tok = order // k);
- *   otherwise a gather kernel first copies them into expert-sorted order.
+ *   The dispatch gather ("It is removable in plain PyTorch": x[tok], tok =
+ *   order // k) runs where it costs least: with n*k <= 2E slots and the
+ *   swap-operand kernel, the w13 contraction fetches its token rows from x
+ *   itself; else, when the cooperative route + metadata kernel runs on at
+ *   least half the SMs, it copies the rows into expert-sorted order after
+ *   its scatter; else a gather kernel does.
  *   topk_indx / topk_vals ([n, k]) and meta: optional outputs (NULL = keep
  *   them inside the workspace). When given, all five meta arrays must be
  *   non-NULL. */
@@ -361,12 +363,13 @@ moe_status moe_forward_timed(const uint16_t *x, const float *logits, const uint1
 
 /* Number of kernels moe_forward (and moe_forward_timed) enqueues for these
  * sizes on the current device with the default grouped-GEMM kernel
- * (MOE_FFN_AUTO) and no expert map: route and metadata (one fused kernel when a CTA's slots
- * fit its shared memory, else two), the gather (none when n*k <= 2E: the
- * w13 contraction gathers), the two expert contractions and, when k > 1,
- * the combine; 0 for n = 0; -1 for sizes moe_forward rejects. Host-only:
- * launches nothing. No counterpart on the pages: lets a caller size a CUDA
- * graph or count its launches. */
+ * (MOE_FFN_AUTO) and no expert map: route and metadata (one fused kernel
+ * when a CTA's slots fit its shared memory, else two), the gather (none when
+ * n*k <= 2E, where the w13 contraction gathers, nor when the cooperative
+ * routing kernel copies the rows, on at least half the SMs), the two expert
+ * contractions and, when k > 1, the combine; 0 for n = 0; -1 for sizes
+ * moe_forward rejects. Host-only: launches nothing. No counterpart on the
+ * pages: lets a caller size a CUDA graph or count its launches. */
 int32_t moe_forward_launch_count(int64_t n, int32_t E, int32_t k, int32_t H, int32_t I);
 
 /* How moe_grouped_ffn / moe_forward tile the two expert contractions for these

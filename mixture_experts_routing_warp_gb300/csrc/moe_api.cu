@@ -276,6 +276,13 @@ static moe_status forward_impl(const uint16_t *x, const float *logits, const uin
   auto mark = [&](int i) { return ev ? record_stage_event(ev[i], s) : cudaSuccess; };
 
   int32_t *hist = ws_at<int32_t>(workspace, L.hist);
+  // Where the dispatch rows come from: the w13 contraction gathers them with
+  // a row or two per expert; else the cooperative route + metadata kernel
+  // copies them after its scatter; else (router matmul path, very large or
+  // decode-size batches) the gather kernel.
+  const bool fused_gather = fused_gather_rows(n, E_loc, k, act.ffn_kernel);
+  const bool rows_in_routing =
+      !fused_gather && !w_gate && route_metadata_moves_rows(n, E, k);
   if (w_gate) {
     // router matmul + top-k in one kernel, then the metadata kernel
     if (mark(MOE_STAGE_ROUTE) != cudaSuccess ||
@@ -286,10 +293,12 @@ static moe_status forward_impl(const uint16_t *x, const float *logits, const uin
             cudaSuccess)
       return MOE_ERR_CUDA;
   } else if (route_metadata_fits(n, k)) {
-    // one cooperative kernel for both stages; the metadata stage time is 0
+    // one cooperative kernel for both stages (and the dispatch rows, unless
+    // the w13 contraction gathers them itself); the metadata stage time is 0
     if (mark(MOE_STAGE_ROUTE) != cudaSuccess ||
         launch_route_metadata(logits, n, E, k, gating, indx, vals, m, hist, ctrl, s, scr.sync,
-                              emap, E_loc) != cudaSuccess ||
+                              emap, E_loc, rows_in_routing ? x : nullptr, H,
+                              x_sorted) != cudaSuccess ||
         mark(MOE_STAGE_METADATA) != cudaSuccess)
       return MOE_ERR_CUDA;
   } else {
@@ -303,13 +312,11 @@ static moe_status forward_impl(const uint16_t *x, const float *logits, const uin
   }
   // A row or two per expert: the swap-operand kernel gathers its token rows
   // from x itself (tile::gather4, one instruction per 4 rows). Otherwise they
-  // come from X_sorted, materialised by the gather kernel: a gather4 costs
-  // about as much TMA time as a whole 2-D box, so 128 rows per K step as 32
-  // gathers ran w13 3.4x slower at prefill.
-  const bool fused_gather = fused_gather_rows(n, E_loc, k, act.ffn_kernel);
+  // come from X_sorted: a gather4 costs about as much TMA time as a whole 2-D
+  // box, so 128 rows per K step as 32 gathers ran w13 3.4x slower at prefill.
   const GatherSrc src{x, n, k};
   if (mark(MOE_STAGE_GATHER) != cudaSuccess ||
-      (!fused_gather &&
+      (!fused_gather && !rows_in_routing &&
        launch_gather_rows(x, m.row_sorted, n, k, H, x_sorted, scr.sync, s) != cudaSuccess))
     return MOE_ERR_CUDA;
   if (launch_ffn(x_sorted, m.offs, m.col_sorted, m.gate_scal, w13, w2, N, E_loc, H, I, act, h,
@@ -349,9 +356,11 @@ int32_t moe_forward_launch_count(int64_t n, int32_t E, int32_t k, int32_t H, int
   if (check_sizes(n, E, k, H, I, true) != MOE_OK) return -1;
   if (n == 0) return 0;
   // the same choices forward_impl makes (default kernel: the swap-operand
-  // one), then the gather unless w13 gathers its rows, ffn1, ffn2, combine
-  return (route_metadata_fits(n, k) ? 1 : 2) + (fused_gather_rows(n, E, k, MOE_FFN_AUTO) ? 0 : 1) +
-         2 + (k > 1 ? 1 : 0);
+  // one), then the gather unless w13 or the cooperative routing kernel moves
+  // the rows, ffn1, ffn2, combine
+  const bool gather_kernel =
+      !fused_gather_rows(n, E, k, MOE_FFN_AUTO) && !route_metadata_moves_rows(n, E, k);
+  return (route_metadata_fits(n, k) ? 1 : 2) + (gather_kernel ? 1 : 0) + 2 + (k > 1 ? 1 : 0);
 }
 
 moe_status moe_forward(const uint16_t *x, const float *logits, const uint16_t *w13,

@@ -384,7 +384,13 @@ cudaError_t launch_route_metadata(const float *logits, int64_t n, int E, int k, 
                                   int32_t *topk_indx, uint16_t *topk_vals,
                                   const moe_routing_meta &meta, int32_t *ws_hist,
                                   uint32_t *ctrl, cudaStream_t s, uint32_t *sync = nullptr,
-                                  const int32_t *expert_map = nullptr, int E_loc = 0);
+                                  const int32_t *expert_map = nullptr, int E_loc = 0,
+                                  const uint16_t *x = nullptr, int H = 0,
+                                  uint16_t *x_sorted = nullptr);
+// launch_route_metadata with x given copies the dispatch rows into x_sorted;
+// moe_forward gives it x exactly when this holds for (n, E, k) (the
+// cooperative kernel runs on at least half the SMs).
+bool route_metadata_moves_rows(int64_t n, int E, int k);
 
 // sync (may be null): the kSyncWords per-forward sync words of the expert
 // contractions, zeroed by these kernels (and by the gather)

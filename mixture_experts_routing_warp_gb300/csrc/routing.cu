@@ -254,48 +254,25 @@ cudaError_t launch_metadata_noalloc(const int32_t *topk_indx, const uint16_t *to
 
 // ======================================================= gather rows ==
 // X_sorted[p] = x[col_sorted[p] / k]: the dispatch index_select of the
-// MiniMind issue ("It is removable in plain PyTorch"), done token-major: a
-// warp per (token t, group of 128 16-byte chunks) reads its chunks of x[t]
-// once (up to 4 loads in flight per thread) and writes them to the k sorted
-// positions row_sorted[t*k + j] of the token's slots, so x is read from
-// memory once rather than once per slot. Block 0 also zeroes the sync words
-// of this forward's expert contractions.
+// MiniMind issue ("It is removable in plain PyTorch"), done token-major by
+// copy_token_rows: x is read from memory once rather than once per slot.
+// (moe_forward runs it only where neither the fused route + metadata kernel
+// nor the w13 contraction moves the rows.) Block 0 also zeroes the sync
+// words of this forward's expert contractions.
 constexpr int kCopyThreads = 256;
 
-constexpr int kChunksPerLane = 4;  // 16-byte chunks in flight per thread
+constexpr int kChunksPerLane = 4;  // 16-byte chunks in flight per thread (copy_token_rows)
 
 __global__ void __launch_bounds__(kCopyThreads) gather_rows_kernel(
     const uint4 *__restrict__ x, const int32_t *__restrict__ row_sorted, int64_t n, int k,
-    int vec_per_row, int groups_per_row, uint4 *__restrict__ x_sorted, uint32_t *sync) {
+    int vec_per_row, uint4 *__restrict__ x_sorted, uint32_t *sync) {
   pdl_launch_dependents();
   pdl_wait();  // row_sorted comes from the metadata kernel
   if (sync && blockIdx.x == 0)
     for (int i = threadIdx.x; i < kSyncWords; i += kCopyThreads) sync[i] = 0;
-  const int lane = threadIdx.x & 31;
-  const int64_t N = n * k;
-  const int64_t units = n * groups_per_row;  // (token, group of 32 * kChunksPerLane chunks)
-  const int64_t warps = (int64_t)gridDim.x * (kCopyThreads / 32);
-  for (int64_t u = (int64_t)blockIdx.x * (kCopyThreads / 32) + (threadIdx.x >> 5); u < units;
-       u += warps) {
-    const int64_t t = u / groups_per_row;
-    const int c0 = (int)(u - t * groups_per_row) * 32 * kChunksPerLane + lane;
-    const uint4 *src = x + t * vec_per_row;
-    uint4 v[kChunksPerLane];
-#pragma unroll
-    for (int q = 0; q < kChunksPerLane; ++q)
-      if (c0 + 32 * q < vec_per_row) v[q] = __ldcs(src + c0 + 32 * q);
-    for (int j = 0; j < k; ++j) {
-      const int32_t p = __ldg(row_sorted + t * k + j);
-      // a slot without a position: another rank's expert under an expert map,
-      // or an out-of-range expert id (the metadata kernel flags
-      // MOE_ERR_INVALID_ARG)
-      if ((uint32_t)p >= (uint32_t)N) continue;
-      uint4 *dst = x_sorted + (int64_t)p * vec_per_row;
-#pragma unroll
-      for (int q = 0; q < kChunksPerLane; ++q)
-        if (c0 + 32 * q < vec_per_row) dst[c0 + 32 * q] = v[q];
-    }
-  }
+  copy_token_rows(x, row_sorted, 0, n, k, vec_per_row, n * k, x_sorted,
+                  (int64_t)blockIdx.x * (kCopyThreads / 32) + (threadIdx.x >> 5),
+                  (int64_t)gridDim.x * (kCopyThreads / 32));
 }
 
 cudaError_t launch_gather_rows(const uint16_t *x, const int32_t *row_sorted, int64_t n, int k,
@@ -313,7 +290,7 @@ cudaError_t launch_gather_rows(const uint16_t *x, const int32_t *row_sorted, int
   if (blocks > cap) blocks = cap;
   cudaError_t err = launch_dependent(gather_rows_kernel, dim3((unsigned)blocks), dim3(kCopyThreads),
                                      0, s, reinterpret_cast<const uint4 *>(x), row_sorted, n, k,
-                                     vpr, gpr, reinterpret_cast<uint4 *>(x_sorted), sync);
+                                     vpr, reinterpret_cast<uint4 *>(x_sorted), sync);
   return err != cudaSuccess ? err : cudaGetLastError();
 }
 

@@ -460,6 +460,41 @@ __device__ __forceinline__ const int *load_expert_map(const int32_t *expert_map,
   return s_map;
 }
 
+// Dispatch rows X_sorted[row_sorted[t*k + j]] = x[t] for tokens [t_lo, t_hi)
+// ("It is removable in plain PyTorch": x[tok], tok = order // k), token-major:
+// a warp per (token, group of 128 16-byte chunks), 4 chunks in flight per
+// lane, x[t] read once and written to the token's k sorted positions; a
+// position outside [0, N) (a dropped slot) is skipped. row_sorted is read
+// through L2 (the calling kernel may have written it). `warp` of `warps`:
+// this warp's share of the (token, group) units.
+__device__ __forceinline__ void copy_token_rows(const uint4 *__restrict__ x,
+                                                const int32_t *row_sorted, int64_t t_lo,
+                                                int64_t t_hi, int k, int vpr, int64_t N,
+                                                uint4 *__restrict__ x_sorted, int64_t warp,
+                                                int64_t warps) {
+  constexpr int kChunks = 4;  // 16-byte chunks in flight per lane
+  const int lane = threadIdx.x & 31;
+  const int gpr = (vpr + 32 * kChunks - 1) / (32 * kChunks);
+  const int64_t units = (t_hi - t_lo) * gpr;
+  for (int64_t u = warp; u < units; u += warps) {
+    const int64_t t = t_lo + u / gpr;
+    const int c0 = (int)(u % gpr) * 32 * kChunks + lane;
+    const uint4 *src = x + t * vpr;
+    uint4 v[kChunks];
+#pragma unroll
+    for (int q = 0; q < kChunks; ++q)
+      if (c0 + 32 * q < vpr) v[q] = __ldcs(src + c0 + 32 * q);
+    for (int j = 0; j < k; ++j) {
+      const int32_t p = __ldcg(row_sorted + t * k + j);
+      if ((uint64_t)(uint32_t)p >= (uint64_t)N) continue;
+      uint4 *dst = x_sorted + (int64_t)p * vpr;
+#pragma unroll
+      for (int q = 0; q < kChunks; ++q)
+        if (c0 + 32 * q < vpr) dst[c0 + 32 * q] = v[q];
+    }
+  }
+}
+
 // Decode sizes (n*k <= kSmallSlots): route + metadata in one CTA
 // (routing_small.cu).
 constexpr int kSmallSlots = 32;

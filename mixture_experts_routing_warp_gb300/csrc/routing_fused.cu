@@ -14,7 +14,8 @@ namespace moe {
 // token as above), keeping its slots and histogram in shared memory, then
 // publishes, gathers and scatters its slots from shared memory. With an
 // expert map the metadata covers the E_loc local experts and drops the slots
-// of other ranks' experts.
+// of other ranks' experts. With x given, the CTA then copies its tokens' rows
+// to their sorted positions in X_sorted (the dispatch gather, token-major).
 template <int K, int G, int NQ>
 __global__ void __launch_bounds__(kFusedThreads, 1) route_metadata_kernel(
     const float *__restrict__ logits, int64_t n, int E, int gating, int T, int vec4,
@@ -22,7 +23,8 @@ __global__ void __launch_bounds__(kFusedThreads, 1) route_metadata_kernel(
     int32_t *__restrict__ col_sum, int32_t *__restrict__ offs, int32_t *__restrict__ col_sorted,
     int32_t *__restrict__ row_sorted, uint16_t *__restrict__ gate_scal,
     int32_t *__restrict__ ws_hist, uint32_t *ctrl, unsigned long long timeout_ns,
-    uint32_t *sync, const int32_t *__restrict__ expert_map, int E_loc) {
+    uint32_t *sync, const int32_t *__restrict__ expert_map, int E_loc,
+    const uint4 *__restrict__ x, int vpr, uint4 *__restrict__ x_sorted) {
   extern __shared__ uint8_t smem_raw[];
   __shared__ MetaShared<kFusedThreads> sh;
   __shared__ int s_map_buf[kMaxExperts];
@@ -67,6 +69,11 @@ __global__ void __launch_bounds__(kFusedThreads, 1) route_metadata_kernel(
         w = s_slot_v[i];
       },
       col_sorted, row_sorted, gate_scal);
+  if (x) {
+    __syncthreads();  // this CTA's row_sorted entries are written
+    copy_token_rows(x, row_sorted, t0, t1, K, vpr, n * K, x_sorted, tid >> 5,
+                    kFusedThreads / 32);
+  }
 }
 
 // Tokens per CTA of the fused kernel: spread over the SMs, a multiple of 4;
@@ -96,6 +103,9 @@ struct RouteMetaLaunch {
   uint32_t *sync;
   const int32_t *expert_map;
   int E_loc;
+  const uint16_t *x;
+  int H;
+  uint16_t *x_sorted;
   cudaStream_t s;
   template <int K, int G, int NQ>
   cudaError_t go() {
@@ -119,11 +129,15 @@ struct RouteMetaLaunch {
     int E_ = E, g_ = gating;
     int vec4 = (E % 4) == 0 && ((uintptr_t)logits % 16) == 0;
     unsigned long long timeout = kWaitTimeoutNs;
+    const uint4 *xv = reinterpret_cast<const uint4 *>(x);
+    uint4 *xs = reinterpret_cast<uint4 *>(x_sorted);
+    int vpr = H / 8;
     void *args[] = {(void *)&logits, (void *)&nn, (void *)&E_, (void *)&g_, (void *)&Ti,
                     (void *)&vec4, (void *)&indx, (void *)&vals, (void *)&meta->col_sum, (void *)&meta->offs,
                     (void *)&meta->col_sorted, (void *)&meta->row_sorted,
                     (void *)&meta->gate_scal, (void *)&ws_hist, (void *)&ctrl,
-                    (void *)&timeout, (void *)&sync, (void *)&expert_map, (void *)&E_loc};
+                    (void *)&timeout, (void *)&sync, (void *)&expert_map, (void *)&E_loc,
+                    (void *)&xv, (void *)&vpr, (void *)&xs};
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)B);
     cfg.blockDim = dim3(kFusedThreads);
@@ -146,18 +160,33 @@ bool route_metadata_fits(int64_t n, int k) {
   return fused_tokens_per_cta(n, 0) * k <= kSlotCap;  // the larger of the two T
 }
 
+// True when launch_route_metadata, given x, also moves the dispatch rows for
+// (n, E, k): the cooperative kernel runs (not the decode-size one) on at
+// least half the SMs. Each CTA copies its own tokens' rows, so a narrow grid
+// would copy at the pace of a few SMs (GPT-OSS, 64 tokens on one CTA: +25 us;
+// MiniMind, 4096 tokens on 32 CTAs: +2 us); at prefill widths the copy
+// replaces the gather kernel (GPT-OSS n=8192: 1.153 -> 1.142 ms per layer).
+bool route_metadata_moves_rows(int64_t n, int E, int k) {
+  if (!route_metadata_fits(n, k) || n * k <= kSmallSlots) return false;
+  const int G = E <= 16 ? 1 : E <= 32 ? 2 : E <= 64 ? 4 : 8;  // as dispatch_kg
+  const int64_t T = fused_tokens_per_cta(n, kFusedThreads / G);
+  return 2 * ((n + T - 1) / T) >= device_sm_count();
+}
+
 cudaError_t launch_route_metadata(const float *logits, int64_t n, int E, int k, int gating,
                                   int32_t *topk_indx, uint16_t *topk_vals,
                                   const moe_routing_meta &meta, int32_t *ws_hist,
                                   uint32_t *ctrl, cudaStream_t s, uint32_t *sync,
-                                  const int32_t *expert_map, int E_loc) {
+                                  const int32_t *expert_map, int E_loc, const uint16_t *x,
+                                  int H, uint16_t *x_sorted) {
   if (!expert_map) E_loc = E;
   // every G (<= 8) lanes take a token: n <= 32 tokens fit one 256-thread CTA
   if (n * k <= kSmallSlots)
     return launch_route_metadata_small(logits, (int)n, E, k, gating, topk_indx, topk_vals, meta,
                                        sync, expert_map, E_loc, ctrl, s);
   return dispatch_kg(k, E, RouteMetaLaunch{logits, n, E, gating, topk_indx, topk_vals, &meta,
-                                           ws_hist, ctrl, sync, expert_map, E_loc, s});
+                                           ws_hist, ctrl, sync, expert_map, E_loc, x, H,
+                                           x_sorted, s});
 }
 
 }  // namespace moe

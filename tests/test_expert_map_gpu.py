@@ -95,7 +95,7 @@ def test_gptoss_shaped_rank(n, E, k, ranks, r):
 
 def test_rank_on_the_tokens_on_m_kernel():
     """The same contract through the tokens-on-M grouped GEMM (X_sorted from
-    the gather kernel, which skips dropped slots)."""
+    the routing kernel's row copy, which skips dropped slots)."""
     case = I.LayerCase("ep_tiled", n=700, H=256, E=16, k=4, I=128, act="swiglu_oai",
                        layout="interleaved", w_std=0.05, seed=17)
     m, inv = _rank_map(16, 2, 1, permute=True)

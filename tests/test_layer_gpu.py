@@ -256,6 +256,26 @@ def test_fused_gather_matches_materialised_rows(n, E, k, H, I_, act, layout):
     _check_full(L)
 
 
+@pytest.mark.parametrize("act,layout", [("swiglu_oai", "interleaved"), ("swiglu", "packed")])
+def test_routing_kernel_rows_match_the_gather_kernel(act, layout):
+    """With the cooperative route + metadata kernel on all SMs, moe_forward's
+    dispatch rows are copied by that kernel after its scatter (no gather
+    kernel); the stage path copies them with the gather kernel. Same rows,
+    same arithmetic: the outputs agree bit for bit."""
+    case = I.LayerCase(f"rows_in_routing_{act}", n=4096, H=256, E=32, k=4, I=128, act=act,
+                       layout=layout, w_std=0.05, seed=41)
+    assert moe.forward_launch_count(case.n, case.E, case.k, case.H, case.I) == 4
+    L = Layer(case)
+    out_fwd = L.forward()[0]
+    ws = moe.workspace(case.n, case.E, case.k, case.H, case.I)
+    indx, vals = moe.route(L.logits, case.k, case.gating)
+    meta = moe.build_metadata(indx, vals, case.E, ws)
+    y_flat = moe.grouped_ffn(L.x, meta, L.w13, L.w2, case.k, ws, L.params)
+    out = moe.combine(y_flat, case.n, case.k)
+    torch.cuda.synchronize()
+    assert torch.equal(out.view(torch.int16), out_fwd.view(torch.int16))
+
+
 def test_empty_batch_is_a_noop():
     c = I.TINY
     L = Layer(c)
