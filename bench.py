@@ -44,7 +44,7 @@ os.environ.setdefault("OMP_NUM_THREADS", str(os.cpu_count() or 1))
 
 import numpy as np  # noqa: E402
 
-from mixture_experts_routing_warp_gb300 import inputs as I  # noqa: E402
+import moe_inputs as I  # noqa: E402
 
 METRIC = "MoE-layer tokens/s and routing-metadata µs/call on 1 GB300; % of roofline"
 WORKLOADS = {

@@ -1,4 +1,5 @@
-"""Seeded synthetic inputs for the MoE layer forward.
+"""Seeded synthetic inputs for the MoE layer forward (test and benchmark
+support, not part of the library package).
 
 This module is the only code that both the CUDA path's tests/bench and the
 CPU oracle's tests use. It draws random numbers and stores them as fp32 or

@@ -17,7 +17,7 @@ sys.path.insert(0, os.path.dirname(os.path.dirname(HERE)))
 import numpy as np  # noqa: E402
 
 import oracle  # noqa: E402
-from mixture_experts_routing_warp_gb300 import inputs as I  # noqa: E402
+import moe_inputs as I  # noqa: E402
 
 OUT = os.path.join(HERE, "tiny_layer_oracle.txt")
 

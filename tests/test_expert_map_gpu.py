@@ -16,7 +16,7 @@ import torch
 
 import mixture_experts_routing_warp_gb300 as moe
 import oracle
-from mixture_experts_routing_warp_gb300 import inputs as I
+import moe_inputs as I
 
 from helpers import assert_layer_close, dev, dev_bf16, host_bits
 

@@ -14,7 +14,7 @@ import pytest
 import torch
 
 import mixture_experts_routing_warp_gb300 as moe
-from mixture_experts_routing_warp_gb300 import inputs as I
+import moe_inputs as I
 
 from helpers import dev, dev_bf16
 

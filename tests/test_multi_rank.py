@@ -31,7 +31,7 @@ def _rank_main(rank: int, world: int, port: int, q) -> None:
                       MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
     sys.path.insert(0, ROOT)
     import bench
-    from mixture_experts_routing_warp_gb300 import inputs as I
+    import moe_inputs as I
 
     r, w, _, pg = bench.dist_setup(argparse.Namespace(impl="ours"))
     out = {"rank": r, "world": w, "backend": pg.get_backend()}

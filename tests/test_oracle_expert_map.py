@@ -12,7 +12,7 @@ import numpy as np
 import pytest
 
 import oracle
-from mixture_experts_routing_warp_gb300 import inputs as I
+import moe_inputs as I
 
 E, H, I_ = 8, 64, 128
 

@@ -24,7 +24,7 @@ import numpy as np
 import pytest
 
 import oracle
-from mixture_experts_routing_warp_gb300 import inputs as I
+import moe_inputs as I
 
 ONE = 0x3F80  # bf16 1.0
 
@@ -242,7 +242,7 @@ def test_token_subset_matches_full_run():
 def test_thread_count_does_not_change_bits(monkeypatch):
     import subprocess, sys, os
     code = ("import sys; sys.path.insert(0, '.'); import oracle, numpy as np;"
-            "from mixture_experts_routing_warp_gb300 import inputs as I;"
+            "import moe_inputs as I;"
             "c = I.TINY; d = I.layer_inputs(c); i, v = oracle.route(d['logits'], c.k);"
             "print(oracle.ffn(d['x'], i, v, d['w13'], d['w2']).tobytes().hex())")
     root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))

@@ -11,7 +11,7 @@ import os
 import numpy as np
 
 import oracle
-from mixture_experts_routing_warp_gb300 import inputs as I
+import moe_inputs as I
 
 GOLDEN = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden")
 

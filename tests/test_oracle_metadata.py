@@ -10,7 +10,7 @@ import pytest
 import torch
 
 import oracle
-from mixture_experts_routing_warp_gb300 import inputs as I
+import moe_inputs as I
 
 CASES = [(n, E, k) for n in (1, 33, 512, 4096) for (E, k) in ((32, 4), (128, 4))] + [
     (0, 8, 2), (5, 1, 1), (100, 3, 3), (257, 16, 1)]

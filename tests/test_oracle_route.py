@@ -11,7 +11,7 @@ import numpy as np
 import pytest
 
 import oracle
-from mixture_experts_routing_warp_gb300 import inputs as I
+import moe_inputs as I
 
 
 def _brute_topk(row: np.ndarray, k: int):

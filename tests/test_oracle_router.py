@@ -12,7 +12,7 @@ MoE forward" report (功能与动机) names as the fusion issue #28986 asks for:
 import numpy as np
 
 import oracle
-from mixture_experts_routing_warp_gb300 import inputs as I
+import moe_inputs as I
 
 ONE = 0x3F80
 

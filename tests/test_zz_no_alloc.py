@@ -18,7 +18,7 @@ import pytest
 import torch
 
 import mixture_experts_routing_warp_gb300 as moe
-from mixture_experts_routing_warp_gb300 import inputs as I
+import moe_inputs as I
 
 pytestmark = pytest.mark.gpu
 
