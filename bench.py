@@ -213,6 +213,15 @@ class ClockSampler:
                 "samples": len(rows_used)}
 
 
+def workload_config(c: I.LayerCase, world: int) -> dict:
+    """The workload a line is measured on (both arms print the same dict)."""
+    return {"workload": c.name, "n_tokens": c.n, "hidden": c.H, "n_experts": c.E,
+            "topk": c.k, "intermediate": c.I, "gating": c.gating, "activation": c.act,
+            "w13_layout": c.layout,
+            "l2": "inputs of consecutive steps exceed L2 (rotated input sets)",
+            "parallelism": f"replicas x{world} (token batches per rank)"}
+
+
 # ---------------------------------------------------------- algorithmic --
 def stage_work(c: I.LayerCase, touched: float = None, pk: dict = None) -> dict:
     """Algorithmic work of one launch of each stage kernel: ("hbm", bytes) or
@@ -690,10 +699,42 @@ def oracle_sample(c: I.LayerCase, d: dict, budget_s: float = 12.0, max_tokens: i
         if dt >= budget_s * 0.4 or toks.size >= min(c.n, max_tokens) or spent >= budget_s:
             break
         m = int(min(c.n, max_tokens, max(2 * m, toks.size * budget_s * 0.5 / max(dt, 1e-3))))
-    cores = int(os.environ.get("OMP_NUM_THREADS", os.cpu_count() or 1))
-    return {"value": round(rate, 3), "unit": "tokens/s", "cores": cores, "kind": "oracle",
+    return {"value": round(rate, 3), "unit": "tokens/s", "cores": oracle.num_threads(),
+            "affinity_cores": len(os.sched_getaffinity(0)), "kind": "oracle",
             "sample": f"route+metadata over all {c.n} tokens, FFN+combine over the first "
-                      f"{toks.size} tokens ({dt:.1f} s); float64 C oracle, OpenMP over tokens"}
+                      f"{toks.size} tokens ({dt:.1f} s); float64 C oracle, OpenMP over tokens",
+            "ffn_tokens": int(toks.size), "sample_s": round(route_meta_s + dt, 3)}
+
+
+def oracle_sample_with_output(c: I.LayerCase, d: dict, budget_s: float = 12.0,
+                              max_tokens: int = 4096):
+    """oracle_sample, plus the oracle's layer output for the first m tokens
+    (recomputed untimed) so that the GPU's output can be checked against it."""
+    import oracle
+    rec = oracle_sample(c, d, budget_s, max_tokens)
+    m = rec["ffn_tokens"]
+    indx, vals = oracle.route(d["logits"], c.k, c.gating)
+    toks = np.arange(m, dtype=np.int64)
+    ref = oracle.ffn(d["x"], indx, vals, d["w13"], d["w2"], tokens=toks, act=c.act,
+                     layout=c.layout)
+    return rec, toks, ref
+
+
+def parity_vs_oracle(got_bits: np.ndarray, ref_bits: np.ndarray) -> dict:
+    """|gpu - ref| <= 3e-2 + 2e-2 |ref| elementwise, cosine > 0.99 and relative
+    L2 <= 1e-2 over the sampled rows (the tolerance the parity tests use)."""
+    def f64(b):
+        return (np.asarray(b, np.uint16).astype(np.uint32) << np.uint32(16)).view(
+            np.float32).astype(np.float64)
+    got, ref = f64(got_bits), f64(ref_bits)
+    err = np.abs(got - ref)
+    nref = float(np.linalg.norm(ref))
+    cos = float(np.dot(got.ravel(), ref.ravel()) / (np.linalg.norm(got) * nref)) if nref else 0.0
+    rel = float(np.linalg.norm(got - ref) / nref) if nref else 0.0
+    n_bad = int((err > 3e-2 + 2e-2 * np.abs(ref)).sum())
+    return {"rows": int(got.shape[0]), "max_abs": float(err.max()) if err.size else 0.0,
+            "cos": round(cos, 6), "rel_l2": rel, "n_bad": n_bad,
+            "ok": bool(n_bad == 0 and cos > 0.99 and rel <= 1e-2)}
 
 
 def run_reference(args, rank, world, pg):
@@ -704,23 +745,30 @@ def run_reference(args, rank, world, pg):
     budget = max(1.0, 90.0 / max(args.steps + args.warmup, 1))
     for _ in range(args.warmup):
         oracle_sample(c, d, budget_s=budget, max_tokens=64)
-    steps_v = []
+    steps_v, steps_s = [], []
     t0 = time.time()
     for i in range(args.steps):
+        t = time.perf_counter()
         r = oracle_sample(c, d, budget_s=budget, max_tokens=512)
+        steps_s.append(time.perf_counter() - t)
         steps_v.append(r["value"])
     wall = time.time() - t0
     value = float(np.median(steps_v))
+    # a step is one bounded sample of the workload (routing of every token,
+    # the FFN of the first tokens); ms_per_step is the time such a step took
     line = {"impl": "reference", "metric": METRIC, "value": round(value, 3), "unit": "tokens/s",
             "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
-            "ms_per_step": round(1e3 * c.n / value, 1) if value else None,
+            "ms_per_step": round(1e3 * float(np.mean(steps_s)), 1),
+            "step": "one bounded sample of the workload (see cpu_baseline.sample)",
+            "ms_per_layer_extrapolated": round(1e3 * c.n / value, 1) if value else None,
+            "extrapolated": True,
             "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": {"workload": c.name, "n_tokens": c.n, "hidden": c.H, "n_experts": c.E,
-                       "topk": c.k, "intermediate": c.I, "gating": c.gating,
-                       "activation": c.act, "w13_layout": c.layout, "l2": "n/a (CPU)"},
+            "config": workload_config(c, world),
+            "l2_note": "CPU run: the GPU arm's input rotation does not apply",
             "cpu_baseline": {"value": round(value, 3), "unit": "tokens/s", "kind": "oracle",
-                             "cores": r["cores"], "sample": r["sample"]},
+                             "cores": r["cores"], "affinity_cores": r["affinity_cores"],
+                             "sample": r["sample"]},
             "e2e": {"value": round(value, 3), "unit": "tokens/s", "h2d_bytes_per_step": 0,
                     "d2h_bytes_per_step": 0},
             "gpu_launches": 0, "wall_s": round(wall, 1)}
@@ -790,12 +838,11 @@ def run_ours(args, rank, world, local, pg):
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 4),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
             "data": "synthetic (seeded numpy PCG64, N(0,1) tokens, N(0,0.02) weights)",
-            "config": {"workload": c.name, "n_tokens": c.n, "hidden": c.H, "n_experts": c.E,
-                       "topk": c.k, "intermediate": c.I, "gating": c.gating,
-                       "activation": c.act, "w13_layout": c.layout, "ffn_kernel": args.ffn_kernel,
-                       "l2": f"inputs rotated over {dc.n_xsets} token sets and {dc.n_wsets} "
-                             f"weight sets (> 2x L2 per step cycle)",
-                       "parallelism": f"replicas x{world} (token batches per rank)"},
+            "config": workload_config(c, world),
+            "ffn_kernel": args.ffn_kernel,
+            "l2_sets": {"token_sets": dc.n_xsets, "weight_sets": dc.n_wsets,
+                        "how": "x / logits and the weights rotated so that consecutive steps' "
+                               "inputs total more than 2x L2"},
             "roofline": roof,
             "stage_ms": {k: round(v, 4) for k, v in stage_ms.items()},
             "gpu_launches": kernels_per_step * args.steps,
@@ -820,7 +867,7 @@ def run_ours(args, rank, world, local, pg):
                                                                         device, l2, pk, source),
                     "routing_metadata_16k_e32": time_routing(16384, 32, 4, device, l2, pk,
                                                              source)}
-            for name in ("minimind_e4", "minimind_e16"):
+            for name in ("minimind_e4", "minimind_e8", "minimind_e16"):
                 if WORKLOADS[name] != c:
                     mm = DeviceCase(WORKLOADS[name], device, l2)
                     also[name] = time_layer_graph(mm, 64, pk, source)
@@ -833,11 +880,81 @@ def run_ours(args, rank, world, local, pg):
                         key = f"gptoss_decode_n{nd}" + ("" if fk == "auto" else "_tiled")
                         also[key] = time_layer_graph(cd, 64, pk, source)
                         del cd
+                if c.n != 2048:
+                    cp = DeviceCase(I.GPTOSS.with_n(2048), device, l2, weights=dc)
+                    also["gptoss_prefill_n2048"] = time_layer_graph(cp, 32, pk, source)
+                    del cp
+            if WORKLOADS["skewed_n16384"] != c:
+                del dc.w13, dc.w2   # make room for the 128 experts' weights
+                torch.cuda.empty_cache()
+                sk = DeviceCase(WORKLOADS["skewed_n16384"], device, l2)
+                also["skewed_n16384"] = time_layer_graph(sk, 16, pk, source)
+                del sk
+                torch.cuda.empty_cache()
+            also["host_sync_roundtrip_us"] = host_sync_roundtrip_us(device)
             line["also"] = also
         if not args.no_cpu_baseline:
-            line["cpu_baseline"] = oracle_sample(c, oracle_inputs(c))
+            rec, toks, ref = oracle_sample_with_output(c, oracle_inputs(c))
+            line["cpu_baseline"] = rec
+        else:
+            import oracle
+            d0 = oracle_inputs(c)
+            toks = np.arange(min(c.n, 64), dtype=np.int64)
+            ix, vx = oracle.route(d0["logits"], c.k, c.gating)
+            ref = oracle.ffn(d0["x"], ix, vx, d0["w13"], d0["w2"], tokens=toks, act=c.act,
+                             layout=c.layout)
+        line["parity"] = check_timed_output(c, device, l2, toks, ref, args.ffn_kernel)
         print(json.dumps(line), flush=True)
+        if not line["parity"]["ok"]:
+            log(f"parity against the oracle failed: {line['parity']}")
+            return 1
     return 0
+
+
+def host_sync_roundtrip_us(device, reps: int = 100) -> dict:
+    """What one device->host synchronisation costs on this host: a one-element
+    reduction whose result the host reads (.item()), repeated; the cost a
+    layer pays per readback in a loop that syncs ([P2] Measurement: the
+    per-sync ruler)."""
+    import torch
+    flag = torch.zeros(1, dtype=torch.bool, device=device)
+    for _ in range(20):
+        flag.any().item()
+    torch.cuda.synchronize()
+    ts = []
+    for _ in range(reps):
+        t = time.perf_counter()
+        flag.any().item()
+        ts.append(time.perf_counter() - t)
+    return {"us_median": round(1e6 * float(np.median(ts)), 2),
+            "us_mean": round(1e6 * float(np.mean(ts)), 2), "reps": reps,
+            "syncs_per_layer_here": 0,
+            "how": "1-element bool any() + .item(), 100 times after 20 warm-up calls"}
+
+
+def check_timed_output(c: I.LayerCase, device, l2, toks, ref, ffn_kernel) -> dict:
+    """One more forward of the benchmarked call on token set 0 / weight set 0
+    (the oracle's inputs) and its first rows against the oracle's output."""
+    import torch
+    import mixture_experts_routing_warp_gb300 as moe
+    hx = I.layer_x(c)
+    x = torch.from_numpy(hx.view(np.int16)).view(torch.bfloat16).to(device)
+    lg = torch.from_numpy(I.layer_logits(c, hx)).to(device)
+    w13 = torch.from_numpy(I.all_w13(c).view(np.int16)).view(torch.bfloat16).to(device)
+    w2 = torch.from_numpy(I.all_w2(c).view(np.int16)).view(torch.bfloat16).to(device)
+    params = moe.make_params(c.gating, c.act, c.layout, ffn_kernel=ffn_kernel)
+    ws = moe.workspace(c.n, c.E, c.k, c.H, c.I, device)
+    out = moe.forward(x, lg, w13, w2, c.k, params, ws)
+    torch.cuda.synchronize()
+    status = moe.read_status(ws)
+    got = out.cpu().view(torch.int16).numpy().view(np.uint16)[toks]
+    rec = parity_vs_oracle(got, ref)
+    rec["status"] = int(status)
+    rec["ok"] = rec["ok"] and status == 0
+    rec["what"] = f"output rows of the first {toks.size} tokens vs the CPU oracle"
+    del x, lg, w13, w2, ws, out
+    torch.cuda.empty_cache()
+    return rec
 
 
 def main():

@@ -18,7 +18,8 @@
  * router matmul fused with 1), moe_forward_gate (the layer from x and the
  * gate weights), moe_forward_timed (stage events), moe_forward_launch_count,
  * moe_ffn_plan,
- * the workspace calls, moe_read_status and moe_selftest_wait_timeout.
+ * the workspace calls (moe_workspace_size, moe_workspace_init,
+ * moe_workspace_regions), moe_read_status and moe_selftest_wait_timeout.
  *
  * Sources (page title, section):
  *  [R1] "Reuse topk SparseMatrix routing metadata in GPT-OSS MoE forward"
@@ -197,6 +198,21 @@ const char *moe_status_string(moe_status status);
  * the SMs). The sync words are rewritten by every FFN call, so one
  * workspace serves one stream at a time. Returns 0 for invalid sizes. */
 size_t moe_workspace_size(int64_t n, int32_t E, int32_t k, int32_t H, int32_t I);
+
+/* Where the workspace's regions lie for these sizes (no counterpart on the
+ * pages: a debugging aid). Writes MOE_WS_REGIONS byte offsets from the
+ * workspace start and the bytes each region uses, in layout order: control
+ * block, metadata histograms, topk_indx, topk_vals, col_sum, offs,
+ * col_sorted, row_sorted, gate_scal, contraction sync words, stream-K
+ * partial sums, X_sorted [n*k, H], h [n*k, I], y_flat [n*k, H]. Every region
+ * starts 256-byte aligned; the bytes between one region's end and the next
+ * region's start (and after the last, up to moe_workspace_size) are never
+ * written, so a test can fill them with a canary and check them after a
+ * forward. offset and bytes are host arrays of MOE_WS_REGIONS entries.
+ * Returns MOE_ERR_INVALID_ARG for invalid sizes or null arrays. */
+#define MOE_WS_REGIONS 14
+moe_status moe_workspace_regions(int64_t n, int32_t E, int32_t k, int32_t H, int32_t I,
+                                 size_t *offset, size_t *bytes);
 
 /* Prepare a freshly allocated workspace: zero its control block (the first
  * 4 KB: status word and the grid-barrier counter). Must run once, in stream

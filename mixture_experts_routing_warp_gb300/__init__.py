@@ -11,10 +11,12 @@ from ._binding import (ACT, FFN_KERNEL, GATING, LAYOUT, MoEError, MoeParams, Rou
                        STAGES, build_metadata, combine, empty_meta, forward, forward_gate,
                        ffn_plan, forward_launch_count, forward_timed, grouped_ffn, lib, library_path,
                        make_params, read_status, route, route_gemm, route_metadata,
-                       selftest_wait_timeout, status_string, workspace, workspace_size)
+                       selftest_wait_timeout, status_string, workspace, workspace_regions,
+                       workspace_size)
 
 __all__ = ["ACT", "FFN_KERNEL", "GATING", "LAYOUT", "MoEError", "MoeParams", "RoutingMeta",
            "STAGES", "build_metadata", "combine", "empty_meta", "forward", "forward_gate",
            "ffn_plan", "forward_launch_count", "forward_timed", "grouped_ffn", "lib", "library_path",
            "make_params", "read_status", "route", "route_gemm", "route_metadata",
-           "selftest_wait_timeout", "status_string", "workspace", "workspace_size"]
+           "selftest_wait_timeout", "status_string", "workspace", "workspace_regions",
+           "workspace_size"]

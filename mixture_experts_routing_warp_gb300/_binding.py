@@ -61,6 +61,7 @@ SIGNATURES = {
     "moe_status_string": (ctypes.c_char_p, [_I32]),
     "moe_workspace_size": (_SZ, [_I64, _I32, _I32, _I32, _I32]),
     "moe_workspace_init": (_I32, [_P, _SZ, _P]),
+    "moe_workspace_regions": (_I32, [_I64, _I32, _I32, _I32, _I32, _P, _P]),
     "moe_route": (_I32, [_P, _I64, _I32, _I32, _I32, _P, _P, _P]),
     "moe_build_metadata": (_I32, [_P, _P, _I64, _I32, _I32, _PM, _P, _SZ, _P]),
     "moe_route_metadata": (_I32, [_P, _I64, _I32, _I32, _I32, _P, _P, _PM, _P, _SZ, _P]),
@@ -168,6 +169,18 @@ def status_string(status: int) -> str:
 
 def workspace_size(n: int, E: int, k: int, H: int, I: int) -> int:
     return int(lib().moe_workspace_size(n, E, k, H, I))
+
+
+WS_REGIONS = ("ctrl", "hist", "topk_indx", "topk_vals", "col_sum", "offs", "col_sorted",
+              "row_sorted", "gate_scal", "sync", "sk_part", "x_sorted", "h", "y_flat")
+
+
+def workspace_regions(n: int, E: int, k: int, H: int, I: int) -> dict:
+    """name -> (byte offset, bytes used) of each workspace region."""
+    off = (ctypes.c_size_t * len(WS_REGIONS))()
+    used = (ctypes.c_size_t * len(WS_REGIONS))()
+    _check(lib().moe_workspace_regions(n, E, k, H, I, off, used), "moe_workspace_regions")
+    return {name: (int(off[i]), int(used[i])) for i, name in enumerate(WS_REGIONS)}
 
 
 def workspace(n: int, E: int, k: int, H: int, I: int,

@@ -429,13 +429,14 @@ cudaError_t launch_gemm(const CUtensorMap &ta, const CUtensorMap &tb, const Gemm
                         cudaStream_t s) {
   using C = TCfg<RB>;
   auto kern = grouped_gemm_kernel<EPI, PACKED, RB>;
-  static bool attr_set = false;  // one value for every device of the process
-  if (!attr_set) {
-    cudaError_t err =
-        cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
+  static PerDeviceOnce attr_set;
+  {
+    cudaError_t err = attr_set.run([kern] {
+      cudaError_t e =
+          cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
+      return e != cudaSuccess ? e : uniform_carveout(kern);
+    });
     if (err != cudaSuccess) return err;
-    if ((err = uniform_carveout(kern)) != cudaSuccess) return err;
-    attr_set = true;
   }
   const cudaError_t err = launch_dependent(kern, dim3(device_sm_count()), dim3(kThreads),
                                            C::kSmemBytes, s, ta, tb, a);

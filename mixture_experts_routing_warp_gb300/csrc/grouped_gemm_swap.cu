@@ -711,13 +711,14 @@ cudaError_t launch_swap(const CUtensorMap &tw, const CUtensorMap &tx, const SwAr
                         cudaStream_t s) {
   using C = SwCfg<NT, PAIR>;
   auto kern = grouped_gemm_swap_kernel<EPI, PACKED, NT, PAIR>;
-  static bool attr_set = false;
-  if (!attr_set) {
-    cudaError_t err =
-        cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
+  static PerDeviceOnce attr_set;
+  {
+    cudaError_t err = attr_set.run([kern] {
+      cudaError_t e =
+          cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
+      return e != cudaSuccess ? e : uniform_carveout(kern);
+    });
     if (err != cudaSuccess) return err;
-    if ((err = uniform_carveout(kern)) != cudaSuccess) return err;
-    attr_set = true;
   }
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(PAIR ? device_sm_count() & ~1 : device_sm_count());

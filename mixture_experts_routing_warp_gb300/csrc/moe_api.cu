@@ -119,6 +119,22 @@ size_t moe_workspace_size(int64_t n, int32_t E, int32_t k, int32_t H, int32_t I)
   return workspace_layout(n, E, k, H, I).total;
 }
 
+moe_status moe_workspace_regions(int64_t n, int32_t E, int32_t k, int32_t H, int32_t I,
+                                 size_t *offset, size_t *bytes) {
+  if (!offset || !bytes || check_sizes(n, E, k, H, I, true) != MOE_OK)
+    return MOE_ERR_INVALID_ARG;
+  const WorkspaceLayout L = workspace_layout(n, E, k, H, I);
+  const size_t at[MOE_WS_REGIONS] = {L.ctrl,      L.hist,       L.topk_indx,  L.topk_vals,
+                                     L.col_sum,   L.offs,       L.col_sorted, L.row_sorted,
+                                     L.gate_scal, L.sync,       L.sk_part,    L.x_sorted,
+                                     L.h,         L.y_flat};
+  for (int r = 0; r < MOE_WS_REGIONS; ++r) {
+    offset[r] = at[r];
+    bytes[r] = L.bytes[r];
+  }
+  return MOE_OK;
+}
+
 moe_status moe_workspace_init(void *workspace, size_t workspace_bytes, moe_stream stream) {
   if (!workspace || workspace_bytes < kCtrlBytes) return MOE_ERR_INVALID_ARG;
   if (!aligned(workspace, kAlign)) return MOE_ERR_MISALIGNED;

@@ -6,6 +6,9 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <atomic>
+#include <mutex>
+
 #include "../../include/moe.h"
 
 namespace moe {
@@ -46,6 +49,8 @@ constexpr unsigned long long kWaitTimeoutNs = 1000000000ull;
 struct WorkspaceLayout {
   size_t ctrl, hist, topk_indx, topk_vals, col_sum, offs, col_sorted, row_sorted, gate_scal;
   size_t sync, sk_part, x_sorted, h, y_flat, total;
+  size_t bytes[MOE_WS_REGIONS];  // bytes each region uses, in layout order
+  int regions;
 };
 
 // What the expert contractions use besides their operands: the control
@@ -70,7 +75,12 @@ inline WorkspaceLayout workspace_layout(int64_t n, int E, int k, int H, int I) {
   WorkspaceLayout L{};
   const size_t N = (size_t)n * (size_t)k;
   size_t o = 0;
-  auto take = [&](size_t bytes) { size_t at = o; o = align_up(o + bytes, kAlign); return at; };
+  auto take = [&](size_t bytes) {
+    size_t at = o;
+    o = align_up(o + bytes, kAlign);
+    L.bytes[L.regions++] = bytes;
+    return at;
+  };
   L.ctrl = take(kCtrlBytes);
   L.hist = take((size_t)kMetaMaxCtas * (size_t)((E + 3) & ~3) * 4);  // rows padded to 4
   L.topk_indx = take(N * 4);
@@ -359,13 +369,41 @@ inline cudaError_t launch_dependent(void (*kern)(KArgs...), dim3 grid, dim3 bloc
 
 // Every kernel of the library asks for the same L1 / shared-memory split
 // (all shared: the grouped GEMM needs ~200 KB), so that consecutive kernels
-// never wait for an SM to drain and reconfigure. Call once per kernel
-// before its first launch (cheap: a flag per kernel).
+// never wait for an SM to drain and reconfigure. Call once per kernel and
+// device before its first launch there (through PerDeviceOnce).
 template <typename Kern>
 inline cudaError_t uniform_carveout(Kern kern) {
   return cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout,
                               (int)cudaSharedmemCarveoutMaxShared);
 }
+
+// A kernel's function attributes (cudaFuncSetAttribute) belong to the
+// context of the device that is current when they are set, so each device
+// ordinal is configured on its own. run(fn) calls fn once per device, the
+// first time any thread calls it with that device current; concurrent first
+// calls serialise on a mutex, later calls cost one atomic load. A failed fn
+// is retried on the next call.
+class PerDeviceOnce {
+ public:
+  static constexpr int kMaxDevices = 64;
+  template <typename F>
+  cudaError_t run(F &&fn) {
+    int dev = 0;
+    cudaError_t err = cudaGetDevice(&dev);
+    if (err != cudaSuccess) return err;
+    if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+    if (done_[dev].load(std::memory_order_acquire)) return cudaSuccess;
+    std::lock_guard<std::mutex> lock(mu_);
+    if (done_[dev].load(std::memory_order_relaxed)) return cudaSuccess;
+    err = fn();
+    if (err == cudaSuccess) done_[dev].store(true, std::memory_order_release);
+    return err;
+  }
+
+ private:
+  std::mutex mu_;
+  std::atomic<bool> done_[kMaxDevices] = {};
+};
 
 // ----------------------------------------------------- kernel launchers --
 // launch_ffn records ev_ffn[0] before the w13 kernel and ev_ffn[1] before the

@@ -16,14 +16,18 @@
 namespace moe {
 
 int device_sm_count() {
-  static int cached[64] = {};  // per device ordinal
+  static std::atomic<int> cached[PerDeviceOnce::kMaxDevices] = {};  // per device ordinal
   int dev = 0;
   cudaGetDevice(&dev);
-  if (dev >= 0 && dev < 64 && cached[dev] > 0) return cached[dev];
+  const bool slot = dev >= 0 && dev < PerDeviceOnce::kMaxDevices;
+  if (slot) {
+    const int v = cached[dev].load(std::memory_order_relaxed);
+    if (v > 0) return v;
+  }
   int sms = 0;
   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   if (sms < 1) sms = 1;
-  if (dev >= 0 && dev < 64) cached[dev] = sms;
+  if (slot) cached[dev].store(sms, std::memory_order_relaxed);
   return sms;
 }
 
@@ -57,12 +61,9 @@ struct RouteLaunch {
     const int64_t cap = (int64_t)device_sm_count() * 8;
     if (blocks > cap) blocks = cap;
     const int vec4 = (E % 4) == 0 && ((uintptr_t)logits % 16) == 0;
-    static bool configured = false;
-    if (!configured) {
-      cudaError_t err = uniform_carveout(route_kernel<K, G, NQ>);
-      if (err != cudaSuccess) return err;
-      configured = true;
-    }
+    static PerDeviceOnce configured;
+    cudaError_t err = configured.run([] { return uniform_carveout(route_kernel<K, G, NQ>); });
+    if (err != cudaSuccess) return err;
     route_kernel<K, G, NQ><<<(unsigned)blocks, kRouteThreads, 0, s>>>(logits, n, E, gating, vec4,
                                                                    indx, vals);
     return cudaGetLastError();
@@ -121,15 +122,22 @@ __global__ void __launch_bounds__(kMetaThreads) metadata_kernel(
 }
 
 int metadata_ctas_per_sm() {
-  static int per_sm = 0;  // CTAs per SM of metadata_kernel (same on every GB300)
-  if (per_sm == 0) {
-    int v = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&v, metadata_kernel, kMetaThreads, 0) !=
-        cudaSuccess)
-      return 1;
-    per_sm = v > 0 ? v : 1;
+  // CTAs per SM of metadata_kernel, per device ordinal
+  static std::atomic<int> cached[PerDeviceOnce::kMaxDevices] = {};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  const bool slot = dev >= 0 && dev < PerDeviceOnce::kMaxDevices;
+  if (slot) {
+    const int v = cached[dev].load(std::memory_order_relaxed);
+    if (v > 0) return v;
   }
-  return per_sm;
+  int v = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&v, metadata_kernel, kMetaThreads, 0) !=
+      cudaSuccess)
+    return 1;
+  v = v > 0 ? v : 1;
+  if (slot) cached[dev].store(v, std::memory_order_relaxed);
+  return v;
 }
 
 cudaError_t launch_metadata_kernel(const int32_t *topk_indx, const uint16_t *topk_vals, int N,
@@ -138,11 +146,10 @@ cudaError_t launch_metadata_kernel(const int32_t *topk_indx, const uint16_t *top
                                    uint32_t *sync = nullptr, const int32_t *expert_map = nullptr,
                                    int E_loc = 0) {
   if (!expert_map) E_loc = E;
-  static bool configured = false;
-  if (!configured) {
-    cudaError_t err = uniform_carveout(metadata_kernel);
+  static PerDeviceOnce configured;
+  {
+    cudaError_t err = configured.run([] { return uniform_carveout(metadata_kernel); });
     if (err != cudaSuccess) return err;
-    configured = true;
   }
   const int64_t slots_per_cta = 1024;
   int64_t B = (N + slots_per_cta - 1) / slots_per_cta;
@@ -278,11 +285,10 @@ __global__ void __launch_bounds__(kCopyThreads) gather_rows_kernel(
 cudaError_t launch_gather_rows(const uint16_t *x, const int32_t *row_sorted, int64_t n, int k,
                                int H, uint16_t *x_sorted, uint32_t *sync, cudaStream_t s) {
   if (n == 0) return cudaSuccess;
-  static bool configured = false;
-  if (!configured) {
-    cudaError_t err = uniform_carveout(gather_rows_kernel);
+  static PerDeviceOnce configured;
+  {
+    cudaError_t err = configured.run([] { return uniform_carveout(gather_rows_kernel); });
     if (err != cudaSuccess) return err;
-    configured = true;
   }
   const int vpr = H / 8, gpr = (vpr + 32 * kChunksPerLane - 1) / (32 * kChunksPerLane);
   int64_t blocks = (n * gpr + kCopyThreads / 32 - 1) / (kCopyThreads / 32);
@@ -363,14 +369,14 @@ cudaError_t launch_combine(const uint16_t *y_flat, int64_t n, int k, int H, uint
   if (blocks > cap) blocks = cap;
   const uint4 *y = reinterpret_cast<const uint4 *>(y_flat);
   uint4 *o = reinterpret_cast<uint4 *>(out);
-  static bool configured[9] = {};
+  static PerDeviceOnce configured[9];
   switch (k) {
 #define MOE_COMBINE_CASE(K_)                                                       \
   case K_:                                                                         \
-    if (!configured[K_]) {                                                         \
-      cudaError_t err = uniform_carveout(combine_kernel<K_>);                      \
+    {                                                                              \
+      cudaError_t err =                                                            \
+          configured[K_].run([] { return uniform_carveout(combine_kernel<K_>); }); \
       if (err != cudaSuccess) return err;                                          \
-      configured[K_] = true;                                                       \
     }                                                                              \
     {                                                                              \
       cudaError_t err = launch_dependent(combine_kernel<K_>, dim3((unsigned)blocks),  \

@@ -114,15 +114,14 @@ struct RouteMetaLaunch {
     const size_t slots = (size_t)T * K;
     const size_t smem = ((slots + 15) & ~(size_t)15) + slots * 2;
     auto kern = route_metadata_kernel<K, G, NQ>;
-    static bool configured = false;
-    if (!configured) {
+    static PerDeviceOnce configured;
+    cudaError_t e1 = configured.run([kern] {
       const int max_smem = kSlotCap * 3 + 16;
-      cudaError_t e1 =
+      cudaError_t e =
           cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, max_smem);
-      if (e1 != cudaSuccess) return e1;
-      if ((e1 = uniform_carveout(kern)) != cudaSuccess) return e1;
-      configured = true;
-    }
+      return e != cudaSuccess ? e : uniform_carveout(kern);
+    });
+    if (e1 != cudaSuccess) return e1;
     cudaError_t err = cudaSuccess;
     int Ti = (int)T;
     int64_t nn = n;

@@ -104,12 +104,9 @@ struct RouteMetaSmallLaunch {
   template <int K, int G, int NQ>
   cudaError_t go() {
     auto kern = route_metadata_small_kernel<K, G, NQ>;
-    static bool configured = false;
-    if (!configured) {
-      cudaError_t err = uniform_carveout(kern);
-      if (err != cudaSuccess) return err;
-      configured = true;
-    }
+    static PerDeviceOnce configured;
+    cudaError_t err = configured.run([kern] { return uniform_carveout(kern); });
+    if (err != cudaSuccess) return err;
     const int vec4 = (E % 4) == 0 && ((uintptr_t)logits % 16) == 0;
     kern<<<1, kSmallThreads, 0, s>>>(logits, n, E, gating, vec4, indx, vals, meta->col_sum,
                                       meta->offs, meta->col_sorted, meta->row_sorted,

@@ -74,6 +74,8 @@ def lib() -> ctypes.CDLL:
         L.orc_f64_to_bf16.argtypes = [ctypes.c_double]
         L.orc_f64_to_bf16.restype = ctypes.c_uint16
         L.orc_f64_to_bf16_array.argtypes = [p, i64, p]
+        L.orc_num_threads.argtypes = []
+        L.orc_num_threads.restype = ctypes.c_int
         for f in (L.orc_route, L.orc_metadata, L.orc_expert_row, L.orc_ffn):
             f.restype = ctypes.c_int
         _lib = L
@@ -109,6 +111,11 @@ def act_params(act: str = "swiglu", layout: str = "packed", alpha: Optional[floa
             raise ValueError("ReLU2 takes no clamp limit")
         a, b, lim = 1.0, 0.0, math.inf
     return _ActParams(ACT[act], LAYOUT[layout], float(a), float(b), float(lim))
+
+
+def num_threads() -> int:
+    """OpenMP threads the oracle's FFN runs with."""
+    return int(lib().orc_num_threads())
 
 
 def f64_to_bf16(v) -> np.ndarray:

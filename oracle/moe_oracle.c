@@ -44,6 +44,7 @@
  *    id, the order of the masked per-expert loop.
  */
 #include <math.h>
+#include <omp.h>
 #include <stdint.h>
 #include <stdlib.h>
 #include <string.h>
@@ -408,3 +409,7 @@ int orc_ffn(const uint16_t *x, const int32_t *topk_indx, const uint16_t *topk_va
 void orc_f64_to_bf16_array(const double *v, int64_t m, uint16_t *out) {
   for (int64_t i = 0; i < m; ++i) out[i] = orc_f64_to_bf16(v[i]);
 }
+
+/* The number of OpenMP threads the FFN's parallel region runs with (the
+ * benchmark states it beside the oracle's timing). */
+int orc_num_threads(void) { return omp_get_max_threads(); }

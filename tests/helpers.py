@@ -6,6 +6,10 @@ import numpy as np
 # output cannot pass ("CuteDSL NVFP4 MoE adds SwiGLU-OAI and ReLU2",
 # 关键源码片段: atol 3e-2 plus a cosine check; rtol tightened to 2e-2).
 ATOL, RTOL, COS_MIN = 3e-2, 2e-2, 0.99
+# Relative L2 error ||gpu - ref|| / ||ref|| over the whole compared output:
+# a stricter diagnostic than the elementwise bound (bf16 rounding of the
+# output alone gives ~1e-3).
+REL_L2_MAX = 1e-2
 
 
 def dev_bf16(a: np.ndarray, device="cuda"):
@@ -43,4 +47,5 @@ def assert_layer_close(got_bits: np.ndarray, ref_bits: np.ndarray, what: str = "
              "n_bad": int(bad.sum())}
     assert not bad.any(), f"{what}: {stats}"
     assert cos > COS_MIN, f"{what}: {stats}"
+    assert rel_l2 <= REL_L2_MAX, f"{what}: {stats}"
     return stats

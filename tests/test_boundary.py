@@ -64,6 +64,25 @@ def test_workspace_size(L):
     assert moe.workspace_size(0, 8, 2, 64, 128) > 0
 
 
+@pytest.mark.parametrize("sizes", [(33, 8, 2, 64, 128), (1, 32, 4, 2880, 2880),
+                                   (8191, 256, 8, 192, 320), (0, 4, 1, 64, 64)])
+def test_workspace_regions(L, sizes):
+    """Regions in layout order, each 256-byte aligned and inside the
+    workspace, none overlapping the next; sized for the arrays they hold."""
+    n, E, k, H, I_ = sizes
+    reg = moe.workspace_regions(*sizes)
+    total = moe.workspace_size(*sizes)
+    N = n * k
+    assert reg["x_sorted"][1] == N * H * 2 and reg["h"][1] == N * I_ * 2
+    assert reg["y_flat"][1] == N * H * 2 and reg["col_sorted"][1] == N * 4
+    assert reg["offs"][1] == (E + 1) * 4 and reg["gate_scal"][1] == N * 2
+    spans = list(reg.values())
+    for (o, b), (o2, _) in zip(spans, spans[1:] + [(total, 0)]):
+        assert o % 256 == 0 and o + b <= o2, (o, b, o2)
+    with pytest.raises(moe.MoEError):
+        moe.workspace_regions(33, 0, 2, 64, 128)
+
+
 def _p(v):
     return ctypes.c_void_p(v)
 

@@ -3,9 +3,9 @@
 Routing and metadata must match bit for bit; the layer output within
 |gpu - ref| <= 3e-2 + 2e-2 |ref| elementwise and cosine > 0.99.
 Workloads: the tiny layer, the MiniMind layer (E = 4, 8, 16, top-1, softmax
-over all experts), the GPT-OSS layer (decode n = 1, 8, 64 checked in full;
-prefill n = 2048, 8192 on sampled tokens), the skewed 128-expert prefill
-(n = 16384, sampled tokens), and variants over layouts, activations,
+over all experts), the GPT-OSS layer (decode n = 1, 8, 64 and prefill n = 2048 checked in
+full; prefill n = 8192 on tokens from every 128-row block of every expert's
+slice), the skewed 128-expert prefill (n = 16384, the same per-block tokens), and variants over layouts, activations,
 activation parameters and ragged tile tails, each through both grouped-GEMM
 kernels (tokens on the MMA's M side, and weights on it for small batches)."""
 import numpy as np
@@ -72,27 +72,54 @@ def _check_full(L):
     return assert_layer_close(host_bits(out), ref, L.case.name)
 
 
-def _sample_tokens(indx: np.ndarray, col_sum: np.ndarray, count: int = 48) -> np.ndarray:
-    n = indx.shape[0]
-    rng = np.random.default_rng(123)
-    pick = {0, n - 1}
-    rare = np.nonzero((col_sum > 0) & (col_sum <= 4))[0]
-    for e in rare[:16]:  # tokens that reach the rarest experts (ragged tails)
-        pick.add(int(np.nonzero((indx == e).any(axis=1))[0][0]))
-    while len(pick) < min(n, count):
-        pick.add(int(rng.integers(0, n)))
+def _tile_sample(meta: dict, k: int, rows: int = 128, seed: int = 123) -> np.ndarray:
+    """Tokens covering every token tile of both contraction kernels: for each
+    expert, one random sorted position in every 128-row block from the
+    expert's first row (a CTA-pair half of a 256-row swap tile, a whole
+    tiled-kernel tile) plus the expert's last row (its ragged tail)."""
+    offs = meta["offs"].cpu().numpy()
+    col_sorted = meta["col_sorted"].cpu().numpy()
+    rng = np.random.default_rng(seed)
+    pick = set()
+    for e in range(offs.size - 1):
+        a, b = int(offs[e]), int(offs[e + 1])
+        for s0 in range(a, b, rows):
+            pick.add(int(col_sorted[rng.integers(s0, min(s0 + rows, b))]) // k)
+        if b > a:
+            pick.add(int(col_sorted[b - 1]) // k)
     return np.array(sorted(pick), dtype=np.int64)
 
 
-def _check_sampled(L):
+# oracle outputs already computed for a case's routing (both kernels share it)
+_ORACLE_CACHE = {}
+
+
+def _oracle_cached(L, indx: np.ndarray, vals_bits: np.ndarray, toks=None) -> np.ndarray:
+    key = (L.case.name, indx.tobytes(), vals_bits.tobytes(),
+           None if toks is None else toks.tobytes())
+    if key not in _ORACLE_CACHE:
+        _ORACLE_CACHE.clear()
+        _ORACLE_CACHE[key] = oracle.ffn(L.h["x"], indx, vals_bits, L.h["w13"], L.h["w2"],
+                                        tokens=toks, **L.oracle_kw())
+    return _ORACLE_CACHE[key]
+
+
+def _check_full_cached(L):
+    """_check_full with the oracle's output reused across kernels."""
     out, indx, vals, meta = L.forward()
     _check_routing(L, indx, vals, meta)
-    ind = indx.cpu().numpy()
-    toks = _sample_tokens(ind, meta["col_sum"].cpu().numpy())
-    ref = oracle.ffn(L.h["x"], ind, host_bits(vals), L.h["w13"], L.h["w2"], tokens=toks,
-                     **L.oracle_kw())
-    got = host_bits(out)[toks]
-    return assert_layer_close(got, ref, L.case.name)
+    ref = _oracle_cached(L, indx.cpu().numpy(), host_bits(vals))
+    return assert_layer_close(host_bits(out), ref, L.case.name)
+
+
+def _check_tiles(L):
+    """The layer on the tokens of _tile_sample (every token tile of every
+    expert contributes rows), against the oracle."""
+    out, indx, vals, meta = L.forward()
+    _check_routing(L, indx, vals, meta)
+    toks = _tile_sample(meta, L.case.k)
+    ref = _oracle_cached(L, indx.cpu().numpy(), host_bits(vals), toks)
+    return assert_layer_close(host_bits(out)[toks], ref, L.case.name)
 
 
 def test_tiny_layer_and_golden():
@@ -128,16 +155,28 @@ def test_gptoss_decode(n):
 
 
 @pytest.mark.parametrize("ffn_kernel", ["auto", "tiled"])
-@pytest.mark.parametrize("n", I.GPTOSS_PREFILL_N)
-def test_gptoss_prefill_sampled(n, ffn_kernel):
-    _check_sampled(Layer(I.GPTOSS.with_n(n), ffn_kernel=ffn_kernel))
+def test_gptoss_prefill_n2048_every_token(ffn_kernel):
+    """GPT-OSS prefill at 2048 tokens: every output element against the oracle."""
+    _check_full_cached(Layer(I.GPTOSS.with_n(2048), ffn_kernel=ffn_kernel))
 
 
 @pytest.mark.parametrize("ffn_kernel", ["auto", "tiled"])
-def test_skewed_prefill_sampled(ffn_kernel):
+def test_gptoss_prefill_n8192_every_tile(ffn_kernel):
+    """GPT-OSS prefill at 8192 tokens: tokens from every 128-row block of
+    every expert's slice (each CTA-pair half of each 256-row tile)."""
+    L = Layer(I.GPTOSS.with_n(8192), ffn_kernel=ffn_kernel)
+    plan = moe.ffn_plan(8192, L.case.E, L.case.k, L.case.H, L.case.I, L.params)
+    if ffn_kernel == "auto":
+        assert plan["pair_w13"] and plan["pair_w2"]
+    _check_tiles(L)
+
+
+@pytest.mark.parametrize("ffn_kernel", ["auto", "tiled"])
+def test_skewed_prefill_every_tile(ffn_kernel):
+    """The skewed 128-expert prefill (n = 16384; one expert holds almost every
+    token, most hold 0-2): tokens from every 128-row block of every expert."""
     L = Layer(I.SKEWED, ffn_kernel=ffn_kernel)
-    stats = _check_sampled(L)
-    assert stats["cos"] > 0.99
+    _check_tiles(L)
 
 
 VARIANTS = [
