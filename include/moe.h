@@ -202,7 +202,7 @@ size_t moe_workspace_size(int64_t n, int32_t E, int32_t k, int32_t H, int32_t I)
 /* Where the workspace's regions lie for these sizes (no counterpart on the
  * pages: a debugging aid). Writes MOE_WS_REGIONS byte offsets from the
  * workspace start and the bytes each region uses, in layout order: control
- * block, metadata histograms, topk_indx, topk_vals, col_sum, offs,
+ * block, the fused routing kernel's count rows, metadata histograms, topk_indx, topk_vals, col_sum, offs,
  * col_sorted, row_sorted, gate_scal, contraction sync words, stream-K
  * partial sums, X_sorted [n*k, H], h [n*k, I], y_flat [n*k, H]. Every region
  * starts 256-byte aligned; the bytes between one region's end and the next
@@ -210,7 +210,7 @@ size_t moe_workspace_size(int64_t n, int32_t E, int32_t k, int32_t H, int32_t I)
  * written, so a test can fill them with a canary and check them after a
  * forward. offset and bytes are host arrays of MOE_WS_REGIONS entries.
  * Returns MOE_ERR_INVALID_ARG for invalid sizes or null arrays. */
-#define MOE_WS_REGIONS 14
+#define MOE_WS_REGIONS 15
 moe_status moe_workspace_regions(int64_t n, int32_t E, int32_t k, int32_t H, int32_t I,
                                  size_t *offset, size_t *bytes);
 

@@ -171,7 +171,7 @@ def workspace_size(n: int, E: int, k: int, H: int, I: int) -> int:
     return int(lib().moe_workspace_size(n, E, k, H, I))
 
 
-WS_REGIONS = ("ctrl", "hist", "topk_indx", "topk_vals", "col_sum", "offs", "col_sorted",
+WS_REGIONS = ("ctrl", "frows", "hist", "topk_indx", "topk_vals", "col_sum", "offs", "col_sorted",
               "row_sorted", "gate_scal", "sync", "sk_part", "x_sorted", "h", "y_flat")
 
 

@@ -124,10 +124,10 @@ moe_status moe_workspace_regions(int64_t n, int32_t E, int32_t k, int32_t H, int
   if (!offset || !bytes || check_sizes(n, E, k, H, I, true) != MOE_OK)
     return MOE_ERR_INVALID_ARG;
   const WorkspaceLayout L = workspace_layout(n, E, k, H, I);
-  const size_t at[MOE_WS_REGIONS] = {L.ctrl,      L.hist,       L.topk_indx,  L.topk_vals,
-                                     L.col_sum,   L.offs,       L.col_sorted, L.row_sorted,
-                                     L.gate_scal, L.sync,       L.sk_part,    L.x_sorted,
-                                     L.h,         L.y_flat};
+  const size_t at[MOE_WS_REGIONS] = {L.ctrl,       L.frows,     L.hist,    L.topk_indx,
+                                     L.topk_vals,  L.col_sum,   L.offs,    L.col_sorted,
+                                     L.row_sorted, L.gate_scal, L.sync,    L.sk_part,
+                                     L.x_sorted,   L.h,         L.y_flat};
   for (int r = 0; r < MOE_WS_REGIONS; ++r) {
     offset[r] = at[r];
     bytes[r] = L.bytes[r];
@@ -193,7 +193,7 @@ moe_status moe_route_metadata(const float *logits, int64_t n, int32_t E, int32_t
   uint32_t *ctrl = ws_at<uint32_t>(workspace, L.ctrl);
   if (n > 0 && route_metadata_fits(n, k))
     return from_cuda(launch_route_metadata(logits, n, E, k, gating, topk_indx, topk_vals, *meta,
-                                           hist, ctrl, s));
+                                           ctrl, s));
   if (launch_route(logits, n, E, k, gating, topk_indx, topk_vals, ctrl, s) != cudaSuccess)
     return MOE_ERR_CUDA;
   return from_cuda(launch_metadata(topk_indx, topk_vals, n, E, k, *meta, hist, ctrl, s));
@@ -312,7 +312,7 @@ static moe_status forward_impl(const uint16_t *x, const float *logits, const uin
     // one cooperative kernel for both stages (and the dispatch rows, unless
     // the w13 contraction gathers them itself); the metadata stage time is 0
     if (mark(MOE_STAGE_ROUTE) != cudaSuccess ||
-        launch_route_metadata(logits, n, E, k, gating, indx, vals, m, hist, ctrl, s, scr.sync,
+        launch_route_metadata(logits, n, E, k, gating, indx, vals, m, ctrl, s, scr.sync,
                               emap, E_loc, rows_in_routing ? x : nullptr, H,
                               x_sorted) != cudaSuccess ||
         mark(MOE_STAGE_METADATA) != cudaSuccess)

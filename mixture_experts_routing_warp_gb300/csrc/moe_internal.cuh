@@ -45,9 +45,15 @@ constexpr size_t kSkPartFloats = 2 * 2 * 128 * 32;
 // Default limit of a device-side wait (ns). Legitimate waits last microseconds.
 constexpr unsigned long long kWaitTimeoutNs = 1000000000ull;
 
+// Count rows of the cooperative route + metadata kernel (routing_common.cuh):
+// kFusedMaxRows rows (one per CTA, one CTA per SM) of up to kMaxExperts
+// 16-bit counts, right after the control block.
+constexpr int kFusedMaxRows = 256;
+constexpr size_t kFusedRowsBytes = (size_t)kFusedMaxRows * kMaxExperts * 2;
+
 // ------------------------------------------------------ workspace layout --
 struct WorkspaceLayout {
-  size_t ctrl, hist, topk_indx, topk_vals, col_sum, offs, col_sorted, row_sorted, gate_scal;
+  size_t ctrl, frows, hist, topk_indx, topk_vals, col_sum, offs, col_sorted, row_sorted, gate_scal;
   size_t sync, sk_part, x_sorted, h, y_flat, total;
   size_t bytes[MOE_WS_REGIONS];  // bytes each region uses, in layout order
   int regions;
@@ -64,7 +70,8 @@ struct FfnScratch {
 
 inline size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
-// Regions: control block; per-CTA histograms of the metadata kernel; the
+// Regions: control block; the route + metadata kernel's count rows;
+// per-CTA histograms of the metadata kernel; the
 // routing result and metadata used when moe_forward's caller keeps them
 // internal; the sync words of the expert contractions; the decode stream-K
 // partial sums (n*k <= 32 * E only); the expert-sorted activations X_sorted
@@ -82,6 +89,7 @@ inline WorkspaceLayout workspace_layout(int64_t n, int E, int k, int H, int I) {
     return at;
   };
   L.ctrl = take(kCtrlBytes);
+  L.frows = take(kFusedRowsBytes);  // at kCtrlBytes: right after the control block
   L.hist = take((size_t)kMetaMaxCtas * (size_t)((E + 3) & ~3) * 4);  // rows padded to 4
   L.topk_indx = take(N * 4);
   L.topk_vals = take(N * 2);
@@ -120,6 +128,46 @@ __device__ __forceinline__ uint32_t atom_add_release_gpu(uint32_t *p, uint32_t v
   asm volatile("atom.add.release.gpu.global.u32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v)
                : "memory");
   return old;
+}
+
+// ------------------------------------------------------------- clusters --
+// Rank of this CTA in its cluster, the cluster's CTA count and its index in
+// the grid (x); a launch without cluster dimensions is a cluster of one.
+__device__ __forceinline__ uint32_t cluster_rank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+__device__ __forceinline__ uint32_t cluster_ctas() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_nctarank;" : "=r"(r));
+  return r;
+}
+__device__ __forceinline__ uint32_t cluster_index_x() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%clusterid.x;" : "=r"(r));
+  return r;
+}
+
+// Every thread of every CTA of the cluster; orders shared-memory writes (and
+// mbarrier initialisation) before the other CTAs' accesses that follow.
+__device__ __forceinline__ void cluster_sync() {
+  asm volatile(
+      "barrier.cluster.arrive.release.aligned;\n\t"
+      "barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+// Shared::cluster address of the same shared-memory offset in CTA `rank`.
+__device__ __forceinline__ uint32_t map_to_rank(uint32_t saddr, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(saddr), "r"(rank));
+  return r;
+}
+
+__device__ __forceinline__ int ld_shared_cluster(uint32_t cluster_addr) {
+  int v;
+  asm volatile("ld.shared::cluster.s32 %0, [%1];" : "=r"(v) : "r"(cluster_addr) : "memory");
+  return v;
 }
 
 // Sticky first error in the control block (no-op without one, as for
@@ -420,8 +468,7 @@ cudaError_t launch_route(const float *logits, int64_t n, int E, int k, int gatin
 bool route_metadata_fits(int64_t n, int k);
 cudaError_t launch_route_metadata(const float *logits, int64_t n, int E, int k, int gating,
                                   int32_t *topk_indx, uint16_t *topk_vals,
-                                  const moe_routing_meta &meta, int32_t *ws_hist,
-                                  uint32_t *ctrl, cudaStream_t s, uint32_t *sync = nullptr,
+                                  const moe_routing_meta &meta, uint32_t *ctrl, cudaStream_t s, uint32_t *sync = nullptr,
                                   const int32_t *expert_map = nullptr, int E_loc = 0,
                                   const uint16_t *x = nullptr, int H = 0,
                                   uint16_t *x_sorted = nullptr);

@@ -35,13 +35,15 @@ template <int K, int G, int NQ>
 __global__ void __launch_bounds__(kRouteThreads) route_kernel(
     const float *__restrict__ logits, int64_t n, int E, int gating, int vec4,
     int32_t *__restrict__ topk_indx, uint16_t *__restrict__ topk_vals) {
+  __shared__ float4 stash[NQ * kRouteThreads];  // the top-k's logit stash
   const int64_t groups = (int64_t)gridDim.x * (kRouteThreads / G);
   for (int64_t t0 = (int64_t)blockIdx.x * (kRouteThreads / G); t0 < n; t0 += groups) {
     const int64_t t = t0 + threadIdx.x / G;  // the loop bound is uniform over the block
     const bool valid = t < n;
     TopK<K> tk;
     float w[K];
-    topk_group<K, G, NQ>(logits + (valid ? t : 0) * E, valid, E, gating, vec4 != 0, tk, w);
+    topk_group<K, G, NQ>(logits + (valid ? t : 0) * E, valid, E, gating, vec4 != 0, tk, w,
+                         stash);
     if (valid) write_token<K, G, false>(t, 0, tk, w, topk_indx, topk_vals, nullptr, nullptr,
                                         nullptr);
   }

@@ -7,7 +7,7 @@
 // Sources (page title, section): as routing.cu.
 #pragma once
 
-#include "moe_internal.cuh"
+#include "tc_ptx.cuh"
 
 namespace moe {
 
@@ -76,11 +76,73 @@ __device__ __forceinline__ void merge4_desc(unsigned long long (&top)[4],
   cx(top[2], top[3]);
 }
 
+// 32-bit selection keys. trunc_key replaces the IDB low bits of the order
+// key by (2^IDB - 1 - e): keys are unique, and a larger key has a larger
+// value in the upper 32 - IDB bits of the order key or, on equal upper bits,
+// a lower expert id. Two elements whose upper bits differ are ordered as their
+// exact (value, id) keys are; only elements that share the upper bits can be
+// ordered differently (their low value bits are ignored).
+template <int IDB>
+__device__ __forceinline__ uint32_t trunc_key(float v, int e) {
+  constexpr uint32_t m = (1u << IDB) - 1u;
+  return (order_key(v) & ~m) | (m - (uint32_t)e);
+}
+
+__device__ __forceinline__ void cx32(uint32_t &a, uint32_t &b) {
+  const uint32_t hi = max(a, b), lo = min(a, b);
+  a = hi;
+  b = lo;
+}
+
+__device__ __forceinline__ void sort4_desc32(uint32_t (&c)[4]) {
+  cx32(c[0], c[1]);
+  cx32(c[2], c[3]);
+  cx32(c[0], c[2]);
+  cx32(c[1], c[3]);
+  cx32(c[1], c[2]);
+}
+
+// top <- the 4 largest of top and o (both sorted descending), sorted; the
+// 4 smallest are dropped, and `dropped` keeps the largest key ever dropped.
+__device__ __forceinline__ void merge4_desc32(uint32_t (&top)[4], const uint32_t (&o)[4],
+                                              uint32_t &dropped) {
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    dropped = max(dropped, min(top[j], o[3 - j]));
+    top[j] = max(top[j], o[3 - j]);
+  }
+  cx32(top[0], top[2]);
+  cx32(top[1], top[3]);
+  cx32(top[0], top[1]);
+  cx32(top[2], top[3]);
+}
+
+constexpr int ilog2_ce(int v) { return v <= 1 ? 0 : 1 + ilog2_ce(v / 2); }
+
 // vec4: rows are 16-byte aligned (E % 4 == 0 and a 16-byte aligned base),
 // so a chunk is one 128-bit load; otherwise four 32-bit loads.
+//
+// K <= 4: the G lanes select on 32-bit trunc_keys (IDB = log2(NQ * 4 * G)
+// id bits): each lane sorts its 4-element chunks with a 5-comparator network
+// and bitonic-merges the sorted 4-lists (inside the lane, then across the G
+// lanes), keeping the top 4. The selection S = s_1..s_K is exact -- the same
+// experts in the same order as with full (value, id) keys -- when the upper
+// bits h of the selected keys are pairwise distinct and no other element
+// shares h(s_K): then every selected element beats every other on its upper
+// bits alone. Each lane checks the second condition on its own top 5 (its
+// final local top-4 list and the largest key its local merges dropped): an
+// unselected element y of the lane with h(y) = h(s_K) either is among those
+// five, or lies below five of the lane's elements that beat it, one of which
+// is then unselected with h = h(s_K) as well, or is the fifth itself when the
+// lane's top 4 are S. A warp with a token that fails the test (equal upper
+// bits near the cut: ties, near-ties, NaN) redoes its tokens on 64-bit
+// (order key, ~id) keys. The selected logits are read back from `stash`,
+// where each lane leaves its chunks ([NQ][blockDim.x] float4, this thread's
+// column), so the gate weights see the exact values.
 template <int K, int G, int NQ>  // NQ chunks of 4 elements per lane: NQ*4*G >= E
 __device__ __forceinline__ void topk_group(const float *__restrict__ row, bool valid, int E,
-                                           int gating, bool vec4, TopK<K> &tk, float (&w)[K]) {
+                                           int gating, bool vec4, TopK<K> &tk, float (&w)[K],
+                                           float4 *stash) {
   const int lane = threadIdx.x & 31, g = lane % G;
   tk.init();
   // a warp without a token (the tail of a CTA's range) has nothing to rank;
@@ -111,39 +173,93 @@ __device__ __forceinline__ void topk_group(const float *__restrict__ row, bool v
     }
   }
   if constexpr (K <= 4) {
-    // Branch-free: packed keys ((order key << 32) | ~id) are unique and
-    // "larger" means (value descending, id ascending). Sort each chunk of 4
-    // with a 5-comparator network, then bitonic-merge the sorted 4-lists
-    // (inside the lane, then across the G lanes), keeping the top 4.
-    unsigned long long top[4];
+    constexpr int IDB = ilog2_ce(NQ * 4 * G);
+    static_assert((1 << IDB) == NQ * 4 * G, "NQ * 4 * G must be a power of two");
+    __syncwarp();  // the group's reads of the previous pass's stash are done
+#pragma unroll
+    for (int i = 0; i < NQ; ++i) stash[i * blockDim.x + threadIdx.x] = x[i];
+    uint32_t top[4], dropped = 0u;
 #pragma unroll
     for (int i = 0; i < NQ; ++i) {
       if (i > 0 && i * G * 4 >= E) break;  // uniform: no lane's chunk holds an expert
       const int e0 = (i * G + g) * 4;
-      unsigned long long c[4];
-      c[0] = e0 < E ? pack_key(order_key(x[i].x), e0) : 0ull;
-      c[1] = e0 + 1 < E ? pack_key(order_key(x[i].y), e0 + 1) : 0ull;
-      c[2] = e0 + 2 < E ? pack_key(order_key(x[i].z), e0 + 2) : 0ull;
-      c[3] = e0 + 3 < E ? pack_key(order_key(x[i].w), e0 + 3) : 0ull;
-      sort4_desc(c);
+      uint32_t c[4];
+      c[0] = e0 < E ? trunc_key<IDB>(x[i].x, e0) : 0u;
+      c[1] = e0 + 1 < E ? trunc_key<IDB>(x[i].y, e0 + 1) : 0u;
+      c[2] = e0 + 2 < E ? trunc_key<IDB>(x[i].z, e0 + 2) : 0u;
+      c[3] = e0 + 3 < E ? trunc_key<IDB>(x[i].w, e0 + 3) : 0u;
+      sort4_desc32(c);
       if (i == 0) {
 #pragma unroll
         for (int j = 0; j < 4; ++j) top[j] = c[j];
       } else {
-        merge4_desc(top, c);
+        merge4_desc32(top, c, dropped);
       }
     }
+    const uint32_t local[4] = {top[0], top[1], top[2], top[3]};
 #pragma unroll
     for (int off = 1; off < G; off <<= 1) {
-      unsigned long long o[4];
+      uint32_t o[4], unused = 0u;
 #pragma unroll
       for (int j = 0; j < 4; ++j) o[j] = __shfl_xor_sync(0xffffffffu, top[j], off);
-      merge4_desc(top, o);
+      merge4_desc32(top, o, unused);
     }
+    // exactness: distinct upper bits among the selected, and s_K's upper
+    // bits on no other element of this lane's top 5
+    bool exact = true;
 #pragma unroll
-    for (int j = 0; j < K; ++j) {
-      tk.key[j] = (uint32_t)(top[j] >> 32);
-      tk.e[j] = (int)~(uint32_t)top[j];
+    for (int j = 1; j < K; ++j) exact = exact && (top[j - 1] >> IDB) != (top[j] >> IDB);
+    const uint32_t sk = top[K - 1], hk = sk >> IDB;
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+      exact = exact && !(local[j] != sk && local[j] != 0u && (local[j] >> IDB) == hk);
+    exact = exact && !(dropped != 0u && (dropped >> IDB) == hk);
+    if (__all_sync(0xffffffffu, exact || !valid)) {
+      __syncwarp();  // the group's stash entries are written
+      const float *sf = reinterpret_cast<const float *>(stash);
+      const int base = threadIdx.x - g;  // the group's first thread
+#pragma unroll
+      for (int j = 0; j < K; ++j) {
+        const int e = (int)((1u << IDB) - 1u - (top[j] & ((1u << IDB) - 1u)));
+        const int q = e >> 2;
+        const float v = sf[((q / G) * (int)blockDim.x + base + q % G) * 4 + (e & 3)];
+        tk.key[j] = order_key(v);
+        tk.e[j] = e;
+      }
+    } else {
+      // Exact selection on packed 64-bit keys ((order key << 32) | ~id):
+      // the same networks on unique keys whose order is (value descending,
+      // id ascending).
+      unsigned long long top64[4];
+#pragma unroll
+      for (int i = 0; i < NQ; ++i) {
+        if (i > 0 && i * G * 4 >= E) break;  // uniform: no lane's chunk holds an expert
+        const int e0 = (i * G + g) * 4;
+        unsigned long long c[4];
+        c[0] = e0 < E ? pack_key(order_key(x[i].x), e0) : 0ull;
+        c[1] = e0 + 1 < E ? pack_key(order_key(x[i].y), e0 + 1) : 0ull;
+        c[2] = e0 + 2 < E ? pack_key(order_key(x[i].z), e0 + 2) : 0ull;
+        c[3] = e0 + 3 < E ? pack_key(order_key(x[i].w), e0 + 3) : 0ull;
+        sort4_desc(c);
+        if (i == 0) {
+#pragma unroll
+          for (int j = 0; j < 4; ++j) top64[j] = c[j];
+        } else {
+          merge4_desc(top64, c);
+        }
+      }
+#pragma unroll
+      for (int off = 1; off < G; off <<= 1) {
+        unsigned long long o[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) o[j] = __shfl_xor_sync(0xffffffffu, top64[j], off);
+        merge4_desc(top64, o);
+      }
+#pragma unroll
+      for (int j = 0; j < K; ++j) {
+        tk.key[j] = (uint32_t)(top64[j] >> 32);
+        tk.e[j] = (int)~(uint32_t)top64[j];
+      }
     }
   } else {
 #pragma unroll
@@ -399,6 +515,142 @@ __device__ bool meta_barrier_prefix(int32_t *__restrict__ ws_hist, int E, MetaSh
   return true;
 }
 
+// ------------------------------------------------ 16-bit count rows ----
+//
+// The cooperative route + metadata kernel's exchange: CTA b writes its counts
+// as row b of `rows` ([kFusedMaxRows][S] u16, S = E rounded up to 8: a CTA
+// holds at most kSlotCap = 8192 slots), passes the bounded grid barrier, and
+// copies all B rows into its shared memory with bulk copies (TMA, whole
+// 128-byte lines: when every CTA reads the same few tens of KB at once, one
+// request per line keeps the lines' L2 slices far less busy than a 16-byte
+// load per row and column). Threads then sum columns of the rows in parts,
+// and an exclusive scan over experts, 32 experts per warp in parallel, gives
+// offs; base[e] = offs[e] + the counts of expert e in lower CTAs.
+constexpr uint32_t kBulkChunk = 32768;  // bytes per bulk copy
+
+__device__ __forceinline__ void bulk_load(uint32_t dst, const void *src, uint32_t bytes,
+                                          uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::
+          "r"(dst),
+      "l"(src), "r"(bytes), "r"(bar)
+      : "memory");
+}
+
+// sh.base[0..E) holds this CTA's counts; on return sh.base = offs + before,
+// and CTA 0 has written col_sum and offs. `staging` is shared memory for B
+// rows (B * S * 2 bytes, 16-byte aligned), free at this point. `between`
+// runs (every thread) after this CTA's arrival and before its wait. Returns
+// false after a timeout.
+template <int THREADS, typename Between>
+__device__ bool meta_exchange_rows(uint16_t *__restrict__ rows, void *staging, int E,
+                                   MetaShared<THREADS> &sh, int32_t *__restrict__ col_sum,
+                                   int32_t *__restrict__ offs, uint32_t *ctrl,
+                                   unsigned long long timeout_ns, Between between) {
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int B = gridDim.x, b = blockIdx.x;
+  const int S = (E + 7) & ~7, S8 = S / 8;  // u16 counts per row, int4 per row
+  __shared__ int s_chunk[kMaxExperts / 32];
+  __shared__ __align__(8) uint64_t s_bar;
+  int nparts = 1;
+  if (B == 1) {  // one CTA holds every slot: no exchange, no barrier
+    between();
+    for (int e = tid; e < S; e += THREADS) {
+      sh.tot[e] = e < E ? sh.base[e] : 0;
+      sh.pre[e] = 0;
+    }
+  } else {
+    const uint32_t bar = tc::smem_u32(&s_bar);
+    if (tid == 0) {
+      tc::mbar_init(bar, 1);
+      asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    for (int i = tid; i < S8; i += THREADS) {
+      uint32_t w[4];
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const int e = i * 8 + 2 * q;
+        const uint32_t lo = e < E ? (uint32_t)sh.base[e] : 0u;
+        const uint32_t hi = e + 1 < E ? (uint32_t)sh.base[e + 1] : 0u;
+        w[q] = lo | (hi << 16);
+      }
+      reinterpret_cast<int4 *>(rows + (size_t)b * S)[i] =
+          make_int4((int)w[0], (int)w[1], (int)w[2], (int)w[3]);
+    }
+    const uint32_t arrived = grid_arrive(ctrl);  // (its __syncthreads covers the init)
+    between();
+    if (!grid_wait(ctrl, arrived, timeout_ns)) return false;
+    const uint32_t bytes = (uint32_t)B * (uint32_t)S * 2u;
+    if (tid == 0) {
+      tc::fence_proxy_async_global();  // the acquired rows, for the bulk copies
+      tc::mbar_arrive_expect_tx(bar, bytes);
+      for (uint32_t off = 0; off < bytes; off += kBulkChunk)
+        bulk_load(tc::smem_u32(staging) + off, reinterpret_cast<const uint8_t *>(rows) + off,
+                  min(kBulkChunk, bytes - off), bar);
+    }
+    bool ok = tc::mbar_try_wait(bar, 0);
+    if (!ok) {
+      const long long deadline = wait_deadline(timeout_ns);
+      while (!(ok = tc::mbar_try_wait(bar, 0)))
+        if (clock64() > deadline) break;
+    }
+    if (__syncthreads_or(!ok)) {
+      if (tid == 0) record_status(ctrl, MOE_ERR_TIMEOUT);
+      tc::wait_drain(bar, 0, timeout_ns);  // no copy may still write here at exit
+      return false;
+    }
+    // part q of nparts sums rows [B q / nparts, B (q + 1) / nparts) of each column
+    nparts = min(32, THREADS / S);
+    const int part = tid / S, e = tid % S;
+    if (part < nparts) {
+      const uint16_t *rs = reinterpret_cast<const uint16_t *>(staging);
+      const int r0 = B * part / nparts, r1 = B * (part + 1) / nparts;
+      int t = 0, p = 0;
+#pragma unroll 4
+      for (int r = r0; r < r1; ++r) {
+        const int c = rs[r * S + e];
+        t += c;
+        p += r < b ? c : 0;
+      }
+      sh.tot[part * S + e] = t;
+      sh.pre[part * S + e] = p;
+    }
+  }
+  __syncthreads();
+  // sums over the parts, then an exclusive scan over experts: warp c scans
+  // experts [32c, 32c + 32), the chunk totals are added afterwards
+  int tot = 0, pre = 0, incl = 0;
+  if (warp * 32 < E) {  // warp-uniform
+    if (tid < E) {
+      for (int q = 0; q < nparts; ++q) {
+        tot += sh.tot[q * S + tid];
+        pre += sh.pre[q * S + tid];
+      }
+    }
+    incl = tot;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const int o = __shfl_up_sync(0xffffffffu, incl, off);
+      if (lane >= off) incl += o;
+    }
+    if (lane == 31) s_chunk[warp] = incl;
+  }
+  __syncthreads();
+  if (tid < E) {
+    int carry = 0;
+    for (int c = 0; c < warp; ++c) carry += s_chunk[c];
+    const int excl = carry + incl - tot;
+    sh.base[tid] = excl + pre;
+    if (b == 0) {
+      col_sum[tid] = tot;
+      offs[tid] = excl;
+      if (tid == E - 1) offs[E] = excl + tot;
+    }
+  }
+  __syncthreads();
+  return true;
+}
+
 template <int THREADS, typename Get>
 __device__ void meta_scatter(int64_t f_lo, int count, int E, MetaShared<THREADS> &sh, Get get,
                              int32_t *__restrict__ col_sorted, int32_t *__restrict__ row_sorted,
@@ -422,7 +674,7 @@ __device__ void meta_scatter(int64_t f_lo, int count, int E, MetaShared<THREADS>
     if (e >= 0 && rank == 0) sh.cnt[warp][e] = __popc(peers);
     __syncthreads();
     // cnt[w][e] -> base[e] + (slots of expert e in warps < w); base[e] += all
-    for (int ee = tid; ee < E; ee += THREADS) {
+    for (int ee = tid; ee < E; ee += THREADS) {  // consecutive experts: no bank conflicts
       int run = sh.base[ee];
 #pragma unroll
       for (int ww = 0; ww < MetaShared<THREADS>::kWarps; ++ww) {

@@ -12,24 +12,28 @@ namespace moe {
 // moe_route_metadata / moe_forward's first two stages in one cooperative
 // kernel, one CTA per SM: CTA b routes tokens [b*T, b*T + T) (G lanes per
 // token as above), keeping its slots and histogram in shared memory, then
-// publishes, gathers and scatters its slots from shared memory. With an
-// expert map the metadata covers the E_loc local experts and drops the slots
-// of other ranks' experts. With x given, the CTA then copies its tokens' rows
-// to their sorted positions in X_sorted (the dispatch gather, token-major).
+// exchanges its counts through 16-bit rows and a grid barrier, and scatters
+// its slots from shared memory. With an expert map the metadata
+// covers the E_loc local experts and drops the slots of other ranks'
+// experts. With x given, the CTA then copies its tokens' rows to their
+// sorted positions in X_sorted (the dispatch gather, token-major). Dynamic
+// shared memory: the top-k's logit stash ([NQ][1024] float4), then the
+// slots' experts (u8) and weights (bf16).
 template <int K, int G, int NQ>
 __global__ void __launch_bounds__(kFusedThreads, 1) route_metadata_kernel(
     const float *__restrict__ logits, int64_t n, int E, int gating, int T, int vec4,
     int32_t *__restrict__ topk_indx, uint16_t *__restrict__ topk_vals,
     int32_t *__restrict__ col_sum, int32_t *__restrict__ offs, int32_t *__restrict__ col_sorted,
     int32_t *__restrict__ row_sorted, uint16_t *__restrict__ gate_scal,
-    int32_t *__restrict__ ws_hist, uint32_t *ctrl, unsigned long long timeout_ns,
-    uint32_t *sync, const int32_t *__restrict__ expert_map, int E_loc,
-    const uint4 *__restrict__ x, int vpr, uint4 *__restrict__ x_sorted) {
-  extern __shared__ uint8_t smem_raw[];
+    uint16_t *__restrict__ rows, uint32_t *ctrl,
+    unsigned long long timeout_ns, uint32_t *sync, const int32_t *__restrict__ expert_map,
+    int E_loc, const uint4 *__restrict__ x, int vpr, uint4 *__restrict__ x_sorted) {
+  extern __shared__ __align__(16) uint8_t smem_raw[];
   __shared__ MetaShared<kFusedThreads> sh;
   __shared__ int s_map_buf[kMaxExperts];
-  uint8_t *s_slot_e = smem_raw;
-  uint16_t *s_slot_v = reinterpret_cast<uint16_t *>(smem_raw + (((size_t)T * K + 15) & ~15ull));
+  float4 *stash = reinterpret_cast<float4 *>(smem_raw);
+  uint8_t *s_slot_e = smem_raw + (size_t)NQ * kFusedThreads * sizeof(float4);
+  uint16_t *s_slot_v = reinterpret_cast<uint16_t *>(s_slot_e + (((size_t)T * K + 15) & ~15ull));
 
   const int tid = threadIdx.x;
   pdl_launch_dependents();  // the next kernel may be scheduled (it waits for this grid)
@@ -46,7 +50,8 @@ __global__ void __launch_bounds__(kFusedThreads, 1) route_metadata_kernel(
     const bool valid = t < t1;
     TopK<K> tk;
     float w[K];
-    topk_group<K, G, NQ>(logits + (valid ? t : 0) * E, valid, E, gating, vec4 != 0, tk, w);
+    topk_group<K, G, NQ>(logits + (valid ? t : 0) * E, valid, E, gating, vec4 != 0, tk, w,
+                         stash);
     if (valid)
       write_token<K, G, true>(t, t0, tk, w, topk_indx, topk_vals, s_slot_e, s_slot_v, sh.base,
                               s_map);
@@ -60,7 +65,7 @@ __global__ void __launch_bounds__(kFusedThreads, 1) route_metadata_kernel(
       topk_vals[t0 * K + i] = s_slot_v[i];
     }
   };
-  if (!meta_barrier_prefix(ws_hist, E_loc, sh, col_sum, offs, ctrl, timeout_ns, write_topk))
+  if (!meta_exchange_rows(rows, stash, E_loc, sh, col_sum, offs, ctrl, timeout_ns, write_topk))
     return;
   meta_scatter(
       t0 * K, (int)(t1 - t0) * K, E_loc, sh,
@@ -91,6 +96,12 @@ int64_t fused_tokens_per_cta(int64_t n, int per_pass) {
   return (T + 3) / 4 * 4;
 }
 
+// Dynamic shared memory of route_metadata_kernel<K, G, NQ> for T tokens per CTA.
+inline size_t fused_smem_bytes(int64_t T, int K, int NQ) {
+  const size_t slots = (size_t)T * K;
+  return (size_t)NQ * kFusedThreads * sizeof(float4) + ((slots + 15) & ~(size_t)15) + slots * 2;
+}
+
 struct RouteMetaLaunch {
   const float *logits;
   int64_t n;
@@ -98,7 +109,6 @@ struct RouteMetaLaunch {
   int32_t *indx;
   uint16_t *vals;
   const moe_routing_meta *meta;
-  int32_t *ws_hist;
   uint32_t *ctrl;
   uint32_t *sync;
   const int32_t *expert_map;
@@ -109,20 +119,17 @@ struct RouteMetaLaunch {
   cudaStream_t s;
   template <int K, int G, int NQ>
   cudaError_t go() {
-    const int64_t T = fused_tokens_per_cta(n, kFusedThreads / G);
-    const int64_t B = (n + T - 1) / T;
-    const size_t slots = (size_t)T * K;
-    const size_t smem = ((slots + 15) & ~(size_t)15) + slots * 2;
     auto kern = route_metadata_kernel<K, G, NQ>;
+    const size_t max_smem = fused_smem_bytes(kSlotCap / K, K, NQ);
     static PerDeviceOnce configured;
-    cudaError_t e1 = configured.run([kern] {
-      const int max_smem = kSlotCap * 3 + 16;
+    cudaError_t err = configured.run([kern, max_smem] {
       cudaError_t e =
-          cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, max_smem);
+          cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)max_smem);
       return e != cudaSuccess ? e : uniform_carveout(kern);
     });
-    if (e1 != cudaSuccess) return e1;
-    cudaError_t err = cudaSuccess;
+    if (err != cudaSuccess) return err;
+    const int64_t T = fused_tokens_per_cta(n, kFusedThreads / G);
+    const int64_t B = (n + T - 1) / T;
     int Ti = (int)T;
     int64_t nn = n;
     int E_ = E, g_ = gating;
@@ -131,16 +138,17 @@ struct RouteMetaLaunch {
     const uint4 *xv = reinterpret_cast<const uint4 *>(x);
     uint4 *xs = reinterpret_cast<uint4 *>(x_sorted);
     int vpr = H / 8;
+    // the count rows follow the control block
+    uint16_t *rows = reinterpret_cast<uint16_t *>(reinterpret_cast<uint8_t *>(ctrl) + kCtrlBytes);
     void *args[] = {(void *)&logits, (void *)&nn, (void *)&E_, (void *)&g_, (void *)&Ti,
-                    (void *)&vec4, (void *)&indx, (void *)&vals, (void *)&meta->col_sum, (void *)&meta->offs,
-                    (void *)&meta->col_sorted, (void *)&meta->row_sorted,
-                    (void *)&meta->gate_scal, (void *)&ws_hist, (void *)&ctrl,
-                    (void *)&timeout, (void *)&sync, (void *)&expert_map, (void *)&E_loc,
-                    (void *)&xv, (void *)&vpr, (void *)&xs};
+                    (void *)&vec4, (void *)&indx, (void *)&vals, (void *)&meta->col_sum,
+                    (void *)&meta->offs, (void *)&meta->col_sorted, (void *)&meta->row_sorted,
+                    (void *)&meta->gate_scal, (void *)&rows, (void *)&ctrl, (void *)&timeout, (void *)&sync, (void *)&expert_map,
+                    (void *)&E_loc, (void *)&xv, (void *)&vpr, (void *)&xs};
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)B);
     cfg.blockDim = dim3(kFusedThreads);
-    cfg.dynamicSmemBytes = smem;
+    cfg.dynamicSmemBytes = fused_smem_bytes(T, K, NQ);
     cfg.stream = s;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeCooperative;
@@ -156,7 +164,8 @@ struct RouteMetaLaunch {
 // True when the fused kernel can take (n, k): each CTA's slots fit in
 // shared memory. Otherwise the two kernels run.
 bool route_metadata_fits(int64_t n, int k) {
-  return fused_tokens_per_cta(n, 0) * k <= kSlotCap;  // the larger of the two T
+  // the larger of the two T; one CTA per SM, each with a row of counts
+  return fused_tokens_per_cta(n, 0) * k <= kSlotCap && device_sm_count() <= kFusedMaxRows;
 }
 
 // True when launch_route_metadata, given x, also moves the dispatch rows for
@@ -174,7 +183,7 @@ bool route_metadata_moves_rows(int64_t n, int E, int k) {
 
 cudaError_t launch_route_metadata(const float *logits, int64_t n, int E, int k, int gating,
                                   int32_t *topk_indx, uint16_t *topk_vals,
-                                  const moe_routing_meta &meta, int32_t *ws_hist,
+                                  const moe_routing_meta &meta,
                                   uint32_t *ctrl, cudaStream_t s, uint32_t *sync,
                                   const int32_t *expert_map, int E_loc, const uint16_t *x,
                                   int H, uint16_t *x_sorted) {
@@ -184,7 +193,7 @@ cudaError_t launch_route_metadata(const float *logits, int64_t n, int E, int k, 
     return launch_route_metadata_small(logits, (int)n, E, k, gating, topk_indx, topk_vals, meta,
                                        sync, expert_map, E_loc, ctrl, s);
   return dispatch_kg(k, E, RouteMetaLaunch{logits, n, E, gating, topk_indx, topk_vals, &meta,
-                                           ws_hist, ctrl, sync, expert_map, E_loc, x, H,
+                                           ctrl, sync, expert_map, E_loc, x, H,
                                            x_sorted, s});
 }
 

@@ -28,6 +28,7 @@ __global__ void __launch_bounds__(kSmallThreads) route_metadata_small_kernel(
   __shared__ int s_map_buf[kMaxExperts];
   __shared__ int s_e[kSmallSlots];
   __shared__ uint16_t s_w[kSmallSlots];
+  __shared__ float4 stash[NQ * kSmallThreads];  // the top-k's logit stash
   const int tid = threadIdx.x, lane = tid & 31;
   pdl_launch_dependents();  // the next kernel may be scheduled (it waits for this grid)
   zero_sync_words(sync);
@@ -40,7 +41,7 @@ __global__ void __launch_bounds__(kSmallThreads) route_metadata_small_kernel(
     TopK<K> tk;
     float w[K];
     topk_group<K, G, NQ>(logits + (valid ? t : 0) * (int64_t)E, valid, E, gating, vec4 != 0, tk,
-                         w);
+                         w, stash);
     if (valid) {
 #pragma unroll
       for (int j = 0; j < K; ++j) {

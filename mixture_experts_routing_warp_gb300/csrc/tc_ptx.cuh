@@ -85,26 +85,7 @@ __device__ __forceinline__ void tma_gather4(uint32_t dst, const CUtensorMap *map
 // 128 rows of A and half of B's rows in its shared memory (same offsets), the
 // leader (rank 0) issues the MMA, and each CTA's TMEM receives its 128 rows
 // of D.
-__device__ __forceinline__ uint32_t cluster_rank() {
-  uint32_t r;
-  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
-  return r;
-}
-
-// Every thread of both CTAs; orders shared-memory writes (and mbarrier
-// initialisation) before the peer's accesses that follow.
-__device__ __forceinline__ void cluster_sync() {
-  asm volatile(
-      "barrier.cluster.arrive.release.aligned;\n\t"
-      "barrier.cluster.wait.acquire.aligned;" ::: "memory");
-}
-
-// Shared::cluster address of the same shared-memory offset in CTA `rank`.
-__device__ __forceinline__ uint32_t map_to_rank(uint32_t saddr, uint32_t rank) {
-  uint32_t r;
-  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(saddr), "r"(rank));
-  return r;
-}
+// (cluster_rank, cluster_sync and map_to_rank: moe_internal.cuh)
 
 // Arrive on an mbarrier of either CTA of the cluster.
 __device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_bar) {
