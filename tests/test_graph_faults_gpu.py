@@ -164,6 +164,8 @@ _OUR_KERNELS = ("route", "metadata", "gather_rows", "grouped_gemm", "combine")
 @pytest.mark.parametrize("case", [
     I.TINY,                                                           # fused routing, k = 2
     I.MINIMIND_E4,                                                    # k = 1: no combine
+    I.LayerCase("decode_n1", n=1, H=256, E=32, k=4, I=128, act="swiglu_oai",
+                layout="interleaved"),                                # one-CTA routing, w13 gathers
     I.LayerCase("unfused_n300000", n=300000, H=64, E=8, k=8, I=64),  # route + metadata apart
 ], ids=lambda c: c.name)
 def test_forward_launch_count_matches_the_kernels_launched(case):
