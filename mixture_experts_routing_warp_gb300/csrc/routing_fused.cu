@@ -84,14 +84,16 @@ __global__ void __launch_bounds__(kFusedThreads, 1) route_metadata_kernel(
 // Tokens per CTA of the fused kernel: spread over the SMs, a multiple of 4;
 // a batch that one pass of one CTA covers (1024 / G tokens) gets one CTA,
 // which skips the cross-CTA exchange. With one lane per token (E <= 16) a CTA
-// takes at least 128 tokens: the rows are short, and fewer CTAs make the
-// exchange cheaper (4096 tokens over 4 experts: 8.8 -> 8.1 us per call at
-// 128 instead of 28 tokens per CTA; 16 experts 9.4 -> 8.8 us).
+// takes at least 32 tokens: the rows are short, and fewer CTAs make the
+// exchange cheaper, while at 32 a 4096-token batch still spans 128 CTAs --
+// enough for the kernel to copy the dispatch rows itself (MiniMind, E = 4 /
+// 8 / 16: 38.6 / 41.2 / 45.7 -> 37.9 / 40.5 / 45.0 us per layer against 128
+// tokens per CTA and a gather kernel; the routing call alone 5.83 -> 5.93 us).
 int64_t fused_tokens_per_cta(int64_t n, int per_pass) {
   if (n <= per_pass) return (n + 3) / 4 * 4;
   const int sms = device_sm_count();
   int64_t T = (n + sms - 1) / sms;
-  if (per_pass >= kFusedThreads && T < 128) T = 128;
+  if (per_pass >= kFusedThreads && T < 32) T = 32;
   if (T < 4) T = 4;
   return (T + 3) / 4 * 4;
 }
