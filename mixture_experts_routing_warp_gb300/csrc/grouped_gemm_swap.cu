@@ -200,8 +200,10 @@ __device__ __forceinline__ bool wait_expert_ready(const SwArgs &args, int e, int
     const int wr = args.w_rows - f0 < SW_M ? args.w_rows - f0 : SW_M;
     const char *base = reinterpret_cast<const char *>(args.w + ((size_t)e * args.w_rows + f0) * K);
     const uint32_t bytes = (uint32_t)wr * (uint32_t)K * 2u;
+    // kept in L2 (evict_last) against the w13 contraction's streaming loads
+    const uint64_t keep = l2_policy_evict_last();
     for (uint32_t o = 0; o < bytes; o += 65536u)
-      prefetch_l2(base + o, bytes - o < 65536u ? bytes - o : 65536u);
+      prefetch_l2_hint(base + o, bytes - o < 65536u ? bytes - o : 65536u, keep);
     const long long deadline = wait_deadline(args.timeout_ns);
     uint32_t spins = 0;
     while (ld_acquire_gpu(p) < need) {
@@ -476,6 +478,7 @@ __global__ void __launch_bounds__(SwCfg<NT, PAIR>::kThreads, 1)
     // Lane 0 waits for free stages and issues the weight (and plain token)
     // copies; with the fused gather every lane then fetches four token rows.
     const bool gather = args.gather_rows != nullptr;
+    const uint64_t read_once = l2_policy_evict_first();
     int stage = 0;
     uint32_t phase = 0, issued = 0;
     bool ok = true;
@@ -538,10 +541,22 @@ __global__ void __launch_bounds__(SwCfg<NT, PAIR>::kThreads, 1)
         } else {
           if (lane == 0) {
             mbar_arrive_expect_tx(full_bar(stage), tx_bytes);
-            if constexpr (PACKED)
+            if constexpr (NT == SW_NGRAN) {
+              // decode: every weight line is read once (evict_first), leaving
+              // L2 to the w2 tiles fetched ahead while their expert's h is
+              // still being computed (GPT-OSS n = 4 / 8 / 64: 109.6 / 162.6 /
+              // 255.7 -> 108.5 / 160.9 / 253.2 us per layer)
+              if constexpr (PACKED)
+                tma_load_4d_hint(a_addr(stage), &tmap_w, full_bar(stage), kb * SW_BK, 0, f0 / 2,
+                                 d.e, read_once);
+              else
+                tma_load_3d_hint(a_addr(stage), &tmap_w, full_bar(stage), kb * SW_BK, f0, d.e,
+                                 read_once);
+            } else if constexpr (PACKED) {
               tma_load_4d(a_addr(stage), &tmap_w, full_bar(stage), kb * SW_BK, 0, f0 / 2, d.e);
-            else
+            } else {
               tma_load_3d(a_addr(stage), &tmap_w, full_bar(stage), kb * SW_BK, f0, d.e);
+            }
             if (!gather) tma_load_2d(b_addr(stage), &tmap_x, full_bar(stage), kb * SW_BK, d.m0);
           }
           __syncwarp();  // the expected bytes are posted before any gathered row lands
