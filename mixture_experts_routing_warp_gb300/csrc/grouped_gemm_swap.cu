@@ -42,6 +42,10 @@
 // roughly 70 GB/s at most, so a decode w13 contraction with fewer than two
 // waves of tiles splits its (tile, K step) units evenly over the grid
 // (stream-K) instead of leaving most SMs idle behind a few whole tiles.
+// At decode sizes one launch runs both contractions: each CTA takes its w2
+// tiles (in reverse CTA order, or split the same way under one wave) after
+// its w13 work, and fetches a w2 tile's weights into free stages before the
+// tile's h rows are complete.
 //
 // Warps: 0 TMA producer, 1 TMEM allocation + MMA issue, 2-5 epilogue (warp
 // q reads TMEM lanes 32*(q%4)..). Every mbarrier wait is bounded.
@@ -129,6 +133,14 @@ struct SwArgs {
   int stream_k;
   uint32_t *sk_cnt;
   float *sk_part;
+  // Both contractions in one launch (decode tiling): once a CTA has done its
+  // w13 work it runs w2 tiles (num_kb2 K steps, f_tiles2 weight tiles per
+  // expert, through the second pair of tensor maps), each after its expert's
+  // h rows are complete (ready_in, the counts ready_out collects). With
+  // stream_k and less than one wave of w2 tiles, the w2 units are split
+  // evenly over the grid as well (counters sk_cnt + 4 * kSkMaxCtas, the
+  // second half of each partial slot).
+  int num_kb2, f_tiles2;
 };
 
 // ------------------------------------------------------------- stream-K --
@@ -146,64 +158,99 @@ __device__ __forceinline__ int sk_pieces(int c_first, int c_last, int64_t U, int
   return pieces;
 }
 
-// One unit of a CTA's work: K steps [k_lo, k_hi) of tile t.
+// One unit of a CTA's work: K steps [k_lo, k_hi) of tile t of contraction
+// ph (0: the kernel's own; 1: the w2 tiles of a launch that runs both).
 struct Work {
-  int t, k_lo, k_hi;
+  int t, k_lo, k_hi, ph;
 };
 
 // The CTA's work items in order: whole tiles t = first + i * step, or
-// (stream-K) the pieces of its unit range. Every role walks the same list.
+// (stream-K) the pieces of its unit range; then, in a launch that runs both
+// contractions, whole w2 tiles t = (step - 1 - first) + i * step of total2:
+// in reverse CTA order, so the CTAs left with one w13 tile fewer (the last
+// total % step) take one w2 tile more. Every role walks the same list.
 struct WorkIter {
-  int64_t u, hi;
+  int64_t u, hi, u2, hi2;
   int t, total, kb;
-  bool sk;
+  bool sk, sk2;
   int step;
-  // first, step: this CTA's (or CTA pair's) index and the number of them
-  __device__ WorkIter(bool stream_k, int total_tiles, int num_kb, int first, int step_)
-      : u(0), hi(0), t(first), total(total_tiles), kb(num_kb), sk(stream_k), step(step_) {
+  int t2, total2, kb2;
+  // first, step: this CTA's (or CTA pair's) index and the number of them;
+  // stream_k / stream_k2: split the first / second contraction's units
+  __device__ WorkIter(bool stream_k, int total_tiles, int num_kb, int first, int step_,
+                      int total2_ = 0, int num_kb2 = 0, bool stream_k2 = false)
+      : u(0), hi(0), u2(0), hi2(0), t(first), total(total_tiles), kb(num_kb), sk(stream_k),
+        sk2(stream_k2), step(step_), t2(step_ - 1 - first), total2(total2_), kb2(num_kb2) {
     if (sk) {
       const int64_t U = (int64_t)total * kb;
       u = sk_lo(first, U, step);
       hi = sk_lo(first + 1, U, step);
     }
+    if (sk2) {
+      const int64_t U2 = (int64_t)total2 * kb2;
+      u2 = sk_lo(first, U2, step);
+      hi2 = sk_lo(first + 1, U2, step);
+    }
+  }
+  // the next piece of [u, hi) in tiles of k units
+  __device__ static bool piece(int64_t &u, int64_t hi, int k, Work &w) {
+    if (u >= hi) return false;
+    w.t = (int)(u / k);
+    const int64_t base = (int64_t)w.t * k, end = base + k < hi ? base + k : hi;
+    w.k_lo = (int)(u - base);
+    w.k_hi = (int)(end - base);
+    u = end;
+    return true;
   }
   __device__ bool next(Work &w) {
+    w.ph = 0;
     if (sk) {
-      if (u >= hi) return false;
-      w.t = (int)(u / kb);
-      const int64_t base = (int64_t)w.t * kb, end = base + kb < hi ? base + kb : hi;
-      w.k_lo = (int)(u - base);
-      w.k_hi = (int)(end - base);
-      u = end;
+      if (piece(u, hi, kb, w)) return true;
+    } else if (t < total) {
+      w.t = t;
+      w.k_lo = 0;
+      w.k_hi = kb;
+      t += step;
       return true;
     }
-    if (t >= total) return false;
-    w.t = t;
+    w.ph = 1;
+    if (sk2) return piece(u2, hi2, kb2, w);
+    if (t2 >= total2) return false;
+    w.t = t2;
     w.k_lo = 0;
-    w.k_hi = kb;
-    t += step;
+    w.k_hi = kb2;
+    t2 += step;
     return true;
   }
 };
 
-// Producer side of the handoff for tile (e, weight rows f0..): true once
-// expert e's h rows are complete and visible to this thread's TMA loads.
-__device__ __forceinline__ bool wait_expert_ready(const SwArgs &args, int e, int f0,
-                                                  const int *s_offs, volatile int *abort_flag) {
+// Producer side of the handoff for tile (e, weight rows f0..), K steps
+// [k_lo, k_hi) of num_kb: true once expert e's h rows are complete and
+// visible to this thread's TMA loads. Meanwhile the weights of those K
+// steps are fetched into L2.
+__device__ __forceinline__ bool wait_expert_ready(const SwArgs &args, int e, int f0, int num_kb,
+                                                  int k_lo, int k_hi, const int *s_offs,
+                                                  volatile int *abort_flag) {
   const int rows = s_offs[e + 1] - s_offs[e];
   const uint32_t need =
       (uint32_t)((rows + args.ready_nt - 1) / args.ready_nt) * (uint32_t)args.ready_per_tile;
   const uint32_t *p = args.ready_in + e;
   if (ld_acquire_gpu(p) < need) {
     // the tile's weight rows are contiguous: W[e, f0 .. f0 + wr, 0 .. K)
-    const int K = args.num_kb * SW_BK;
+    const int K = num_kb * SW_BK;
     const int wr = args.w_rows - f0 < SW_M ? args.w_rows - f0 : SW_M;
     const char *base = reinterpret_cast<const char *>(args.w + ((size_t)e * args.w_rows + f0) * K);
-    const uint32_t bytes = (uint32_t)wr * (uint32_t)K * 2u;
     // kept in L2 (evict_last) against the w13 contraction's streaming loads
     const uint64_t keep = l2_policy_evict_last();
-    for (uint32_t o = 0; o < bytes; o += 65536u)
-      prefetch_l2_hint(base + o, bytes - o < 65536u ? bytes - o : 65536u, keep);
+    if (k_lo == 0 && k_hi == num_kb) {
+      const uint32_t bytes = (uint32_t)wr * (uint32_t)K * 2u;
+      for (uint32_t o = 0; o < bytes; o += 65536u)
+        prefetch_l2_hint(base + o, bytes - o < 65536u ? bytes - o : 65536u, keep);
+    } else {  // a piece of the tile: its K range of every row
+      const uint32_t seg = (uint32_t)(k_hi - k_lo) * SW_BK * 2u;
+      for (int r = 0; r < wr; ++r)
+        prefetch_l2_hint(base + ((size_t)r * K + (size_t)k_lo * SW_BK) * 2, seg, keep);
+    }
     const long long deadline = wait_deadline(args.timeout_ns);
     uint32_t spins = 0;
     while (ld_acquire_gpu(p) < need) {
@@ -307,6 +354,20 @@ __device__ __forceinline__ void epi_chunk(EpiTile &t, int c0, const SwArgs &args
   epi_apply<EPI, W, FULL>(t, c0, r0, args);
 }
 
+// A whole tile's token columns for one epilogue warp: chunks of 32 columns
+// (every column valid), then of 8; a lane quarter's kPer warps take
+// alternate chunks (`half`: this warp's turn).
+template <int EPI, int NT, int kPer>
+__device__ __forceinline__ void epi_tile(EpiTile &et, int half, const SwArgs &args) {
+  int c0 = 0;
+  if constexpr (NT > SW_NGRAN) {
+    const int full = et.rows & ~31;
+    for (int c = 32 * half; c < full; c += 32 * kPer) epi_chunk<EPI, 32, true>(et, c, args);
+    c0 = full;
+  }
+  for (int c = c0 + 8 * half; c < et.rows; c += 8 * kPer) epi_chunk<EPI, 8>(et, c, args);
+}
+
 // The w13 epilogue's handoff: this warp's h rows of a tile of expert e are
 // stored; count them for the w2 kernel (the warp barrier orders every lane's
 // stores before lane 0's release).
@@ -323,15 +384,19 @@ __device__ __forceinline__ void publish_ready(const SwArgs &args, int e, int lan
 // piece. The warp that counts the tile's last piece of its lane quarter adds
 // the pieces' partials in piece order (a fixed order: the result does not
 // depend on which piece finishes last) and applies the epilogue.
+// ph: the contraction (0: w13; 1: the w2 tiles of a launch that runs both,
+// with their own counters and the second half of each slot).
 template <int EPI, int NT>
-__device__ __forceinline__ void sk_piece(EpiTile &et, const SwArgs &args, int64_t u0,
+__device__ __forceinline__ void sk_piece(EpiTile &et, const SwArgs &args, int ph, int64_t u0,
                                          int c_first, int c_last, int pieces, int k_lo,
                                          int64_t U, int G, int q, int e, uint32_t tempty) {
   constexpr size_t kSlot = kSkPartFloats / 2;
-  static_assert(SW_M * NT <= (int)kSlot, "partial slot");
+  static_assert(2 * SW_M * NT <= (int)kSlot, "partial slot");
   const int w_row = q * 32 + et.lane;
   const int my_slot = u0 + k_lo == sk_lo(blockIdx.x, U, G) ? 0 : 1;
-  float *mine = args.sk_part + ((size_t)blockIdx.x * 2 + my_slot) * kSlot;
+  float *const part0 = args.sk_part + (size_t)ph * SW_M * NT;
+  uint32_t *const cnt = args.sk_cnt + (size_t)ph * 4 * kSkMaxCtas;
+  float *mine = part0 + ((size_t)blockIdx.x * 2 + my_slot) * kSlot;
   for (int c = 0; c < et.rows; c += 8) {
     uint32_t r0[8];
     tmem_ld<8>(et.taddr + c, r0);
@@ -348,7 +413,7 @@ __device__ __forceinline__ void sk_piece(EpiTile &et, const SwArgs &args, int64_
   uint32_t old = 0;
   if (et.lane == 0) {
     mbar_arrive(tempty);
-    old = atom_add_acq_rel_gpu(args.sk_cnt + (size_t)c_first * 4 + q, 1u);
+    old = atom_add_acq_rel_gpu(cnt + (size_t)c_first * 4 + q, 1u);
   }
   old = __shfl_sync(0xffffffffu, old, 0);
   if (old != (uint32_t)pieces - 1) return;
@@ -361,7 +426,7 @@ __device__ __forceinline__ void sk_piece(EpiTile &et, const SwArgs &args, int64_
       const int64_t lo = sk_lo(cta, U, G);
       if (lo == sk_lo(cta + 1, U, G)) continue;  // owns no unit
       const int slot = (u0 > lo ? u0 : lo) == lo ? 0 : 1;
-      const float *part = args.sk_part + ((size_t)cta * 2 + slot) * kSlot;
+      const float *part = part0 + ((size_t)cta * 2 + slot) * kSlot;
 #pragma unroll
       for (int i = 0; i < 8; ++i)
         if (c + i < et.rows) s0[i] += __ldcg(part + (size_t)(c + i) * SW_M + w_row);
@@ -371,16 +436,22 @@ __device__ __forceinline__ void sk_piece(EpiTile &et, const SwArgs &args, int64_
     for (int i = 0; i < 8; ++i) r0[i] = __float_as_uint(s0[i]);
     epi_apply<EPI, 8>(et, c, r0, args);
   }
-  if (args.ready_out) publish_ready(args, e, et.lane);
+  if (args.ready_out && ph == 0) publish_ready(args, e, et.lane);
 }
 
 // PACKED: the weights are a packed gated w13, read through the 4-D map that
 // interleaves gate and up rows (box coordinates: column, 0, pair, expert).
-template <int EPI, bool PACKED, int NT, bool PAIR>
+// FUSE: the w13 contraction (EPI) and then the w2 one (gate scale + scatter,
+// weights tmap_w2, h rows tmap_h) in one launch; its CTAs wait only for h
+// rows that other CTAs of the same grid, all resident, compute first.
+template <int EPI, bool PACKED, int NT, bool PAIR, bool FUSE>
 __global__ void __launch_bounds__(SwCfg<NT, PAIR>::kThreads, 1)
     grouped_gemm_swap_kernel(const __grid_constant__ CUtensorMap tmap_w,
-                             const __grid_constant__ CUtensorMap tmap_x, const SwArgs args) {
+                             const __grid_constant__ CUtensorMap tmap_x,
+                             const __grid_constant__ CUtensorMap tmap_w2,
+                             const __grid_constant__ CUtensorMap tmap_h, const SwArgs args) {
   static_assert(!PACKED || EPI == SW_ACT, "the packed layout is a gated w13");
+  static_assert(!FUSE || EPI != SW_SCATTER, "a fused launch starts with the w13 contraction");
   using C = SwCfg<NT, PAIR>;
   // PAIR: tiles of 256 weight rows; this CTA's half starts at row `rank` * 128
   constexpr int kTileRows = PAIR ? 2 * SW_M : SW_M;
@@ -434,6 +505,10 @@ __global__ void __launch_bounds__(SwCfg<NT, PAIR>::kThreads, 1)
   if (warp == 0 && lane == 0) {
     prefetch_tmap(&tmap_w);
     prefetch_tmap(&tmap_x);
+    if constexpr (FUSE) {
+      prefetch_tmap(&tmap_w2);
+      prefetch_tmap(&tmap_h);
+    }
   }
   if (warp == 1) {
     if constexpr (PAIR) {  // one warp of each CTA of the pair, collectively
@@ -454,7 +529,7 @@ __global__ void __launch_bounds__(SwCfg<NT, PAIR>::kThreads, 1)
   // kernel of a handoff skips the grid-wide wait: the w13 kernel triggered it
   // only after its own pdl_wait, so everything but h is complete, and h is
   // waited for per expert.
-  if (!args.ready_in) pdl_wait();
+  if (FUSE || !args.ready_in) pdl_wait();
   if (args.ready_out) pdl_launch_dependents();
   for (int i = threadIdx.x; i <= E; i += C::kThreads) s_offs[i] = args.offs[i];
   __syncthreads();
@@ -469,25 +544,37 @@ __global__ void __launch_bounds__(SwCfg<NT, PAIR>::kThreads, 1)
   const uint32_t tmem_base = *tmem_slot;
   const int total = s_tstart[E] * args.f_tiles;
   const int num_kb = args.num_kb;
+  const int total2 = FUSE ? s_tstart[E] * args.f_tiles2 : 0;  // w2 tiles after the w13 work
+  const int num_kb2 = FUSE ? args.num_kb2 : 0;
   // stream-K pays only where whole tiles leave a large last wave idle; with
   // two or more waves, CTAs that finish early start the next contraction
   const bool sk = NT == SW_NGRAN && args.stream_k && total < 2 * (int)gridDim.x;
+  // the w2 tiles of a fused launch: split only under one wave (GPT-OSS n = 1:
+  // 92 tiles, 52.1 -> 50.8 us; at n = 4, ~2 waves, the split lost 3 us)
+  const bool sk2 = FUSE && NT == SW_NGRAN && args.stream_k && total2 < (int)gridDim.x;
+  // K steps of a fused launch's w2 tile whose weights may be fetched before
+  // the expert's h rows are complete: the whole ring
+  constexpr int kPreload = C::kStages;
 
   if (warp == 0) {
     // ------------------------------------------------------ TMA producer --
     // Lane 0 waits for free stages and issues the weight (and plain token)
     // copies; with the fused gather every lane then fetches four token rows.
-    const bool gather = args.gather_rows != nullptr;
+    const bool gather_rows = args.gather_rows != nullptr;
     const uint64_t read_once = l2_policy_evict_first();
     int stage = 0;
     uint32_t phase = 0, issued = 0;
     bool ok = true;
     int ready_e = -1;  // expert whose h rows this warp has seen complete
-    WorkIter it(sk, total, num_kb, first, step);
+    WorkIter it(sk, total, num_kb, first, step, total2, num_kb2, sk2);
     Work w;
     while (ok && it.next(w)) {
-      const Tile d = decode_tile(w.t, args.f_tiles, s_tstart, s_offs, E, NT);
+      const bool p1 = FUSE && w.ph == 1;  // a w2 tile of a fused launch
+      const Tile d = decode_tile(w.t, p1 ? args.f_tiles2 : args.f_tiles, s_tstart, s_offs, E, NT);
       const int f0 = d.nt * kTileRows + (int)rank * SW_M;  // first weight row of this CTA
+      const bool gather = gather_rows && !p1;
+      const CUtensorMap *mw = p1 ? &tmap_w2 : &tmap_w;
+      const CUtensorMap *mx = p1 ? &tmap_h : &tmap_x;
       // PAIR: the MMA reads its first n_mma / 2 token rows from the leader
       // and the rest from the peer
       const int rows = d.m_end - d.m0;
@@ -513,13 +600,49 @@ __global__ void __launch_bounds__(SwCfg<NT, PAIR>::kThreads, 1)
       const uint32_t b_bytes = gather ? 512u * (uint32_t)((n_lead + 3) / 4 + (n_peer + 3) / 4)
                                       : (uint32_t)(PAIR ? 2 : 1) * C::kBBytes;
       const uint32_t tx_bytes = (uint32_t)(PAIR ? 2 : 1) * SW_A_BYTES + b_bytes;
-      if (args.ready_in && d.e != ready_e) {
-        if (lane == 0) ok = wait_expert_ready(args, d.e, f0, s_offs, s_abort);
+      int pre = 0;  // K steps whose weights went out before the expert's h was ready
+      if ((FUSE ? p1 : args.ready_in != nullptr) && d.e != ready_e) {
+        const int kbt = p1 ? num_kb2 : num_kb;
+        if constexpr (FUSE && !PAIR) {
+          // A w2 tile of a fused launch: its weights need no h, so the
+          // weights of up to kPreload K steps go into free stages first and
+          // their h boxes follow once the expert's h rows are complete.
+          if (lane == 0) {
+            const int s0 = stage;
+            while (ok && pre < w.k_hi - w.k_lo && pre < kPreload) {
+              ok = wait_bounded(empty_bar(stage), phase ^ 1u, s_abort, args.ctrl, args.timeout_ns);
+              if (!ok) break;
+              mbar_arrive_expect_tx(full_bar(stage), tx_bytes);
+              tma_load_3d_hint(a_addr(stage), mw, full_bar(stage), (w.k_lo + pre) * SW_BK, f0,
+                               d.e, read_once);
+              ++pre;
+              issued = issued < (uint32_t)C::kStages ? issued + 1 : (uint32_t)C::kStages;
+              if (++stage == C::kStages) {
+                stage = 0;
+                phase ^= 1u;
+              }
+            }
+            if (ok) ok = wait_expert_ready(args, d.e, f0, kbt, w.k_lo, w.k_hi, s_offs, s_abort);
+            // the h boxes of those stages, after a failed wait too, so that
+            // every posted stage completes (in-bounds reads) and the drain ends
+            for (int i = 0; i < pre; ++i) {
+              const int si = (s0 + i) % C::kStages;
+              tma_load_2d(b_addr(si), mx, full_bar(si), (w.k_lo + i) * SW_BK, d.m0);
+            }
+          }
+          pre = __shfl_sync(0xffffffffu, pre, 0);
+          stage = __shfl_sync(0xffffffffu, stage, 0);
+          phase = __shfl_sync(0xffffffffu, phase, 0);
+          issued = __shfl_sync(0xffffffffu, issued, 0);
+        } else {
+          if (lane == 0)
+            ok = wait_expert_ready(args, d.e, f0, kbt, w.k_lo, w.k_hi, s_offs, s_abort);
+        }
         ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
         if (!ok) break;
         ready_e = d.e;
       }
-      for (int kb = w.k_lo; kb < w.k_hi; ++kb) {
+      for (int kb = w.k_lo + pre; kb < w.k_hi; ++kb) {
         if (lane == 0)
           ok = wait_bounded(empty_bar(stage), phase ^ 1u, s_abort, args.ctrl, args.timeout_ns);
         ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
@@ -529,11 +652,11 @@ __global__ void __launch_bounds__(SwCfg<NT, PAIR>::kThreads, 1)
           const uint32_t fb = map_to_rank(full_bar(stage), 0);
           if (lane == 0) {
             if (leader) mbar_arrive_expect_tx(full_bar(stage), tx_bytes);
-            if constexpr (PACKED)
-              tma_load_4d_pair(a_addr(stage), &tmap_w, fb, kb * SW_BK, 0, f0 / 2, d.e);
+            if (PACKED && !p1)
+              tma_load_4d_pair(a_addr(stage), mw, fb, kb * SW_BK, 0, f0 / 2, d.e);
             else
-              tma_load_3d_pair(a_addr(stage), &tmap_w, fb, kb * SW_BK, f0, d.e);
-            if (!gather) tma_load_2d_pair(b_addr(stage), &tmap_x, fb, kb * SW_BK, m_b);
+              tma_load_3d_pair(a_addr(stage), mw, fb, kb * SW_BK, f0, d.e);
+            if (!gather) tma_load_2d_pair(b_addr(stage), mx, fb, kb * SW_BK, m_b);
           }
           __syncwarp();
           if (gather && 4 * lane < n_cta)
@@ -546,18 +669,18 @@ __global__ void __launch_bounds__(SwCfg<NT, PAIR>::kThreads, 1)
               // L2 to the w2 tiles fetched ahead while their expert's h is
               // still being computed (GPT-OSS n = 4 / 8 / 64: 109.6 / 162.6 /
               // 255.7 -> 108.5 / 160.9 / 253.2 us per layer)
-              if constexpr (PACKED)
-                tma_load_4d_hint(a_addr(stage), &tmap_w, full_bar(stage), kb * SW_BK, 0, f0 / 2,
-                                 d.e, read_once);
-              else
-                tma_load_3d_hint(a_addr(stage), &tmap_w, full_bar(stage), kb * SW_BK, f0, d.e,
+              if (PACKED && !p1)
+                tma_load_4d_hint(a_addr(stage), mw, full_bar(stage), kb * SW_BK, 0, f0 / 2, d.e,
                                  read_once);
-            } else if constexpr (PACKED) {
-              tma_load_4d(a_addr(stage), &tmap_w, full_bar(stage), kb * SW_BK, 0, f0 / 2, d.e);
+              else
+                tma_load_3d_hint(a_addr(stage), mw, full_bar(stage), kb * SW_BK, f0, d.e,
+                                 read_once);
+            } else if (PACKED && !p1) {
+              tma_load_4d(a_addr(stage), mw, full_bar(stage), kb * SW_BK, 0, f0 / 2, d.e);
             } else {
-              tma_load_3d(a_addr(stage), &tmap_w, full_bar(stage), kb * SW_BK, f0, d.e);
+              tma_load_3d(a_addr(stage), mw, full_bar(stage), kb * SW_BK, f0, d.e);
             }
-            if (!gather) tma_load_2d(b_addr(stage), &tmap_x, full_bar(stage), kb * SW_BK, d.m0);
+            if (!gather) tma_load_2d(b_addr(stage), mx, full_bar(stage), kb * SW_BK, d.m0);
           }
           __syncwarp();  // the expected bytes are posted before any gathered row lands
           if (gather && 4 * lane < n_cta)
@@ -591,10 +714,11 @@ __global__ void __launch_bounds__(SwCfg<NT, PAIR>::kThreads, 1)
       uint32_t phase = 0;
       bool ok = true;
       int local = 0;
-      WorkIter it(sk, total, num_kb, first, step);
+      WorkIter it(sk, total, num_kb, first, step, total2, num_kb2, sk2);
       Work w;
       for (; ok && it.next(w); ++local) {
-        const Tile d = decode_tile(w.t, args.f_tiles, s_tstart, s_offs, E, NT);
+        const Tile d = decode_tile(w.t, FUSE && w.ph == 1 ? args.f_tiles2 : args.f_tiles,
+                                   s_tstart, s_offs, E, NT);
         const int rows = d.m_end - d.m0;
         // MMA N: the tile's rows rounded up to 32 (a multiple of 16, <= 256)
         const int n_mma = (rows + SW_NGRAN - 1) / SW_NGRAN * SW_NGRAN;
@@ -649,12 +773,12 @@ __global__ void __launch_bounds__(SwCfg<NT, PAIR>::kThreads, 1)
     const int half = (warp - 2) >> 2;   // which of the quarter's warps: chunk parity
     constexpr int kPer = C::kEpiWarps / 4;  // warps per lane quarter
     int local = 0;
-    WorkIter it(sk, total, num_kb, first, step);
+    WorkIter it(sk, total, num_kb, first, step, total2, num_kb2, sk2);
     Work w;
-    const int64_t U = (int64_t)total * num_kb;
     const int G = (int)gridDim.x;
     for (; it.next(w); ++local) {
-      const Tile d = decode_tile(w.t, args.f_tiles, s_tstart, s_offs, E, NT);
+      const bool p1 = FUSE && w.ph == 1;  // a w2 tile of a fused launch
+      const Tile d = decode_tile(w.t, p1 ? args.f_tiles2 : args.f_tiles, s_tstart, s_offs, E, NT);
       const int acc = local & 1;
       const uint32_t acc_phase = (uint32_t)(local >> 1) & 1u;
       if (!wait_bounded(tfull_bar(acc), acc_phase, s_abort, args.ctrl, args.timeout_ns)) break;
@@ -669,27 +793,27 @@ __global__ void __launch_bounds__(SwCfg<NT, PAIR>::kThreads, 1)
       et.dst_mine = 0;
       et.g_mine = 0.f;
       if constexpr (NT == SW_NGRAN) {
-        if (sk) {
-          const int64_t u0 = (int64_t)w.t * num_kb;
-          const int c_first = sk_cta(u0, U, G), c_last = sk_cta(u0 + num_kb - 1, U, G);
+        if (p1 ? sk2 : sk) {
+          const int kbt = p1 ? num_kb2 : num_kb;  // K steps of this contraction's tiles
+          const int64_t U = (int64_t)(p1 ? total2 : total) * kbt;
+          const int64_t u0 = (int64_t)w.t * kbt;
+          const int c_first = sk_cta(u0, U, G), c_last = sk_cta(u0 + kbt - 1, U, G);
           if (c_last > c_first) {
-            sk_piece<EPI, NT>(et, args, u0, c_first, c_last,
-                                    sk_pieces(c_first, c_last, U, G), w.k_lo, U, G, q, d.e,
-                                    tempty_bar(acc));
+            const int pieces = sk_pieces(c_first, c_last, U, G);
+            if (p1)
+              sk_piece<SW_SCATTER, NT>(et, args, 1, u0, c_first, c_last, pieces, w.k_lo, U, G,
+                                       q, d.e, tempty_bar(acc));
+            else
+              sk_piece<EPI, NT>(et, args, 0, u0, c_first, c_last, pieces, w.k_lo, U, G, q, d.e,
+                                tempty_bar(acc));
             continue;  // the piece released its accumulator buffer
           }
         }
       }
-      // chunks of 32 token columns, then of 8; the quarter's two warps take
-      // alternate chunks
-      int c0 = 0;
-      if constexpr (NT > SW_NGRAN) {
-        const int full = et.rows & ~31;
-        for (int c = 32 * half; c < full; c += 32 * kPer)
-          epi_chunk<EPI, 32, true>(et, c, args);
-        c0 = full;
-      }
-      for (int c = c0 + 8 * half; c < et.rows; c += 8 * kPer) epi_chunk<EPI, 8>(et, c, args);
+      if (p1)
+        epi_tile<SW_SCATTER, NT, kPer>(et, half, args);
+      else
+        epi_tile<EPI, NT, kPer>(et, half, args);
       tc_fence_before();
       __syncwarp();
       if (lane == 0) {
@@ -698,7 +822,7 @@ __global__ void __launch_bounds__(SwCfg<NT, PAIR>::kThreads, 1)
         else
           mbar_arrive(tempty_bar(acc));
       }
-      if (args.ready_out) publish_ready(args, d.e, lane);
+      if (args.ready_out && !p1) publish_ready(args, d.e, lane);
     }
   }
 
@@ -721,11 +845,12 @@ __global__ void __launch_bounds__(SwCfg<NT, PAIR>::kThreads, 1)
   }
 }
 
-template <int EPI, bool PACKED, int NT, bool PAIR = false>
-cudaError_t launch_swap(const CUtensorMap &tw, const CUtensorMap &tx, const SwArgs &a,
-                        cudaStream_t s) {
+// tw2 / th: the w2 weights and h rows of a fused launch (FUSE), else unused.
+template <int EPI, bool PACKED, int NT, bool PAIR = false, bool FUSE = false>
+cudaError_t launch_swap(const CUtensorMap &tw, const CUtensorMap &tx, const CUtensorMap &tw2,
+                        const CUtensorMap &th, const SwArgs &a, cudaStream_t s) {
   using C = SwCfg<NT, PAIR>;
-  auto kern = grouped_gemm_swap_kernel<EPI, PACKED, NT, PAIR>;
+  auto kern = grouped_gemm_swap_kernel<EPI, PACKED, NT, PAIR, FUSE>;
   static PerDeviceOnce attr_set;
   {
     cudaError_t err = attr_set.run([kern] {
@@ -749,7 +874,7 @@ cudaError_t launch_swap(const CUtensorMap &tw, const CUtensorMap &tx, const SwAr
   attr[1].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = PAIR ? 2 : 1;
-  const cudaError_t err = cudaLaunchKernelEx(&cfg, kern, tw, tx, a);
+  const cudaError_t err = cudaLaunchKernelEx(&cfg, kern, tw, tx, tw2, th, a);
   return err != cudaSuccess ? err : cudaGetLastError();
 }
 
@@ -782,9 +907,9 @@ cudaError_t swap_ffn1(const uint16_t *x_sorted, const uint16_t *w13, int64_t N, 
   }
   a.num_kb = H / SW_BK;
   a.f_tiles = (w13_rows(act, I) + tile_rows - 1) / tile_rows;
-  return relu2_act ? launch_swap<SW_RELU2, false, NT, PAIR>(tw, tx, a, s)
-         : packed  ? launch_swap<SW_ACT, true, NT, PAIR>(tw, tx, a, s)
-                   : launch_swap<SW_ACT, false, NT, PAIR>(tw, tx, a, s);
+  return relu2_act ? launch_swap<SW_RELU2, false, NT, PAIR>(tw, tx, tw, tx, a, s)
+         : packed  ? launch_swap<SW_ACT, true, NT, PAIR>(tw, tx, tw, tx, a, s)
+                   : launch_swap<SW_ACT, false, NT, PAIR>(tw, tx, tw, tx, a, s);
 }
 
 // The w2 contraction (gate scale + scatter) at token-tile width NT.
@@ -799,7 +924,41 @@ cudaError_t swap_ffn2(const uint16_t *h_buf, const uint16_t *w2, int64_t N, int 
     return cudaErrorInvalidValue;
   a.num_kb = I / SW_BK;
   a.f_tiles = (H + tile_rows - 1) / tile_rows;
-  return launch_swap<SW_SCATTER, false, NT, PAIR>(tw, tx, a, s);
+  return launch_swap<SW_SCATTER, false, NT, PAIR>(tw, tx, tw, tx, a, s);
+}
+
+// Both contractions of the decode tiling (32-row token tiles, one CTA per
+// SM) in one launch: the w13 work (stream-K when short), then whole w2
+// tiles, each waiting for its expert's h rows. It saves the second launch,
+// its set-up, and the gap between a w13 CTA leaving an SM and a w2 CTA
+// arriving there.
+cudaError_t swap_ffn_fused(const uint16_t *x_sorted, const uint16_t *w13, const uint16_t *h_buf,
+                           const uint16_t *w2, int64_t N, int E, int H, int I,
+                           const ActParams &act, SwArgs a, cudaStream_t s,
+                           const GatherSrc *gather) {
+  constexpr int NT = SW_NGRAN;
+  const bool relu2_act = act.act == MOE_ACT_RELU2;
+  const bool packed = !relu2_act && act.layout == MOE_W13_PACKED;
+  CUtensorMap tw, tx, tw2, th;
+  const bool w_ok =
+      packed ? map_w13_packed_interleaved(&tw, w13, (uint64_t)E, (uint64_t)I, (uint64_t)H, SW_M / 2)
+             : map_3d(&tw, w13, (uint64_t)E, (uint64_t)w13_rows(act, I), (uint64_t)H, SW_M);
+  const bool x_ok = gather ? map_2d_rows(&tx, gather->x, (uint64_t)gather->n, (uint64_t)H)
+                           : map_2d(&tx, x_sorted, (uint64_t)N, (uint64_t)H, NT);
+  if (!w_ok || !x_ok || !map_3d(&tw2, w2, (uint64_t)E, (uint64_t)H, (uint64_t)I, SW_M) ||
+      !map_2d(&th, h_buf, (uint64_t)N, (uint64_t)I, NT))
+    return cudaErrorInvalidValue;
+  if (gather) {
+    a.gather_rows = a.col_sorted;
+    a.gather_k = gather->k;
+  }
+  a.num_kb = H / SW_BK;
+  a.f_tiles = (w13_rows(act, I) + SW_M - 1) / SW_M;
+  a.num_kb2 = I / SW_BK;
+  a.f_tiles2 = (H + SW_M - 1) / SW_M;
+  return relu2_act ? launch_swap<SW_RELU2, false, NT, false, true>(tw, tx, tw2, th, a, s)
+         : packed  ? launch_swap<SW_ACT, true, NT, false, true>(tw, tx, tw2, th, a, s)
+                   : launch_swap<SW_ACT, false, NT, false, true>(tw, tx, tw2, th, a, s);
 }
 
 // Token-tile width of a contraction with f_tiles weight tiles per expert and
@@ -845,6 +1004,9 @@ SwapPlan plan_ffn_swap(int64_t N, int E, int H, int I, const ActParams &act) {
   }
   p.pair1 = use_pair(p.nt1);
   p.pair2 = use_pair(p.nt2);
+  // decode tiling: both contractions in one launch (it needs every CTA of
+  // the grid resident at once: one per SM)
+  p.fused = p.decode;
   return p;
 }
 
@@ -877,6 +1039,18 @@ cudaError_t launch_ffn_swap(const uint16_t *x_sorted, const int32_t *offs,
   if (a.stream_k) {
     a.sk_cnt = scr.sync + kSyncSk;
     a.sk_part = scr.sk_part;
+  }
+  if (plan.fused) {
+    // one launch: arrivals per token tile are every epilogue warp of every
+    // w13 weight tile; the w2 weights are fetched into L2 while a tile waits
+    a.ready_in = ready;
+    a.ready_nt = SW_NGRAN;
+    a.ready_per_tile = f_tiles1 * sw_epi_warps(SW_NGRAN);
+    a.w = w2;
+    a.w_rows = H;
+    const cudaError_t err = swap_ffn_fused(x_sorted, w13, h_buf, w2, N, E, H, I, act, a, s, gather);
+    if (err != cudaSuccess) return err;
+    return ev_ffn ? record_stage_event(ev_ffn[1], s) : cudaSuccess;
   }
   cudaError_t err;
   switch (nt1) {

@@ -373,10 +373,12 @@ int32_t moe_forward_launch_count(int64_t n, int32_t E, int32_t k, int32_t H, int
   if (n == 0) return 0;
   // the same choices forward_impl makes (default kernel: the swap-operand
   // one), then the gather unless w13 or the cooperative routing kernel moves
-  // the rows, ffn1, ffn2, combine
+  // the rows, ffn1 and ffn2 (one launch at decode sizes), combine
   const bool gather_kernel =
       !fused_gather_rows(n, E, k, MOE_FFN_AUTO) && !route_metadata_moves_rows(n, E, k);
-  return (route_metadata_fits(n, k) ? 1 : 2) + (gather_kernel ? 1 : 0) + 2 + (k > 1 ? 1 : 0);
+  const bool one_ffn_launch = n * k <= (int64_t)kDecodeRowsPerExpert * E;
+  return (route_metadata_fits(n, k) ? 1 : 2) + (gather_kernel ? 1 : 0) +
+         (one_ffn_launch ? 1 : 2) + (k > 1 ? 1 : 0);
 }
 
 moe_status moe_forward(const uint16_t *x, const float *logits, const uint16_t *w13,

@@ -26,20 +26,24 @@ constexpr int kCtrlBarArrive = 32;       // grid barrier counter (top bit flips 
 constexpr int kCtrlNeverSet = 96;        // a word no kernel writes (bounded-wait self-test)
 
 // Per-forward synchronisation words of the expert contractions, zeroed by the
-// dispatch gather of each forward (grouped_gemm_swap.cu):
+// routing kernels (or the dispatch gather) of each forward:
 //   [kSyncReady, +kMaxExperts): per-expert completion counts of the w13
 //     contraction; the w2 contraction starts an expert's tiles once complete;
 //   [kSyncSk, +4 * kSkMaxCtas): arrival counters (per first CTA of a split
 //     tile and TMEM lane quarter) of the w13 contraction's decode stream-K
-//     partition.
+//     partition;
+//   [kSyncSk2, +4 * kSkMaxCtas): the same for the w2 tiles of a decode
+//     launch that runs both contractions.
 constexpr int kSkMaxCtas = 256;
 constexpr int kSyncReady = 0;
 constexpr int kSyncSk = kMaxExperts;
-constexpr int kSyncWords = kMaxExperts + 4 * kSkMaxCtas;
+constexpr int kSyncSk2 = kSyncSk + 4 * kSkMaxCtas;
+constexpr int kSyncWords = kMaxExperts + 2 * 4 * kSkMaxCtas;
 // Decode tiling (32-row token tiles, stream-K) applies when n*k <= 32 * E.
 constexpr int kDecodeRowsPerExpert = 32;
 // fp32 partial sums per stream-K CTA: 2 slots (the CTA's first and last
-// piece) x up to 2 accumulators x 128 weight rows x 32 token columns.
+// piece) x 2 contractions (w13, then w2 in a launch that runs both) x 128
+// weight rows x 32 token columns.
 constexpr size_t kSkPartFloats = 2 * 2 * 128 * 32;
 
 // Default limit of a device-side wait (ns). Legitimate waits last microseconds.
@@ -512,11 +516,11 @@ cudaError_t launch_ffn(const uint16_t *x_sorted, const int32_t *offs, const int3
 
 // Tiling of the swap-operand contractions for N rows (host only): token-tile
 // rows of each, weight tiles per expert of the w13 one, CTA pairs, decode
-// tiling (32-row tiles; the w13 kernel may then split its units evenly over
-// the grid).
+// tiling (32-row tiles; the w13 work may then split its units evenly over
+// the grid), both contractions in one launch.
 struct SwapPlan {
   int nt1, nt2, f_tiles1;
-  bool decode, pair1, pair2;
+  bool decode, pair1, pair2, fused;
 };
 SwapPlan plan_ffn_swap(int64_t N, int E, int H, int I, const ActParams &act);
 

@@ -78,7 +78,8 @@ def test_rank_and_decode_paths_capture_in_a_cuda_graph(variant):
         h = I.layer_inputs(case)
         params = moe.make_params(case.gating, case.act, case.layout)
         w13, w2 = dev_bf16(h["w13"]), dev_bf16(h["w2"])
-        assert moe.forward_launch_count(case.n, case.E, case.k, case.H, case.I) == 4
+        # routing, both contractions in one launch, combine
+        assert moe.forward_launch_count(case.n, case.E, case.k, case.H, case.I) == 3
     x, logits = dev_bf16(h["x"]), dev(h["logits"])
     ws = moe.workspace(case.n, case.E, case.k, case.H, case.I)
     eager = moe.forward(x, logits, w13, w2, case.k, params, ws)
@@ -108,14 +109,17 @@ def test_repeated_runs_bit_identical():
 
 
 @pytest.mark.parametrize("case", [
-    I.GPTOSS.with_n(1),      # decode: w2 tiles start beside the w13 kernel's last wave
+    I.GPTOSS.with_n(1),      # decode: one launch, stream-K w13 units, then w2 tiles
     I.GPTOSS.with_n(8),
+    I.GPTOSS.with_n(64),     # decode: one launch, several waves of w13 tiles first
     I.GPTOSS.with_n(300),    # 64..256-row token tiles, ragged experts
     I.MINIMIND_E4,           # k = 1: the w2 kernel writes out directly
 ], ids=lambda c: c.name)
 def test_expert_handoff_replays_alternating_inputs(case):
-    """The w2 kernel starts an expert's tiles once the w13 kernel has counted
-    that expert's h rows complete (no grid-wide wait between the two). Graph
+    """The w2 contraction starts an expert's tiles once the w13 one has
+    counted that expert's h rows complete (no grid-wide wait between the two;
+    at decode sizes both run in one launch, whose CTAs wait on h rows that
+    other CTAs of the grid compute). Graph
     replays alternate between two token batches under the same routing, so a
     w2 tile that read h before it was complete would see the other batch's
     values: every replay must equal the eager result of its own batch."""

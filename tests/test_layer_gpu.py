@@ -278,9 +278,10 @@ def test_fused_gather_matches_materialised_rows(n, E, k, H, I_, act, layout):
     each tile's token rows from x (tile::gather4 of rows col_sorted[p] / k,
     only the tile's own rows); the stage path reads the rows the gather
     kernel materialised in X_sorted. Same arithmetic on the same rows: the
-    outputs agree bit for bit. The forward launches no gather kernel there."""
+    outputs agree bit for bit. The forward launches no gather kernel there,
+    and one kernel for both contractions."""
     assert moe.ffn_plan(n, E, k, H, I_, moe.make_params())["decode"]
-    assert moe.forward_launch_count(n, E, k, H, I_) == 3 + (k > 1)
+    assert moe.forward_launch_count(n, E, k, H, I_) == 2 + (k > 1)
     case = I.LayerCase(f"fused_gather_n{n}", n=n, H=H, E=E, k=k, I=I_, act=act, layout=layout,
                        w_std=0.05, seed=n + E)
     L = Layer(case)
