@@ -383,7 +383,8 @@ moe_status moe_forward_timed(const uint16_t *x, const float *logits, const uint1
  * when a CTA's slots fit its shared memory, else two), the gather (none when
  * n*k <= 2E, where the w13 contraction gathers, nor when the cooperative
  * routing kernel copies the rows, on at least half the SMs), the two expert
- * contractions (one launch when n*k <= 32E) and, when k > 1, the combine;
+ * contractions (one launch when n*k <= 32E, or when both run 256-row token
+ * tiles on CTA pairs; counted for a gated w13) and, when k > 1, the combine;
  * 0 for n = 0; -1 for sizes
  * moe_forward rejects. Host-only: launches nothing. No counterpart on the
  * pages: lets a caller size a CUDA graph or count its launches. */
@@ -394,9 +395,9 @@ int32_t moe_forward_launch_count(int64_t n, int32_t E, int32_t k, int32_t H, int
  * choice). Writes plan[0..4]: token rows per tile of the w13 and of the w2
  * contraction; 1 if the w13 / the w2 contraction runs on CTA pairs (one
  * M = 256 MMA over two SMs), else 0; 1 for the decode tiling (32-row tiles,
- * the w13 units split evenly over the SMs when they make under two waves,
- * both contractions in one launch whose CTAs run the w2 tiles after their
- * w13 work).
+ * the w13 units split evenly over the SMs when they make under two waves).
+ * Both contractions run in one launch, whose CTAs take w2 tiles after their
+ * w13 work, at the decode tiling and where both run on CTA pairs.
  * With params->ffn_kernel = MOE_FFN_TILED: 128, 128, 0, 0, 0. Returns the
  * validation status of moe_forward for the same arguments (MOE_ERR_INVALID_ARG
  * for a null plan). No counterpart on the pages: introspection for callers

@@ -42,9 +42,10 @@
 // roughly 70 GB/s at most, so a decode w13 contraction with fewer than two
 // waves of tiles splits its (tile, K step) units evenly over the grid
 // (stream-K) instead of leaving most SMs idle behind a few whole tiles.
-// At decode sizes one launch runs both contractions: each CTA takes its w2
-// tiles (in reverse CTA order, or split the same way under one wave) after
-// its w13 work, and fetches a w2 tile's weights into free stages before the
+// At decode sizes, and where both contractions run 256-row tiles on CTA
+// pairs, one launch runs both: each CTA takes its w2 tiles (in reverse CTA
+// order, or at decode split the same way under one wave) after its w13 work;
+// at decode it fetches a w2 tile's weights into free stages before the
 // tile's h rows are complete.
 //
 // Warps: 0 TMA producer, 1 TMEM allocation + MMA issue, 2-5 epilogue (warp
@@ -874,6 +875,32 @@ cudaError_t launch_swap(const CUtensorMap &tw, const CUtensorMap &tx, const CUte
   attr[1].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = PAIR ? 2 : 1;
+  if constexpr (FUSE) {
+    // CTAs of a fused launch wait for h rows that other CTAs compute: the
+    // grid is only as large as can be resident at once (queried once per
+    // device; the kernel takes any grid size)
+    static std::atomic<int> resident[PerDeviceOnce::kMaxDevices] = {};
+    int dev = 0;
+    cudaGetDevice(&dev);
+    const bool slot = dev >= 0 && dev < PerDeviceOnce::kMaxDevices;
+    int fit = slot ? resident[dev].load(std::memory_order_relaxed) : 0;
+    if (fit <= 0) {
+      int n = 0;
+      cudaError_t e;
+      if constexpr (PAIR) {
+        e = cudaOccupancyMaxActiveClusters(&n, kern, &cfg);
+        n *= 2;
+      } else {
+        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kern, C::kThreads, C::kSmemBytes);
+        n *= device_sm_count();
+      }
+      if (e != cudaSuccess) return e;
+      if (n < (PAIR ? 2 : 1)) return cudaErrorInvalidConfiguration;
+      fit = n;
+      if (slot) resident[dev].store(fit, std::memory_order_relaxed);
+    }
+    if ((int)cfg.gridDim.x > fit) cfg.gridDim.x = (unsigned)(PAIR ? fit & ~1 : fit);
+  }
   const cudaError_t err = cudaLaunchKernelEx(&cfg, kern, tw, tx, tw2, th, a);
   return err != cudaSuccess ? err : cudaGetLastError();
 }
@@ -932,11 +959,13 @@ cudaError_t swap_ffn2(const uint16_t *h_buf, const uint16_t *w2, int64_t N, int 
 // tiles, each waiting for its expert's h rows. It saves the second launch,
 // its set-up, and the gap between a w13 CTA leaving an SM and a w2 CTA
 // arriving there.
+template <int NT>
 cudaError_t swap_ffn_fused(const uint16_t *x_sorted, const uint16_t *w13, const uint16_t *h_buf,
                            const uint16_t *w2, int64_t N, int E, int H, int I,
                            const ActParams &act, SwArgs a, cudaStream_t s,
                            const GatherSrc *gather) {
-  constexpr int NT = SW_NGRAN;
+  constexpr bool PAIR = use_pair(NT);
+  constexpr int tile_rows = PAIR ? 2 * SW_M : SW_M;
   const bool relu2_act = act.act == MOE_ACT_RELU2;
   const bool packed = !relu2_act && act.layout == MOE_W13_PACKED;
   CUtensorMap tw, tx, tw2, th;
@@ -944,21 +973,25 @@ cudaError_t swap_ffn_fused(const uint16_t *x_sorted, const uint16_t *w13, const 
       packed ? map_w13_packed_interleaved(&tw, w13, (uint64_t)E, (uint64_t)I, (uint64_t)H, SW_M / 2)
              : map_3d(&tw, w13, (uint64_t)E, (uint64_t)w13_rows(act, I), (uint64_t)H, SW_M);
   const bool x_ok = gather ? map_2d_rows(&tx, gather->x, (uint64_t)gather->n, (uint64_t)H)
-                           : map_2d(&tx, x_sorted, (uint64_t)N, (uint64_t)H, NT);
+                           : map_2d(&tx, x_sorted, (uint64_t)N, (uint64_t)H, PAIR ? NT / 2 : NT);
   if (!w_ok || !x_ok || !map_3d(&tw2, w2, (uint64_t)E, (uint64_t)H, (uint64_t)I, SW_M) ||
-      !map_2d(&th, h_buf, (uint64_t)N, (uint64_t)I, NT))
+      !map_2d(&th, h_buf, (uint64_t)N, (uint64_t)I, PAIR ? NT / 2 : NT))
     return cudaErrorInvalidValue;
   if (gather) {
     a.gather_rows = a.col_sorted;
     a.gather_k = gather->k;
   }
   a.num_kb = H / SW_BK;
-  a.f_tiles = (w13_rows(act, I) + SW_M - 1) / SW_M;
+  a.f_tiles = (w13_rows(act, I) + tile_rows - 1) / tile_rows;
   a.num_kb2 = I / SW_BK;
-  a.f_tiles2 = (H + SW_M - 1) / SW_M;
-  return relu2_act ? launch_swap<SW_RELU2, false, NT, false, true>(tw, tx, tw2, th, a, s)
-         : packed  ? launch_swap<SW_ACT, true, NT, false, true>(tw, tx, tw2, th, a, s)
-                   : launch_swap<SW_ACT, false, NT, false, true>(tw, tx, tw2, th, a, s);
+  a.f_tiles2 = (H + tile_rows - 1) / tile_rows;
+  // arrivals per token tile: every epilogue warp of every w13 weight tile
+  // (a pair tile counts both CTAs' warps)
+  a.ready_nt = NT;
+  a.ready_per_tile = a.f_tiles * (PAIR ? 2 : 1) * sw_epi_warps(NT);
+  return relu2_act ? launch_swap<SW_RELU2, false, NT, PAIR, true>(tw, tx, tw2, th, a, s)
+         : packed  ? launch_swap<SW_ACT, true, NT, PAIR, true>(tw, tx, tw2, th, a, s)
+                   : launch_swap<SW_ACT, false, NT, PAIR, true>(tw, tx, tw2, th, a, s);
 }
 
 // Token-tile width of a contraction with f_tiles weight tiles per expert and
@@ -991,6 +1024,12 @@ int pick_token_tile(int64_t N, int E, int f_tiles, int num_kb) {
 
 }  // namespace
 
+// Both contractions in one launch where both run on CTA pairs (256-row token
+// tiles): same-box A/B, GPT-OSS prefill n = 8192 1.17 -> 1.14 ms, the skewed
+// 128-expert n = 16384 layer 2.182 -> 2.145 ms. Where w2 would pick narrower
+// tiles (MiniMind: 128 rows on single CTAs), forcing pairs on it lost 1.3 us.
+constexpr bool kFusePairs = true;
+
 SwapPlan plan_ffn_swap(int64_t N, int E, int H, int I, const ActParams &act) {
   SwapPlan p{};
   p.f_tiles1 = (w13_rows(act, I) + SW_M - 1) / SW_M;
@@ -1004,9 +1043,10 @@ SwapPlan plan_ffn_swap(int64_t N, int E, int H, int I, const ActParams &act) {
   }
   p.pair1 = use_pair(p.nt1);
   p.pair2 = use_pair(p.nt2);
-  // decode tiling: both contractions in one launch (it needs every CTA of
-  // the grid resident at once: one per SM)
-  p.fused = p.decode;
+  // both contractions in one launch (it needs every CTA of the grid
+  // resident at once): the decode tiling, and 256-row tiles on CTA pairs for
+  // both
+  p.fused = p.decode || (kFusePairs && p.pair1 && p.pair2);
   return p;
 }
 
@@ -1041,14 +1081,15 @@ cudaError_t launch_ffn_swap(const uint16_t *x_sorted, const int32_t *offs,
     a.sk_part = scr.sk_part;
   }
   if (plan.fused) {
-    // one launch: arrivals per token tile are every epilogue warp of every
-    // w13 weight tile; the w2 weights are fetched into L2 while a tile waits
+    // one launch; the w2 weights are fetched into L2 while a tile waits
     a.ready_in = ready;
-    a.ready_nt = SW_NGRAN;
-    a.ready_per_tile = f_tiles1 * sw_epi_warps(SW_NGRAN);
     a.w = w2;
     a.w_rows = H;
-    const cudaError_t err = swap_ffn_fused(x_sorted, w13, h_buf, w2, N, E, H, I, act, a, s, gather);
+    const cudaError_t err =
+        plan.decode ? swap_ffn_fused<SW_NGRAN>(x_sorted, w13, h_buf, w2, N, E, H, I, act, a, s,
+                                              gather)
+                    : swap_ffn_fused<256>(x_sorted, w13, h_buf, w2, N, E, H, I, act, a, s,
+                                          gather);
     if (err != cudaSuccess) return err;
     return ev_ffn ? record_stage_event(ev_ffn[1], s) : cudaSuccess;
   }

@@ -373,10 +373,14 @@ int32_t moe_forward_launch_count(int64_t n, int32_t E, int32_t k, int32_t H, int
   if (n == 0) return 0;
   // the same choices forward_impl makes (default kernel: the swap-operand
   // one), then the gather unless w13 or the cooperative routing kernel moves
-  // the rows, ffn1 and ffn2 (one launch at decode sizes), combine
+  // the rows, ffn1 and ffn2 (one launch at decode sizes and on CTA pairs;
+  // counted for a gated w13), combine
   const bool gather_kernel =
       !fused_gather_rows(n, E, k, MOE_FFN_AUTO) && !route_metadata_moves_rows(n, E, k);
-  const bool one_ffn_launch = n * k <= (int64_t)kDecodeRowsPerExpert * E;
+  ActParams act{};
+  act.act = MOE_ACT_SWIGLU;
+  act.ffn_kernel = MOE_FFN_AUTO;
+  const bool one_ffn_launch = plan_ffn_swap(n * k, E, H, I, act).fused;
   return (route_metadata_fits(n, k) ? 1 : 2) + (gather_kernel ? 1 : 0) +
          (one_ffn_launch ? 1 : 2) + (k > 1 ? 1 : 0);
 }
