@@ -66,7 +66,7 @@
 extern "C" {
 #endif
 
-#define MOE_ABI_VERSION 3
+#define MOE_ABI_VERSION 4
 
 typedef void *moe_stream;  /* a cudaStream_t */
 
@@ -392,13 +392,13 @@ int32_t moe_forward_launch_count(int64_t n, int32_t E, int32_t k, int32_t H, int
 
 /* How moe_grouped_ffn / moe_forward tile the two expert contractions for these
  * sizes and params (no launch; the current device's SM count enters the
- * choice). Writes plan[0..4]: token rows per tile of the w13 and of the w2
+ * choice). Writes plan[0..5]: token rows per tile of the w13 and of the w2
  * contraction; 1 if the w13 / the w2 contraction runs on CTA pairs (one
  * M = 256 MMA over two SMs), else 0; 1 for the decode tiling (32-row tiles,
- * the w13 units split evenly over the SMs when they make under two waves).
- * Both contractions run in one launch, whose CTAs take w2 tiles after their
- * w13 work, at the decode tiling and where both run on CTA pairs.
- * With params->ffn_kernel = MOE_FFN_TILED: 128, 128, 0, 0, 0. Returns the
+ * the w13 units split evenly over the SMs when they make under two waves);
+ * 1 when both contractions run in one launch, whose CTAs take w2 tiles after
+ * their w13 work (the decode tiling, and where both run on CTA pairs).
+ * With params->ffn_kernel = MOE_FFN_TILED: 128, 128, 0, 0, 0, 0. Returns the
  * validation status of moe_forward for the same arguments (MOE_ERR_INVALID_ARG
  * for a null plan). No counterpart on the pages: introspection for callers
  * and tests. */

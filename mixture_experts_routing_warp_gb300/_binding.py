@@ -22,7 +22,7 @@ ACT = {"swiglu": 0, "swiglu_oai": 1, "relu2": 2}
 LAYOUT = {"packed": 0, "interleaved": 1}
 SET_ALPHA, SET_BETA, SET_LIMIT = 1, 2, 4
 FFN_KERNEL = {"auto": 0, "tiled": 1, "swap": 2}
-ABI_VERSION = 3
+ABI_VERSION = 4
 
 STATUS = {0: "MOE_OK", 1: "MOE_ERR_INVALID_ARG", 2: "MOE_ERR_UNSUPPORTED",
           3: "MOE_ERR_WORKSPACE_TOO_SMALL", 4: "MOE_ERR_CUDA", 5: "MOE_ERR_TIMEOUT",
@@ -390,12 +390,12 @@ def forward_launch_count(n: int, E: int, k: int, H: int, I: int) -> int:
 
 def ffn_plan(n: int, E: int, k: int, H: int, I: int, params: MoeParams) -> dict:
     """How the two expert contractions are tiled for these sizes (no launch):
-    token rows per tile of each, whether each runs on CTA pairs, and whether
-    the decode tiling applies."""
-    plan = (ctypes.c_int32 * 5)()
+    token rows per tile of each, whether each runs on CTA pairs, whether the
+    decode tiling applies, and whether both run in one launch."""
+    plan = (ctypes.c_int32 * 6)()
     _check(lib().moe_ffn_plan(n, E, k, H, I, ctypes.byref(params), plan), "moe_ffn_plan")
     return {"token_tile_w13": plan[0], "token_tile_w2": plan[1], "pair_w13": bool(plan[2]),
-            "pair_w2": bool(plan[3]), "decode": bool(plan[4])}
+            "pair_w2": bool(plan[3]), "decode": bool(plan[4]), "fused": bool(plan[5])}
 
 
 def read_status(ws: torch.Tensor, reset: bool = False) -> int:

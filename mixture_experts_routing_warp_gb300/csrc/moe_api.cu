@@ -356,7 +356,7 @@ moe_status moe_ffn_plan(int64_t n, int32_t E, int32_t k, int32_t H, int32_t I,
   if (!plan) return MOE_ERR_INVALID_ARG;
   if (act.ffn_kernel == MOE_FFN_TILED) {
     plan[0] = plan[1] = 128;  // BM: token rows per tile of the tokens-on-M kernel
-    plan[2] = plan[3] = plan[4] = 0;
+    plan[2] = plan[3] = plan[4] = plan[5] = 0;
     return MOE_OK;
   }
   const SwapPlan p = plan_ffn_swap(n * k, E, H, I, act);
@@ -365,6 +365,7 @@ moe_status moe_ffn_plan(int64_t n, int32_t E, int32_t k, int32_t H, int32_t I,
   plan[2] = p.pair1;
   plan[3] = p.pair2;
   plan[4] = p.decode;
+  plan[5] = p.fused;
   return MOE_OK;
 }
 

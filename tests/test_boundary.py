@@ -45,7 +45,7 @@ def test_exports_every_declared_function(L):
 
 
 def test_abi_and_status_strings(L):
-    assert L.moe_abi_version() == 3
+    assert L.moe_abi_version() == 4
     for code in range(7):
         s = moe.status_string(code)
         assert s.startswith("MOE_"), s
@@ -112,16 +112,17 @@ def test_ffn_plan_host_rules(L):
     """moe_ffn_plan validates like moe_forward, reports the tokens-on-M
     kernel's fixed tiling, and flags the decode tiling (n*k <= 32 E) on the
     host alone."""
-    plan = (ctypes.c_int32 * 5)()
+    plan = (ctypes.c_int32 * 6)()
     p = ctypes.byref(moe.make_params())
     assert L.moe_ffn_plan(8, 0, 1, 128, 128, p, plan) == 1      # E < 1
     assert L.moe_ffn_plan(8, 4, 2, 96, 128, p, plan) == 1       # H not a multiple of 64
     assert L.moe_ffn_plan(8, 4, 2, 128, 128, p, None) == 1      # no output
     assert L.moe_ffn_plan(8, 4, 2, 128, 128, ctypes.byref(moe.make_params(ffn_kernel="tiled")),
                           plan) == 0
-    assert list(plan) == [128, 128, 0, 0, 0]
+    assert list(plan) == [128, 128, 0, 0, 0, 0]
     assert L.moe_ffn_plan(1, 32, 4, 2880, 2880, p, plan) == 0
     assert plan[4] == 1 and plan[0] == plan[1] == 32 and plan[2] == plan[3] == 0
+    assert plan[5] == 1  # decode: both contractions in one launch
     assert L.moe_ffn_plan(256, 32, 4, 2880, 2880, p, plan) == 0  # n*k = 32 E: still decode
     assert plan[4] == 1
     assert L.moe_ffn_plan(257, 32, 4, 2880, 2880, p, plan) == 0
