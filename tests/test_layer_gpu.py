@@ -151,13 +151,19 @@ def test_gptoss_decode(n):
     c = L.case
     plan = moe.ffn_plan(c.n, c.E, c.k, c.H, c.I, L.params)
     assert plan["decode"] == (c.n * c.k <= 32 * c.E)
+    # both contractions in one launch at decode (and on pairs beyond it)
+    assert plan["fused"] == (plan["decode"] or (plan["pair_w13"] and plan["pair_w2"]))
     _check_full(L)
 
 
 @pytest.mark.parametrize("ffn_kernel", ["auto", "tiled"])
 def test_gptoss_prefill_n2048_every_token(ffn_kernel):
-    """GPT-OSS prefill at 2048 tokens: every output element against the oracle."""
-    _check_full_cached(Layer(I.GPTOSS.with_n(2048), ffn_kernel=ffn_kernel))
+    """GPT-OSS prefill at 2048 tokens: every output element against the oracle
+    (AUTO: both contractions in one launch on CTA pairs)."""
+    L = Layer(I.GPTOSS.with_n(2048), ffn_kernel=ffn_kernel)
+    plan = moe.ffn_plan(2048, L.case.E, L.case.k, L.case.H, L.case.I, L.params)
+    assert plan["fused"] == (ffn_kernel == "auto")
+    _check_full_cached(L)
 
 
 @pytest.mark.parametrize("ffn_kernel", ["auto", "tiled"])
@@ -167,15 +173,20 @@ def test_gptoss_prefill_n8192_every_tile(ffn_kernel):
     L = Layer(I.GPTOSS.with_n(8192), ffn_kernel=ffn_kernel)
     plan = moe.ffn_plan(8192, L.case.E, L.case.k, L.case.H, L.case.I, L.params)
     if ffn_kernel == "auto":
-        assert plan["pair_w13"] and plan["pair_w2"]
+        assert plan["pair_w13"] and plan["pair_w2"] and plan["fused"]
     _check_tiles(L)
 
 
 @pytest.mark.parametrize("ffn_kernel", ["auto", "tiled"])
 def test_skewed_prefill_every_tile(ffn_kernel):
     """The skewed 128-expert prefill (n = 16384; one expert holds almost every
-    token, most hold 0-2): tokens from every 128-row block of every expert."""
+    token, most hold 0-2): tokens from every 128-row block of every expert.
+    AUTO runs both contractions in one launch on CTA pairs, where the w2
+    tiles of the many tiny experts wait on few h rows each."""
     L = Layer(I.SKEWED, ffn_kernel=ffn_kernel)
+    if ffn_kernel == "auto":
+        c = L.case
+        assert moe.ffn_plan(c.n, c.E, c.k, c.H, c.I, L.params)["fused"]
     _check_tiles(L)
 
 
