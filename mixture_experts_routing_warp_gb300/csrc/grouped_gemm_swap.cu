@@ -29,8 +29,9 @@
 //   ffn2: y_flat[col_sorted[m0 + j], f0 + w] = gate_scal[m0 + j] * D[w, j].
 // TMEM is read in chunks of 32 (then 8) token columns up to the tile's rows.
 //
-// Token rows come from X_sorted (the gather kernel's expert-sorted copy) as
-// 2-D boxes, or, with at most 2 slots per expert, straight from the unsorted
+// Token rows come from X_sorted (the expert-sorted copy that the gather
+// kernel or the routing kernel writes) as 2-D boxes, or, with at most 2 slots
+// per expert, straight from the unsorted
 // x: the producer warp reads the tile's rows col_sorted[p] / k and each lane
 // fetches 4 of them per K step with tile::gather4 (one-row boxes). A gather4
 // costs about as much TMA time as a whole box, so wide tiles keep X_sorted.
@@ -48,8 +49,9 @@
 // at decode it fetches a w2 tile's weights into free stages before the
 // tile's h rows are complete.
 //
-// Warps: 0 TMA producer, 1 TMEM allocation + MMA issue, 2-5 epilogue (warp
-// q reads TMEM lanes 32*(q%4)..). Every mbarrier wait is bounded.
+// Warps: 0 TMA producer, 1 TMEM allocation + MMA issue, then the epilogue
+// warps (4; 8 for tiles wider than 32 rows, two per TMEM lane quarter): warp
+// q reads TMEM lanes 32*(q%4).. . Every mbarrier and counter wait is bounded.
 #include "tc_ptx.cuh"
 
 namespace moe {
@@ -167,9 +169,10 @@ struct Work {
 
 // The CTA's work items in order: whole tiles t = first + i * step, or
 // (stream-K) the pieces of its unit range; then, in a launch that runs both
-// contractions, whole w2 tiles t = (step - 1 - first) + i * step of total2:
-// in reverse CTA order, so the CTAs left with one w13 tile fewer (the last
-// total % step) take one w2 tile more. Every role walks the same list.
+// contractions, whole w2 tiles t = (step - 1 - first) + i * step of total2
+// (in reverse CTA order, so the CTAs left with one w13 tile fewer -- the last
+// total % step -- take one w2 tile more), or with stream_k2 the pieces of its
+// range of the w2 units. Every role walks the same list.
 struct WorkIter {
   int64_t u, hi, u2, hi2;
   int t, total, kb;
