@@ -314,6 +314,13 @@ moe_status moe_combine(const uint16_t *y_flat, int64_t n, int32_t k, int32_t H, 
  *   itself; else, when the cooperative route + metadata kernel runs on at
  *   least half the SMs, it copies the rows into expert-sorted order after
  *   its scatter; else a gather kernel does.
+ *   The two expert contractions run as one persistent launch at decode sizes
+ *   (n*k <= 32E) and where both use CTA pairs (moe_ffn_plan "fused"): its
+ *   CTAs take w2 tiles once other CTAs of the same grid have stored the
+ *   expert's h rows, so the grid is sized to what can be resident at once.
+ *   Work on other streams that holds SMs for long delays it; a wait past
+ *   one second records MOE_ERR_TIMEOUT in the workspace status word (no
+ *   hang; moe_read_status).
  *   topk_indx / topk_vals ([n, k]) and meta: optional outputs (NULL = keep
  *   them inside the workspace). When given, all five meta arrays must be
  *   non-NULL. */
