@@ -402,6 +402,27 @@ def test_token_tile_widths(act, layout, Idim):
     _check_full(L)
 
 
+@pytest.mark.parametrize("n,H,I_,act,layout", [
+    (6144, 768, 768, "swiglu_oai", "interleaved"),   # one launch on CTA pairs
+    (32, 256, 256, "swiglu", "packed"),              # decode (n*k <= 32E): stream-K units
+])
+def test_single_expert_in_one_launch(n, H, I_, act, layout):
+    """E = 1 (a dense layer): in the launch that runs both contractions every
+    w2 tile waits for all of the grid's w13 work. Against the oracle, twice,
+    bit for bit."""
+    case = I.LayerCase(f"one_expert_n{n}", n=n, H=H, E=1, k=1, I=I_, act=act, layout=layout,
+                       w_std=0.05, seed=n)
+    L = Layer(case)
+    plan = moe.ffn_plan(n, 1, 1, H, I_, L.params)
+    assert plan["fused"]
+    _check_full(L)
+    ws = moe.workspace(n, 1, 1, H, I_)
+    outs = [moe.forward(L.x, L.logits, L.w13, L.w2, 1, L.params, ws).clone() for _ in range(2)]
+    torch.cuda.synchronize()
+    assert moe.read_status(ws) == 0
+    assert torch.equal(outs[0].view(torch.int16), outs[1].view(torch.int16))
+
+
 @pytest.mark.parametrize("act,layout", [("swiglu_oai", "interleaved"), ("relu2", "packed"),
                                         ("swiglu", "packed")])
 def test_cta_pair_tiles(act, layout):
